@@ -1,0 +1,333 @@
+"""Pins for the CPU oracle: closed forms, invariants, finite differences, brute force.
+
+Every check here fixes the oracle against something other than itself: a
+hand-worked example, a closed form (geometric series, symmetric sums), an
+invariant of softmax attention, central finite differences of the loss, or
+the tiled online-softmax recurrence of the attnax Pallas kernel body.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle.attention as A
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def _rand(*shape, seed=0):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+
+def test_two_token_golden():
+    g = json.load(open(os.path.join(GOLDEN, "two_token.json")))
+    i, e = g["inputs"], g["expected"]
+    q, k, v, do = (np.array(i[n]) for n in ("q", "k", "v", "dout"))
+    o, lse = A.attn_fwd(q, k, v, scale=i["scale"])
+    dq, dk, dv = A.attn_bwd(q, k, v, do, scale=i["scale"])
+    np.testing.assert_allclose(A.attn_probs(q, k, 0, 0, scale=i["scale"])[0], e["P"], rtol=1e-14)
+    np.testing.assert_allclose(o, e["o"], rtol=1e-14)
+    np.testing.assert_allclose(lse, e["lse"], rtol=1e-14)
+    np.testing.assert_allclose(dq, e["dq"], rtol=1e-13)
+    np.testing.assert_allclose(dk, e["dk"], rtol=1e-13)
+    np.testing.assert_allclose(dv, e["dv"], rtol=1e-14)
+    # the same numbers from their closed forms in e
+    E = math.e
+    assert abs(o[0, 0, 0, 0] - E / (1 + E)) < 1e-15
+    assert abs(lse[0, 0, 0] - math.log(1 + E)) < 1e-15
+    assert abs(dq[0, 0, 0, 0] - E / (1 + E) ** 2) < 1e-15
+
+
+@pytest.mark.parametrize("H,h", [(8, 0), (8, 3), (8, 7), (4, 1)])
+def test_alibi_closed_form(H, h):
+    """q = k = 0: P_ij = r^j (r-1)/(r^n - 1) with r = e^slope (a geometric series)."""
+    Sq, Skv, D = 5, 7, 4
+    q = np.zeros((1, H, Sq, D))
+    k = np.zeros((1, H, Skv, D))
+    v = np.zeros((1, H, Skv, Skv))
+    v[0, :, np.arange(Skv), np.arange(Skv)] = 1.0          # one-hot rows: O = P
+    slope = 2.0 ** (-8.0 * (h + 1) / H)
+    r = math.exp(slope)
+    o, lse = A.attn_fwd(q, k, v, score_mod="alibi", scale=1.0)
+    j = np.arange(Skv)
+    p_expect = r ** j * (r - 1) / (r ** Skv - 1)
+    for i in range(Sq):
+        np.testing.assert_allclose(o[0, h, i], p_expect, rtol=1e-12)
+        assert abs(lse[0, h, i] - (-slope * i + math.log((r ** Skv - 1) / (r - 1)))) < 1e-12
+
+
+def test_checkerboard_closed_form():
+    """q = k = 0, even Skv: each row has Skv/2 entries at +0.5 and Skv/2 at -0.5."""
+    Sq, Skv = 4, 6
+    q = np.zeros((1, 1, Sq, 2))
+    k = np.zeros((1, 1, Skv, 2))
+    v = np.zeros((1, 1, Skv, Skv))
+    v[0, 0, np.arange(Skv), np.arange(Skv)] = 1.0
+    o, lse = A.attn_fwd(q, k, v, score_mod="checkerboard", scale=1.0)
+    Z = (Skv / 2) * (math.exp(0.5) + math.exp(-0.5))
+    for i in range(Sq):
+        expect = np.array([math.exp(0.5 if (i + j) % 2 == 0 else -0.5) / Z for j in range(Skv)])
+        np.testing.assert_allclose(o[0, 0, i], expect, rtol=1e-13)
+        assert abs(lse[0, 0, i] - math.log(Z)) < 1e-13
+
+
+def test_causal_first_row_and_scale():
+    """Causal row 0 sees only key 0: O_0 = v_0 and lse_0 = scale q_0.k_0."""
+    q, k, v = _rand(1, 2, 6, 4, seed=1), _rand(1, 2, 6, 4, seed=2), _rand(1, 2, 6, 4, seed=3)
+    for mode in ("score_mod", "block_mask"):
+        if mode == "score_mod":
+            o, lse = A.attn_fwd(q, k, v, score_mod="causal", scale=0.3)
+        else:
+            bm = A.BlockMask(A.build_block_mask("causal", 1, 2, 6, 6, 2, 2), "causal", 2, 2)
+            o, lse = A.attn_fwd(q, k, v, block_mask=bm, scale=0.3)
+        np.testing.assert_allclose(o[0, :, 0], v[0, :, 0], rtol=1e-14)
+        np.testing.assert_allclose(lse[0, :, 0], 0.3 * (q[0, :, 0] * k[0, :, 0]).sum(-1), rtol=1e-13)
+
+
+def test_default_scale_is_inverse_sqrt_d():
+    q, k, v = _rand(1, 1, 3, 9, seed=4), _rand(1, 1, 3, 9, seed=5), _rand(1, 1, 3, 9, seed=6)
+    o1, l1 = A.attn_fwd(q, k, v)
+    o2, l2 = A.attn_fwd(q, k, v, scale=1.0 / 3.0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------------------
+# invariants
+# ---------------------------------------------------------------------------
+
+MODS = ["none", "alibi", "checkerboard", "causal"]
+
+
+@pytest.mark.parametrize("mod", MODS)
+def test_rows_sum_to_one(mod):
+    q, k = _rand(2, 3, 7, 4, seed=7), _rand(2, 3, 9, 4, seed=8)
+    km = (np.random.default_rng(9).random((2, 9)) > 0.3).astype(np.uint8)
+    km[:, 0] = 1
+    for b in range(2):
+        for h in range(3):
+            p = A.attn_probs(q, k, b, h, key_mask=km, score_mod=mod)
+            np.testing.assert_allclose(p.sum(1), 1.0, rtol=1e-14)
+            assert (p[:, km[b] == 0] == 0).all()
+
+
+@pytest.mark.parametrize("mod", MODS)
+def test_constant_v(mod):
+    """V = c gives O = c and, for any dO, dQ = dK = 0."""
+    q, k = _rand(1, 2, 5, 3, seed=10), _rand(1, 2, 5, 3, seed=11)
+    v = np.full((1, 2, 5, 3), 0.75)
+    do = _rand(1, 2, 5, 3, seed=12)
+    o, _ = A.attn_fwd(q, k, v, score_mod=mod)
+    np.testing.assert_allclose(o, 0.75, rtol=1e-14)
+    dq, dk, _ = A.attn_bwd(q, k, v, do, score_mod=mod)
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+
+
+def test_one_hot_v_selects_weights():
+    q, k = _rand(1, 1, 4, 6, seed=13), _rand(1, 1, 6, 6, seed=14)
+    v = np.eye(6)[None, None]
+    o, _ = A.attn_fwd(q, k, v, score_mod="alibi")
+    np.testing.assert_allclose(o[0, 0], A.attn_probs(q, k, 0, 0, score_mod="alibi"), rtol=1e-14)
+
+
+def test_fully_masked_rows_are_zero():
+    q, k, v = _rand(2, 2, 4, 3, seed=15), _rand(2, 2, 5, 3, seed=16), _rand(2, 2, 5, 3, seed=17)
+    do = _rand(2, 2, 4, 3, seed=18)
+    km = np.ones((2, 5), np.uint8)
+    km[1] = 0                              # batch 1 has no key left
+    o, lse = A.attn_fwd(q, k, v, key_mask=km)
+    dq, dk, dv = A.attn_bwd(q, k, v, do, key_mask=km)
+    assert (o[1] == 0).all() and np.isneginf(lse[1]).all()
+    assert (dq[1] == 0).all() and (dk[1] == 0).all() and (dv[1] == 0).all()
+    assert np.isfinite(o[0]).all() and np.isfinite(lse[0]).all()
+    # padded keys receive no gradient
+    km2 = np.ones((2, 5), np.uint8)
+    km2[:, 2] = 0
+    dq, dk, dv = A.attn_bwd(q, k, v, do, key_mask=km2)
+    assert (dk[:, :, 2] == 0).all() and (dv[:, :, 2] == 0).all()
+
+
+@pytest.mark.parametrize("mod", MODS)
+def test_delta_identity_and_dk_sums_to_zero(mod):
+    """rowsum(dO o O) = rowsum(P o dP), and sum_j dK_j = 0 (each dS row sums to 0)."""
+    q, k, v = _rand(1, 2, 6, 4, seed=19), _rand(1, 2, 8, 4, seed=20), _rand(1, 2, 8, 4, seed=21)
+    do = _rand(1, 2, 6, 4, seed=22)
+    o, _ = A.attn_fwd(q, k, v, score_mod=mod)
+    for h in range(2):
+        p = A.attn_probs(q, k, 0, h, score_mod=mod)
+        dp = do[0, h] @ v[0, h].T
+        np.testing.assert_allclose((do[0, h] * o[0, h]).sum(1), (p * dp).sum(1), rtol=1e-12, atol=1e-14)
+    _, dk, _ = A.attn_bwd(q, k, v, do, score_mod=mod)
+    assert np.abs(dk.sum(axis=2)).max() < 1e-13
+
+
+def test_alibi_row_constant_only_shifts_lse():
+    """ALiBi's -slope*q_idx term is constant in a row: O depends only on slope*kv_idx.
+
+    Appending slope*kv_idx to the keys through an extra feature dimension
+    (q gets a 1, k gets slope*j/scale) must give ALiBi's O exactly, with
+    lse shifted by slope*q_idx.
+    """
+    H, Sq, Skv, D = 4, 5, 6, 3
+    q, k, v = _rand(1, H, Sq, D, seed=23), _rand(1, H, Skv, D, seed=24), _rand(1, H, Skv, D, seed=25)
+    scale = 0.5
+    o_ali, lse_ali = A.attn_fwd(q, k, v, score_mod="alibi", scale=scale)
+    q2 = np.concatenate([q, np.ones((1, H, Sq, 1))], axis=3)
+    k2 = np.concatenate([k, np.zeros((1, H, Skv, 1))], axis=3)
+    for h in range(H):
+        k2[0, h, :, D] = A.alibi_slope(h, H) * np.arange(Skv) / scale
+    o_lin, lse_lin = A.attn_fwd(q2, k2, v, scale=scale)
+    np.testing.assert_allclose(o_ali, o_lin, rtol=1e-12, atol=1e-14)
+    for h in range(H):
+        np.testing.assert_allclose(lse_ali[0, h], lse_lin[0, h] - A.alibi_slope(h, H) * np.arange(Sq),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_key_permutation_invariance():
+    q, k, v = _rand(2, 2, 5, 4, seed=26), _rand(2, 2, 7, 4, seed=27), _rand(2, 2, 7, 4, seed=28)
+    km = (np.random.default_rng(29).random((2, 7)) > 0.4).astype(np.uint8)
+    km[:, 3] = 1
+    perm = np.random.default_rng(30).permutation(7)
+    o1, l1 = A.attn_fwd(q, k, v, key_mask=km)
+    o2, l2 = A.attn_fwd(q, k[:, :, perm], v[:, :, perm], key_mask=km[:, perm])
+    np.testing.assert_allclose(o1, o2, rtol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=1e-12)
+
+
+def test_decode_is_forward_with_one_query():
+    q, k, v = _rand(2, 3, 1, 4, seed=31), _rand(2, 3, 9, 4, seed=32), _rand(2, 3, 9, 4, seed=33)
+    for mod in ("none", "checkerboard", "alibi"):
+        o1, l1 = A.attn_decode(q, k, v, score_mod=mod)
+        # a longer query block whose first row is the same query sees the same keys
+        q2 = np.concatenate([q, _rand(2, 3, 3, 4, seed=34)], axis=2)
+        o2, l2 = A.attn_fwd(q2, k, v, score_mod=mod)
+        np.testing.assert_allclose(o1[:, :, 0], o2[:, :, 0], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(l1[:, :, 0], l2[:, :, 0], rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# finite differences
+# ---------------------------------------------------------------------------
+
+def _loss(q, k, v, do, **kw):
+    o, _ = A.attn_fwd(q, k, v, **kw)
+    return float((o * do).sum())
+
+
+def _fd_grad(f, x, h=1e-6):
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        idx = it.multi_index
+        xp = x.copy(); xp[idx] += h
+        xm = x.copy(); xm[idx] -= h
+        g[idx] = (f(xp) - f(xm)) / (2 * h)
+    return g
+
+
+FD_CASES = [(S, D, mod, mask) for S, D in [(3, 2), (5, 4), (8, 2)] for mod in MODS
+            for mask in ("none", "key", "block")]
+
+
+@pytest.mark.parametrize("S,D,mod,mask", FD_CASES)
+def test_finite_differences(S, D, mod, mask):
+    H = 2
+    q, k, v = _rand(1, H, S, D, seed=40 + S), _rand(1, H, S, D, seed=50 + S), _rand(1, H, S, D, seed=60 + S)
+    do = _rand(1, H, S, D, seed=70 + S)
+    kw = {"score_mod": mod, "scale": 0.7}
+    if mask == "key":
+        km = np.ones((1, S), np.uint8)
+        km[0, 1::2] = 0
+        kw["key_mask"] = km
+    elif mask == "block":
+        kw["block_mask"] = A.BlockMask(A.build_block_mask("causal", 1, H, S, S, 2, 2), "causal", 2, 2)
+    dq, dk, dv = A.attn_bwd(q, k, v, do, **kw)
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        def f(xx, name=name):
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xx
+            return _loss(args["q"], args["k"], args["v"], do, **kw)
+        gfd = _fd_grad(f, x)
+        err = np.abs(gfd - g).max() / max(1e-12, np.abs(g).max())
+        assert err < 1e-6, (name, err)
+
+
+# ---------------------------------------------------------------------------
+# the online recurrence (attnax Pallas kernel body) against the plain definition
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mod", MODS)
+@pytest.mark.parametrize("mask", ["none", "key", "block", "key+block"])
+def test_online_recurrence_matches_plain(mod, mask):
+    B, H, Sq, Skv, D, bq, bk = 2, 2, 24, 32, 5, 8, 8
+    q, k, v = _rand(B, H, Sq, D, seed=80), _rand(B, H, Skv, D, seed=81), _rand(B, H, Skv, D, seed=82)
+    kw = {"score_mod": mod}
+    if "key" in mask:
+        km = (np.random.default_rng(83).random((B, Skv)) > 0.5).astype(np.uint8)
+        km[1, 8:16] = 0                   # one kv block of batch 1 fully padded
+        km[0, :] = 1
+        km[0, 0] = 0
+        kw["key_mask"] = km
+    if "block" in mask:
+        kw["block_mask"] = A.BlockMask(A.build_block_mask("causal", 1, 1, Sq, Skv, bq, bk), "causal", bq, bk)
+    o1, l1 = A.attn_fwd(q, k, v, **kw)
+    o2, l2 = A.attn_fwd_online(q, k, v, block_q=bq, block_kv=bk, **kw)
+    fin = np.isfinite(l1)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l2[fin], l1[fin], rtol=1e-12, atol=1e-12)
+    assert (np.isneginf(l2) == np.isneginf(l1)).all()
+
+
+# ---------------------------------------------------------------------------
+# block mask builder and the tile skip set
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Sq,Skv,bq,bk", [(2048, 2048, 128, 128), (512, 512, 128, 128),
+                                          (256, 384, 128, 128), (24, 32, 8, 8), (16, 16, 4, 8)])
+def test_causal_block_mask_closed_form(Sq, Skv, bq, bk):
+    tiles = A.build_block_mask("causal", 1, 1, Sq, Skv, bq, bk)[0, 0]
+    nqb, nkb = tiles.shape
+    for qb in range(nqb):
+        for kb in range(nkb):
+            q_lo, q_hi = qb * bq, min(Sq, (qb + 1) * bq) - 1
+            k_lo, k_hi = kb * bk, min(Skv, (kb + 1) * bk) - 1
+            expect = 2 if k_hi <= q_lo else (0 if k_lo > q_hi else 1)
+            assert tiles[qb, kb] == expect
+    if Sq == Skv and bq == bk:
+        n = nqb
+        assert (tiles != 0).sum() == n * (n + 1) // 2        # 136 for 16 x 16
+        assert (tiles == 2).sum() == n * (n - 1) // 2
+    assert (A.build_block_mask("none", 2, 3, Sq, Skv, bq, bk) == 2).all()
+
+
+def test_visited_tiles_skip_padded_blocks():
+    km = np.ones((2, 512), np.uint8)
+    km[1, 128:256] = 0
+    bm = A.BlockMask(A.build_block_mask("causal", 2, 2, 512, 512), "causal")
+    vis = A.visited_tiles(2, 2, 512, 512, key_mask=km, block_mask=bm)
+    assert vis[0, 0].sum() == 10 and vis[1, 0].sum() == 10 - 3
+    assert (vis[1, :, :, 1] == 0).all()
+
+
+def test_block_mask_full_tile_skips_mask_mod():
+    """A tile marked FULL is not filtered by the mask_mod (its state decides)."""
+    q, k, v = _rand(1, 1, 4, 2, seed=90), _rand(1, 1, 4, 2, seed=91), _rand(1, 1, 4, 2, seed=92)
+    tiles = np.full((1, 1, 1, 1), 2, np.uint8)
+    o_full, _ = A.attn_fwd(q, k, v, block_mask=A.BlockMask(tiles, "causal", 4, 4))
+    o_none, _ = A.attn_fwd(q, k, v)
+    np.testing.assert_array_equal(o_full, o_none)
+    tiles[:] = 1
+    o_part, _ = A.attn_fwd(q, k, v, block_mask=A.BlockMask(tiles, "causal", 4, 4))
+    o_caus, _ = A.attn_fwd(q, k, v, score_mod="causal")
+    np.testing.assert_array_equal(o_part, o_caus)
+    tiles[:] = 0
+    o_empty, l_empty = A.attn_fwd(q, k, v, block_mask=A.BlockMask(tiles, "causal", 4, 4))
+    assert (o_empty == 0).all() and np.isneginf(l_empty).all()
