@@ -1,0 +1,249 @@
+"""ctypes binding of ``libattn_gb300.so`` (the C ABI of include/attn.h).
+
+Argument marshalling only: torch supplies device memory and the current
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing or a tensor is not on a
+CUDA device, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb300.so")
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_SHAPE, ATTN_ERR_ALIGN = 0, 1, 2, 3
+ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 4, 5, 6, 7
+ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
+OP_FWD, OP_BWD, OP_DECODE = 0, 1, 2
+MODS = {"none": 0, "alibi": 1, "checkerboard": 2, "causal": 3}
+MASK_MODS = {"none": 0, "causal": 1}
+
+SYMBOLS = ("attn_workspace_size", "attn_build_block_mask", "attn_fwd", "attn_bwd", "attn_bwd_preprocess",
+           "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_poll_status", "attn_status_string")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("Sq", ctypes.c_int), ("Skv", ctypes.c_int),
+                ("D", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class BlockMaskC(ctypes.Structure):
+    _fields_ = [("tiles", ctypes.c_void_p), ("bcast_b", ctypes.c_int), ("bcast_h", ctypes.c_int),
+                ("block_q", ctypes.c_int), ("block_kv", ctypes.c_int), ("mask_mod", ctypes.c_int)]
+
+
+_lib = None
+_lock = threading.Lock()
+P = ctypes.c_void_p
+I = ctypes.c_int
+SZ = ctypes.c_size_t
+F = ctypes.c_float
+
+
+def load():
+    """Loads the shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m exact_attention_59_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        sp, bp = ctypes.POINTER(Shape), ctypes.POINTER(BlockMaskC)
+        sig = {
+            "attn_workspace_size": (SZ, [I, sp]),
+            "attn_build_block_mask": (I, [I, I, I, I, I, I, I, P, P]),
+            "attn_fwd": (I, [sp, P, P, P, P, bp, I, F, P, P, P, SZ, P, P]),
+            "attn_bwd": (I, [sp, P, P, P, P, P, P, P, bp, I, F, P, P, P, P, SZ, P]),
+            "attn_bwd_preprocess": (I, [sp, P, P, P, P, P, SZ, P]),
+            "attn_bwd_dkdv": (I, [sp, P, P, P, P, P, bp, I, F, P, P, P, SZ, P]),
+            "attn_bwd_dq": (I, [sp, P, P, P, P, P, bp, I, F, P, P, SZ, P]),
+            "attn_decode": (I, [sp, P, P, P, P, I, F, P, P, P, SZ, P]),
+            "attn_poll_status": (I, [P, P]),
+            "attn_status_string": (ctypes.c_char_p, [I]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().attn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _dtype_id(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return ATTN_F32
+    if t == torch.float16:
+        return ATTN_F16
+    if t == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("attention tensors must live on a CUDA device (no CPU path)")
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def make_shape(q, k) -> Shape:
+    B, H, Sq, D = q.shape
+    return Shape(B, H, Sq, k.shape[2], D, _dtype_id(q.dtype))
+
+
+def workspace_size(op: int, shape: Shape) -> int:
+    return int(load().attn_workspace_size(op, ctypes.byref(shape)))
+
+
+# One zero-initialised workspace per (device, stream, op), grown on demand.
+_ws_cache: dict = {}
+
+
+def workspace(op: int, shape: Shape, device) -> torch.Tensor:
+    n = workspace_size(op, shape)
+    if n == 0:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "workspace_size")
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream, op)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.zeros(max(n, 1 << 16), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+class BlockMask:
+    """Device tile states (B|1, H|1, Sq/128, Skv/128) uint8 plus the mask_mod of partial tiles."""
+
+    def __init__(self, tiles: torch.Tensor, mask_mod="causal", block_q=128, block_kv=128):
+        assert tiles.dtype == torch.uint8 and tiles.dim() == 4 and tiles.is_contiguous()
+        self.tiles = tiles
+        self.mask_mod = MASK_MODS[mask_mod] if isinstance(mask_mod, str) else int(mask_mod)
+        self.block_q, self.block_kv = block_q, block_kv
+
+    def c(self) -> BlockMaskC:
+        return BlockMaskC(self.tiles.data_ptr(), int(self.tiles.shape[0] == 1), int(self.tiles.shape[1] == 1),
+                          self.block_q, self.block_kv, self.mask_mod)
+
+
+def create_block_mask(mask_mod, B, H, Sq, Skv, device="cuda", block_q=128, block_kv=128) -> BlockMask:
+    """Tile states built on the device by attn_build_block_mask."""
+    mm = MASK_MODS[mask_mod] if isinstance(mask_mod, str) else int(mask_mod)
+    tiles = torch.empty((B, H, -(-Sq // block_q), -(-Skv // block_kv)), dtype=torch.uint8, device=device)
+    _check(load().attn_build_block_mask(mm, B, H, Sq, Skv, block_q, block_kv, _ptr(tiles), _stream(tiles.device)),
+           "attn_build_block_mask")
+    return BlockMask(tiles, mm, block_q, block_kv)
+
+
+def _mod(m) -> int:
+    return MODS[m] if isinstance(m, str) else int(m)
+
+
+def _bm(bm):
+    return None if bm is None else ctypes.byref(bm.c())
+
+
+def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_mod="none", scale=None,
+             out=None, lse=None, debug_visited=None, ws=None):
+    """(out, lse) of the forward pass on q's device and current stream."""
+    _cuda(q, k, v, key_mask, out, lse)
+    shape = make_shape(q, k)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(OP_FWD, shape, q.device) if ws is None else ws
+    code = load().attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _bm(block_mask),
+                           _mod(score_mod), scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device),
+                           _ptr(debug_visited))
+    _check(code, "attn_fwd")
+    return out, lse
+
+
+def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod="none", scale=None,
+             dq=None, dk=None, dv=None, ws=None):
+    """(dq, dk, dv) of sum(dout * out)."""
+    _cuda(q, k, v, out, lse, dout, key_mask)
+    shape = make_shape(q, k)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    code = load().attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                           _ptr(key_mask), _bm(block_mask), _mod(score_mod), scale, _ptr(dq), _ptr(dk), _ptr(dv),
+                           _ptr(ws), ws.numel(), _stream(q.device))
+    _check(code, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_preprocess(q, k, out, lse, dout, key_mask=None, ws=None):
+    shape = make_shape(q, k)
+    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    _check(load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(out), _ptr(lse), _ptr(dout), _ptr(key_mask),
+                                      _ptr(ws), ws.numel(), _stream(q.device)), "attn_bwd_preprocess")
+    return ws
+
+
+def attn_bwd_dkdv(q, k, v, dout, dk, dv, key_mask=None, block_mask=None, score_mod="none", scale=None, ws=None):
+    shape = make_shape(q, k)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    _check(load().attn_bwd_dkdv(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(key_mask),
+                                _bm(block_mask), _mod(score_mod), scale, _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+                                _stream(q.device)), "attn_bwd_dkdv")
+
+
+def attn_bwd_dq(q, k, v, dout, dq, key_mask=None, block_mask=None, score_mod="none", scale=None, ws=None):
+    shape = make_shape(q, k)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    _check(load().attn_bwd_dq(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(key_mask),
+                              _bm(block_mask), _mod(score_mod), scale, _ptr(dq), _ptr(ws), ws.numel(),
+                              _stream(q.device)), "attn_bwd_dq")
+
+
+def attn_decode(q, k, v, key_mask=None, score_mod="none", scale=None, out=None, lse=None, ws=None):
+    """(out, lse) for a single query per (b, h): q (B, H, 1, D)."""
+    _cuda(q, k, v, key_mask, out, lse)
+    shape = make_shape(q, k)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(OP_DECODE, shape, q.device) if ws is None else ws
+    code = load().attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _mod(score_mod),
+                              scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
+    _check(code, "attn_decode")
+    return out, lse
+
+
+def poll_status(ws: torch.Tensor) -> int:
+    """Synchronises the current stream and returns (and clears) the workspace status code."""
+    return int(load().attn_poll_status(_ptr(ws), _stream(ws.device)))

@@ -1,0 +1,461 @@
+// api.cu - the C ABI declared in include/attn.h: validation, workspace
+// layout, TMA descriptor encoding and kernel dispatch.  No allocation, no
+// synchronisation (except attn_poll_status), no state beyond two cached
+// process-wide values (the driver's tensor-map encoder and the wait limit).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+using namespace attn;
+
+namespace {
+
+constexpr long long kMaxRows = (1LL << 31) - 1;
+
+unsigned long long timeout_ns() {
+  static unsigned long long t = [] {
+    const char* e = std::getenv("ATTN_TIMEOUT_NS");
+    unsigned long long v = 2000000000ULL;
+    if (e && *e) {
+      char* end = nullptr;
+      const unsigned long long x = std::strtoull(e, &end, 10);
+      if (end && *end == '\0' && x > 0) v = x;
+    }
+    return v;
+  }();
+  return t;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view (rows, cols) of a row-major tensor, box {64 columns, 128 rows}, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, long long rows, int cols, attn_dtype dt) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType t = dt == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, t, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t esize(attn_dtype d) { return d == ATTN_F32 ? 4 : 2; }
+
+bool shape_ok(const attn_shape* s) {
+  return s && s->B > 0 && s->H > 0 && s->Sq > 0 && s->Skv > 0 && s->D > 0 &&
+         (s->dtype == ATTN_F32 || s->dtype == ATTN_F16 || s->dtype == ATTN_BF16) &&
+         (long long)s->B * s->H * s->Sq <= kMaxRows && (long long)s->B * s->H * s->Skv <= kMaxRows;
+}
+
+struct DecodeSplit {
+  int nsplit, kps;
+};
+DecodeSplit decode_split(const attn_shape* s) {
+  int ns = decode_num_splits(s->B, s->H, s->Skv);
+  const int kps = (s->Skv + ns - 1) / ns;
+  ns = (s->Skv + kps - 1) / kps;
+  return {ns, kps};
+}
+
+WsLayout layout(attn_op op, const attn_shape* s) {
+  WsLayout w;
+  size_t off = 256;
+  const size_t B = s->B, BH = (size_t)s->B * s->H;
+  w.km_bits = off;
+  off = align256(off + B * ((s->Skv + 31) / 32) * 4);
+  w.km_sum = off;
+  off = align256(off + B * ((s->Skv + 127) / 128));
+  if (op == ATTN_OP_BWD) {
+    w.delta = off;
+    off = align256(off + BH * s->Sq * 4);
+    w.lse2 = off;
+    off = align256(off + BH * s->Sq * 4);
+  }
+  if (op == ATTN_OP_DECODE) {
+    const DecodeSplit d = decode_split(s);
+    w.partial = off;
+    off = align256(off + BH * d.nsplit * (2 + 64) * 4);
+    w.counter = off;
+    off = align256(off + BH * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Checks shared by every prefill call.
+attn_status check_prefill(const attn_shape* s, bool backward) {
+  if (!shape_ok(s)) return ATTN_ERR_INVALID_ARG;
+  if (s->Sq % 128 != 0 || s->Skv % 128 != 0) return ATTN_ERR_SHAPE;
+  if (s->Skv / 128 > FWD_MAXKB || s->Sq / 128 > FWD_MAXKB) return ATTN_ERR_SHAPE;
+  if (s->D == 64) return ATTN_OK;
+  if (s->D == 512 && !backward && s->dtype != ATTN_F32) return ATTN_OK;
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status check_mod(attn_score_mod mod, float scale) {
+  if ((int)mod < 0 || (int)mod > 3) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status check_bm(const attn_block_mask* bm) {
+  if (!bm) return ATTN_OK;
+  if (!bm->tiles) return ATTN_ERR_INVALID_ARG;
+  if ((int)bm->mask_mod < 0 || (int)bm->mask_mod > 1) return ATTN_ERR_INVALID_ARG;
+  if (bm->block_q != 128 || bm->block_kv != 128) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status check_ws(attn_op op, const attn_shape* s, void* ws, size_t ws_bytes) {
+  if (!ws) return ATTN_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return ATTN_ERR_ALIGN;
+  if (ws_bytes < layout(op, s).total) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+void bm_strides(const attn_shape* s, const attn_block_mask* bm, long long& sb, long long& sh) {
+  const long long tile = (long long)(s->Sq / 128) * (s->Skv / 128);
+  sh = bm->bcast_h ? 0 : tile;
+  sb = bm->bcast_b ? 0 : (bm->bcast_h ? 1 : s->H) * tile;
+}
+
+#define ATTN_TRY(x)                   \
+  do {                                \
+    const attn_status _st = (x);      \
+    if (_st != ATTN_OK) return _st;   \
+  } while (0)
+
+#define ATTN_PTR(p)                                  \
+  do {                                               \
+    if (!(p)) return ATTN_ERR_INVALID_ARG;           \
+    if (!aligned((p), 16)) return ATTN_ERR_ALIGN;    \
+  } while (0)
+
+#define ATTN_OPT_PTR(p)                              \
+  do {                                               \
+    if ((p) && !aligned((p), 16)) return ATTN_ERR_ALIGN; \
+  } while (0)
+
+attn_status run_keymask(const attn_shape* s, const uint8_t* km, void* ws, cudaStream_t st) {
+  if (!km) return ATTN_OK;
+  const WsLayout w = layout(ATTN_OP_FWD, s);
+  return cuda_status(launch_keymask_pack(km, s->B, s->Skv, at<uint32_t>(ws, w.km_bits), at<uint8_t>(ws, w.km_sum), st));
+}
+
+BwdParams bwd_params(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                     const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale, void* ws,
+                     bool& ok) {
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long rq = (long long)s->B * s->H * s->Sq, rk = (long long)s->B * s->H * s->Skv;
+  ok = true;
+  if (s->dtype != ATTN_F32) {
+    ok = make_tmap(&p.tm_q, q, rq, s->D, s->dtype) && make_tmap(&p.tm_k, k, rk, s->D, s->dtype) &&
+         make_tmap(&p.tm_v, v, rk, s->D, s->dtype) && make_tmap(&p.tm_do, dout, rq, s->D, s->dtype);
+  }
+  const WsLayout wb = layout(ATTN_OP_BWD, s);
+  p.delta = at<float>(ws, wb.delta);
+  p.lse2 = at<float>(ws, wb.lse2);
+  p.km_bits = key_mask ? at<uint32_t>(ws, wb.km_bits) : nullptr;
+  p.km_sum = key_mask ? at<uint8_t>(ws, wb.km_sum) : nullptr;
+  p.bm_tiles = bm ? bm->tiles : nullptr;
+  if (bm) bm_strides(s, bm, p.bm_sb, p.bm_sh);
+  p.bm_mod = bm ? (int)bm->mask_mod : 0;
+  p.status = at<int>(ws, 0);
+  p.B = s->B;
+  p.H = s->H;
+  p.Sq = s->Sq;
+  p.Skv = s->Skv;
+  p.nqb = s->Sq / 128;
+  p.nkb = s->Skv / 128;
+  p.sc = scale * kLog2e;
+  p.scale = scale;
+  p.timeout_ns = timeout_ns();
+  return p;
+}
+
+SimtParams simt_params(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                       const attn_block_mask* bm, attn_score_mod mod, float scale) {
+  SimtParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = (const float*)q;
+  p.k = (const float*)k;
+  p.v = (const float*)v;
+  p.key_mask = key_mask;
+  p.bm_tiles = bm ? bm->tiles : nullptr;
+  if (bm) bm_strides(s, bm, p.bm_sb, p.bm_sh);
+  p.bm_mod = bm ? (int)bm->mask_mod : 0;
+  p.B = s->B;
+  p.H = s->H;
+  p.Sq = s->Sq;
+  p.Skv = s->Skv;
+  p.nqb = s->Sq / 128;
+  p.nkb = s->Skv / 128;
+  p.mod = (int)mod;
+  p.sc = scale * kLog2e;
+  p.scale = scale;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_workspace_size(attn_op op, const attn_shape* shape) {
+  if (!shape_ok(shape)) return 0;
+  if ((int)op < 0 || (int)op > 2) return 0;
+  return layout(op, shape).total;
+}
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_SHAPE: return "unsupported shape (prefill needs Sq, Skv multiples of 128; decode needs Sq == 1)";
+    case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case ATTN_ERR_UNSUPPORTED: return "dtype / head dim / mod / block size combination not built";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+attn_status attn_build_block_mask(attn_mask_mod mask_mod, int B, int H, int Sq, int Skv, int bq, int bkv,
+                                  uint8_t* tiles, attn_stream_t stream) {
+  if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0 || bq <= 0 || bkv <= 0 || !tiles) return ATTN_ERR_INVALID_ARG;
+  if ((int)mask_mod < 0 || (int)mask_mod > 1) return ATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_build_block_mask((int)mask_mod, B, H, Sq, Skv, bq, bkv, tiles, (cudaStream_t)stream));
+}
+
+attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                     const attn_block_mask* bm, attn_score_mod mod, float scale, void* out, float* lse, void* ws,
+                     size_t ws_bytes, attn_stream_t stream, uint8_t* debug_visited) {
+  ATTN_TRY(check_prefill(s, false));
+  ATTN_TRY(check_mod(mod, scale));
+  ATTN_TRY(check_bm(bm));
+  ATTN_PTR(q);
+  ATTN_PTR(k);
+  ATTN_PTR(v);
+  ATTN_PTR(out);
+  ATTN_PTR(lse);
+  ATTN_OPT_PTR(key_mask);
+  ATTN_TRY(check_ws(ATTN_OP_FWD, s, ws, ws_bytes));
+  if (s->D == 512) {
+    if (key_mask) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_ERR_UNSUPPORTED;   // the D = 512 kernel is dispatched below once built
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout w = layout(ATTN_OP_FWD, s);
+  if (s->dtype == ATTN_F32) {
+    SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
+    p.o = (float*)out;
+    p.lse = lse;
+    p.visited = debug_visited;
+    return cuda_status(launch_simt_fwd(p, st));
+  }
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long rq = (long long)s->B * s->H * s->Sq, rk = (long long)s->B * s->H * s->Skv;
+  if (!make_tmap(&p.tm_q, q, rq, 64, s->dtype) || !make_tmap(&p.tm_k, k, rk, 64, s->dtype) ||
+      !make_tmap(&p.tm_v, v, rk, 64, s->dtype))
+    return ATTN_ERR_CUDA;
+  ATTN_TRY(run_keymask(s, key_mask, ws, st));
+  p.out = out;
+  p.lse = lse;
+  p.km_bits = key_mask ? at<uint32_t>(ws, w.km_bits) : nullptr;
+  p.km_sum = key_mask ? at<uint8_t>(ws, w.km_sum) : nullptr;
+  p.bm_tiles = bm ? bm->tiles : nullptr;
+  if (bm) bm_strides(s, bm, p.bm_sb, p.bm_sh);
+  p.bm_mod = bm ? (int)bm->mask_mod : 0;
+  p.visited = debug_visited;
+  p.status = at<int>(ws, 0);
+  p.B = s->B;
+  p.H = s->H;
+  p.Sq = s->Sq;
+  p.Skv = s->Skv;
+  p.nqb = s->Sq / 128;
+  p.nkb = s->Skv / 128;
+  p.npairs = (p.nqb + 1) / 2;
+  p.sc = scale * kLog2e;
+  p.timeout_ns = timeout_ns();
+  return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
+}
+
+attn_status attn_bwd_preprocess(const attn_shape* s, const void* out, const float* lse, const void* dout,
+                                const uint8_t* key_mask, void* ws, size_t ws_bytes, attn_stream_t stream) {
+  ATTN_TRY(check_prefill(s, true));
+  ATTN_PTR(out);
+  ATTN_PTR(lse);
+  ATTN_PTR(dout);
+  ATTN_OPT_PTR(key_mask);
+  ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout w = layout(ATTN_OP_BWD, s);
+  ATTN_TRY(run_keymask(s, key_mask, ws, st));
+  return cuda_status(launch_bwd_preprocess(out, dout, lse, (int)s->dtype, (long long)s->B * s->H * s->Sq, s->D,
+                                           at<float>(ws, w.delta), at<float>(ws, w.lse2), st));
+}
+
+attn_status attn_bwd_dkdv(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                          const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale,
+                          void* dk, void* dv, void* ws, size_t ws_bytes, attn_stream_t stream) {
+  ATTN_TRY(check_prefill(s, true));
+  ATTN_TRY(check_mod(mod, scale));
+  ATTN_TRY(check_bm(bm));
+  ATTN_PTR(q);
+  ATTN_PTR(k);
+  ATTN_PTR(v);
+  ATTN_PTR(dout);
+  ATTN_PTR(dk);
+  ATTN_PTR(dv);
+  ATTN_OPT_PTR(key_mask);
+  ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (s->dtype == ATTN_F32) {
+    SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
+    const WsLayout w = layout(ATTN_OP_BWD, s);
+    p.dout = (const float*)dout;
+    p.dk = (float*)dk;
+    p.dv = (float*)dv;
+    p.delta = at<float>(ws, w.delta);
+    p.lse2 = at<float>(ws, w.lse2);
+    return cuda_status(launch_simt_bwd_dkdv(p, st));
+  }
+  bool ok;
+  BwdParams p = bwd_params(s, q, k, v, dout, key_mask, bm, mod, scale, ws, ok);
+  if (!ok) return ATTN_ERR_CUDA;
+  p.dk = dk;
+  p.dv = dv;
+  return cuda_status(launch_bwd_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
+}
+
+attn_status attn_bwd_dq(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                        const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq,
+                        void* ws, size_t ws_bytes, attn_stream_t stream) {
+  ATTN_TRY(check_prefill(s, true));
+  ATTN_TRY(check_mod(mod, scale));
+  ATTN_TRY(check_bm(bm));
+  ATTN_PTR(q);
+  ATTN_PTR(k);
+  ATTN_PTR(v);
+  ATTN_PTR(dout);
+  ATTN_PTR(dq);
+  ATTN_OPT_PTR(key_mask);
+  ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (s->dtype == ATTN_F32) {
+    SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
+    const WsLayout w = layout(ATTN_OP_BWD, s);
+    p.dout = (const float*)dout;
+    p.dq = (float*)dq;
+    p.delta = at<float>(ws, w.delta);
+    p.lse2 = at<float>(ws, w.lse2);
+    return cuda_status(launch_simt_bwd_dq(p, st));
+  }
+  bool ok;
+  BwdParams p = bwd_params(s, q, k, v, dout, key_mask, bm, mod, scale, ws, ok);
+  if (!ok) return ATTN_ERR_CUDA;
+  p.dq = dq;
+  return cuda_status(launch_bwd_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
+}
+
+attn_status attn_bwd(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, const uint8_t* key_mask, const attn_block_mask* bm,
+                     attn_score_mod mod, float scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     attn_stream_t stream) {
+  // validate everything before the first launch
+  ATTN_TRY(check_prefill(s, true));
+  ATTN_TRY(check_mod(mod, scale));
+  ATTN_TRY(check_bm(bm));
+  ATTN_PTR(q);
+  ATTN_PTR(k);
+  ATTN_PTR(v);
+  ATTN_PTR(out);
+  ATTN_PTR(lse);
+  ATTN_PTR(dout);
+  ATTN_PTR(dq);
+  ATTN_PTR(dk);
+  ATTN_PTR(dv);
+  ATTN_OPT_PTR(key_mask);
+  ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
+  ATTN_TRY(attn_bwd_preprocess(s, out, lse, dout, key_mask, ws, ws_bytes, stream));
+  ATTN_TRY(attn_bwd_dkdv(s, q, k, v, dout, key_mask, bm, mod, scale, dk, dv, ws, ws_bytes, stream));
+  return attn_bwd_dq(s, q, k, v, dout, key_mask, bm, mod, scale, dq, ws, ws_bytes, stream);
+}
+
+attn_status attn_decode(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                        attn_score_mod mod, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                        attn_stream_t stream) {
+  if (!shape_ok(s)) return ATTN_ERR_INVALID_ARG;
+  if (s->Sq != 1) return ATTN_ERR_SHAPE;
+  if (s->D != 64 || s->dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+  ATTN_TRY(check_mod(mod, scale));
+  ATTN_PTR(q);
+  ATTN_PTR(k);
+  ATTN_PTR(v);
+  ATTN_PTR(out);
+  ATTN_PTR(lse);
+  if (key_mask && !aligned(key_mask, 16)) return ATTN_ERR_ALIGN;
+  ATTN_TRY(check_ws(ATTN_OP_DECODE, s, ws, ws_bytes));
+  const WsLayout w = layout(ATTN_OP_DECODE, s);
+  const DecodeSplit d = decode_split(s);
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.key_mask = key_mask;
+  p.partial = at<float>(ws, w.partial);
+  p.counter = at<unsigned>(ws, w.counter);
+  p.B = s->B;
+  p.H = s->H;
+  p.Skv = s->Skv;
+  p.nsplit = d.nsplit;
+  p.keys_per_split = d.kps;
+  p.sc = scale * kLog2e;
+  p.mod = (int)mod;
+  return cuda_status(launch_decode(p, s->dtype == ATTN_BF16, (cudaStream_t)stream));
+}
+
+attn_status attn_poll_status(void* ws, attn_stream_t stream) {
+  if (!ws) return ATTN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word == 0) return ATTN_OK;
+  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return (word & 0xFF) == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,576 @@
+// bwd_d64.cu - backward passes, head dim 64, f16/bf16, tcgen05 + TMA.
+//
+// Gradients of sum(dO * O) (the flaxattention README differentiates
+// sum(attention(...)) with jax.grad; the attnax page traces jvp through its
+// forward).  Here the backward is written out, recomputing P from the saved
+// lse instead of storing it (FlashAttention-2 style):
+//   P = 2^(S scale log2e + bias log2e - lse log2e),  dV = P^T dO,
+//   dP = dO V^T,  dS = P o (dP - D),  D_i = rowsum(dO o O),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+// Two passes, no atomics (bitwise reproducible):
+//   dK/dV pass: one CTA per (b, h, kv block j); computes S^T = K_j Q_i^T and
+//     dP^T = V_j dO_i^T directly (kv rows on TMEM lanes), so P^T and dS^T are
+//     left in TMEM and feed dV += P^T dO_i and dK += dS^T Q_i as the A operand.
+//   dQ pass: one CTA per (b, h, q block i); S = Q_i K_j^T, dP = dO_i V_j^T,
+//     dS into TMEM, dQ += dS K_j.
+// Both: warp 0 TMA, warp 1 TMEM owner + MMA issue (lane 0), warps 2-5 and
+// 6-9 split the 128 columns of each 128x128 score tile in two halves of 64.
+// S is double-buffered in TMEM so the next S product overlaps this tile's
+// elementwise work.
+#include "kernels.h"
+
+namespace attn {
+
+constexpr int BWD_NST = 3;
+constexpr int BWD_T = 320;
+constexpr uint32_t BWD_TILE = 128 * 64 * 2;
+constexpr int BWD_MAXB = 2048;
+
+DEVI void drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion on an mbarrier (16-byte aligned, size % 16 == 0)
+DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Logit in log2 units of one score, -inf where masked.  q, kv: global indices.
+template <int MOD>
+DEVI float logit2(float s, float sc, float slope2, int q, int kv, bool causal) {
+  float x;
+  if constexpr (MOD == MOD_ALIBI)
+    x = fmaf(s, sc, slope2 * float(kv - q));
+  else if constexpr (MOD == MOD_CHECKER)
+    x = fmaf(s, sc, ((q + kv) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e);
+  else
+    x = s * sc;
+  if (causal && kv > q) x = -INFINITY;
+  return x;
+}
+
+// A operand of a K = 128 product whose 16-bit values sit in TMEM columns
+// [base, base+32) (k = 0..63) and [base+64, base+96) (k = 64..127).
+DEVI uint32_t split_a_col(uint32_t base, int kk) { return base + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); }
+
+// ============================================================================
+// dK / dV pass
+// ============================================================================
+struct __align__(1024) DkdvSmem {
+  uint8_t k[BWD_TILE], v[BWD_TILE];
+  uint8_t q[BWD_NST][BWD_TILE], dO[BWD_NST][BWD_TILE];
+  float lse2[BWD_NST][128], delta[BWD_NST][128];
+  uint64_t kvfull, full[BWD_NST], empty[BWD_NST], sfull[2], dpfull, pready, dsready, done;
+  uint32_t tmem_base;
+  int abort;
+  int nlist;
+  uint16_t list[BWD_MAXB];   // visited q blocks, in order
+  uint8_t lflags[BWD_MAXB];
+};
+
+template <bool BF16, int MOD>
+__global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.H;
+  const int kb = blockIdx.x / BH;   // causal: low kv blocks see the most q blocks, so they go first
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.H, h = bh % p.H;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sm.kvfull), 1);
+    for (int s = 0; s < BWD_NST; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm.sfull[0]), 1);
+    mbar_init(smem_u32(&sm.sfull[1]), 1);
+    mbar_init(smem_u32(&sm.dpfull), 1);
+    mbar_init(smem_u32(&sm.pready), 256);
+    mbar_init(smem_u32(&sm.dsready), 256);
+    mbar_init(smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    // list of q blocks that see this kv block
+    const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
+    int n = 0;
+    if (ks != 0) {
+      for (int qb = 0; qb < p.nqb; ++qb) {
+        const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
+        if (st == TILE_EMPTY) continue;
+        sm.list[n] = (uint16_t)qb;
+        sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0);
+        ++n;
+      }
+    }
+    sm.nlist = n;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int N = sm.nlist;
+  constexpr uint32_t C_SB = 0, C_DP = 256, C_DV = 384, C_DK = 448;
+
+  if (warp == 0) {
+    if (lane == 0 && N > 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 11};
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      const uint32_t kvb = smem_u32(&sm.kvfull);
+      mbar_expect_tx(kvb, 2 * BWD_TILE);
+      tma_load_2d(smem_u32(sm.k), &p.tm_k, kvb, 0, bh * p.Skv + kb * 128);
+      tma_load_2d(smem_u32(sm.v), &p.tm_v, kvb, 0, bh * p.Skv + kb * 128);
+      int last_u[BWD_NST] = {-1, -1, -1};
+      for (int u = 0; u < N; ++u) {
+        const int s = u % BWD_NST;
+        if (u >= BWD_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
+        const int qb = sm.list[u];
+        const uint32_t fb = smem_u32(&sm.full[s]);
+        mbar_expect_tx(fb, 2 * BWD_TILE + 2 * 512);
+        const int row = bh * p.Sq + qb * 128;
+        tma_load_2d(smem_u32(sm.q[s]), &p.tm_q, fb, 0, row);
+        tma_load_2d(smem_u32(sm.dO[s]), &p.tm_do, fb, 0, row);
+        bulk_load(smem_u32(sm.lse2[s]), p.lse2 + row, 512, fb);
+        bulk_load(smem_u32(sm.delta[s]), p.delta + row, 512, fb);
+        last_u[s] = u;
+      }
+      if (sm.abort) {
+        drain(kvb, 0, p.timeout_ns);
+        for (int s = 0; s < BWD_NST; ++s)
+          if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && N > 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 12};
+      constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
+      const uint32_t kA = smem_u32(sm.k), vA = smem_u32(sm.v);
+      auto issue_s = [&](int u) {   // S^T_u = K Q_u^T into buffer u & 1
+        const int s = u % BWD_NST;
+        const uint32_t d = tmem + C_SB + 128 * (u & 1);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(d, sdesc_sw128(kA + 32 * kk, 16, 1024), sdesc_sw128(smem_u32(sm.q[s]) + 32 * kk, 16, 1024), ID_SS,
+                 kk > 0);
+        tc_commit(smem_u32(&sm.sfull[u & 1]));
+      };
+      auto issue_dp = [&](int u) {  // dP^T_u = V dO_u^T
+        const int s = u % BWD_NST;
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem + C_DP, sdesc_sw128(vA + 32 * kk, 16, 1024), sdesc_sw128(smem_u32(sm.dO[s]) + 32 * kk, 16, 1024),
+                 ID_SS, kk > 0);
+        tc_commit(smem_u32(&sm.dpfull));
+      };
+      bool ok = wait_one(smem_u32(&sm.kvfull), 0, c) && wait_one(smem_u32(&sm.full[0]), 0, c);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int u = 0; ok && u < N; ++u) {
+        const int s = u % BWD_NST;
+        if (u + 1 < N) {
+          if (!wait_one(smem_u32(&sm.full[(u + 1) % BWD_NST]), ((u + 1) / BWD_NST) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(u + 1);
+        }
+        if (!wait_one(smem_u32(&sm.pready), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        {   // dV += P^T dO_u
+          const uint32_t a = tmem + C_SB + 128 * (u & 1);
+          const uint32_t bb = smem_u32(sm.dO[s]);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C_DV, split_a_col(a, kk), sdesc_sw128(bb + 2048 * kk, 8192, 1024), ID_TS, (u > 0 || kk > 0));
+        }
+        if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        {   // dK += dS^T Q_u
+          const uint32_t a = tmem + C_DP;
+          const uint32_t bb = smem_u32(sm.q[s]);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C_DK, split_a_col(a, kk), sdesc_sw128(bb + 2048 * kk, 8192, 1024), ID_TS, (u > 0 || kk > 0));
+        }
+        tc_commit(smem_u32(&sm.empty[s]));
+        if (u + 1 < N) issue_dp(u + 1);
+      }
+      tc_commit(smem_u32(&sm.done));
+      drain(smem_u32(&sm.done), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    const int w = (warp - 2) >> 2;   // column half: q columns [64 w, 64 w + 64)
+    const int quad = warp & 3;
+    const int r = 32 * quad + lane;  // kv row in the block
+    const int kv = kb * 128 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 13 + w};
+    const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+    bool my_key = true;
+    if (p.km_bits) my_key = (__ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + (kv >> 5)) >> (kv & 31)) & 1u;
+    bool ok = true;
+    for (int u = 0; u < N; ++u) {
+      const int s = u % BWD_NST;
+      const int qb = sm.list[u];
+      const uint8_t f = sm.lflags[u];
+      const bool causal = (MOD == MOD_CAUSAL) || ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+      const bool dead = (f & KB_KEYMASK) && !my_key;
+      if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
+      float pr[64];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t rr[32];
+        tmem_ld32(tS + 32 * j, rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int cidx = 64 * w + 32 * j + i;
+          const int q = qb * 128 + cidx;
+          const float x = logit2<MOD>(__uint_as_float(rr[i]), p.sc, slope2, q, kv, causal);
+          pr[32 * j + i] = dead ? 0.f : ex2(x - sm.lse2[s][cidx]);
+        }
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pr[2 * i], pr[2 * i + 1]);
+        tmem_st32(tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.pready));
+      if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tP = tmem + lane_off + C_DP + 64 * w;
+      uint32_t dsk[32];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t rr[32];
+        tmem_ld32(tP + 32 * j, rr);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = 32 * j + 2 * i;
+          const float d0 = pr[c0] * (__uint_as_float(rr[2 * i]) - sm.delta[s][64 * w + c0]);
+          const float d1 = pr[c0 + 1] * (__uint_as_float(rr[2 * i + 1]) - sm.delta[s][64 * w + c0 + 1]);
+          dsk[16 * j + i] = pack2<BF16>(d0, d1);
+        }
+      }
+      tmem_st32(tP, dsk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.dsready));
+    }
+    tmem_st_wait();
+    // epilogue: warps 2-5 write dV rows, warps 6-9 write dK rows (scaled)
+    if (ok && N > 0) {
+      if (!wait_warp(smem_u32(&sm.done), 0, c)) ok = false;
+      else tc_fence_after();
+    }
+    if (ok) {
+      const float mul = w == 0 ? 1.f : p.scale;
+      uint32_t o[32];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t rr[32];
+        if (N > 0) {
+          tmem_ld32(tmem + lane_off + (w == 0 ? C_DV : C_DK) + 32 * j, rr);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[16 * j + i] = pack2<BF16>(__uint_as_float(rr[2 * i]) * mul, __uint_as_float(rr[2 * i + 1]) * mul);
+      }
+      uint16_t* base = reinterpret_cast<uint16_t*>(w == 0 ? p.dv : p.dk);
+      uint4* dst = reinterpret_cast<uint4*>(base + ((size_t)bh * p.Skv + kv) * 64);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================
+// dQ pass
+// ============================================================================
+struct __align__(1024) DqSmem {
+  uint8_t q[BWD_TILE], dO[BWD_TILE];
+  uint8_t k[BWD_NST][BWD_TILE], v[BWD_NST][BWD_TILE];
+  uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull[2], dpfull, dsready, done;
+  uint32_t tmem_base;
+  int abort;
+  int nlist;
+  uint16_t list[BWD_MAXB];
+  uint8_t lflags[BWD_MAXB];
+};
+
+template <bool BF16, int MOD>
+__global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.H;
+  const int L = blockIdx.x;
+  const int qb = p.nqb - 1 - L / BH;   // longest causal rows first
+  const int bh = L % BH;
+  const int b = bh / p.H, h = bh % p.H;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sm.qfull), 1);
+    for (int s = 0; s < BWD_NST; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm.sfull[0]), 1);
+    mbar_init(smem_u32(&sm.sfull[1]), 1);
+    mbar_init(smem_u32(&sm.dpfull), 1);
+    mbar_init(smem_u32(&sm.dsready), 256);
+    mbar_init(smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    int n = 0;
+    for (int kb = 0; kb < p.nkb; ++kb) {
+      const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
+      if (ks == 0) continue;
+      const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
+      if (st == TILE_EMPTY) continue;
+      sm.list[n] = (uint16_t)kb;
+      sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0);
+      ++n;
+    }
+    sm.nlist = n;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int N = sm.nlist;
+  constexpr uint32_t C_SB = 0, C_DP = 256, C_DQ = 384;
+
+  if (warp == 0) {
+    if (lane == 0 && N > 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 21};
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      const uint32_t qbar = smem_u32(&sm.qfull);
+      mbar_expect_tx(qbar, 2 * BWD_TILE);
+      tma_load_2d(smem_u32(sm.q), &p.tm_q, qbar, 0, bh * p.Sq + qb * 128);
+      tma_load_2d(smem_u32(sm.dO), &p.tm_do, qbar, 0, bh * p.Sq + qb * 128);
+      int last_u[BWD_NST] = {-1, -1, -1};
+      for (int u = 0; u < N; ++u) {
+        const int s = u % BWD_NST;
+        if (u >= BWD_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
+        const int kb = sm.list[u];
+        const uint32_t fb = smem_u32(&sm.full[s]);
+        mbar_expect_tx(fb, 2 * BWD_TILE);
+        tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
+        tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
+        last_u[s] = u;
+      }
+      if (sm.abort) {
+        drain(qbar, 0, p.timeout_ns);
+        for (int s = 0; s < BWD_NST; ++s)
+          if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && N > 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 22};
+      constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
+      const uint32_t qA = smem_u32(sm.q), dA = smem_u32(sm.dO);
+      auto issue_s = [&](int u) {   // S_u = Q K_u^T into buffer u & 1
+        const uint32_t kB = smem_u32(sm.k[u % BWD_NST]);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem + C_SB + 128 * (u & 1), sdesc_sw128(qA + 32 * kk, 16, 1024), sdesc_sw128(kB + 32 * kk, 16, 1024),
+                 ID_SS, kk > 0);
+        tc_commit(smem_u32(&sm.sfull[u & 1]));
+      };
+      auto issue_dp = [&](int u) {  // dP_u = dO V_u^T
+        const uint32_t vB = smem_u32(sm.v[u % BWD_NST]);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem + C_DP, sdesc_sw128(dA + 32 * kk, 16, 1024), sdesc_sw128(vB + 32 * kk, 16, 1024), ID_SS, kk > 0);
+        tc_commit(smem_u32(&sm.dpfull));
+      };
+      bool ok = wait_one(smem_u32(&sm.qfull), 0, c) && wait_one(smem_u32(&sm.full[0]), 0, c);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int u = 0; ok && u < N; ++u) {
+        const int s = u % BWD_NST;
+        if (u + 1 < N) {
+          if (!wait_one(smem_u32(&sm.full[(u + 1) % BWD_NST]), ((u + 1) / BWD_NST) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(u + 1);
+        }
+        if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        {   // dQ += dS_u K_u
+          const uint32_t a = tmem + C_SB + 128 * (u & 1);
+          const uint32_t kB = smem_u32(sm.k[s]);
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C_DQ, split_a_col(a, kk), sdesc_sw128(kB + 2048 * kk, 8192, 1024), ID_TS, (u > 0 || kk > 0));
+        }
+        tc_commit(smem_u32(&sm.empty[s]));
+        if (u + 1 < N) issue_dp(u + 1);
+      }
+      tc_commit(smem_u32(&sm.done));
+      drain(smem_u32(&sm.done), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    const int w = (warp - 2) >> 2;   // kv columns [64 w, 64 w + 64)
+    const int quad = warp & 3;
+    const int r = 32 * quad + lane;
+    const int q = qb * 128 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 23 + w};
+    const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+    const float l2 = p.lse2[(size_t)bh * p.Sq + q];
+    const float dl = p.delta[(size_t)bh * p.Sq + q];
+    bool ok = true;
+    for (int u = 0; u < N; ++u) {
+      const int kb = sm.list[u];
+      const uint8_t f = sm.lflags[u];
+      const bool causal = (MOD == MOD_CAUSAL) || ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+      uint32_t kw[2] = {0xffffffffu, 0xffffffffu};
+      if (f & KB_KEYMASK) {
+        const uint32_t* wp = p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 64 * w) >> 5);
+        kw[0] = __ldg(wp);
+        kw[1] = __ldg(wp + 1);
+      }
+      if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
+      float pr[64];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t rr[32];
+        tmem_ld32(tS + 32 * j, rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int kv = kb * 128 + 64 * w + 32 * j + i;
+          float x = logit2<MOD>(__uint_as_float(rr[i]), p.sc, slope2, q, kv, causal);
+          if (!((kw[j] >> i) & 1u)) x = -INFINITY;
+          pr[32 * j + i] = ex2(x - l2);
+        }
+      }
+      if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tP = tmem + lane_off + C_DP + 64 * w;
+      uint32_t dsk[32];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t rr[32];
+        tmem_ld32(tP + 32 * j, rr);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = 32 * j + 2 * i;
+          dsk[16 * j + i] = pack2<BF16>(pr[c0] * (__uint_as_float(rr[2 * i]) - dl),
+                                        pr[c0 + 1] * (__uint_as_float(rr[2 * i + 1]) - dl));
+        }
+      }
+      tmem_st32(tS, dsk);   // dS over this half's S columns [64 w, 64 w + 32)
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.dsready));
+    }
+    tmem_st_wait();
+    if (w == 0) {
+      if (ok && N > 0) {
+        if (!wait_warp(smem_u32(&sm.done), 0, c)) ok = false;
+        else tc_fence_after();
+      }
+      if (ok) {
+        uint32_t o[32];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t rr[32];
+          if (N > 0) {
+            tmem_ld32(tmem + lane_off + C_DQ + 32 * j, rr);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            o[16 * j + i] =
+                pack2<BF16>(__uint_as_float(rr[2 * i]) * p.scale, __uint_as_float(rr[2 * i + 1]) * p.scale);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dq) + ((size_t)bh * p.Sq + q) * 64);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+template <typename Smem, bool BF16, int MOD, bool DKDV>
+static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
+  auto kern = DKDV ? bwd_dkdv_kernel<BF16, MOD> : bwd_dq_kernel<BF16, MOD>;
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(p.B * p.H * (DKDV ? p.nkb : p.nqb));
+  kern<<<grid, BWD_T, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename Smem, bool DKDV>
+static cudaError_t launch_bwd_any(const BwdParams& p, bool bf16, int mod, cudaStream_t st) {
+  if (bf16) {
+    switch (mod) {
+      case MOD_NONE: return launch_bwd_t<Smem, true, MOD_NONE, DKDV>(p, st);
+      case MOD_ALIBI: return launch_bwd_t<Smem, true, MOD_ALIBI, DKDV>(p, st);
+      case MOD_CHECKER: return launch_bwd_t<Smem, true, MOD_CHECKER, DKDV>(p, st);
+      default: return launch_bwd_t<Smem, true, MOD_CAUSAL, DKDV>(p, st);
+    }
+  }
+  switch (mod) {
+    case MOD_NONE: return launch_bwd_t<Smem, false, MOD_NONE, DKDV>(p, st);
+    case MOD_ALIBI: return launch_bwd_t<Smem, false, MOD_ALIBI, DKDV>(p, st);
+    case MOD_CHECKER: return launch_bwd_t<Smem, false, MOD_CHECKER, DKDV>(p, st);
+    default: return launch_bwd_t<Smem, false, MOD_CAUSAL, DKDV>(p, st);
+  }
+}
+
+cudaError_t launch_bwd_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t st) {
+  return launch_bwd_any<DkdvSmem, true>(p, bf16, mod, st);
+}
+cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, int mod, cudaStream_t st) {
+  return launch_bwd_any<DqSmem, false>(p, bf16, mod, st);
+}
+
+}  // namespace attn

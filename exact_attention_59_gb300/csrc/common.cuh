@@ -1,0 +1,42 @@
+// common.cuh - definitions shared by the attention kernels and their launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// score_mod ids (same values as attn_score_mod in attn.h)
+constexpr int MOD_NONE = 0, MOD_ALIBI = 1, MOD_CHECKER = 2, MOD_CAUSAL = 3;
+constexpr int MASKMOD_NONE = 0, MASKMOD_CAUSAL = 1;
+constexpr int TILE_EMPTY = 0, TILE_PARTIAL = 1, TILE_FULL = 2;
+
+// Per-(q tile, kv block) work flags staged in shared memory by the prefill kernels.
+constexpr uint8_t KB_VISIT = 1;    // the tile is computed
+constexpr uint8_t KB_MASKMOD = 2;  // partial tile: evaluate the mask_mod per entry
+constexpr uint8_t KB_KEYMASK = 4;  // some keys of the kv block are padding: test the key bits
+
+// Workspace layout (offsets in bytes; every region 256-byte aligned).
+//   [0, 256)            status word (int32 at offset 0) + reserved
+//   key-mask bits       uint32 (B, Skv/32)         if a key mask may be given
+//   key-mask summary    uint8  (B, ceil(Skv/128))  0 = no key kept, 1 = some, 2 = all
+//   bwd: delta          float  (B, H, Sq)          D_i = rowsum(dO * O)
+//   bwd: lse2           float  (B, H, Sq)          lse * log2(e), +inf for empty rows
+//   decode: partials    float  (B*H, nsplit, D + 2)
+//   decode: counters    uint32 (B*H)
+struct WsLayout {
+  size_t status = 0, km_bits = 0, km_sum = 0, delta = 0, lse2 = 0, partial = 0, counter = 0, total = 0;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ALiBi slope of head h (0-based) out of H, times log2(e): 2^(-8 (h+1) / H) * log2(e).
+DEVI float alibi_slope_log2(int h, int H) { return exp2f(-8.0f * float(h + 1) / float(H)) * kLog2e; }
+
+}  // namespace attn

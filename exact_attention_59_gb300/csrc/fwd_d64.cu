@@ -1,0 +1,359 @@
+// fwd_d64.cu - prefill forward, head dim 64, f16/bf16, tcgen05 + TMA.
+//
+// The online-softmax forward of the attnax Pallas kernel body (per kv block:
+// scores = q k^T scale, score_mod, mask, m_new = max(m, rowmax),
+// alpha = exp(m - m_new), p = exp(s - m_new), l = l alpha + sum p,
+// acc = acc alpha + p v; finally o = acc / l), in base 2 as the flaxattention
+// README's "log2 trick": the scale and the mods' biases carry a log2(e) factor
+// and every exp is one MUFU ex2.
+//
+// One CTA owns two 128-row query tiles of one (b, h) and streams the union of
+// their kv-block lists once:
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles of each kv
+//               block into a 3-stage ring (128B swizzle, 16 KB per tile).
+//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//               S_t = Q_t K^T (128x128, f32 in TMEM), then O_t += P_t V with P_t
+//               read from TMEM (written there by the softmax warps over S_t).
+//   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one thread per
+//               query row (TMEM lane), 128 scores per kv block in registers,
+//               running max/sum per thread, P packed to 16-bit into TMEM,
+//               O rescaled in TMEM when the row max grows, then the epilogue.
+// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384).
+// While tile 0's softmax runs, the tensor core computes tile 1's S (ping-pong).
+#include "kernels.h"
+
+namespace attn {
+
+struct __align__(1024) FwdSmem {
+  uint8_t q[2][FWD_TILE_BYTES];
+  uint8_t k[FWD_NST][FWD_TILE_BYTES];
+  uint8_t v[FWD_NST][FWD_TILE_BYTES];
+  uint64_t full[FWD_NST], empty[FWD_NST];
+  uint64_t qfull, sfull[2], pready[2], odone[2], fin;
+  uint32_t tmem_base;
+  int abort;
+  uint8_t flags[2][FWD_MAXKB];
+};
+
+// Waits without honouring the abort flag: used on the way out to drain work in flight.
+DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+template <bool BF16, int MOD>
+__global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = p.B * p.H;
+  const int L = blockIdx.x;
+  const int pair = p.npairs - 1 - L / BH;   // longest causal pairs first
+  const int bh = L % BH;
+  const int b = bh / p.H, h = bh % p.H;
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const bool valid1 = qt1 < p.nqb;
+
+  // ---- setup: barriers, TMEM, per-kv-block flags
+  if (tid == 0) {
+    for (int s = 0; s < FWD_NST; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm.qfull), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.sfull[t]), 1);
+      mbar_init(smem_u32(&sm.pready[t]), 128);
+      mbar_init(smem_u32(&sm.odone[t]), 1);
+    }
+    mbar_init(smem_u32(&sm.fin), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  for (int kb = tid; kb < p.nkb; kb += FWD_THREADS) {
+    const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
+    for (int t = 0; t < 2; ++t) {
+      const int qt = qt0 + t;
+      uint8_t f = 0;
+      if (qt < p.nqb && ks != 0) {
+        const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qt * p.nkb + kb] : TILE_FULL;
+        if (st != TILE_EMPTY)
+          f = KB_VISIT | (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) |
+              (ks == 1 ? KB_KEYMASK : 0);
+      }
+      sm.flags[t][kb] = f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      const uint32_t qbar = smem_u32(&sm.qfull);
+      mbar_expect_tx(qbar, (valid1 ? 2 : 1) * FWD_TILE_BYTES);
+      tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, qbar, 0, bh * p.Sq + qt0 * 128);
+      if (valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, qbar, 0, bh * p.Sq + qt1 * 128);
+      int last_u[FWD_NST];
+      for (int s = 0; s < FWD_NST; ++s) last_u[s] = -1;
+      int u = 0;
+      for (int kb = 0; kb < p.nkb; ++kb) {
+        if (!((sm.flags[0][kb] | sm.flags[1][kb]) & KB_VISIT)) continue;
+        const int s = u % FWD_NST;
+        if (u >= FWD_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) break;
+        const uint32_t fb = smem_u32(&sm.full[s]);
+        mbar_expect_tx(fb, 2 * FWD_TILE_BYTES);
+        tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
+        tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
+        last_u[s] = u;
+        ++u;
+      }
+      if (sm.abort) {   // let the copies in flight land before the CTA exits
+        drain_wait(qbar, 0, p.timeout_ns);
+        for (int s = 0; s < FWD_NST; ++s)
+          if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / FWD_NST) & 1, p.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 2};
+      constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
+      int pend[2] = {-1, -1};
+      uint32_t npv[2] = {0, 0};
+      int uses[FWD_NST];
+      for (int s = 0; s < FWD_NST; ++s) uses[s] = 0;
+      bool ok = wait_one(smem_u32(&sm.qfull), 0, c);
+      if (ok) tc_fence_after();
+      auto issue_pv = [&](int t) -> bool {
+        if (!wait_one(smem_u32(&sm.pready[t]), npv[t] & 1, c)) return false;
+        tc_fence_after();
+        const int s = pend[t];
+        const uint32_t d = tmem + 256 + t * 64;
+        const uint32_t a = tmem + t * 128;
+        const uint32_t vb = smem_u32(sm.v[s]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(d, a + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), IDESC_PV, (kk > 0 || npv[t] > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&sm.odone[t]));
+        ++npv[t];
+        if (--uses[s] == 0) tc_commit(smem_u32(&sm.empty[s]));
+        pend[t] = -1;
+        return true;
+      };
+      int u = 0;
+      for (int kb = 0; ok && kb < p.nkb; ++kb) {
+        const bool in0 = sm.flags[0][kb] & KB_VISIT, in1 = sm.flags[1][kb] & KB_VISIT;
+        if (!in0 && !in1) continue;
+        const int s = u % FWD_NST;
+        if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        uses[s] = int(in0) + int(in1);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (pend[t] >= 0 && !issue_pv(t)) { ok = false; break; }
+          if (t == 0 ? in0 : in1) {
+            const uint32_t d = tmem + t * 128;
+            const uint32_t qa = smem_u32(sm.q[t]), kbse = smem_u32(sm.k[s]);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(d, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(kbse + kk * 32, 16, 1024), IDESC_S,
+                     kk > 0 ? 1u : 0u);
+            tc_commit(smem_u32(&sm.sfull[t]));
+            pend[t] = s;
+          }
+        }
+        ++u;
+      }
+      for (int t = 0; t < 2 && ok; ++t)
+        if (pend[t] >= 0 && !issue_pv(t)) ok = false;
+      // every MMA issued so far completes before the CTA lets go of TMEM
+      tc_commit(smem_u32(&sm.fin));
+      drain_wait(smem_u32(&sm.fin), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax warpgroups =======================
+    const int t = (warp - 2) >> 2;
+    const int quad = warp & 3;   // TMEM lanes [32 quad, 32 quad + 32)
+    const int qt = qt0 + t;
+    if (qt < p.nqb) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 3 + t};
+      const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+      const uint32_t tS = tmem + lane_off + t * 128;
+      const uint32_t tO = tmem + lane_off + 256 + t * 64;
+      const int row = 32 * quad + lane;
+      const int q = qt * 128 + row;
+      const bool writer = (quad == ((2 + 4 * t) & 3)) && lane == 0;   // first warp of the group
+      const float sc = p.sc;
+      float slope2 = 0.f, cb_even = 0.f;
+      if constexpr (MOD == MOD_ALIBI) slope2 = alibi_slope_log2(h, p.H);
+      if constexpr (MOD == MOD_CHECKER) cb_even = (q & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;
+      float m = -INFINITY, l = 0.f;
+      uint32_t n = 0;
+      bool ok = true;
+      for (int kb = 0; kb < p.nkb; ++kb) {
+        const uint8_t f = sm.flags[t][kb];
+        if (p.visited && writer)
+          p.visited[((size_t)bh * p.nqb + qt) * p.nkb + kb] = (f & KB_VISIT) ? 1 : 0;
+        if (!(f & KB_VISIT)) continue;
+        if (!wait_warp(smem_u32(&sm.sfull[t]), n & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld32(tS + 32 * j, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * j + i] = __uint_as_float(r[i]);
+        }
+        // logits in log2 units, masks as -inf
+        const int kv0 = kb * 128;
+        const bool causal = (MOD == MOD_CAUSAL) || ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+        const int lim = q - kv0;   // keep column c iff c <= lim (causal)
+        uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+        if (f & KB_KEYMASK) {
+          const uint32_t* wp = p.km_bits + (size_t)b * (p.Skv >> 5) + (kv0 >> 5);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) kw[j] = __ldg(wp + j);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc) {
+          float x;
+          if constexpr (MOD == MOD_ALIBI)
+            x = fmaf(s[cc], sc, slope2 * float(kv0 - q + cc));
+          else if constexpr (MOD == MOD_CHECKER)
+            x = fmaf(s[cc], sc, (cc & 1) ? -cb_even : cb_even);
+          else
+            x = s[cc] * sc;
+          if (causal && cc > lim) x = -INFINITY;
+          if (!((kw[cc >> 5] >> (cc & 31)) & 1u)) x = -INFINITY;
+          s[cc] = x;
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m, mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2(m - m_use);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = ex2(s[64 * j + 2 * i] - m_use);
+            const float p1 = ex2(s[64 * j + 2 * i + 1] - m_use);
+            sum += p0 + p1;
+            pk[i] = pack2<BF16>(p0, p1);
+          }
+          tmem_st32(tS + 32 * j, pk);
+        }
+        if (n > 0) {
+          // O_t must hold the previous P V before it is rescaled
+          if (!wait_warp(smem_u32(&sm.odone[t]), (n - 1) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              uint32_t r[32];
+              tmem_ld32(tO + 32 * j, r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tmem_st32(tO + 32 * j, r);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.pready[t]));
+        l = l * alpha + sum;
+        m = m_new;
+        ++n;
+      }
+      tmem_st_wait();
+      if (ok && n > 0) {
+        if (!wait_warp(smem_u32(&sm.odone[t]), (n - 1) & 1, c))
+          ok = false;
+        else
+          tc_fence_after();
+      }
+      if (ok) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint32_t o[32];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t r[32];
+          if (n > 0) {
+            tmem_ld32(tO + 32 * j, r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            o[16 * j + i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((size_t)bh * p.Sq + q) * 64);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        const float m_fin = (m == -INFINITY) ? 0.f : m;
+        p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (m_fin + lg2(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  // ---- teardown: all tcgen05 traffic of this CTA is finished before TMEM is freed
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// host-side launcher
+// ---------------------------------------------------------------------------
+size_t fwd_d64_smem_bytes() { return sizeof(FwdSmem) + 1024; }
+
+template <bool BF16, int MOD>
+static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
+  auto kern = fwd_d64_kernel<BF16, MOD>;
+  const size_t smem = fwd_d64_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(p.npairs * p.B * p.H);
+  kern<<<grid, FWD_THREADS, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t st) {
+  if (bf16) {
+    switch (mod) {
+      case MOD_NONE: return launch_fwd_t<true, MOD_NONE>(p, st);
+      case MOD_ALIBI: return launch_fwd_t<true, MOD_ALIBI>(p, st);
+      case MOD_CHECKER: return launch_fwd_t<true, MOD_CHECKER>(p, st);
+      default: return launch_fwd_t<true, MOD_CAUSAL>(p, st);
+    }
+  }
+  switch (mod) {
+    case MOD_NONE: return launch_fwd_t<false, MOD_NONE>(p, st);
+    case MOD_ALIBI: return launch_fwd_t<false, MOD_ALIBI>(p, st);
+    case MOD_CHECKER: return launch_fwd_t<false, MOD_CHECKER>(p, st);
+    default: return launch_fwd_t<false, MOD_CAUSAL>(p, st);
+  }
+}
+
+}  // namespace attn

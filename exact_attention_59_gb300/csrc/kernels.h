@@ -1,0 +1,126 @@
+// kernels.h - parameter blocks and launchers of the attention kernels.
+// Included by the kernel translation units and by the C-ABI layer (api.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace attn {
+
+// ---------------------------------------------------------------- forward, D = 64
+constexpr int FWD_NST = 3;
+constexpr int FWD_THREADS = 320;
+constexpr uint32_t FWD_TILE_BYTES = 128 * 64 * 2;
+constexpr int FWD_MAXKB = 2048;   // Skv <= 262144
+
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v;   // 2-D views (rows = B*H*S, cols = 64), box {64, 128}, 128B swizzle
+  void* out;
+  float* lse;
+  const uint32_t* km_bits;        // (B, Skv/32) or nullptr
+  const uint8_t* km_sum;          // (B, nkb) or nullptr
+  const uint8_t* bm_tiles;        // block-mask states or nullptr
+  long long bm_sb, bm_sh;         // element strides of b and h in bm_tiles (0 = broadcast)
+  int bm_mod;
+  uint8_t* visited;               // (B, H, nqb, nkb) or nullptr
+  int* status;
+  int B, H, Sq, Skv, nqb, nkb, npairs;
+  float sc;                       // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+size_t fwd_d64_smem_bytes();
+cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t st);
+
+// ---------------------------------------------------------------- forward, D = 512
+struct FwdBigParams {
+  CUtensorMap tm_q, tm_k, tm_v;   // 2-D views (rows = B*H*S, cols = 512), box {64, 128}, 128B swizzle
+  void* out;
+  float* lse;
+  const uint8_t* bm_tiles;
+  long long bm_sb, bm_sh;
+  int bm_mod;
+  uint8_t* visited;
+  int* status;
+  int B, H, Sq, Skv, nqb, nkb;
+  float sc;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_fwd_d512(const FwdBigParams& p, bool bf16, int mod, cudaStream_t st);
+
+// ---------------------------------------------------------------- backward, D = 64
+constexpr int BWD_THREADS = 384;
+
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 2-D views, box {64, 128}, 128B swizzle
+  void* dq;
+  void* dk;
+  void* dv;
+  const float* delta;     // (B, H, Sq)
+  const float* lse2;      // (B, H, Sq), log2 units, +inf for rows with no kept key
+  const uint32_t* km_bits;
+  const uint8_t* km_sum;
+  const uint8_t* bm_tiles;
+  long long bm_sb, bm_sh;
+  int bm_mod;
+  int* status;
+  int B, H, Sq, Skv, nqb, nkb;
+  float sc;               // scale * log2(e)
+  float scale;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_bwd_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
+cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
+
+// ---------------------------------------------------------------- small kernels
+// key mask (B, Skv) uint8 -> bits (B, Skv/32) + summary (B, ceil(Skv/128))
+cudaError_t launch_keymask_pack(const uint8_t* km, int B, int Skv, uint32_t* bits, uint8_t* summary,
+                                cudaStream_t st);
+cudaError_t launch_build_block_mask(int mask_mod, int B, int H, int Sq, int Skv, int bq, int bkv, uint8_t* tiles,
+                                    cudaStream_t st);
+// delta = rowsum(dout * out) (f32), lse2 = lse * log2(e) (+inf where lse = -inf)
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, int dtype, long long rows,
+                                  int D, float* delta, float* lse2, cudaStream_t st);
+
+// ---------------------------------------------------------------- decode (Sq = 1)
+struct DecodeParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  const uint8_t* key_mask;   // (B, Skv) or nullptr
+  float* partial;            // (B*H, nsplit, 2 + 64): m, l, o[64]
+  unsigned* counter;         // (B*H)
+  int B, H, Skv, nsplit, keys_per_split;
+  float sc;
+  int mod;
+};
+int decode_num_splits(int B, int H, int Skv);
+cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t st);
+
+// ---------------------------------------------------------------- f32 path (SIMT FMA)
+struct SimtParams {
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* out;
+  const float* dout;
+  float* o;
+  float* lse;
+  float* dq;
+  float* dk;
+  float* dv;
+  const float* delta;
+  const float* lse2;
+  const uint8_t* key_mask;
+  const uint8_t* bm_tiles;
+  long long bm_sb, bm_sh;
+  int bm_mod;
+  uint8_t* visited;
+  int B, H, Sq, Skv, nqb, nkb, mod;
+  float sc, scale;
+};
+cudaError_t launch_simt_fwd(const SimtParams& p, cudaStream_t st);
+cudaError_t launch_simt_bwd_dkdv(const SimtParams& p, cudaStream_t st);
+cudaError_t launch_simt_bwd_dq(const SimtParams& p, cudaStream_t st);
+
+}  // namespace attn

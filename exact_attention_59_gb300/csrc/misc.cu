@@ -1,0 +1,140 @@
+// misc.cu - the small bandwidth-bound kernels around the attention passes:
+//   * key-mask packing: uint8 (B, Skv) -> bits (B, ceil(Skv/32)) and a per-(b,
+//     kv block) summary that lets whole 128-key blocks be skipped or kept;
+//   * the block-mask builder (the analogue of create_block_mask(mask_mod, B, H,
+//     Sq, Skv) in the flaxattention README "Example usage");
+//   * the backward preprocess: D_i = sum_d dO_id O_id, and lse in log2 units.
+#include "kernels.h"
+
+namespace attn {
+
+// One CTA of 128 threads per (b, kv block): 4 ballots give the block's 128 key bits.
+__global__ void keymask_pack_kernel(const uint8_t* __restrict__ km, int Skv, uint32_t* __restrict__ bits,
+                                    uint8_t* __restrict__ summary) {
+  const int b = blockIdx.y, kb = blockIdx.x;
+  const int kv = kb * 128 + threadIdx.x;
+  const bool keep = kv < Skv && km[(size_t)b * Skv + kv] != 0;
+  const unsigned w = __ballot_sync(0xffffffffu, keep);
+  __shared__ int cnt[4];
+  const int words = (Skv + 31) >> 5;
+  const int wi = kb * 4 + (threadIdx.x >> 5);
+  if ((threadIdx.x & 31) == 0) {
+    if (wi < words) bits[(size_t)b * words + wi] = w;
+    cnt[threadIdx.x >> 5] = __popc(w);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int valid = min(128, Skv - kb * 128);
+    const int c = cnt[0] + cnt[1] + cnt[2] + cnt[3];
+    summary[(size_t)b * gridDim.x + kb] = c == 0 ? 0 : (c == valid ? 2 : 1);
+  }
+}
+
+cudaError_t launch_keymask_pack(const uint8_t* km, int B, int Skv, uint32_t* bits, uint8_t* summary,
+                                cudaStream_t st) {
+  dim3 grid((Skv + 127) / 128, B);
+  keymask_pack_kernel<<<grid, 128, 0, st>>>(km, Skv, bits, summary);
+  return cudaGetLastError();
+}
+
+// Tile state from the mask_mod over the tile's index ranges (exact for the
+// mask_mods built: NONE keeps everything; CAUSAL keeps kv <= q).
+__global__ void build_block_mask_kernel(int mask_mod, long long total, int Sq, int Skv, int bq, int bkv, int nqb,
+                                        int nkb, uint8_t* __restrict__ tiles) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int kb = (int)(i % nkb);
+    const int qb = (int)((i / nkb) % nqb);
+    uint8_t st = TILE_FULL;
+    if (mask_mod == MASKMOD_CAUSAL) {
+      const long long q_lo = (long long)qb * bq, q_hi = min((long long)Sq, (long long)(qb + 1) * bq) - 1;
+      const long long k_lo = (long long)kb * bkv, k_hi = min((long long)Skv, (long long)(kb + 1) * bkv) - 1;
+      st = k_hi <= q_lo ? TILE_FULL : (k_lo > q_hi ? TILE_EMPTY : TILE_PARTIAL);
+    }
+    tiles[i] = st;
+  }
+}
+
+cudaError_t launch_build_block_mask(int mask_mod, int B, int H, int Sq, int Skv, int bq, int bkv, uint8_t* tiles,
+                                    cudaStream_t st) {
+  const int nqb = (Sq + bq - 1) / bq, nkb = (Skv + bkv - 1) / bkv;
+  const long long total = (long long)B * H * nqb * nkb;
+  if (total == 0) return cudaSuccess;
+  const long long blocks = std::min<long long>((total + 255) / 256, 152LL * 8);
+  build_block_mask_kernel<<<(unsigned)blocks, 256, 0, st>>>(mask_mod, total, Sq, Skv, bq, bkv, nqb, nkb, tiles);
+  return cudaGetLastError();
+}
+
+// delta_i = sum_d dout_id * out_id in f32; 16-byte loads, LPR lanes per row.
+template <typename T>
+DEVI void load8(const T* p, float (&f)[8]);
+template <>
+DEVI void load8<float>(const float* p, float (&f)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+struct h16 { uint16_t x; };
+struct b16 { uint16_t x; };
+template <>
+DEVI void load8<h16>(const h16* p, float (&f)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = unpack2<false>(w[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+template <>
+DEVI void load8<b16>(const b16* p, float (&f)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = unpack2<true>(w[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+template <typename T>
+__global__ void bwd_preprocess_kernel(const T* __restrict__ out, const T* __restrict__ dout,
+                                      const float* __restrict__ lse, long long rows, int D,
+                                      float* __restrict__ delta, float* __restrict__ lse2) {
+  const int lpr = D / 8;   // lanes per row (8 elements per lane)
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row = tid / lpr;
+  const int part = (int)(tid % lpr);
+  float acc = 0.f;
+  if (row < rows) {
+    float a[8], g[8];
+    load8<T>(out + row * D + part * 8, a);
+    load8<T>(dout + row * D + part * 8, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(a[i], g[i], acc);
+  }
+  for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) {
+    delta[row] = acc;
+    const float l = lse[row];
+    lse2[row] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+  }
+}
+
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, int dtype, long long rows,
+                                  int D, float* delta, float* lse2, cudaStream_t st) {
+  const long long threads = rows * (D / 8);
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (rows == 0) return cudaSuccess;
+  if (dtype == 0)
+    bwd_preprocess_kernel<float><<<blocks, 256, 0, st>>>((const float*)out, (const float*)dout, lse, rows, D, delta,
+                                                         lse2);
+  else if (dtype == 1)
+    bwd_preprocess_kernel<h16><<<blocks, 256, 0, st>>>((const h16*)out, (const h16*)dout, lse, rows, D, delta, lse2);
+  else
+    bwd_preprocess_kernel<b16><<<blocks, 256, 0, st>>>((const b16*)out, (const b16*)dout, lse, rows, D, delta, lse2);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

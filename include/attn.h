@@ -1,0 +1,179 @@
+/*
+ * attn.h - C ABI of a GB300 (sm_103a) exact softmax attention library.
+ *
+ * The operation is the tiled, IO-aware exact attention of FlashAttention
+ * (Dao et al. 2022, cited by the attnax Pallas kernel page, "FlashAttention
+ * forward pass compiled with Pallas"): per query row,
+ *     S = scale * q K^T + score_mod bias,  masked entries = -inf,
+ *     P = softmax(S),  O = P V,  lse = log sum_j exp(S_j),
+ * computed with the online-softmax recurrence of the attnax Pallas kernel body
+ * (running max m, running sum l, accumulator rescaled by exp(m_old - m_new)),
+ * plus the FlexAttention-style hooks of the flaxattention README ("Example
+ * usage": score_mod, create_block_mask(causal_mask, ...)) and the key-padding
+ * mask of shape (batch, seq) of the flash-attention-jax docs ("3. Use
+ * flash_attention").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned DEVICE memory, BHSD contiguous:
+ *      q (B, H, Sq, D), k and v (B, H, Skv, D), out/dout/dq (B, H, Sq, D),
+ *      dk/dv (B, H, Skv, D), all in the dtype of attn_shape.dtype;
+ *      lse (B, H, Sq) float32, natural log (the second return value of
+ *      flash_attention, read as the row log-sum-exp).
+ *    This is the (batch, heads, seq, dim) layout of the attnax Pallas
+ *    forward's arguments.
+ *  - key_mask is uint8 (B, Skv), nonzero = attend; NULL = no key mask.
+ *  - Every pointer must be 16-byte aligned (the TMA engine needs it), else
+ *    ATTN_ERR_ALIGN.
+ *  - Prefill (attn_fwd / attn_bwd) needs Sq and Skv to be multiples of 128,
+ *    as the attnax Pallas forward requires seq_q % block_q == 0 and
+ *    seq_kv % block_kv == 0 with block_q = block_kv = 128; else
+ *    ATTN_ERR_SHAPE.  D must be 64 (all dtypes) or 512 (bf16/f16 forward).
+ *  - The library allocates no memory and keeps no state.  Scratch space
+ *    ("workspace") is caller-owned device memory of attn_workspace_size()
+ *    bytes, 256-byte aligned, and must be zero-filled before its first use;
+ *    every call leaves it ready for the next one.  Calls on one workspace
+ *    must not overlap in time (use one workspace per stream).
+ *  - Calls are asynchronous on `stream` and never synchronise, except
+ *    attn_poll_status().  Arguments are validated before anything is
+ *    launched: a call that returns an error has launched nothing.
+ *  - Device-side waits are bounded (ATTN_TIMEOUT_NS environment variable,
+ *    default 2 s).  A kernel whose wait runs out stops, writes
+ *    ATTN_ERR_TIMEOUT into the workspace status word and returns; read it
+ *    with attn_poll_status().
+ *  - Masked scores are -inf: a row with no kept key gets O = 0, lse = -inf
+ *    and zero gradients.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream; the same handle as cudaStream_t / CUstream.  NULL = legacy default stream. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad enum, bad scale */
+  ATTN_ERR_SHAPE = 2,       /* Sq/Skv not a multiple of 128 (prefill), Sq != 1 (decode), size overflow */
+  ATTN_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  ATTN_ERR_UNSUPPORTED = 4, /* dtype / D / mod / block-size combination not built */
+  ATTN_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than attn_workspace_size() */
+  ATTN_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+  ATTN_ERR_TIMEOUT = 7      /* a device-side wait ran out (reported by attn_poll_status) */
+} attn_status;
+
+typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
+
+/* score_mod hooks (flaxattention README "Example usage"; attnax Pallas kernel
+ * body applies score_mod(scores, b, h, q_idx, kv_idx) with global indices after
+ * the scale and before the mask).  h is 0-based.
+ *   NONE          no change
+ *   ALIBI         + slope_h * (kv_idx - q_idx),  slope_h = 2^(-8 (h+1) / H)
+ *   CHECKERBOARD  + 0.5 if (q_idx + kv_idx) is even, else - 0.5
+ *   CAUSAL        -inf where kv_idx > q_idx (no tile skipping by itself)   */
+typedef enum {
+  ATTN_MOD_NONE = 0,
+  ATTN_MOD_ALIBI = 1,
+  ATTN_MOD_CHECKERBOARD = 2,
+  ATTN_MOD_CAUSAL = 3
+} attn_score_mod;
+
+/* mask_mod of a block mask (flaxattention README: create_block_mask(causal_mask, ...)). */
+typedef enum { ATTN_MASKMOD_NONE = 0, ATTN_MASKMOD_CAUSAL = 1 } attn_mask_mod;
+
+/* Block-mask tile states. */
+enum { ATTN_TILE_EMPTY = 0, ATTN_TILE_PARTIAL = 1, ATTN_TILE_FULL = 2 };
+
+typedef enum { ATTN_OP_FWD = 0, ATTN_OP_BWD = 1, ATTN_OP_DECODE = 2 } attn_op;
+
+typedef struct {
+  int B, H, Sq, Skv, D;
+  attn_dtype dtype;
+} attn_shape;
+
+/* Block mask: one uint8 state per (q-block, kv-block) tile, laid out
+ * (bcast_b ? 1 : B, bcast_h ? 1 : H, ceil(Sq/block_q), ceil(Skv/block_kv)),
+ * row-major, device memory.  EMPTY tiles are skipped (all entries masked),
+ * PARTIAL tiles apply mask_mod elementwise, FULL tiles are kept whole.
+ * block_q = block_kv = 128 is the only size built. */
+typedef struct {
+  const uint8_t* tiles;
+  int bcast_b, bcast_h;
+  int block_q, block_kv;
+  attn_mask_mod mask_mod;
+} attn_block_mask;
+
+/* Bytes of workspace that `op` needs for `shape` (0 if the shape is invalid).
+ * Monotonic non-decreasing in every dimension of the shape. */
+size_t attn_workspace_size(attn_op op, const attn_shape* shape);
+
+/* Builds block-mask tile states on the device: the analogue of
+ * create_block_mask(mask_mod, B, H, Sq, Skv) in the flaxattention README.
+ * tiles: device uint8 (B, H, ceil(Sq/bq), ceil(Skv/bkv)).  A tile is FULL
+ * when mask_mod keeps all its entries, EMPTY when it keeps none, else PARTIAL. */
+attn_status attn_build_block_mask(attn_mask_mod mask_mod, int B, int H, int Sq, int Skv, int bq,
+                                  int bkv, uint8_t* tiles, attn_stream_t stream);
+
+/* Forward: out = softmax(mask(scale q k^T + mod)) v and lse (attnax Pallas
+ * kernel body, online softmax with exp2/log2 arithmetic as in the
+ * flaxattention README's "log2 trick").
+ *   key_mask: nullable; bm: nullable (NULL = no block mask);
+ *   debug_visited: nullable uint8 (B, H, Sq/128, Skv/128); when given, each
+ *   entry is set to 1 if the kernel computed that tile and 0 if it skipped it.
+ *   D = 512 is built for f16/bf16 without key mask. */
+attn_status attn_fwd(const attn_shape* shape, const void* q, const void* k, const void* v,
+                     const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod,
+                     float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                     attn_stream_t stream, uint8_t* debug_visited);
+
+/* Backward of sum(dout * out): dq, dk, dv (same shapes and dtype as q, k, v).
+ * Takes the forward's out and lse and the same key_mask, bm, mod and scale.
+ * Runs three kernels: a preprocess (D_i = rowsum(dout * out)), a dK/dV pass
+ * over kv blocks and a dQ pass over q blocks; no atomics, so results are
+ * bitwise reproducible.  D = 64 only. */
+attn_status attn_bwd(const attn_shape* shape, const void* q, const void* k, const void* v,
+                     const void* out, const float* lse, const void* dout,
+                     const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod,
+                     float scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                     attn_stream_t stream);
+
+/* The three phases of attn_bwd as separate calls, in this order, on one
+ * workspace (for timing a phase alone).  Same arguments as attn_bwd. */
+attn_status attn_bwd_preprocess(const attn_shape* shape, const void* out, const float* lse,
+                                const void* dout, const uint8_t* key_mask, void* ws,
+                                size_t ws_bytes, attn_stream_t stream);
+attn_status attn_bwd_dkdv(const attn_shape* shape, const void* q, const void* k, const void* v,
+                          const void* dout, const uint8_t* key_mask, const attn_block_mask* bm,
+                          attn_score_mod mod, float scale, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, attn_stream_t stream);
+attn_status attn_bwd_dq(const attn_shape* shape, const void* q, const void* k, const void* v,
+                        const void* dout, const uint8_t* key_mask, const attn_block_mask* bm,
+                        attn_score_mod mod, float scale, void* dq, void* ws, size_t ws_bytes,
+                        attn_stream_t stream);
+
+/* Single-query decode (shape->Sq must be 1; q_idx = 0): split-KV partial
+ * softmax per (b, h, split) streamed with 16-byte loads, combined in the same
+ * launch by the last split to finish (flaxattention README "Decoding").
+ * f16/bf16, D = 64. */
+attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, const void* v,
+                        const uint8_t* key_mask, attn_score_mod mod, float scale, void* out,
+                        float* lse, void* ws, size_t ws_bytes, attn_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the workspace status word.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT (a device wait ran out), or
+ * ATTN_ERR_CUDA (the stream reported an error). */
+attn_status attn_poll_status(void* ws, attn_stream_t stream);
+
+/* Static text for a status code. */
+const char* attn_status_string(attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTN_GB300_H */

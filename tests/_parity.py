@@ -1,0 +1,66 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI and
+the float64 oracle on the same seeded inputs, and compare.
+
+Tolerances (written here once, used by every parity test):
+  16-bit inputs:  max |err| <= 2e-2 and mean |err| <= 2e-3 on out, dq, dk, dv;
+                  lse max |err| <= 2e-2 (lse is float32 on both sides' inputs).
+  float32 inputs: max |err| <= 1e-4 on out and lse, <= 1e-3 on dq, dk, dv.
+Masking is exact: the visited-tile map must equal the oracle's skip set, and
+a row with no kept key must give out = 0 and lse = -inf bit for bit.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle.attention as OR
+from exact_attention_59_gb300 import inputs as IN
+
+TOL = {
+    "f32": dict(o_max=1e-4, lse_max=1e-4, g_max=1e-3, o_mean=None, g_mean=None),
+    "f16": dict(o_max=2e-2, lse_max=2e-2, g_max=2e-2, o_mean=2e-3, g_mean=2e-3),
+    "bf16": dict(o_max=2e-2, lse_max=2e-2, g_max=2e-2, o_mean=2e-3, g_mean=2e-3),
+}
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def compare(name, got, ref, max_tol, mean_tol=None, mask=None):
+    g = np.asarray(got)
+    r = np.asarray(ref)
+    if mask is not None:
+        g, r = g[mask], r[mask]
+    assert np.isfinite(g).all(), f"{name}: non-finite values"
+    err = np.abs(g - r)
+    mx = float(err.max()) if err.size else 0.0
+    mn = float(err.mean()) if err.size else 0.0
+    assert mx <= max_tol, f"{name}: max abs err {mx:.3e} > {max_tol}"
+    if mean_tol is not None:
+        assert mn <= mean_tol, f"{name}: mean abs err {mn:.3e} > {mean_tol}"
+    return mx, mn
+
+
+def make_dev(B, H, Sq, Skv, D, dtype, key_mask=False, dout="randn", seed=IN.SEED):
+    c = IN.make_case(B, H, Sq, Skv, D, dtype, seed=seed, with_key_mask=key_mask, dout=dout)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in c.items()}
+    return c, dev
+
+
+def guarded(shape, dtype, fill=float("nan"), canary=4096):
+    """An output tensor filled with `fill`, followed by a canary region of 0x5A bytes."""
+    n = int(np.prod(shape))
+    esz = torch.empty((), dtype=dtype).element_size()
+    extra = canary // esz
+    buf = torch.full((n + extra,), fill, dtype=dtype, device="cuda")
+    buf.view(torch.uint8)[n * esz:].fill_(0x5A)
+    return buf, buf[:n].view(shape)
+
+
+def canary_ok(buf, shape):
+    n = int(np.prod(shape))
+    esz = buf.element_size()
+    tail = buf.view(torch.uint8)[n * esz:]
+    return bool((tail == 0x5A).all().item())

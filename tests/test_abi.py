@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/attn.h
+declares, and rejects bad arguments before launching anything (no GPU needed:
+every call here fails validation, so none reaches the CUDA runtime)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_59_gb300 import build
+    build.build()
+    import exact_attention_59_gb300._lib as L
+    return L
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("attn_fwd", "attn_bwd", "attn_decode", "attn_build_block_mask", "attn_workspace_size",
+              "attn_poll_status", "attn_status_string"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for s in declared_symbols():
+        assert hasattr(so, s), f"{s} declared in attn.h but not exported"
+    assert set(declared_symbols()) >= set(lib.SYMBOLS)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert len(lib.status_string(code)) >= 2 and lib.status_string(code) != "unknown status"
+    assert lib.status_string(99) == "unknown status"
+
+
+def _shape(lib, B=1, H=2, Sq=256, Skv=256, D=64, dt=2):
+    return lib.Shape(B, H, Sq, Skv, D, dt)
+
+
+def test_workspace_size_monotonic(lib):
+    base = dict(B=2, H=2, Sq=256, Skv=256, D=64, dt=2)
+    for op in (0, 1, 2):
+        prev = lib.workspace_size(op, _shape(lib, **base))
+        assert prev > 0
+        for key in ("B", "H", "Sq", "Skv"):
+            for mul in (2, 3, 8):
+                kw = dict(base)
+                kw[key] *= mul
+                n = lib.workspace_size(op, _shape(lib, **kw))
+                assert n >= prev
+    assert lib.workspace_size(0, _shape(lib, B=0)) == 0
+    assert lib.load().attn_workspace_size(0, None) == 0
+
+
+FAKE = 0x7F0000000000   # never dereferenced: validation fails first
+
+
+def _fwd(lib, shape, q=FAKE, k=FAKE, v=FAKE, km=None, bm=None, mod=0, scale=0.125, out=FAKE, lse=FAKE, ws=FAKE,
+         ws_bytes=1 << 30):
+    L = lib.load()
+    return L.attn_fwd(ctypes.byref(shape) if shape is not None else None, q, k, v, km,
+                      ctypes.byref(bm) if bm is not None else None, mod, scale, out, lse, ws, ws_bytes, None, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, None) == lib.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(lib, Sq=200)) == lib.ATTN_ERR_SHAPE
+    assert _fwd(lib, _shape(lib, Skv=130)) == lib.ATTN_ERR_SHAPE
+    assert _fwd(lib, _shape(lib, D=96)) == lib.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, _shape(lib, D=512, dt=0)) == lib.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, _shape(lib, dt=7)) == lib.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(lib), q=None) == lib.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(lib), k=FAKE + 8) == lib.ATTN_ERR_ALIGN
+    assert _fwd(lib, _shape(lib), out=FAKE + 2) == lib.ATTN_ERR_ALIGN
+    assert _fwd(lib, _shape(lib), km=FAKE + 1) == lib.ATTN_ERR_ALIGN
+    assert _fwd(lib, _shape(lib), mod=9) == lib.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(lib), scale=float("nan")) == lib.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(lib), ws=None) == lib.ATTN_ERR_WORKSPACE
+    assert _fwd(lib, _shape(lib), ws=FAKE + 16) == lib.ATTN_ERR_ALIGN
+    assert _fwd(lib, _shape(lib), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE
+    bm = lib.BlockMaskC(None, 1, 1, 128, 128, 1)
+    assert _fwd(lib, _shape(lib), bm=bm) == lib.ATTN_ERR_INVALID_ARG
+    bm = lib.BlockMaskC(FAKE, 1, 1, 64, 64, 1)
+    assert _fwd(lib, _shape(lib), bm=bm) == lib.ATTN_ERR_UNSUPPORTED
+    bm = lib.BlockMaskC(FAKE, 1, 1, 128, 128, 5)
+    assert _fwd(lib, _shape(lib), bm=bm) == lib.ATTN_ERR_INVALID_ARG
+
+
+def test_bwd_and_decode_reject_bad_arguments(lib):
+    L = lib.load()
+    s = _shape(lib)
+    args = [FAKE] * 6
+    assert L.attn_bwd(ctypes.byref(_shape(lib, D=512)), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                      None) == lib.ATTN_ERR_UNSUPPORTED
+    assert L.attn_bwd(ctypes.byref(s), *args, None, None, 0, 0.1, None, FAKE, FAKE, FAKE, 1 << 30,
+                      None) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_bwd(ctypes.byref(s), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE, 10,
+                      None) == lib.ATTN_ERR_WORKSPACE
+    d = _shape(lib, Sq=2, Skv=100)
+    assert L.attn_decode(ctypes.byref(d), FAKE, FAKE, FAKE, None, 0, 0.1, FAKE, FAKE, FAKE, 1 << 30,
+                         None) == lib.ATTN_ERR_SHAPE
+    d = _shape(lib, Sq=1, Skv=100, dt=0)
+    assert L.attn_decode(ctypes.byref(d), FAKE, FAKE, FAKE, None, 0, 0.1, FAKE, FAKE, FAKE, 1 << 30,
+                         None) == lib.ATTN_ERR_UNSUPPORTED
+    d = _shape(lib, Sq=1, Skv=100)
+    assert L.attn_decode(ctypes.byref(d), FAKE, FAKE, FAKE, None, 0, 0.1, FAKE, FAKE, FAKE, 8,
+                         None) == lib.ATTN_ERR_WORKSPACE
+    assert L.attn_build_block_mask(1, 0, 1, 128, 128, 128, 128, FAKE, None) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_build_block_mask(4, 1, 1, 128, 128, 128, 128, FAKE, None) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_poll_status(None, None) == lib.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import exact_attention_59_gb300 as E
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        E.attn_fwd(q, q, q)

@@ -1,0 +1,195 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small shapes that span several 128-wide tiles cover every template variant
+(dtype x score_mod x key mask x block mask); the five named workloads run at
+full size with whole heads checked against the oracle (sampled query rows
+for the 131072-token case).  Outputs are NaN-filled before the call, followed
+by canary bytes, and each call is repeated to check bitwise reproducibility.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as OR
+import exact_attention_59_gb300 as E
+from exact_attention_59_gb300 import inputs as IN
+from exact_attention_59_gb300 import workloads as W
+from tests._parity import TOL, canary_ok, compare, f64, guarded, make_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_attention_59_gb300 import build
+    build.build()
+    E.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def _oracle_bm(bm_kind, B, H, Sq, Skv):
+    if bm_kind is None:
+        return None
+    return OR.BlockMask(OR.build_block_mask(bm_kind, 1, 1, Sq, Skv), bm_kind)
+
+
+def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", backward=True, heads=None,
+                  check_det=True, key_mask_override=None):
+    D = 64
+    c, d = make_dev(B, H, Sq, Skv, D, dtype, key_mask=key_mask, dout=dout)
+    if key_mask_override is not None:
+        c["key_mask"] = key_mask_override.clone()
+        d["key_mask"] = key_mask_override.cuda()
+    bm = E.create_block_mask(bm_kind, 1, 1, Sq, Skv) if bm_kind else None
+    tdt = d["q"].dtype
+    nqb, nkb = Sq // 128, Skv // 128
+    ob, out = guarded((B, H, Sq, D), tdt)
+    lb, lse = guarded((B, H, Sq), torch.float32)
+    vis = torch.full((B, H, nqb, nkb), 7, dtype=torch.uint8, device="cuda")
+    E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod, out=out, lse=lse,
+               debug_visited=vis)
+    grads = None
+    if backward:
+        gb = [guarded(d[n].shape, tdt) for n in ("q", "k", "v")]
+        E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
+                   score_mod=mod, dq=gb[0][1], dk=gb[1][1], dv=gb[2][1])
+        grads = gb
+    shp = E.make_shape(d["q"], d["k"])
+    assert E.poll_status(E.workspace(E.OP_FWD, shp, d["q"].device)) == E.ATTN_OK
+    if backward:
+        assert E.poll_status(E.workspace(E.OP_BWD, shp, d["q"].device)) == E.ATTN_OK
+    assert canary_ok(ob, (B, H, Sq, D)) and canary_ok(lb, (B, H, Sq))
+
+    km = None if c["key_mask"] is None else c["key_mask"].numpy()
+    obm = _oracle_bm(bm_kind, B, H, Sq, Skv)
+    q64, k64, v64 = f64(c["q"]), f64(c["k"]), f64(c["v"])
+    o_ref, lse_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, block_mask=obm, score_mod=mod, heads=heads)
+    sel = (slice(None),) if heads is None else tuple(np.array(x) for x in zip(*heads))
+    tol = TOL[dtype]
+    compare("out", f64(out)[sel], o_ref[sel], tol["o_max"], tol["o_mean"])
+    lg, lr = f64(lse)[sel], lse_ref[sel]
+    fin = np.isfinite(lr)
+    assert (np.isneginf(lg) == np.isneginf(lr)).all(), "lse -inf pattern differs"
+    compare("lse", lg, lr, tol["lse_max"], mask=fin)
+    # mask exactness: rows with no kept key are exactly zero
+    dead = ~fin
+    if dead.any():
+        assert (f64(out)[sel][dead] == 0).all()
+    vis_ref = OR.visited_tiles(B, H, Sq, Skv, key_mask=km, block_mask=obm)
+    np.testing.assert_array_equal(vis.cpu().numpy(), vis_ref)
+    if backward:
+        dq_r, dk_r, dv_r = OR.attn_bwd(q64, k64, v64, f64(c["dout"]), key_mask=km, block_mask=obm, score_mod=mod,
+                                       heads=heads)
+        for name, (buf, g), ref, shp in zip(("dq", "dk", "dv"), grads, (dq_r, dk_r, dv_r),
+                                            ((B, H, Sq, D), (B, H, Skv, D), (B, H, Skv, D))):
+            assert canary_ok(buf, shp), f"{name}: canary overwritten"
+            compare(name, f64(g)[sel], ref[sel], tol["g_max"], tol["g_mean"])
+    if check_det:
+        out2, lse2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod)
+        assert torch.equal(out2.view(torch.uint8), out.view(torch.uint8)), "forward not bitwise reproducible"
+        assert torch.equal(lse2.view(torch.uint8), lse.view(torch.uint8)), "lse not bitwise reproducible"
+        if backward:
+            g2 = E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
+                            score_mod=mod)
+            for a, (_, b_) in zip(g2, grads):
+                assert torch.equal(a.view(torch.uint8), b_.view(torch.uint8)), "backward not bitwise reproducible"
+
+
+SMALL = [(B, H, S, dt, mod, km, bmk)
+         for (B, H, S) in [(1, 2, 256), (2, 1, 384)]
+         for dt in ("bf16", "f16")
+         for mod in ("none", "alibi", "checkerboard", "causal")
+         for km in (False, True)
+         for bmk in (None, "causal")]
+
+
+@pytest.mark.parametrize("B,H,S,dtype,mod,km,bm", SMALL)
+def test_small_variants(B, H, S, dtype, mod, km, bm):
+    run_and_check(B, H, S, S, dtype, mod, km, bm)
+
+
+@pytest.mark.parametrize("mod", ["none", "alibi", "checkerboard", "causal"])
+@pytest.mark.parametrize("km,bm", [(False, None), (True, "causal")])
+def test_f32_variants(mod, km, bm):
+    run_and_check(1, 2, 256, 256, "f32", mod, km, bm)
+
+
+def test_rectangular_and_single_tile():
+    run_and_check(1, 2, 128, 512, "bf16", "alibi", True, None)
+    run_and_check(2, 2, 512, 128, "f16", "checkerboard", False, None)
+    run_and_check(1, 1, 128, 128, "bf16", "none", False, "causal")
+    run_and_check(1, 3, 640, 640, "bf16", "none", False, "causal")   # odd number of q tiles
+
+
+def test_fully_masked_batches_and_blocks():
+    """Batch 1 has no key at all; batch 0 has whole 128-key blocks padded (skipped tiles)."""
+    km = torch.ones((2, 512), dtype=torch.uint8)
+    km[1] = 0
+    km[0, 128:256] = 0
+    km[0, 384:] = 0
+    for dt in ("bf16", "f16", "f32"):
+        run_and_check(2, 2, 256, 512, dt, "none", True, None, key_mask_override=km)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def _heads(B, H, n=3):
+    rng = np.random.default_rng(7)
+    idx = rng.choice(B * H, size=n, replace=False)
+    return [(int(i) // H, int(i) % H) for i in sorted(idx)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", [W.TINY_FP32, W.KEYPAD_FP16, W.FLEX_CAUSAL_ALIBI_BF16, W.CHECKERBOARD_FP16],
+                         ids=lambda w: w.name)
+def test_workload_full_size(w):
+    heads = None if w.B * w.H <= 2 else _heads(w.B, w.H)
+    run_and_check(w.B, w.H, w.Sq, w.Skv, w.dtype, w.score_mod, w.key_mask, w.block_mask, dout=w.dout,
+                  heads=heads, check_det=True)
+
+
+# ---------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("mod", ["none", "alibi", "checkerboard", "causal"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("Skv,km", [(2048, False), (1000, True), (64, False), (4096 + 40, True)])
+def test_decode(mod, dtype, Skv, km):
+    B, H, D = 3, 4, 64
+    c, d = make_dev(B, H, 1, Skv, D, dtype, key_mask=km, dout=None)
+    ob, out = guarded((B, H, 1, D), d["q"].dtype)
+    lb, lse = guarded((B, H, 1), torch.float32)
+    for _ in range(2):   # the second call reuses the re-armed tickets
+        E.attn_decode(d["q"], d["k"], d["v"], key_mask=d["key_mask"], score_mod=mod, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert canary_ok(ob, (B, H, 1, D)) and canary_ok(lb, (B, H, 1))
+    kmn = None if c["key_mask"] is None else c["key_mask"].numpy()
+    o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=kmn, score_mod=mod)
+    tol = TOL[dtype]
+    compare("decode out", f64(out), o_ref, tol["o_max"], tol["o_mean"])
+    fin = np.isfinite(l_ref)
+    compare("decode lse", f64(lse), l_ref, tol["lse_max"], mask=fin)
+    assert (np.isneginf(f64(lse)) == ~fin).all()
+
+
+@pytest.mark.slow
+def test_decode_workload_full_size():
+    w = W.CHECKERBOARD_DECODE_FP16
+    c, d = make_dev(w.B, w.H, 1, w.Skv, w.D, w.dtype, dout=None)
+    out, lse = E.attn_decode(d["q"], d["k"], d["v"], score_mod=w.score_mod)
+    out2, lse2 = E.attn_decode(d["q"], d["k"], d["v"], score_mod=w.score_mod)
+    assert torch.equal(out.view(torch.uint8), out2.view(torch.uint8)) and torch.equal(lse, lse2)
+    o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod=w.score_mod)
+    compare("decode out", f64(out), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"])
+    compare("decode lse", f64(lse), l_ref, TOL["f16"]["lse_max"])
+
+
+# ---------------------------------------------------------------- block-mask builder
+
+@pytest.mark.parametrize("Sq,Skv", [(2048, 2048), (384, 640), (1000, 700)])
+@pytest.mark.parametrize("mm", ["causal", "none"])
+def test_block_mask_builder(Sq, Skv, mm):
+    bm = E.create_block_mask(mm, 2, 3, Sq, Skv)
+    ref = OR.build_block_mask(mm, 2, 3, Sq, Skv)
+    np.testing.assert_array_equal(bm.tiles.cpu().numpy(), ref)
