@@ -1,0 +1,399 @@
+"""Throughput of the attention hot path on one GB300 (or N, one process each).
+
+A step is one forward plus one backward (preprocess, dK/dV pass, dQ pass) of
+the key-padding-masked workload: fp16, B=8, H=8, Sq=Skv=2048, D=64, uniform
+{0,1} key mask, dout ~ N(0,1).  FLOPs are counted as 4 B H Sq Skv D for the
+forward and 2.5x that for the backward, so a step is 3.5 x 68.72 GFLOP.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Inputs are resident in HBM when the timed region
+starts; four input sets (about 134 MB each, above the 129 MB L2) are rotated
+so every step reads cold data.  The oracle (float64 NumPy) is timed on the
+host cores on a bounded sample as the CPU baseline.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_attention_59_gb300 import inputs as IN  # noqa: E402
+from exact_attention_59_gb300 import workloads as W  # noqa: E402
+
+WL = W.KEYPAD_FP16
+DEC = W.CHECKERBOARD_DECODE_FP16
+METRIC = "attention fwd+bwd TFLOP/s (fp16, B8 H8 S2048 D64, key-padding mask)"
+UNIT = "TFLOP/s"
+
+
+def counted_flops(w, backward=True):
+    f = 4.0 * w.B * w.H * w.Sq * w.Skv * w.D * (0.5 if w.causal else 1.0)
+    return f * (3.5 if backward else 1.0)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), d["hbm_gbs"], "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import exact_attention_59_gb300 as E
+    from exact_attention_59_gb300 import build as BLD
+    if rank == 0 or not os.path.exists(E.LIB_PATH):
+        BLD.build()
+    if world > 1:
+        torch.distributed.barrier()
+    E.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = WL
+    nsets = 4
+    sets = []
+    for i in range(nsets):
+        c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, seed=IN.SEED + 1000 * rank + 17 * i,
+                         with_key_mask=True)
+        d = {k: v.to(dev) for k, v in c.items()}
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
+        d["dq"], d["dk"], d["dv"] = (torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]))
+        sets.append(d)
+    shape = E.make_shape(sets[0]["q"], sets[0]["k"])
+    ws_f = E.workspace(E.OP_FWD, shape, dev)
+    ws_b = E.workspace(E.OP_BWD, shape, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(d, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], out=d["out"], lse=d["lse"], ws=ws_f)
+        if ev is not None:
+            ev[1].record(stream)
+        E.attn_bwd_preprocess(d["q"], d["k"], d["out"], d["lse"], d["dout"], key_mask=d["key_mask"], ws=ws_b)
+        if ev is not None:
+            ev[2].record(stream)
+        E.attn_bwd_dkdv(d["q"], d["k"], d["v"], d["dout"], d["dk"], d["dv"], key_mask=d["key_mask"], ws=ws_b)
+        if ev is not None:
+            ev[3].record(stream)
+        E.attn_bwd_dq(d["q"], d["k"], d["v"], d["dout"], d["dq"], key_mask=d["key_mask"], ws=ws_b)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for i in range(args.warmup):
+        step(sets[i % nsets])
+    torch.cuda.synchronize()
+    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(dev.index) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(sets[i % nsets], evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout in the timed region"
+    ph = {n: [] for n in ("fwd", "pre", "dkdv", "dq")}
+    for e in evs:
+        for j, n in enumerate(ph):
+            ph[n].append(e[j].elapsed_time(e[j + 1]))
+    ms_t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms = ms_t.item() / args.steps
+
+    # ---- decode (config: checkerboard fp16, q 8x8x1x64, K/V 8x8x2048x64), CUDA graph, rotating K/V
+    dec = bench_decode(E, dev, args)
+
+    # ---- end to end: pinned host buffers, copies inside the timed region
+    e2e = bench_e2e(E, dev, args, w)
+
+    res = {"ms": ms, "phases": {n: statistics.mean(v) for n, v in ph.items()}, "clocks": clk.summary(),
+           "decode": dec, "e2e": e2e}
+    return res
+
+
+def bench_decode(E, dev, args):
+    w = DEC
+    L2 = 129e6
+    per = 2 * w.B * w.H * w.Skv * w.D * 2
+    nsets = max(4, int(math.ceil(4 * L2 / per)))
+    ks, vs = [], []
+    q = IN.randn((w.B, w.H, 1, w.D), IN.SEED + 1, w.dtype).to(dev)
+    for i in range(nsets):
+        ks.append(IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED + 3000 + i, w.dtype).to(dev))
+        vs.append(IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED + 5000 + i, w.dtype).to(dev))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, 1), dtype=torch.float32, device=dev)
+    shape = E.make_shape(q, ks[0])
+    ws = E.workspace(E.OP_DECODE, shape, dev)
+    for i in range(3):
+        E.attn_decode(q, ks[i], vs[i], score_mod=w.score_mod, out=out, lse=lse, ws=ws)
+    torch.cuda.synchronize()
+    reps = nsets * 8
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(reps):
+                E.attn_decode(q, ks[i % nsets], vs[i % nsets], score_mod=w.score_mod, out=out, lse=lse, ws=ws)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / reps)
+    us = statistics.median(times) * 1e3
+    assert E.poll_status(ws) == 0
+    return {"workload": w.name, "us_per_call": us, "bytes_per_call": per + 2 * w.B * w.H * w.D * 2,
+            "GB/s": (per + 2 * w.B * w.H * w.D * 2) / (us * 1e-6) / 1e9, "rotating_sets": nsets}
+
+
+def bench_e2e(E, dev, args, w):
+    c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=True)
+    host = {k: v.pin_memory() for k, v in c.items()}
+    outs_h = {"out": torch.empty_like(host["q"]).pin_memory(),
+              "lse": torch.empty(host["q"].shape[:3], dtype=torch.float32).pin_memory(),
+              "dq": torch.empty_like(host["q"]).pin_memory(), "dk": torch.empty_like(host["k"]).pin_memory(),
+              "dv": torch.empty_like(host["v"]).pin_memory()}
+    dd = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    shape = E.make_shape(dd["q"], dd["k"])
+    ws_f = E.workspace(E.OP_FWD, shape, dev)
+    ws_b = E.workspace(E.OP_BWD, shape, dev)
+    out = torch.empty_like(dd["q"])
+    lse = torch.empty(dd["q"].shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(dd["q"]), torch.empty_like(dd["k"]), torch.empty_like(dd["v"])
+
+    def step():
+        for k in dd:
+            dd[k].copy_(host[k], non_blocking=True)
+        E.attn_fwd(dd["q"], dd["k"], dd["v"], key_mask=dd["key_mask"], out=out, lse=lse, ws=ws_f)
+        E.attn_bwd(dd["q"], dd["k"], dd["v"], out, lse, dd["dout"], key_mask=dd["key_mask"], dq=dq, dk=dk, dv=dv,
+                   ws=ws_b)
+        for k, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            outs_h[k].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 10))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+    return {"ms": ms, "h2d": h2d, "d2h": d2h}
+
+
+# ------------------------------------------------------------------ oracle (CPU) legs
+def oracle_sample(seconds=12.0, max_heads=64):
+    """Times the oracle's fwd+bwd on whole heads of the workload until `seconds` pass."""
+    import numpy as np
+    import oracle.attention as OR
+    w = WL
+    c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=True)
+    q, k, v, do = (c[n].float().double().numpy() for n in ("q", "k", "v", "dout"))
+    km = c["key_mask"].numpy()
+    done, t0 = 0, time.perf_counter()
+    while done < max_heads:
+        b, h = divmod(done, w.H)
+        OR.attn_fwd(q, k, v, key_mask=km, heads=[(b, h)])
+        OR.attn_bwd(q, k, v, do, key_mask=km, heads=[(b, h)])
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    flops = 3.5 * 4.0 * w.Sq * w.Skv * w.D * done
+    return flops / dt / 1e12, done, dt
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(seconds=12.0):
+    v, heads, dt = oracle_sample(seconds)
+    return {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"float64 NumPy fwd+bwd of {heads} of {WL.B * WL.H} (b,h) heads of the workload in {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(seconds=0.0, max_heads=1)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample(seconds=0.0, max_heads=1)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    val = 3.5 * 4.0 * WL.Sq * WL.Skv * WL.D / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": val, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WL.name, "B": WL.B, "H": WL.H, "Sq": WL.Sq, "Skv": WL.Skv, "D": WL.D,
+                       "step": "oracle fwd+bwd of one (b, h) head per step (bounded sample)"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": "one (b, h) head of the workload per step, float64 NumPy"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        res = run_ours(args, rank, world)
+        if rank != 0:
+            return
+        fl = counted_flops(WL)
+        value = fl * world / (res["ms"] * 1e-3) / 1e12
+        burst, sustained, hbm, src = peaks()
+        ph = res["phases"]
+        # dominant kernel: the longest phase
+        dk_ms = ph["dkdv"]
+        dkdv_flops = 8.0 * WL.B * WL.H * WL.Sq * WL.Skv * WL.D
+        achieved = dkdv_flops / (dk_ms * 1e-3) / 1e12
+        dec = res["decode"]
+        e2e = res["e2e"]
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WL.name, "B": WL.B, "H": WL.H, "Sq": WL.Sq, "Skv": WL.Skv, "D": WL.D,
+                       "key_mask": "uniform {0,1}", "l2": "4 rotating input sets of 134 MB (> 129 MB L2)",
+                       "parallelism": f"replicas x{world}"},
+            "fwd_tflops": 4.0 * WL.B * WL.H * WL.Sq * WL.Skv * WL.D / (ph["fwd"] * 1e-3) / 1e12,
+            "bwd_tflops": 10.0 * WL.B * WL.H * WL.Sq * WL.Skv * WL.D / ((ph["pre"] + ph["dkdv"] + ph["dq"]) * 1e-3)
+            / 1e12,
+            "phase_ms": ph,
+            "frac_of_peak": {"burst": value / burst, "sustained": value / sustained, "peak_source": src},
+            "decode": {"workload": dec["workload"], "us_per_call": dec["us_per_call"], "GB/s": dec["GB/s"],
+                       "frac_of_hbm": dec["GB/s"] / hbm},
+            "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": achieved, "peak": sustained,
+                         "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": None,
+                         "peak_kind": f"bf16 sustained, {src}"},
+            "e2e": {"value": fl / (e2e["ms"] * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                    "d2h_bytes_per_step": e2e["d2h"]},
+            "gpu_launches": 6 * args.steps,
+            "clocks": res["clocks"],
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -5,6 +5,10 @@ Tolerances (written here once, used by every parity test):
   16-bit inputs:  max |err| <= 2e-2 and mean |err| <= 2e-3 on out, dq, dk, dv;
                   lse max |err| <= 2e-2 (lse is float32 on both sides' inputs).
   float32 inputs: max |err| <= 1e-4 on out and lse, <= 1e-3 on dq, dk, dv.
+The small extra-coverage shapes (S <= 640) have gradients of magnitude up to
+~4, where a 16-bit value's own rounding step is already ~1e-2; there the
+bounds are scaled by max(1, max |ref|) (a relative bound for large values).
+The named full-size workloads use the plain absolute bounds above.
 Masking is exact: the visited-tile map must equal the oracle's skip set, and
 a row with no kept key must give out = 0 and lse = -inf bit for bit.
 """
@@ -28,11 +32,15 @@ def f64(t):
     return t.detach().float().cpu().double().numpy()
 
 
-def compare(name, got, ref, max_tol, mean_tol=None, mask=None):
+def compare(name, got, ref, max_tol, mean_tol=None, mask=None, scaled=False):
     g = np.asarray(got)
     r = np.asarray(ref)
     if mask is not None:
         g, r = g[mask], r[mask]
+    if scaled and r.size:
+        f = max(1.0, float(np.abs(r).max()))
+        max_tol = max_tol * f
+        mean_tol = None if mean_tol is None else mean_tol * f
     assert np.isfinite(g).all(), f"{name}: non-finite values"
     err = np.abs(g - r)
     mx = float(err.max()) if err.size else 0.0
