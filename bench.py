@@ -334,6 +334,32 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """A few untimed fwd+bwd steps of the workload at batch `--batch`, for ncu captures."""
+    import exact_attention_59_gb300 as E
+    from exact_attention_59_gb300 import build as BLD
+    BLD.build()
+    E.load()
+    dev = torch.device("cuda", 0)
+    w = WL
+    c = IN.make_case(args.batch, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=True)
+    d = {k: v.to(dev) for k, v in c.items()}
+    for _ in range(args.steps):
+        out, lse = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"])
+        E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"])
+    if args.decode:
+        dw = DEC
+        q = IN.randn((args.batch, dw.H, 1, dw.D), IN.SEED + 1, dw.dtype).to(dev)
+        k = IN.randn((args.batch, dw.H, dw.Skv, dw.D), IN.SEED, dw.dtype).to(dev)
+        v = IN.randn((args.batch, dw.H, dw.Skv, dw.D), IN.SEED + 2, dw.dtype).to(dev)
+        for _ in range(args.steps):
+            E.attn_decode(q, k, v, score_mod=dw.score_mod)
+    torch.cuda.synchronize()
+    ws = E.workspace(E.OP_FWD, E.make_shape(d["q"], d["k"]), dev)
+    assert E.poll_status(ws) == 0
+    print(json.dumps({"mode": "profile", "batch": args.batch, "steps": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -341,7 +367,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
+                    help="profile: a few untimed steps at --batch, for ncu captures")
+    ap.add_argument("--batch", type=int, default=16)
+    ap.add_argument("--decode", action="store_true", help="profile mode: also run decode at --batch")
     args = ap.parse_args()
+    if args.mode == "profile":
+        run_profile_case(args)
+        return
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
