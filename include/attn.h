@@ -165,6 +165,29 @@ attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, c
                         const uint8_t* key_mask, attn_score_mod mod, float scale, void* out,
                         float* lse, void* ws, size_t ws_bytes, attn_stream_t stream);
 
+/* attn_decode without a caller workspace, for callers that cannot allocate
+ * device memory: for example an operator running inside a host framework
+ * that owns all device memory and offers no allocation hook, or a serving
+ * loop whose memory plan is fixed at start-up and must not call cudaMalloc
+ * (directly or through a caching allocator) while it serves.  The pages have
+ * no counterpart of this entry point; it exists for those callers only.
+ *   - Same arguments, layout and result as attn_decode (f16/bf16, D = 64,
+ *     Sq = 1), minus ws and ws_bytes.  It allocates nothing: its scratch is a
+ *     4 MiB array built into the library, which every GPU that loads the
+ *     library holds until the process exits.
+ *   - Shapes whose scratch (B*H*nsplit*(D+2)*4 bytes of partials plus B*H*4
+ *     bytes of tickets) exceeds 4 MiB are rejected with ATTN_ERR_WORKSPACE.
+ *   - It runs on the CURRENT device; `stream` must belong to it.  The first
+ *     call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call on a device shares the one array.  Each call zeroes the
+ *     tickets it uses (an asynchronous memset on `stream`) before its kernel.
+ *     Calls that overlap in time on the GPU (other streams, other threads)
+ *     race on the array and give wrong results: serialise them. */
+attn_status attn_decode_noalloc(const attn_shape* shape, const void* q, const void* k, const void* v,
+                                const uint8_t* key_mask, attn_score_mod mod, float scale, void* out,
+                                float* lse, attn_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the workspace status word.
  * Returns ATTN_OK, ATTN_ERR_TIMEOUT (a device wait ran out), or
  * ATTN_ERR_CUDA (the stream reported an error). */
