@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
+from exact_attention_59_gb300 import dist as DIST  # noqa: E402
 from exact_attention_59_gb300 import inputs as IN  # noqa: E402
 from exact_attention_59_gb300 import workloads as W  # noqa: E402
 
@@ -112,8 +113,7 @@ def run_ours(args, rank, world):
     from exact_attention_59_gb300 import build as BLD
     if rank == 0 or not os.path.exists(E.LIB_PATH):
         BLD.build()
-    if world > 1:
-        torch.distributed.barrier()
+    DIST.barrier()
     E.load()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -157,8 +157,7 @@ def run_ours(args, rank, world):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
+    DIST.barrier()
     torch.cuda.synchronize()
     with Clocks(dev.index) as clk:
         t_start.record(stream)
@@ -166,18 +165,14 @@ def run_ours(args, rank, world):
             step(sets[i % nsets], evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    DIST.barrier()
     total_ms = t_start.elapsed_time(t_end)
     assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout in the timed region"
     ph = {n: [] for n in ("fwd", "pre", "dkdv", "dq")}
     for e in evs:
         for j, n in enumerate(ph):
             ph[n].append(e[j].elapsed_time(e[j + 1]))
-    ms_t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms = ms_t.item() / args.steps
+    ms = DIST.max_over_ranks(total_ms, device=dev) / args.steps   # the slowest rank sets the time
 
     # ---- decode (config: checkerboard fp16, q 8x8x1x64, K/V 8x8x2048x64), CUDA graph, rotating K/V
     dec = bench_decode(E, dev, args)
@@ -347,6 +342,14 @@ def run_profile_case(args):
     for _ in range(args.steps):
         out, lse = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"])
         E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"])
+    if args.d512:
+        S = args.d512
+        q = IN.randn((1, 2, S, 512), IN.SEED + 1, "bf16").to(dev)
+        k = IN.randn((1, 2, S, 512), IN.SEED, "bf16").to(dev)
+        v = IN.randn((1, 2, S, 512), IN.SEED + 2, "bf16").to(dev)
+        bm = E.create_block_mask("causal", 1, 1, S, S)
+        for _ in range(args.steps):
+            E.attn_fwd(q, k, v, block_mask=bm)
     if args.decode:
         dw = DEC
         q = IN.randn((args.batch, dw.H, 1, dw.D), IN.SEED + 1, dw.dtype).to(dev)
@@ -363,24 +366,25 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
                     help="profile: a few untimed steps at --batch, for ncu captures")
     ap.add_argument("--batch", type=int, default=16)
     ap.add_argument("--decode", action="store_true", help="profile mode: also run decode at --batch")
+    ap.add_argument("--d512", type=int, default=0,
+                    help="profile mode: also run the causal 1 x 2 x S x S x 512 bf16 forward at this S")
     args = ap.parse_args()
     if args.mode == "profile":
         run_profile_case(args)
         return
     args.warmup = max(3, args.warmup)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
+    rank, world = DIST.world()
     if world > 1:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-        torch.distributed.init_process_group("nccl")
+        DIST.init("nccl")
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
@@ -424,7 +428,7 @@ def main():
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
     finally:
-        if world > 1:
+        if world > 1 and torch.distributed.is_initialized():
             torch.distributed.destroy_process_group()
 
 

@@ -1,7 +1,7 @@
 // api.cu - the C ABI declared in include/attn.h: validation, workspace
 // layout, TMA descriptor encoding and kernel dispatch.  No allocation, no
-// synchronisation (except attn_poll_status), no state beyond two cached
-// process-wide values (the driver's tensor-map encoder and the wait limit).
+// synchronisation (except attn_poll_status), no state beyond one cached
+// process-wide value (the driver's tensor-map encoder).
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -18,18 +18,24 @@ namespace {
 
 constexpr long long kMaxRows = (1LL << 31) - 1;
 
+// Device-side wait limit, read at every call (ATTN_TIMEOUT_NS, default 2 s).
 unsigned long long timeout_ns() {
-  static unsigned long long t = [] {
-    const char* e = std::getenv("ATTN_TIMEOUT_NS");
-    unsigned long long v = 2000000000ULL;
-    if (e && *e) {
-      char* end = nullptr;
-      const unsigned long long x = std::strtoull(e, &end, 10);
-      if (end && *end == '\0' && x > 0) v = x;
-    }
-    return v;
-  }();
-  return t;
+  const char* e = std::getenv("ATTN_TIMEOUT_NS");
+  unsigned long long v = 2000000000ULL;
+  if (e && *e) {
+    char* end = nullptr;
+    const unsigned long long x = std::strtoull(e, &end, 10);
+    if (end && *end == '\0' && x > 0) v = x;
+  }
+  return v;
+}
+
+// Test hook, off unless ATTN_DEBUG_INJECT_STALL=1: the D = 64 forward's producer
+// withholds its first K/V copy, so the kernel's bounded waits run out and it
+// reports ATTN_ERR_TIMEOUT through the status word (no trap, no fault).
+int inject_stall() {
+  const char* e = std::getenv("ATTN_DEBUG_INJECT_STALL");
+  return (e && e[0] == '1' && e[1] == '\0') ? 1 : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -269,11 +275,32 @@ attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const vo
   ATTN_PTR(lse);
   ATTN_OPT_PTR(key_mask);
   ATTN_TRY(check_ws(ATTN_OP_FWD, s, ws, ws_bytes));
-  if (s->D == 512) {
-    if (key_mask) return ATTN_ERR_UNSUPPORTED;
-    return ATTN_ERR_UNSUPPORTED;   // the D = 512 kernel is dispatched below once built
-  }
   cudaStream_t st = (cudaStream_t)stream;
+  if (s->D == 512) {
+    if (key_mask) return ATTN_ERR_UNSUPPORTED;   // the 512-wide kernel is built without a key mask
+    FwdBigParams p;
+    std::memset(&p, 0, sizeof(p));
+    const long long rq = (long long)s->B * s->H * s->Sq, rk = (long long)s->B * s->H * s->Skv;
+    if (!make_tmap(&p.tm_q, q, rq, 512, s->dtype) || !make_tmap(&p.tm_k, k, rk, 512, s->dtype) ||
+        !make_tmap(&p.tm_v, v, rk, 512, s->dtype))
+      return ATTN_ERR_CUDA;
+    p.out = out;
+    p.lse = lse;
+    p.bm_tiles = bm ? bm->tiles : nullptr;
+    if (bm) bm_strides(s, bm, p.bm_sb, p.bm_sh);
+    p.bm_mod = bm ? (int)bm->mask_mod : 0;
+    p.visited = debug_visited;
+    p.status = at<int>(ws, 0);
+    p.B = s->B;
+    p.H = s->H;
+    p.Sq = s->Sq;
+    p.Skv = s->Skv;
+    p.nqb = s->Sq / 128;
+    p.nkb = s->Skv / 128;
+    p.sc = scale * kLog2e;
+    p.timeout_ns = timeout_ns();
+    return cuda_status(launch_fwd_d512(p, s->dtype == ATTN_BF16, (int)mod, st));
+  }
   const WsLayout w = layout(ATTN_OP_FWD, s);
   if (s->dtype == ATTN_F32) {
     SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
@@ -307,6 +334,7 @@ attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const vo
   p.npairs = (p.nqb + 1) / 2;
   p.sc = scale * kLog2e;
   p.timeout_ns = timeout_ns();
+  p.inject_stall = inject_stall();
   return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
@@ -438,6 +466,7 @@ attn_status attn_decode(const attn_shape* s, const void* q, const void* k, const
   p.key_mask = key_mask;
   p.partial = at<float>(ws, w.partial);
   p.counter = at<unsigned>(ws, w.counter);
+  p.status = at<int>(ws, 0);
   p.B = s->B;
   p.H = s->H;
   p.Skv = s->Skv;

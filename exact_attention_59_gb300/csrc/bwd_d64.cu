@@ -5,6 +5,8 @@
 // forward).  Here the backward is written out, recomputing P from the saved
 // lse instead of storing it (FlashAttention-2 style):
 //   P = 2^(S scale log2e + bias log2e - lse log2e),  dV = P^T dO,
+//   (the preprocess stores -lse log2e and -D, so P and dS cost one FFMA and one
+//   FADD + FMUL per pair of scores with the packed f32x2 instructions),
 //   dP = dO V^T,  dS = P o (dP - D),  D_i = rowsum(dO o O),
 //   dQ = scale dS K,  dK = scale dS^T Q.
 // Two passes, no atomics (bitwise reproducible):
@@ -38,20 +40,6 @@ DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
-}
-
-// Logit in log2 units of one score, -inf where masked.  q, kv: global indices.
-template <int MOD>
-DEVI float logit2(float s, float sc, float slope2, int q, int kv, bool causal) {
-  float x;
-  if constexpr (MOD == MOD_ALIBI)
-    x = fmaf(s, sc, slope2 * float(kv - q));
-  else if constexpr (MOD == MOD_CHECKER)
-    x = fmaf(s, sc, ((q + kv) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e);
-  else
-    x = s * sc;
-  if (causal && kv > q) x = -INFINITY;
-  return x;
 }
 
 // A operand of a K = 128 product whose 16-bit values sit in TMEM columns
@@ -147,7 +135,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         bulk_load(smem_u32(sm.delta[s]), p.delta + row, 512, fb);
         last_u[s] = u;
       }
-      if (sm.abort) {
+      {   // every copy issued has landed before the CTA exits (instant unless aborted)
         drain(kvb, 0, p.timeout_ns);
         for (int s = 0; s < BWD_NST; ++s)
           if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
@@ -219,6 +207,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 13 + w};
     const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+    const uint64_t scv = f2(p.sc, p.sc);
+    // A padded key's dK and dV rows are zero.  Its P^T and dS^T rows are not masked
+    // here: row r of an MMA result depends on row r of its A operand only, so
+    // those rows stay confined to the padded key and the epilogue writes zeros.
     bool my_key = true;
     if (p.km_bits) my_key = (__ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + (kv >> 5)) >> (kv & 31)) & 1u;
     bool ok = true;
@@ -226,48 +218,58 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       const int s = u % BWD_NST;
       const int qb = sm.list[u];
       const uint8_t f = sm.lflags[u];
-      const bool causal = (MOD == MOD_CAUSAL) || ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-      const bool dead = (f & KB_KEYMASK) && !my_key;
+      const int q0 = qb * 128 + 64 * w;   // first query of this half
+      const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
+                          ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
       if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
+      uint32_t rr[64];
+      tmem_ld64(tS, rr);
+      const float* nl = &sm.lse2[s][64 * w];
+      uint64_t chk = 0;
+      if constexpr (MOD == MOD_CHECKER) {
+        const float hb = ((kv + q0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
+        chk = f2(hb, -hb);
+      }
+      const float abase = (MOD == MOD_ALIBI) ? slope2 * float(kv - q0) : 0.f;
       float pr[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t rr[32];
-        tmem_ld32(tS + 32 * j, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int cidx = 64 * w + 32 * j + i;
-          const int q = qb * 128 + cidx;
-          const float x = logit2<MOD>(__uint_as_float(rr[i]), p.sc, slope2, q, kv, causal);
-          pr[32 * j + i] = dead ? 0.f : ex2(x - sm.lse2[s][cidx]);
+      for (int i = 0; i < 32; ++i) {
+        uint64_t xv = ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv,
+                            *reinterpret_cast<const uint64_t*>(nl + 2 * i));
+        if constexpr (MOD == MOD_CHECKER) xv = fadd2(xv, chk);
+        if constexpr (MOD == MOD_ALIBI)
+          xv = fadd2(xv, f2(fmaf(-slope2, float(2 * i), abase), fmaf(-slope2, float(2 * i + 1), abase)));
+        float x0, x1;
+        unf2(xv, x0, x1);
+        if (causal) {
+          if (kv > q0 + 2 * i) x0 = -INFINITY;
+          if (kv > q0 + 2 * i + 1) x1 = -INFINITY;
         }
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        pr[2 * i] = p0;
+        pr[2 * i + 1] = p1;
+        pk[i] = pack2<BF16>(p0, p1);
       }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(pr[2 * i], pr[2 * i + 1]);
-        tmem_st32(tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w, pk);
-      }
+      tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.pready));
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tP = tmem + lane_off + C_DP + 64 * w;
+      tmem_ld64(tP, rr);
+      const float* nd = &sm.delta[s][64 * w];
       uint32_t dsk[32];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t rr[32];
-        tmem_ld32(tP + 32 * j, rr);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c0 = 32 * j + 2 * i;
-          const float d0 = pr[c0] * (__uint_as_float(rr[2 * i]) - sm.delta[s][64 * w + c0]);
-          const float d1 = pr[c0 + 1] * (__uint_as_float(rr[2 * i + 1]) - sm.delta[s][64 * w + c0 + 1]);
-          dsk[16 * j + i] = pack2<BF16>(d0, d1);
-        }
+      for (int i = 0; i < 32; ++i) {
+        const uint64_t dd = fadd2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])),
+                                  *reinterpret_cast<const uint64_t*>(nd + 2 * i));
+        float d0, d1;
+        unf2(fmul2(f2(pr[2 * i], pr[2 * i + 1]), dd), d0, d1);
+        dsk[i] = pack2<BF16>(d0, d1);
       }
       tmem_st32(tP, dsk);
       tmem_st_wait();
@@ -281,20 +283,20 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       else tc_fence_after();
     }
     if (ok) {
-      const float mul = w == 0 ? 1.f : p.scale;
-      uint32_t o[32];
+      const float mul = (w == 0 ? 1.f : p.scale) * (my_key ? 1.f : 0.f);
+      uint32_t rr[64], o[32];
+      if (N > 0) {
+        tmem_ld64(tmem + lane_off + (w == 0 ? C_DV : C_DK), rr);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t rr[32];
-        if (N > 0) {
-          tmem_ld32(tmem + lane_off + (w == 0 ? C_DV : C_DK) + 32 * j, rr);
-        } else {
+        for (int i = 0; i < 64; ++i) rr[i] = 0u;
+      }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          o[16 * j + i] = pack2<BF16>(__uint_as_float(rr[2 * i]) * mul, __uint_as_float(rr[2 * i + 1]) * mul);
+      for (int i = 0; i < 32; ++i) {
+        // multiply, not select: a padded key's rows may hold any finite value
+        const float a0 = my_key ? __uint_as_float(rr[2 * i]) * mul : 0.f;
+        const float a1 = my_key ? __uint_as_float(rr[2 * i + 1]) * mul : 0.f;
+        o[i] = pack2<BF16>(a0, a1);
       }
       uint16_t* base = reinterpret_cast<uint16_t*>(w == 0 ? p.dv : p.dk);
       uint4* dst = reinterpret_cast<uint4*>(base + ((size_t)bh * p.Skv + kv) * 64);
@@ -314,6 +316,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
 struct __align__(1024) DqSmem {
   uint8_t q[BWD_TILE], dO[BWD_TILE];
   uint8_t k[BWD_NST][BWD_TILE], v[BWD_NST][BWD_TILE];
+  float cb[BWD_NST][128];   // per-stage key bias (0 or -inf), built by the producer warp
   uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull[2], dpfull, dsready, done;
   uint32_t tmem_base;
   int abort;
@@ -370,28 +373,43 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   constexpr uint32_t C_SB = 0, C_DP = 256, C_DQ = 384;
 
   if (warp == 0) {
-    if (lane == 0 && N > 0) {
+    if (N > 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 21};
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      tma_prefetch_desc(&p.tm_do);
       const uint32_t qbar = smem_u32(&sm.qfull);
-      mbar_expect_tx(qbar, 2 * BWD_TILE);
-      tma_load_2d(smem_u32(sm.q), &p.tm_q, qbar, 0, bh * p.Sq + qb * 128);
-      tma_load_2d(smem_u32(sm.dO), &p.tm_do, qbar, 0, bh * p.Sq + qb * 128);
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+        mbar_expect_tx(qbar, 2 * BWD_TILE);
+        tma_load_2d(smem_u32(sm.q), &p.tm_q, qbar, 0, bh * p.Sq + qb * 128);
+        tma_load_2d(smem_u32(sm.dO), &p.tm_do, qbar, 0, bh * p.Sq + qb * 128);
+      }
       int last_u[BWD_NST] = {-1, -1, -1};
       for (int u = 0; u < N; ++u) {
         const int s = u % BWD_NST;
-        if (u >= BWD_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
+        if (u >= BWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
         const int kb = sm.list[u];
-        const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_expect_tx(fb, 2 * BWD_TILE);
-        tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
-        tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
+        if (p.km_bits) {   // lane owns columns 4 lane .. 4 lane + 3
+          uint32_t bits = 0xffffffffu;
+          if (sm.lflags[u] & KB_KEYMASK)
+            bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = 4 * lane + i;
+            sm.cb[s][col] = ((bits >> (col & 31)) & 1u) ? 0.f : -INFINITY;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&sm.full[s]);
+          mbar_expect_tx(fb, 2 * BWD_TILE);   // release: the table above is visible to its waiters
+          tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
+          tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
+        }
         last_u[s] = u;
       }
-      if (sm.abort) {
+      if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
         drain(qbar, 0, p.timeout_ns);
         for (int s = 0; s < BWD_NST; ++s)
           if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
@@ -453,49 +471,59 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 23 + w};
     const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
-    const float l2 = p.lse2[(size_t)bh * p.Sq + q];
-    const float dl = p.delta[(size_t)bh * p.Sq + q];
+    const float nl2 = p.lse2[(size_t)bh * p.Sq + q];   // -lse log2(e)
+    const float nd = p.delta[(size_t)bh * p.Sq + q];   // -D
+    const uint64_t scv = f2(p.sc, p.sc), nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
+    const bool use_table = p.km_bits != nullptr;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
+      const int s = u % BWD_NST;
       const int kb = sm.list[u];
       const uint8_t f = sm.lflags[u];
-      const bool causal = (MOD == MOD_CAUSAL) || ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-      uint32_t kw[2] = {0xffffffffu, 0xffffffffu};
-      if (f & KB_KEYMASK) {
-        const uint32_t* wp = p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 64 * w) >> 5);
-        kw[0] = __ldg(wp);
-        kw[1] = __ldg(wp + 1);
-      }
+      const int k0 = kb * 128 + 64 * w;   // first key of this half
+      const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
+                          ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
       if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
+      // the stage's key-bias table was written before its full barrier was armed
+      if (use_table && !wait_warp(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
+      uint32_t rr[64];
+      tmem_ld64(tS, rr);
+      const float* tb = &sm.cb[s][64 * w];
+      uint64_t chk = 0;
+      if constexpr (MOD == MOD_CHECKER) {
+        const float hb = ((q + k0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
+        chk = f2(hb, -hb);
+      }
+      const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
       float pr[64];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t rr[32];
-        tmem_ld32(tS + 32 * j, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int kv = kb * 128 + 64 * w + 32 * j + i;
-          float x = logit2<MOD>(__uint_as_float(rr[i]), p.sc, slope2, q, kv, causal);
-          if (!((kw[j] >> i) & 1u)) x = -INFINITY;
-          pr[32 * j + i] = ex2(x - l2);
+      for (int i = 0; i < 32; ++i) {
+        uint64_t add = nl2v;
+        if (use_table) add = fadd2(add, *reinterpret_cast<const uint64_t*>(tb + 2 * i));
+        if constexpr (MOD == MOD_CHECKER) add = fadd2(add, chk);
+        if constexpr (MOD == MOD_ALIBI)
+          add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
+        float x0, x1;
+        unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
+        if (causal) {
+          if (k0 + 2 * i > q) x0 = -INFINITY;
+          if (k0 + 2 * i + 1 > q) x1 = -INFINITY;
         }
+        pr[2 * i] = ex2(x0);
+        pr[2 * i + 1] = ex2(x1);
       }
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tP = tmem + lane_off + C_DP + 64 * w;
+      tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
       uint32_t dsk[32];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t rr[32];
-        tmem_ld32(tP + 32 * j, rr);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c0 = 32 * j + 2 * i;
-          dsk[16 * j + i] = pack2<BF16>(pr[c0] * (__uint_as_float(rr[2 * i]) - dl),
-                                        pr[c0 + 1] * (__uint_as_float(rr[2 * i + 1]) - dl));
-        }
+      for (int i = 0; i < 32; ++i) {
+        float d0, d1;
+        unf2(fmul2(f2(pr[2 * i], pr[2 * i + 1]), fadd2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), ndv)),
+             d0, d1);
+        dsk[i] = pack2<BF16>(d0, d1);
       }
       tmem_st32(tS, dsk);   // dS over this half's S columns [64 w, 64 w + 32)
       tmem_st_wait();
@@ -509,21 +537,16 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         else tc_fence_after();
       }
       if (ok) {
-        uint32_t o[32];
+        uint32_t rr[64], o[32];
+        if (N > 0) {
+          tmem_ld64(tmem + lane_off + C_DQ, rr);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t rr[32];
-          if (N > 0) {
-            tmem_ld32(tmem + lane_off + C_DQ + 32 * j, rr);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = 0u;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            o[16 * j + i] =
-                pack2<BF16>(__uint_as_float(rr[2 * i]) * p.scale, __uint_as_float(rr[2 * i + 1]) * p.scale);
+          for (int i = 0; i < 64; ++i) rr[i] = 0u;
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o[i] = pack2<BF16>(__uint_as_float(rr[2 * i]) * p.scale, __uint_as_float(rr[2 * i + 1]) * p.scale);
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dq) + ((size_t)bh * p.Sq + q) * 64);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);

@@ -26,8 +26,8 @@ constexpr uint8_t KB_KEYMASK = 4;  // some keys of the kv block are padding: tes
 //   [0, 256)            status word (int32 at offset 0) + reserved
 //   key-mask bits       uint32 (B, Skv/32)         if a key mask may be given
 //   key-mask summary    uint8  (B, ceil(Skv/128))  0 = no key kept, 1 = some, 2 = all
-//   bwd: delta          float  (B, H, Sq)          D_i = rowsum(dO * O)
-//   bwd: lse2           float  (B, H, Sq)          lse * log2(e), +inf for empty rows
+//   bwd: delta          float  (B, H, Sq)          -D_i = -rowsum(dO * O)
+//   bwd: lse2           float  (B, H, Sq)          -lse * log2(e), -inf for empty rows
 //   decode: partials    float  (B*H, nsplit, D + 2)
 //   decode: counters    uint32 (B*H)
 struct WsLayout {

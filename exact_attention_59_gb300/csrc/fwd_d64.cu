@@ -30,6 +30,7 @@ struct __align__(1024) FwdSmem {
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
   uint64_t full[FWD_NST], empty[FWD_NST];
   uint64_t qfull, sfull[2], pready[2], odone[2], fin;
+  float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
   uint32_t tmem_base;
   int abort;
   uint8_t flags[2][FWD_MAXKB];
@@ -96,36 +97,64 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
+  constexpr bool kTableMod = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
+  const bool use_table = kTableMod || p.km_bits != nullptr;
   if (warp == 0) {
-    // ======================= TMA producer =======================
+    // ======================= TMA producer (lane 0) + bias tables (all lanes) =======================
+    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
+    const uint32_t qbar = smem_u32(&sm.qfull);
     if (lane == 0) {
-      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      const uint32_t qbar = smem_u32(&sm.qfull);
       mbar_expect_tx(qbar, (valid1 ? 2 : 1) * FWD_TILE_BYTES);
       tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, qbar, 0, bh * p.Sq + qt0 * 128);
       if (valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, qbar, 0, bh * p.Sq + qt1 * 128);
-      int last_u[FWD_NST];
-      for (int s = 0; s < FWD_NST; ++s) last_u[s] = -1;
-      int u = 0;
-      for (int kb = 0; kb < p.nkb; ++kb) {
-        if (!((sm.flags[0][kb] | sm.flags[1][kb]) & KB_VISIT)) continue;
-        const int s = u % FWD_NST;
-        if (u >= FWD_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) break;
+    }
+    const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+    int last_u[FWD_NST];
+    for (int s = 0; s < FWD_NST; ++s) last_u[s] = -1;
+    int u = 0;
+    for (int kb = 0; kb < p.nkb; ++kb) {
+      const uint8_t fu = sm.flags[0][kb] | sm.flags[1][kb];
+      if (!(fu & KB_VISIT)) continue;
+      const int s = u % FWD_NST;
+      if (u >= FWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) break;
+      if (use_table) {
+        // lane owns columns 4 lane .. 4 lane + 3 of this kv block
+        uint32_t bits = 0xffffffffu;
+        if (p.km_bits && (fu & KB_KEYMASK)) bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int col = 4 * lane + i;
+          float base = ((bits >> (col & 31)) & 1u) ? 0.f : -INFINITY;
+          if constexpr (MOD == MOD_ALIBI) base += slope2 * float(col);
+          float e = base, o = base;
+          if constexpr (MOD == MOD_CHECKER) {
+            const float hb = (col & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // row parity 0
+            e = base + hb;
+            o = base - hb;
+          }
+          sm.cb[s][0][col] = e;
+          sm.cb[s][1][col] = o;
+        }
+      }
+      __syncwarp();
+      // test hook: withhold the first copy so the consumers' bounded waits run out
+      const bool withhold = p.inject_stall && u == 0;
+      if (lane == 0 && !withhold) {
         const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_expect_tx(fb, 2 * FWD_TILE_BYTES);
+        mbar_expect_tx(fb, 2 * FWD_TILE_BYTES);   // release: the tables above are visible to its waiters
         tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
         tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
-        last_u[s] = u;
-        ++u;
       }
-      if (sm.abort) {   // let the copies in flight land before the CTA exits
-        drain_wait(qbar, 0, p.timeout_ns);
-        for (int s = 0; s < FWD_NST; ++s)
-          if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / FWD_NST) & 1, p.timeout_ns);
-      }
+      if (!withhold) last_u[s] = u;
+      ++u;
+    }
+    if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
+      drain_wait(qbar, 0, p.timeout_ns);
+      for (int s = 0; s < FWD_NST; ++s)
+        if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / FWD_NST) & 1, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -199,89 +228,103 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       const int row = 32 * quad + lane;
       const int q = qt * 128 + row;
       const bool writer = (quad == ((2 + 4 * t) & 3)) && lane == 0;   // first warp of the group
-      const float sc = p.sc;
-      float slope2 = 0.f, cb_even = 0.f;
-      if constexpr (MOD == MOD_ALIBI) slope2 = alibi_slope_log2(h, p.H);
-      if constexpr (MOD == MOD_CHECKER) cb_even = (q & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;
-      float m = -INFINITY, l = 0.f;
+      const uint64_t scv = f2(p.sc, p.sc);
+      const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+      const int parity = (MOD == MOD_CHECKER) ? (q & 1) : 0;
+      float m_run = -INFINITY, l = 0.f;
       uint32_t n = 0;
+      int u = 0;
       bool ok = true;
       for (int kb = 0; kb < p.nkb; ++kb) {
         const uint8_t f = sm.flags[t][kb];
+        const bool in_union = (f | sm.flags[t ^ 1][kb]) & KB_VISIT;
         if (p.visited && writer)
           p.visited[((size_t)bh * p.nqb + qt) * p.nkb + kb] = (f & KB_VISIT) ? 1 : 0;
-        if (!(f & KB_VISIT)) continue;
+        if (!(f & KB_VISIT)) {
+          u += in_union ? 1 : 0;
+          continue;
+        }
+        const int s = u % FWD_NST;
+        ++u;
         if (!wait_warp(smem_u32(&sm.sfull[t]), n & 1, c)) { ok = false; break; }
+        // the stage's bias table was written before its full barrier was armed
+        if (use_table && !wait_warp(smem_u32(&sm.full[s]), ((u - 1) / FWD_NST) & 1, c)) { ok = false; break; }
         tc_fence_after();
-        float s[128];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t r[32];
-          tmem_ld32(tS + 32 * j, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * j + i] = __uint_as_float(r[i]);
-        }
-        // logits in log2 units, masks as -inf
+        uint32_t r[128];
+        tmem_ld128(tS, r);
         const int kv0 = kb * 128;
-        const bool causal = (MOD == MOD_CAUSAL) || ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-        const int lim = q - kv0;   // keep column c iff c <= lim (causal)
-        uint32_t kw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-        if (f & KB_KEYMASK) {
-          const uint32_t* wp = p.km_bits + (size_t)b * (p.Skv >> 5) + (kv0 >> 5);
+        const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128) ||
+                            ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+        const int lim = q - kv0;   // keep column cc iff cc <= lim
+        const float* tb = sm.cb[s][parity];
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) kw[j] = __ldg(wp + j);
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < 128; ++cc) {
-          float x;
-          if constexpr (MOD == MOD_ALIBI)
-            x = fmaf(s[cc], sc, slope2 * float(kv0 - q + cc));
-          else if constexpr (MOD == MOD_CHECKER)
-            x = fmaf(s[cc], sc, (cc & 1) ? -cb_even : cb_even);
+        for (int i = 0; i < 64; ++i) {
+          const uint64_t sv = f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          uint64_t xv;
+          if (use_table)
+            xv = ffma2(sv, scv, *reinterpret_cast<const uint64_t*>(tb + 2 * i));
           else
-            x = s[cc] * sc;
-          if (causal && cc > lim) x = -INFINITY;
-          if (!((kw[cc >> 5] >> (cc & 31)) & 1u)) x = -INFINITY;
-          s[cc] = x;
-          mx = fmaxf(mx, x);
+            xv = fmul2(sv, scv);
+          float x0, x1;
+          unf2(xv, x0, x1);
+          if (causal) {
+            if (2 * i > lim) x0 = -INFINITY;
+            if (2 * i + 1 > lim) x1 = -INFINITY;
+          }
+          r[2 * i] = __float_as_uint(x0);
+          r[2 * i + 1] = __float_as_uint(x1);
+          mx[i & 3] = fmax3(mx[i & 3], x0, x1);
         }
-        const float m_new = fmaxf(m, mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2(m - m_use);
-        float sum = 0.f;
+        // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
+        // per-score work: scores here are x' = x - base
+        const float base = (MOD == MOD_ALIBI) ? slope2 * float(kv0 - q) : 0.f;
+        const float rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) + base;
+        // stale running max: rescale O only when the max grows by more than 2^8
+        float alpha = 1.f;
+        bool resc = false;
+        if (m_run == -INFINITY) {
+          m_run = rowmax;   // O holds only zero rows so far
+        } else if (rowmax > m_run + 8.f) {
+          alpha = ex2(m_run - rowmax);
+          m_run = rowmax;
+          resc = true;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const uint64_t negm = f2(base - m_use, base - m_use);
+        uint64_t sumv[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+        uint32_t pk[64];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t pk[32];
+        for (int i = 0; i < 64; ++i) {
+          float d0, d1;
+          unf2(fadd2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), negm), d0, d1);
+          const float p0 = ex2(d0), p1 = ex2(d1);
+          sumv[i & 1] = fadd2(sumv[i & 1], f2(p0, p1));
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st64(tS, pk);
+        // S_t(n) complete implies P_t(n-1) V complete (same issuing thread, in order),
+        // so O can be rescaled here without another wait
+        if (__any_sync(0xffffffffu, resc)) {
+          uint32_t o[64];
+          tmem_ld64(tO, o);
+          const uint64_t av = f2(alpha, alpha);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = ex2(s[64 * j + 2 * i] - m_use);
-            const float p1 = ex2(s[64 * j + 2 * i + 1] - m_use);
-            sum += p0 + p1;
-            pk[i] = pack2<BF16>(p0, p1);
+            float a0, a1;
+            unf2(fmul2(f2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), av), a0, a1);
+            o[2 * i] = __float_as_uint(a0);
+            o[2 * i + 1] = __float_as_uint(a1);
           }
-          tmem_st32(tS + 32 * j, pk);
-        }
-        if (n > 0) {
-          // O_t must hold the previous P V before it is rescaled
-          if (!wait_warp(smem_u32(&sm.odone[t]), (n - 1) & 1, c)) { ok = false; break; }
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              uint32_t r[32];
-              tmem_ld32(tO + 32 * j, r);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(tO + 32 * j, r);
-            }
-          }
+          tmem_st64(tO, o);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.pready[t]));
-        l = l * alpha + sum;
-        m = m_new;
+        float s0, s1, s2, s3;
+        unf2(sumv[0], s0, s1);
+        unf2(sumv[1], s2, s3);
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
         ++n;
       }
       tmem_st_wait();
@@ -293,24 +336,20 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       }
       if (ok) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint32_t o[32];
+        uint32_t o[64], w[32];
+        if (n > 0) {
+          tmem_ld64(tO, o);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t r[32];
-          if (n > 0) {
-            tmem_ld32(tO + 32 * j, r);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            o[16 * j + i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+          for (int i = 0; i < 64; ++i) o[i] = 0u;
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((size_t)bh * p.Sq + q) * 64);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        const float m_fin = (m == -INFINITY) ? 0.f : m;
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
         p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (m_fin + lg2(l)) * kLn2 : -INFINITY;
       }
     }

@@ -26,6 +26,7 @@ struct FwdParams {
   int B, H, Sq, Skv, nqb, nkb, npairs;
   float sc;                       // scale * log2(e)
   unsigned long long timeout_ns;
+  int inject_stall;               // test hook: the producer withholds the first K/V copy
 };
 size_t fwd_d64_smem_bytes();
 cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t st);
@@ -47,15 +48,13 @@ struct FwdBigParams {
 cudaError_t launch_fwd_d512(const FwdBigParams& p, bool bf16, int mod, cudaStream_t st);
 
 // ---------------------------------------------------------------- backward, D = 64
-constexpr int BWD_THREADS = 384;
-
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 2-D views, box {64, 128}, 128B swizzle
   void* dq;
   void* dk;
   void* dv;
-  const float* delta;     // (B, H, Sq)
-  const float* lse2;      // (B, H, Sq), log2 units, +inf for rows with no kept key
+  const float* delta;     // (B, H, Sq): -D_i = -rowsum(dO o O)
+  const float* lse2;      // (B, H, Sq): -lse log2(e), -inf for rows with no kept key
   const uint32_t* km_bits;
   const uint8_t* km_sum;
   const uint8_t* bm_tiles;
@@ -76,7 +75,7 @@ cudaError_t launch_keymask_pack(const uint8_t* km, int B, int Skv, uint32_t* bit
                                 cudaStream_t st);
 cudaError_t launch_build_block_mask(int mask_mod, int B, int H, int Sq, int Skv, int bq, int bkv, uint8_t* tiles,
                                     cudaStream_t st);
-// delta = rowsum(dout * out) (f32), lse2 = lse * log2(e) (+inf where lse = -inf)
+// delta = -rowsum(dout * out) (f32), lse2 = -lse * log2(e) (-inf where lse = -inf)
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, int dtype, long long rows,
                                   int D, float* delta, float* lse2, cudaStream_t st);
 
@@ -90,6 +89,7 @@ struct DecodeParams {
   const uint8_t* key_mask;   // (B, Skv) or nullptr
   float* partial;            // (B*H, nsplit, 2 + 64): m, l, o[64]
   unsigned* counter;         // (B*H)
+  int* status;               // workspace status word, or nullptr
   int B, H, Skv, nsplit, keys_per_split;
   float sc;
   int mod;

@@ -3,7 +3,8 @@
 //     kv block) summary that lets whole 128-key blocks be skipped or kept;
 //   * the block-mask builder (the analogue of create_block_mask(mask_mod, B, H,
 //     Sq, Skv) in the flaxattention README "Example usage");
-//   * the backward preprocess: D_i = sum_d dO_id O_id, and lse in log2 units.
+//   * the backward preprocess: -D_i = -sum_d dO_id O_id and -lse_i log2(e)
+//     (-inf for rows with no kept key), negated so the passes use one FFMA.
 #include "kernels.h"
 
 namespace attn {
@@ -116,9 +117,9 @@ __global__ void bwd_preprocess_kernel(const T* __restrict__ out, const T* __rest
   }
   for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (row < rows && part == 0) {
-    delta[row] = acc;
+    delta[row] = -acc;
     const float l = lse[row];
-    lse2[row] = (l == -INFINITY) ? INFINITY : l * kLog2e;
+    lse2[row] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
   }
 }
 

@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(128) simt_bwd_dkdv_kernel(const SimtParams p) 
           dp = fmaf(dos[i][d], vrow[threadIdx.x][d], dp);
         }
         const float x = simt_logit(p, dot * p.sc, h, qi, kj, f, keep, slope2);
-        const float pij = exp2f(x - ls[i]);
-        const float dsij = pij * (dp - ds_[i]);
+        const float pij = exp2f(x + ls[i]);
+        const float dsij = pij * (dp + ds_[i]);
 #pragma unroll
         for (int d = 0; d < SIMT_D; ++d) {
           dv[d] = fmaf(pij, dos[i][d], dv[d]);
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(128) simt_bwd_dq_kernel(const SimtParams p) {
           dp = fmaf(dorow[threadIdx.x][d], vs[j][d], dp);
         }
         const float x = simt_logit(p, dot * p.sc, h, qi, kv0 + c0 + j, f, kk[c0 + j], slope2);
-        const float pij = exp2f(x - l2);
-        const float dsij = pij * (dp - dl);
+        const float pij = exp2f(x + l2);
+        const float dsij = pij * (dp + dl);
 #pragma unroll
         for (int d = 0; d < SIMT_D; ++d) dq[d] = fmaf(dsij, ks[j][d], dq[d]);
       }

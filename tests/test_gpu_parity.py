@@ -36,8 +36,7 @@ def _oracle_bm(bm_kind, B, H, Sq, Skv):
 
 
 def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", backward=True, heads=None,
-                  check_det=True, key_mask_override=None, strict=False):
-    D = 64
+                  check_det=True, key_mask_override=None, strict=False, D=64):
     c, d = make_dev(B, H, Sq, Skv, D, dtype, key_mask=key_mask, dout=dout)
     if key_mask_override is not None:
         c["key_mask"] = key_mask_override.clone()
@@ -90,7 +89,7 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
         out2, lse2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod)
         assert torch.equal(out2.view(torch.uint8), out.view(torch.uint8)), "forward not bitwise reproducible"
         assert torch.equal(lse2.view(torch.uint8), lse.view(torch.uint8)), "lse not bitwise reproducible"
-        if backward:
+        if backward and D == 64:
             g2 = E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
                             score_mod=mod)
             for a, (_, b_) in zip(g2, grads):
@@ -193,3 +192,52 @@ def test_block_mask_builder(Sq, Skv, mm):
     bm = E.create_block_mask(mm, 2, 3, Sq, Skv)
     ref = OR.build_block_mask(mm, 2, 3, Sq, Skv)
     np.testing.assert_array_equal(bm.tiles.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------- head dim 512 (forward)
+
+D512 = [(B, H, S, dt, mod, bmk)
+        for (B, H, S) in [(1, 2, 256), (2, 1, 640)]
+        for dt in ("bf16", "f16")
+        for mod in ("none", "alibi", "checkerboard", "causal")
+        for bmk in (None, "causal")]
+
+
+@pytest.mark.parametrize("B,H,S,dtype,mod,bm", D512)
+def test_d512_forward_variants(B, H, S, dtype, mod, bm):
+    run_and_check(B, H, S, S, dtype, mod, False, bm, backward=False, D=512)
+
+
+def test_d512_rectangular():
+    run_and_check(1, 2, 128, 1024, "bf16", "alibi", False, None, backward=False, D=512)
+    run_and_check(1, 1, 384, 128, "bf16", "none", False, None, backward=False, D=512)
+
+
+@pytest.mark.slow
+def test_long_context_d512_sampled_rows():
+    """1 x 2 x 131072 x 512 bf16, causal block mask: 32 seeded rows per head (0 and Sq-1 included)."""
+    w = W.LONG_CAUSAL_BF16
+    c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, dout=None)
+    d = {k: v.cuda() for k, v in c.items() if v is not None}
+    bm = E.create_block_mask("causal", 1, 1, w.Sq, w.Skv)
+    out, lse = E.attn_fwd(d["q"], d["k"], d["v"], block_mask=bm)
+    torch.cuda.synchronize()
+    obm = OR.BlockMask(OR.build_block_mask("causal", 1, 1, w.Sq, w.Skv), "causal")
+    tol = TOL["bf16"]
+    for h in range(w.H):
+        rows = IN.sample_rows(w.Sq, 32, seed=IN.SEED + 5 + h).numpy()
+        q64 = f64(c["q"][:, h:h + 1, rows])
+        k64, v64 = f64(c["k"][:, h:h + 1]), f64(c["v"][:, h:h + 1])
+        # the oracle computes just these rows over all keys (q_idx = the sampled positions)
+        o_ref, l_ref = _rows_oracle(q64, k64, v64, rows, obm)
+        compare(f"out h{h}", f64(out[:, h:h + 1, rows]), o_ref, tol["o_max"], tol["o_mean"])
+        compare(f"lse h{h}", f64(lse[:, h:h + 1, rows]), l_ref, tol["lse_max"])
+
+
+def _rows_oracle(q_rows, k, v, rows, obm):
+    """Oracle on selected query rows: place them at their positions of a sparse query tensor."""
+    Sq = obm.tiles.shape[2] * obm.block_q
+    qfull = np.zeros((1, 1, Sq, q_rows.shape[-1]))
+    qfull[0, 0, rows] = q_rows[0, 0]
+    o, l = OR.attn_fwd(qfull, k, v, block_mask=obm, rows=rows)
+    return o[:, :, rows], l[:, :, rows]
