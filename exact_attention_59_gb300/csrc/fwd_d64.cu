@@ -11,15 +11,18 @@
 // their kv-block lists once:
 //   warp 0      TMA producer: both Q tiles once, then K and V tiles of each kv
 //               block into a 3-stage ring (128B swizzle, 16 KB per tile).
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//               S_t = Q_t K^T (128x128, f32 in TMEM), then O_t += P_t V with P_t
-//               read from TMEM (written there by the softmax warps over S_t).
-//   warps 2-5   softmax of tile 0, warps 6-9 softmax of tile 1: one thread per
+//   warps 1-2   warp 1 allocates 512 TMEM columns; lane 0 of warp 1 + t issues
+//               tile t's tcgen05.mma: S_t = Q_t K^T (128x128, f32 in TMEM) and
+//               O_t += P_t V with P_t read from TMEM.  Two issuing threads keep
+//               the tensor pipe busier than one (each instruction has a fixed
+//               issue cost), and S_t(n+1) is issued as soon as the softmax has
+//               copied S_t(n) to registers, so it overlaps the exponentials.
+//   warps 3-6   softmax of tile 0, warps 7-10 softmax of tile 1: one thread per
 //               query row (TMEM lane), 128 scores per kv block in registers,
 //               running max/sum per thread, P packed to 16-bit into TMEM,
 //               O rescaled in TMEM when the row max grows, then the epilogue.
-// TMEM columns: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384).
-// While tile 0's softmax runs, the tensor core computes tile 1's S (ping-pong).
+// TMEM columns per tile t: S [256t, 256t+128), P [256t+128, 256t+192),
+// O [256t+192, 256t+256).
 #include "kernels.h"
 
 namespace attn {
@@ -29,7 +32,7 @@ struct __align__(1024) FwdSmem {
   uint8_t k[FWD_NST][FWD_TILE_BYTES];
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
   uint64_t full[FWD_NST], empty[FWD_NST];
-  uint64_t qfull, sfull[2], pready[2], odone[2], fin;
+  uint64_t qfull, sfull[2], sfree[2], pready[2], odone[2], fin[2];
   float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
   uint32_t tmem_base;
   int abort;
@@ -62,15 +65,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < FWD_NST; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), valid1 ? 2 : 1);   // one arrival per tile per kv block
     }
     mbar_init(smem_u32(&sm.qfull), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&sm.sfull[t]), 1);
+      mbar_init(smem_u32(&sm.sfree[t]), 128);
       mbar_init(smem_u32(&sm.pready[t]), 128);
       mbar_init(smem_u32(&sm.odone[t]), 1);
+      mbar_init(smem_u32(&sm.fin[t]), 1);
     }
-    mbar_init(smem_u32(&sm.fin), 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -157,77 +161,84 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / FWD_NST) & 1, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
-      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 2};
+  } else if (warp == 1 || warp == 2) {
+    // ======================= MMA issue, one thread per tile =======================
+    // Tile t's S_t(n+1) is issued as soon as its softmax has S_t(n) in registers
+    // (sfree), so the product overlaps the exponentials; P_t(n) V goes out when
+    // P_t(n) is in TMEM (pready).  Each tile arrives once per kv block on the
+    // stage's empty barrier: a commit after its P V, or a plain arrival for a
+    // block it skips.
+    const int t = warp - 1;
+    if (lane == 0 && (t == 0 || valid1)) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 2 + 16 * t};
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
-      int pend[2] = {-1, -1};
-      uint32_t npv[2] = {0, 0};
-      int uses[FWD_NST];
-      for (int s = 0; s < FWD_NST; ++s) uses[s] = 0;
+      const uint32_t tS = tmem + 256 * t, tP = tS + 128, tO = tS + 192;
+      const uint64_t qd = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
+      uint64_t dk_[FWD_NST], dv_[FWD_NST];
+      for (int s = 0; s < FWD_NST; ++s) {
+        dk_[s] = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
+        dv_[s] = sdesc_sw128(smem_u32(sm.v[s]), 8192, 1024);
+      }
+      uint32_t n = 0;        // S products issued for this tile
+      int s_pend = -1;       // stage of the block whose P V is still to issue
+      uint32_t j_pend = 0;   // that block's index among this tile's visited blocks
       bool ok = wait_one(smem_u32(&sm.qfull), 0, c);
-      if (ok) tc_fence_after();
-      auto issue_pv = [&](int t) -> bool {
-        if (!wait_one(smem_u32(&sm.pready[t]), npv[t] & 1, c)) return false;
+      auto issue_pv = [&]() -> bool {   // P_t(j_pend) V (stage s_pend), then release the stage
+        if (!wait_one(smem_u32(&sm.pready[t]), j_pend & 1, c)) return false;
         tc_fence_after();
-        const int s = pend[t];
-        const uint32_t d = tmem + 256 + t * 64;
-        const uint32_t a = tmem + t * 128;
-        const uint32_t vb = smem_u32(sm.v[s]);
+        const uint64_t vd = dv_[s_pend];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(d, a + kk * 8, sdesc_sw128(vb + kk * 2048, 8192, 1024), IDESC_PV, (kk > 0 || npv[t] > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tP + kk * 8, vd + 128 * kk, IDESC_PV, (kk > 0 || j_pend > 0) ? 1u : 0u);
         tc_commit(smem_u32(&sm.odone[t]));
-        ++npv[t];
-        if (--uses[s] == 0) tc_commit(smem_u32(&sm.empty[s]));
-        pend[t] = -1;
+        tc_commit(smem_u32(&sm.empty[s_pend]));
+        s_pend = -1;
         return true;
       };
       int u = 0;
       for (int kb = 0; ok && kb < p.nkb; ++kb) {
-        const bool in0 = sm.flags[0][kb] & KB_VISIT, in1 = sm.flags[1][kb] & KB_VISIT;
-        if (!in0 && !in1) continue;
+        const uint8_t f = sm.flags[t][kb];
+        if (!((f | sm.flags[t ^ 1][kb]) & KB_VISIT)) continue;
         const int s = u % FWD_NST;
-        if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
-        tc_fence_after();
-        uses[s] = int(in0) + int(in1);
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (pend[t] >= 0 && !issue_pv(t)) { ok = false; break; }
-          if (t == 0 ? in0 : in1) {
-            const uint32_t d = tmem + t * 128;
-            const uint32_t qa = smem_u32(sm.q[t]), kbse = smem_u32(sm.k[s]);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(d, sdesc_sw128(qa + kk * 32, 16, 1024), sdesc_sw128(kbse + kk * 32, 16, 1024), IDESC_S,
-                     kk > 0 ? 1u : 0u);
-            tc_commit(smem_u32(&sm.sfull[t]));
-            pend[t] = s;
-          }
+        if (!(f & KB_VISIT)) {
+          // not this tile's block: first let any pending P V go (its stage must not be held)
+          if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
+          if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
+          mbar_arrive(smem_u32(&sm.empty[s]));
+          ++u;
+          continue;
         }
+        if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
+        if (n > 0 && !wait_one(smem_u32(&sm.sfree[t]), (n - 1) & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kd = dk_[s];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tS, qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(smem_u32(&sm.sfull[t]));
+        if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
+        s_pend = s;
+        j_pend = n++;
         ++u;
       }
-      for (int t = 0; t < 2 && ok; ++t)
-        if (pend[t] >= 0 && !issue_pv(t)) ok = false;
-      // every MMA issued so far completes before the CTA lets go of TMEM
-      tc_commit(smem_u32(&sm.fin));
-      drain_wait(smem_u32(&sm.fin), 0, p.timeout_ns);
+      if (ok && s_pend >= 0 && !issue_pv()) ok = false;
+      // every MMA issued by this thread completes before the CTA lets go of TMEM
+      tc_commit(smem_u32(&sm.fin[t]));
+      drain_wait(smem_u32(&sm.fin[t]), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
     // ======================= softmax warpgroups =======================
-    const int t = (warp - 2) >> 2;
+    const int t = (warp - 3) >> 2;
     const int quad = warp & 3;   // TMEM lanes [32 quad, 32 quad + 32)
     const int qt = qt0 + t;
     if (qt < p.nqb) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 3 + t};
       const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
-      const uint32_t tS = tmem + lane_off + t * 128;
-      const uint32_t tO = tmem + lane_off + 256 + t * 64;
+      const uint32_t tS = tmem + lane_off + 256 * t;
+      const uint32_t tP = tS + 128, tO = tS + 192;
       const int row = 32 * quad + lane;
       const int q = qt * 128 + row;
-      const bool writer = (quad == ((2 + 4 * t) & 3)) && lane == 0;   // first warp of the group
+      const bool writer = quad == 3 && lane == 0;   // first warp of the group (warp 3 or 7)
       const uint64_t scv = f2(p.sc, p.sc);
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
       const int parity = (MOD == MOD_CHECKER) ? (q & 1) : 0;
@@ -252,6 +263,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         tc_fence_after();
         uint32_t r[128];
         tmem_ld128(tS, r);
+        // S_t(n) is in registers: the MMA thread may compute S_t(n+1) over it now
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.sfree[t]));
         const int kv0 = kb * 128;
         const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128) ||
                             ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
@@ -302,9 +316,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           sumv[i & 1] = fadd2(sumv[i & 1], f2(p0, p1));
           pk[i] = pack2<BF16>(p0, p1);
         }
-        tmem_st64(tS, pk);
-        // S_t(n) complete implies P_t(n-1) V complete (same issuing thread, in order),
-        // so O can be rescaled here without another wait
+        // P_t(n-1) V must be done with the P region (and with O, if it is rescaled)
+        if (n > 0) {
+          if (!wait_warp(smem_u32(&sm.odone[t]), (n - 1) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+        }
+        tmem_st64(tP, pk);
         if (__any_sync(0xffffffffu, resc)) {
           uint32_t o[64];
           tmem_ld64(tO, o);

@@ -8,7 +8,7 @@ namespace attn {
 
 // ---------------------------------------------------------------- forward, D = 64
 constexpr int FWD_NST = 3;
-constexpr int FWD_THREADS = 320;
+constexpr int FWD_THREADS = 352;   // warp 0 TMA, warps 1-2 MMA issue (one per tile), warps 3-10 softmax
 constexpr uint32_t FWD_TILE_BYTES = 128 * 64 * 2;
 constexpr int FWD_MAXKB = 2048;   // Skv <= 262144
 
