@@ -33,17 +33,47 @@ struct __align__(1024) FwdSmem {
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
   uint64_t full[FWD_NST], empty[FWD_NST];
   uint64_t qfull, sfull[2], sfree[2], pready[2], odone[2], fin[2];
-  float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
+  alignas(16) float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
   uint32_t tmem_base;
   int abort;
   uint8_t flags[2][FWD_MAXKB];
 };
+
+// the bias table is read 16 bytes at a time
+static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 
 // Waits without honouring the abort flag: used on the way out to drain work in flight.
 DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// Pass 1 over one row's 128 scores of a kv block: x = s * scale (+ column bias
+// from the stage's table), -inf where the causal rule drops column cc > lim,
+// and the running maximum in four independent chains.
+template <bool TABLE, bool CAUSAL>
+DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, float (&mx)[4]) {
+#pragma unroll
+  for (int i = 0; i < 64; i += 2) {
+    float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (TABLE) bias = *reinterpret_cast<const float4*>(tb + 2 * i);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = 2 * (i + j);
+      const uint64_t sv = f2(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+      const uint64_t xv = TABLE ? ffma2(sv, scv, j ? f2(bias.z, bias.w) : f2(bias.x, bias.y)) : fmul2(sv, scv);
+      float x0, x1;
+      unf2(xv, x0, x1);
+      if (CAUSAL) {
+        x0 = c > lim ? -INFINITY : x0;
+        x1 = c + 1 > lim ? -INFINITY : x1;
+      }
+      r[c] = __float_as_uint(x0);
+      r[c + 1] = __float_as_uint(x1);
+      mx[(i + j) & 3] = fmax3(mx[(i + j) & 3], x0, x1);
+    }
   }
 }
 
@@ -272,23 +302,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const int lim = q - kv0;   // keep column cc iff cc <= lim
         const float* tb = sm.cb[s][parity];
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint64_t sv = f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          uint64_t xv;
-          if (use_table)
-            xv = ffma2(sv, scv, *reinterpret_cast<const uint64_t*>(tb + 2 * i));
-          else
-            xv = fmul2(sv, scv);
-          float x0, x1;
-          unf2(xv, x0, x1);
-          if (causal) {
-            if (2 * i > lim) x0 = -INFINITY;
-            if (2 * i + 1 > lim) x1 = -INFINITY;
-          }
-          r[2 * i] = __float_as_uint(x0);
-          r[2 * i + 1] = __float_as_uint(x1);
-          mx[i & 3] = fmax3(mx[i & 3], x0, x1);
+        // one straight-line copy of the pass per (table, causal) pair: a runtime
+        // test inside the unrolled loop would cost instructions on every score
+        if (use_table) {
+          if (causal) scale_scores<true, true>(r, scv, tb, lim, mx);
+          else scale_scores<true, false>(r, scv, tb, lim, mx);
+        } else {
+          if (causal) scale_scores<false, true>(r, scv, tb, lim, mx);
+          else scale_scores<false, false>(r, scv, tb, lim, mx);
         }
         // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
         // per-score work: scores here are x' = x - base
