@@ -19,6 +19,8 @@
 // 6-9 split the 128 columns of each 128x128 score tile in two halves of 64.
 // S is double-buffered in TMEM so the next S product overlaps this tile's
 // elementwise work.
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace attn {
@@ -235,24 +237,30 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       const float abase = (MOD == MOD_ALIBI) ? slope2 * float(kv - q0) : 0.f;
       float pr[64];
       uint32_t pk[32];
+      // one straight-line copy per causal/not: no runtime test inside the unrolled loop
+      auto probs = [&](auto causal_c) {
+        constexpr bool CAUSAL = decltype(causal_c)::value;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        uint64_t xv = ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv,
-                            *reinterpret_cast<const uint64_t*>(nl + 2 * i));
-        if constexpr (MOD == MOD_CHECKER) xv = fadd2(xv, chk);
-        if constexpr (MOD == MOD_ALIBI)
-          xv = fadd2(xv, f2(fmaf(-slope2, float(2 * i), abase), fmaf(-slope2, float(2 * i + 1), abase)));
-        float x0, x1;
-        unf2(xv, x0, x1);
-        if (causal) {
-          if (kv > q0 + 2 * i) x0 = -INFINITY;
-          if (kv > q0 + 2 * i + 1) x1 = -INFINITY;
+        for (int i = 0; i < 32; ++i) {
+          uint64_t xv = ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv,
+                              *reinterpret_cast<const uint64_t*>(nl + 2 * i));
+          if constexpr (MOD == MOD_CHECKER) xv = fadd2(xv, chk);
+          if constexpr (MOD == MOD_ALIBI)
+            xv = fadd2(xv, f2(fmaf(-slope2, float(2 * i), abase), fmaf(-slope2, float(2 * i + 1), abase)));
+          float x0, x1;
+          unf2(xv, x0, x1);
+          if (CAUSAL) {
+            x0 = kv > q0 + 2 * i ? -INFINITY : x0;
+            x1 = kv > q0 + 2 * i + 1 ? -INFINITY : x1;
+          }
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          pr[2 * i] = p0;
+          pr[2 * i + 1] = p1;
+          pk[i] = pack2<BF16>(p0, p1);
         }
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        pr[2 * i] = p0;
-        pr[2 * i + 1] = p1;
-        pk[i] = pack2<BF16>(p0, p1);
-      }
+      };
+      if (causal) probs(std::true_type{});
+      else probs(std::false_type{});
       tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -498,21 +506,32 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       }
       const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
       float pr[64];
+      // one straight-line copy per (key table, causal) pair: no runtime test inside the unrolled loop
+      auto probs = [&](auto table_c, auto causal_c) {
+        constexpr bool TABLE = decltype(table_c)::value, CAUSAL = decltype(causal_c)::value;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        uint64_t add = nl2v;
-        if (use_table) add = fadd2(add, *reinterpret_cast<const uint64_t*>(tb + 2 * i));
-        if constexpr (MOD == MOD_CHECKER) add = fadd2(add, chk);
-        if constexpr (MOD == MOD_ALIBI)
-          add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
-        float x0, x1;
-        unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
-        if (causal) {
-          if (k0 + 2 * i > q) x0 = -INFINITY;
-          if (k0 + 2 * i + 1 > q) x1 = -INFINITY;
+        for (int i = 0; i < 32; ++i) {
+          uint64_t add = nl2v;
+          if (TABLE) add = fadd2(add, *reinterpret_cast<const uint64_t*>(tb + 2 * i));
+          if constexpr (MOD == MOD_CHECKER) add = fadd2(add, chk);
+          if constexpr (MOD == MOD_ALIBI)
+            add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
+          float x0, x1;
+          unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
+          if (CAUSAL) {
+            x0 = k0 + 2 * i > q ? -INFINITY : x0;
+            x1 = k0 + 2 * i + 1 > q ? -INFINITY : x1;
+          }
+          pr[2 * i] = ex2(x0);
+          pr[2 * i + 1] = ex2(x1);
         }
-        pr[2 * i] = ex2(x0);
-        pr[2 * i + 1] = ex2(x1);
+      };
+      if (use_table) {
+        if (causal) probs(std::true_type{}, std::true_type{});
+        else probs(std::true_type{}, std::false_type{});
+      } else {
+        if (causal) probs(std::false_type{}, std::true_type{});
+        else probs(std::false_type{}, std::false_type{});
       }
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
@@ -564,7 +583,7 @@ template <typename Smem, bool BF16, int MOD, bool DKDV>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
   auto kern = DKDV ? bwd_dkdv_kernel<BF16, MOD> : bwd_dq_kernel<BF16, MOD>;
   const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.B * p.H * (DKDV ? p.nkb : p.nqb));
   kern<<<grid, BWD_T, smem, st>>>(p);
