@@ -228,43 +228,69 @@ def bench_decode(E, dev, args):
 
 
 def bench_e2e(E, dev, args, w):
-    c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=True)
-    host = {k: v.pin_memory() for k, v in c.items()}
-    outs_h = {"out": torch.empty_like(host["q"]).pin_memory(),
-              "lse": torch.empty(host["q"].shape[:3], dtype=torch.float32).pin_memory(),
-              "dq": torch.empty_like(host["q"]).pin_memory(), "dk": torch.empty_like(host["k"]).pin_memory(),
-              "dv": torch.empty_like(host["v"]).pin_memory()}
-    dd = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    shape = E.make_shape(dd["q"], dd["k"])
+    """fwd+bwd through the public API with host buffers: every step copies its inputs
+    from pinned host memory and its results back, inside the timed region.  Copies
+    run on their own streams, double-buffered, so step i+1's upload and step i-1's
+    download overlap step i's kernels (as a training input pipeline would)."""
+    hosts = []
+    for j in range(2):
+        c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, seed=IN.SEED + 7000 + j, with_key_mask=True)
+        hosts.append({k: v.pin_memory() for k, v in c.items()})
+    outs_h = [{"out": torch.empty_like(hosts[0]["q"]).pin_memory(),
+               "lse": torch.empty(hosts[0]["q"].shape[:3], dtype=torch.float32).pin_memory(),
+               "dq": torch.empty_like(hosts[0]["q"]).pin_memory(), "dk": torch.empty_like(hosts[0]["k"]).pin_memory(),
+               "dv": torch.empty_like(hosts[0]["v"]).pin_memory()} for _ in range(2)]
+    ins_d = [{k: torch.empty_like(v, device=dev) for k, v in hosts[0].items()} for _ in range(2)]
+    outs_d = [{k: torch.empty_like(v, device=dev) for k, v in outs_h[0].items()} for _ in range(2)]
+    shape = E.make_shape(ins_d[0]["q"], ins_d[0]["k"])
     ws_f = E.workspace(E.OP_FWD, shape, dev)
     ws_b = E.workspace(E.OP_BWD, shape, dev)
-    out = torch.empty_like(dd["q"])
-    lse = torch.empty(dd["q"].shape[:3], dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(dd["q"]), torch.empty_like(dd["k"]), torch.empty_like(dd["v"])
+    s_up, s_cmp, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    up_done, cmp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    first = [True, True]
 
-    def step():
-        for k in dd:
-            dd[k].copy_(host[k], non_blocking=True)
-        E.attn_fwd(dd["q"], dd["k"], dd["v"], key_mask=dd["key_mask"], out=out, lse=lse, ws=ws_f)
-        E.attn_bwd(dd["q"], dd["k"], dd["v"], out, lse, dd["dout"], key_mask=dd["key_mask"], dq=dq, dk=dk, dv=dv,
-                   ws=ws_b)
-        for k, t in (("out", out), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            outs_h[k].copy_(t, non_blocking=True)
+    def step(i):
+        j = i % 2
+        di, do, hi, ho = ins_d[j], outs_d[j], hosts[i % 2], outs_h[j]
+        with torch.cuda.stream(s_up):
+            if not first[j]:
+                s_up.wait_event(cmp_done[j])          # step i-2 has finished reading these inputs
+            for k in di:
+                di[k].copy_(hi[k], non_blocking=True)
+            up_done[j].record(s_up)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(up_done[j])
+            if not first[j]:
+                s_cmp.wait_event(down_done[j])        # step i-2's results have left these buffers
+            E.attn_fwd(di["q"], di["k"], di["v"], key_mask=di["key_mask"], out=do["out"], lse=do["lse"], ws=ws_f)
+            E.attn_bwd(di["q"], di["k"], di["v"], do["out"], do["lse"], di["dout"], key_mask=di["key_mask"],
+                       dq=do["dq"], dk=do["dk"], dv=do["dv"], ws=ws_b)
+            cmp_done[j].record(s_cmp)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(cmp_done[j])
+            for k in do:
+                ho[k].copy_(do[k], non_blocking=True)
+            down_done[j].record(s_down)
+        first[j] = False
 
-    for _ in range(2):
-        step()
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
-    n = max(3, min(args.steps, 10))
+    n = max(4, min(args.steps, 40))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        step()
-    b.record()
+    a.record(s_up)
+    for i in range(n):
+        step(i)
+    s_down.wait_stream(s_up)
+    s_down.wait_stream(s_cmp)
+    b.record(s_down)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
-    return {"ms": ms, "h2d": h2d, "d2h": d2h}
+    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0
+    h2d = sum(v.numel() * v.element_size() for v in hosts[0].values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_h[0].values())
+    return {"ms": ms, "h2d": h2d, "d2h": d2h, "pipeline": "double-buffered, copies on separate streams"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) legs
@@ -420,7 +446,7 @@ def main():
                          "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": None,
                          "peak_kind": f"bf16 sustained, {src}"},
             "e2e": {"value": fl / (e2e["ms"] * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
-                    "d2h_bytes_per_step": e2e["d2h"]},
+                    "d2h_bytes_per_step": e2e["d2h"], "pipeline": e2e["pipeline"]},
             "gpu_launches": 6 * args.steps,
             "clocks": res["clocks"],
         }
