@@ -31,6 +31,10 @@ struct __align__(1024) FwdSmem {
   uint8_t q[2][FWD_TILE_BYTES];
   uint8_t k[FWD_NST][FWD_TILE_BYTES];
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
+  // Key-padding bias folded into S = Q K^T as one more K = 16 step: qaug has a
+  // column of ones, kaug[s] a column holding 0 or -inf per key (128B swizzle).
+  uint8_t qaug[FWD_TILE_BYTES];
+  uint8_t kaug[FWD_NST][FWD_TILE_BYTES];
   uint64_t full[FWD_NST], empty[FWD_NST];
   uint64_t qfull, sfull[2], sfree[2], pready[2], odone[2], fin[2];
   alignas(16) float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
@@ -41,6 +45,10 @@ struct __align__(1024) FwdSmem {
 
 // the bias table is read 16 bytes at a time
 static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
+
+// Byte offset of element (row r, column 0) in a 128-row x 64-column 16-bit tile
+// stored with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
+DEVI uint32_t sw128_col0(int r) { return (uint32_t)r * 128u + (uint32_t)(r & 7) * 16u; }
 
 // Waits without honouring the abort flag: used on the way out to drain work in flight.
 DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -126,13 +134,28 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       sm.flags[t][kb] = f;
     }
   }
+  constexpr bool kTableMod = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
+  // Without ALiBi / checkerboard the key-padding mask rides on the S product
+  // (exact: the extra step adds +0 or -inf to each f32 score); with them the
+  // producer's per-column table carries it.
+  const bool aug = !kTableMod && p.km_bits != nullptr;
+  const bool use_table = kTableMod;
+  if (aug) {
+    const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
+    uint4* qa = reinterpret_cast<uint4*>(sm.qaug);
+    for (int i = tid; i < FWD_TILE_BYTES / 16; i += FWD_THREADS) {
+      const int r = i >> 3, pos = i & 7;
+      qa[i] = make_uint4(pos == (r & 7) ? one : 0u, 0u, 0u, 0u);
+    }
+    uint4* ka = reinterpret_cast<uint4*>(sm.kaug[0]);
+    for (int i = tid; i < FWD_NST * FWD_TILE_BYTES / 16; i += FWD_THREADS) ka[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();   // generic-proxy writes, read by the tensor core
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  constexpr bool kTableMod = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
-  const bool use_table = kTableMod || p.km_bits != nullptr;
   if (warp == 0) {
     // ======================= TMA producer (lane 0) + bias tables (all lanes) =======================
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
@@ -154,7 +177,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       if (!(fu & KB_VISIT)) continue;
       const int s = u % FWD_NST;
       if (u >= FWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) break;
-      if (use_table) {
+      if (aug) {
+        // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column 0 of kaug[s]
+        uint32_t bits = 0xffffffffu;
+        if (fu & KB_KEYMASK) bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+        const uint16_t ninf = BF16 ? 0xFF80u : 0xFC00u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int col = 4 * lane + i;
+          *reinterpret_cast<uint16_t*>(sm.kaug[s] + sw128_col0(col)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+        }
+        fence_async_smem();
+      } else if (use_table) {
         // lane owns columns 4 lane .. 4 lane + 3 of this kv block
         uint32_t bits = 0xffffffffu;
         if (p.km_bits && (fu & KB_KEYMASK)) bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
@@ -205,6 +239,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
       const uint32_t tS = tmem + 256 * t, tP = tS + 128, tO = tS + 192;
       const uint64_t qd = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
+      const uint64_t qad = sdesc_sw128(smem_u32(sm.qaug), 16, 1024);
       uint64_t dk_[FWD_NST], dv_[FWD_NST];
       for (int s = 0; s < FWD_NST; ++s) {
         dk_[s] = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
@@ -244,6 +279,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const uint64_t kd = dk_[s];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_ss(tS, qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
+        if (aug) mma_ss(tS, qad, sdesc_sw128(smem_u32(sm.kaug[s]), 16, 1024), IDESC_S, 1u);
         tc_commit(smem_u32(&sm.sfull[t]));
         if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
         s_pend = s;
