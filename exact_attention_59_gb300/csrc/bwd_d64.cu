@@ -48,6 +48,10 @@ DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
 // [base, base+32) (k = 0..63) and [base+64, base+96) (k = 64..127).
 DEVI uint32_t split_a_col(uint32_t base, int kk) { return base + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); }
 
+// Byte offset of element (row r, column 0) in a 128-row x 64-column 16-bit tile
+// stored with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
+DEVI uint32_t sw128_col0(int r) { return (uint32_t)r * 128u + (uint32_t)(r & 7) * 16u; }
+
 // ============================================================================
 // dK / dV pass
 // ============================================================================
@@ -324,7 +328,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
 struct __align__(1024) DqSmem {
   uint8_t q[BWD_TILE], dO[BWD_TILE];
   uint8_t k[BWD_NST][BWD_TILE], v[BWD_NST][BWD_TILE];
-  float cb[BWD_NST][128];   // per-stage key bias (0 or -inf), built by the producer warp
+  // Key-padding bias folded into S = Q K^T as one more K = 16 step: qaug has a
+  // column of ones, kaug[s] a column holding 0 or -inf per key (128B swizzle).
+  uint8_t qaug[BWD_TILE];
+  uint8_t kaug[BWD_NST][BWD_TILE];
   uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull[2], dpfull, dsready, done;
   uint32_t tmem_base;
   int abort;
@@ -373,6 +380,18 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
   }
+  const bool aug = p.km_bits != nullptr;
+  if (aug) {
+    const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
+    uint4* qa = reinterpret_cast<uint4*>(sm.qaug);
+    for (int i = tid; i < (int)(BWD_TILE / 16); i += BWD_T) {
+      const int r = i >> 3, pos = i & 7;
+      qa[i] = make_uint4(pos == (r & 7) ? one : 0u, 0u, 0u, 0u);
+    }
+    uint4* ka = reinterpret_cast<uint4*>(sm.kaug[0]);
+    for (int i = tid; i < (int)(BWD_NST * BWD_TILE / 16); i += BWD_T) ka[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();   // generic-proxy writes, read by the tensor core
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -398,20 +417,22 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         const int s = u % BWD_NST;
         if (u >= BWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
         const int kb = sm.list[u];
-        if (p.km_bits) {   // lane owns columns 4 lane .. 4 lane + 3
+        if (aug) {   // lane owns keys 4 lane .. 4 lane + 3: column 0 of kaug[s]
           uint32_t bits = 0xffffffffu;
           if (sm.lflags[u] & KB_KEYMASK)
             bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+          const uint16_t ninf = BF16 ? 0xFF80u : 0xFC00u;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int col = 4 * lane + i;
-            sm.cb[s][col] = ((bits >> (col & 31)) & 1u) ? 0.f : -INFINITY;
+            *reinterpret_cast<uint16_t*>(sm.kaug[s] + sw128_col0(col)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
           }
+          fence_async_smem();
         }
         __syncwarp();
         if (lane == 0) {
           const uint32_t fb = smem_u32(&sm.full[s]);
-          mbar_expect_tx(fb, 2 * BWD_TILE);   // release: the table above is visible to its waiters
+          mbar_expect_tx(fb, 2 * BWD_TILE);   // release: the bias column above is visible to its waiters
           tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
           tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
         }
@@ -430,11 +451,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
       const uint32_t qA = smem_u32(sm.q), dA = smem_u32(sm.dO);
-      auto issue_s = [&](int u) {   // S_u = Q K_u^T into buffer u & 1
+      auto issue_s = [&](int u) {   // S_u = Q K_u^T (+ key-padding bias) into buffer u & 1
         const uint32_t kB = smem_u32(sm.k[u % BWD_NST]);
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tmem + C_SB + 128 * (u & 1), sdesc_sw128(qA + 32 * kk, 16, 1024), sdesc_sw128(kB + 32 * kk, 16, 1024),
                  ID_SS, kk > 0);
+        if (aug)
+          mma_ss(tmem + C_SB + 128 * (u & 1), sdesc_sw128(smem_u32(sm.qaug), 16, 1024),
+                 sdesc_sw128(smem_u32(sm.kaug[u % BWD_NST]), 16, 1024), ID_SS, 1u);
         tc_commit(smem_u32(&sm.sfull[u & 1]));
       };
       auto issue_dp = [&](int u) {  // dP_u = dO V_u^T
@@ -482,23 +506,18 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     const float nl2 = p.lse2[(size_t)bh * p.Sq + q];   // -lse log2(e)
     const float nd = p.delta[(size_t)bh * p.Sq + q];   // -D
     const uint64_t scv = f2(p.sc, p.sc), nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
-    const bool use_table = p.km_bits != nullptr;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
-      const int s = u % BWD_NST;
       const int kb = sm.list[u];
       const uint8_t f = sm.lflags[u];
       const int k0 = kb * 128 + 64 * w;   // first key of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
       if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
-      // the stage's key-bias table was written before its full barrier was armed
-      if (use_table && !wait_warp(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
       uint32_t rr[64];
       tmem_ld64(tS, rr);
-      const float* tb = &sm.cb[s][64 * w];
       uint64_t chk = 0;
       if constexpr (MOD == MOD_CHECKER) {
         const float hb = ((q + k0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
@@ -506,13 +525,12 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       }
       const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
       float pr[64];
-      // one straight-line copy per (key table, causal) pair: no runtime test inside the unrolled loop
-      auto probs = [&](auto table_c, auto causal_c) {
-        constexpr bool TABLE = decltype(table_c)::value, CAUSAL = decltype(causal_c)::value;
+      // one straight-line copy per causal/not: no runtime test inside the unrolled loop
+      auto probs = [&](auto causal_c) {
+        constexpr bool CAUSAL = decltype(causal_c)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           uint64_t add = nl2v;
-          if (TABLE) add = fadd2(add, *reinterpret_cast<const uint64_t*>(tb + 2 * i));
           if constexpr (MOD == MOD_CHECKER) add = fadd2(add, chk);
           if constexpr (MOD == MOD_ALIBI)
             add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
@@ -526,13 +544,8 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
           pr[2 * i + 1] = ex2(x1);
         }
       };
-      if (use_table) {
-        if (causal) probs(std::true_type{}, std::true_type{});
-        else probs(std::true_type{}, std::false_type{});
-      } else {
-        if (causal) probs(std::false_type{}, std::true_type{});
-        else probs(std::false_type{}, std::false_type{});
-      }
+      if (causal) probs(std::true_type{});
+      else probs(std::false_type{});
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
