@@ -25,8 +25,13 @@
 
 namespace attn {
 
-constexpr int BWD_NST = 3;
-constexpr int BWD_T = 320;
+constexpr int BWD_NST = 3;    // dQ pass: K/V stages
+#ifndef ATTN_DKDV_NST
+#define ATTN_DKDV_NST 4
+#endif
+constexpr int DKDV_NST = ATTN_DKDV_NST;   // dK/dV pass: Q/dO stages (deep enough to cover the copy latency)
+constexpr int DKDV_T = 352;   // dK/dV: warp 0 TMA, warps 1 and 10 MMA issue, warps 2-9 elementwise
+constexpr int BWD_T = 320;    // dQ: warp 0 TMA, warp 1 MMA issue, warps 2-9 elementwise
 constexpr uint32_t BWD_TILE = 128 * 64 * 2;
 constexpr int BWD_MAXB = 2048;
 
@@ -57,9 +62,9 @@ DEVI uint32_t sw128_col0(int r) { return (uint32_t)r * 128u + (uint32_t)(r & 7) 
 // ============================================================================
 struct __align__(1024) DkdvSmem {
   uint8_t k[BWD_TILE], v[BWD_TILE];
-  uint8_t q[BWD_NST][BWD_TILE], dO[BWD_NST][BWD_TILE];
-  float lse2[BWD_NST][128], delta[BWD_NST][128];
-  uint64_t kvfull, full[BWD_NST], empty[BWD_NST], sfull[2], dpfull, pready, dsready, done;
+  uint8_t q[DKDV_NST][BWD_TILE], dO[DKDV_NST][BWD_TILE];
+  float lse2[DKDV_NST][128], delta[DKDV_NST][128];
+  uint64_t kvfull, full[DKDV_NST], empty[DKDV_NST], sfull, sfree, pready, dvdone, dpfull, dpfree, dsready, dkdone, fin, done;
   uint32_t tmem_base;
   int abort;
   int nlist;
@@ -68,7 +73,7 @@ struct __align__(1024) DkdvSmem {
 };
 
 template <bool BF16, int MOD>
-__global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(DKDV_T, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -79,15 +84,19 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.kvfull), 1);
-    for (int s = 0; s < BWD_NST; ++s) {
+    for (int s = 0; s < DKDV_NST; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 1);
     }
-    mbar_init(smem_u32(&sm.sfull[0]), 1);
-    mbar_init(smem_u32(&sm.sfull[1]), 1);
-    mbar_init(smem_u32(&sm.dpfull), 1);
+    mbar_init(smem_u32(&sm.sfull), 1);
+    mbar_init(smem_u32(&sm.sfree), 256);
     mbar_init(smem_u32(&sm.pready), 256);
+    mbar_init(smem_u32(&sm.dvdone), 1);
+    mbar_init(smem_u32(&sm.dpfull), 1);
+    mbar_init(smem_u32(&sm.dpfree), 256);
     mbar_init(smem_u32(&sm.dsready), 256);
+    mbar_init(smem_u32(&sm.dkdone), 1);
+    mbar_init(smem_u32(&sm.fin), 1);
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     // list of q blocks that see this kv block
@@ -114,7 +123,8 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const int N = sm.nlist;
-  constexpr uint32_t C_SB = 0, C_DP = 256, C_DV = 384, C_DK = 448;
+  // TMEM columns: S^T 128, P^T (16-bit pairs) 64, dP^T 128, dS^T (16-bit pairs) 64, dV 64, dK 64
+  constexpr uint32_t C_S = 0, C_P = 128, C_DP = 192, C_DS = 320, C_DV = 384, C_DK = 448;
 
   if (warp == 0) {
     if (lane == 0 && N > 0) {
@@ -127,10 +137,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       mbar_expect_tx(kvb, 2 * BWD_TILE);
       tma_load_2d(smem_u32(sm.k), &p.tm_k, kvb, 0, bh * p.Skv + kb * 128);
       tma_load_2d(smem_u32(sm.v), &p.tm_v, kvb, 0, bh * p.Skv + kb * 128);
-      int last_u[BWD_NST] = {-1, -1, -1};
+      int last_u[DKDV_NST];
+      for (int s = 0; s < DKDV_NST; ++s) last_u[s] = -1;
       for (int u = 0; u < N; ++u) {
-        const int s = u % BWD_NST;
-        if (u >= BWD_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
+        const int s = u % DKDV_NST;
+        if (u >= DKDV_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / DKDV_NST) - 1) & 1, c)) break;
         const int qb = sm.list[u];
         const uint32_t fb = smem_u32(&sm.full[s]);
         mbar_expect_tx(fb, 2 * BWD_TILE + 2 * 512);
@@ -143,30 +154,30 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       }
       {   // every copy issued has landed before the CTA exits (instant unless aborted)
         drain(kvb, 0, p.timeout_ns);
-        for (int s = 0; s < BWD_NST; ++s)
-          if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
+        for (int s = 0; s < DKDV_NST; ++s)
+          if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / DKDV_NST) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---- MMA issue, thread A: the score products S^T = K Q^T and dP^T = V dO^T.
+    // S^T(u+1) is issued as soon as the softmax warps hold S^T(u) in registers and
+    // dP^T(u+1) as soon as they hold dP^T(u): P^T and dS^T live in TMEM regions of
+    // their own, so the score products never wait for the gradient products.
     if (lane == 0 && N > 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 12};
       constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
-      const uint32_t kA = smem_u32(sm.k), vA = smem_u32(sm.v);
-      auto issue_s = [&](int u) {   // S^T_u = K Q_u^T into buffer u & 1
-        const int s = u % BWD_NST;
-        const uint32_t d = tmem + C_SB + 128 * (u & 1);
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(d, sdesc_sw128(kA + 32 * kk, 16, 1024), sdesc_sw128(smem_u32(sm.q[s]) + 32 * kk, 16, 1024), ID_SS,
-                 kk > 0);
-        tc_commit(smem_u32(&sm.sfull[u & 1]));
+      const uint64_t kd = sdesc_sw128(smem_u32(sm.k), 16, 1024), vd = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      auto issue_s = [&](int u) {   // S^T_u = K Q_u^T
+        const uint64_t qd = sdesc_sw128(smem_u32(sm.q[u % DKDV_NST]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_S, kd + 2 * kk, qd + 2 * kk, ID_SS, kk > 0);
+        tc_commit(smem_u32(&sm.sfull));
       };
       auto issue_dp = [&](int u) {  // dP^T_u = V dO_u^T
-        const int s = u % BWD_NST;
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + C_DP, sdesc_sw128(vA + 32 * kk, 16, 1024), sdesc_sw128(smem_u32(sm.dO[s]) + 32 * kk, 16, 1024),
-                 ID_SS, kk > 0);
+        const uint64_t od = sdesc_sw128(smem_u32(sm.dO[u % DKDV_NST]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_DP, vd + 2 * kk, od + 2 * kk, ID_SS, kk > 0);
         tc_commit(smem_u32(&sm.dpfull));
       };
       bool ok = wait_one(smem_u32(&sm.kvfull), 0, c) && wait_one(smem_u32(&sm.full[0]), 0, c);
@@ -175,31 +186,47 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         issue_s(0);
         issue_dp(0);
       }
+      for (int u = 0; ok && u + 1 < N; ++u) {
+        if (!wait_one(smem_u32(&sm.full[(u + 1) % DKDV_NST]), ((u + 1) / DKDV_NST) & 1, c)) { ok = false; break; }
+        if (!wait_one(smem_u32(&sm.sfree), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(u + 1);
+        if (!wait_one(smem_u32(&sm.dpfree), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        issue_dp(u + 1);
+      }
+      // every MMA issued by this thread completes before the CTA lets go of TMEM
+      tc_commit(smem_u32(&sm.fin));
+      drain(smem_u32(&sm.fin), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---- MMA issue, thread B: the gradient products dV += P^T dO and dK += dS^T Q,
+    // A operands read from TMEM where the softmax warps left P^T and dS^T.
+    if (lane == 0 && N > 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 14};
+      constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
+      bool ok = wait_one(smem_u32(&sm.kvfull), 0, c);
       for (int u = 0; ok && u < N; ++u) {
-        const int s = u % BWD_NST;
-        if (u + 1 < N) {
-          if (!wait_one(smem_u32(&sm.full[(u + 1) % BWD_NST]), ((u + 1) / BWD_NST) & 1, c)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(u + 1);
-        }
+        const int s = u % DKDV_NST;
+        if (!wait_one(smem_u32(&sm.full[s]), (u / DKDV_NST) & 1, c)) { ok = false; break; }
         if (!wait_one(smem_u32(&sm.pready), u & 1, c)) { ok = false; break; }
         tc_fence_after();
         {   // dV += P^T dO_u
-          const uint32_t a = tmem + C_SB + 128 * (u & 1);
-          const uint32_t bb = smem_u32(sm.dO[s]);
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C_DV, split_a_col(a, kk), sdesc_sw128(bb + 2048 * kk, 8192, 1024), ID_TS, (u > 0 || kk > 0));
+          const uint64_t od = sdesc_sw128(smem_u32(sm.dO[s]), 8192, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + C_DV, tmem + C_P + 8 * kk, od + 128 * kk, ID_TS, (u > 0 || kk > 0));
+          tc_commit(smem_u32(&sm.dvdone));
         }
         if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
         tc_fence_after();
         {   // dK += dS^T Q_u
-          const uint32_t a = tmem + C_DP;
-          const uint32_t bb = smem_u32(sm.q[s]);
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C_DK, split_a_col(a, kk), sdesc_sw128(bb + 2048 * kk, 8192, 1024), ID_TS, (u > 0 || kk > 0));
+          const uint64_t qd = sdesc_sw128(smem_u32(sm.q[s]), 8192, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + C_DK, tmem + C_DS + 8 * kk, qd + 128 * kk, ID_TS, (u > 0 || kk > 0));
+          tc_commit(smem_u32(&sm.dkdone));
         }
         tc_commit(smem_u32(&sm.empty[s]));
-        if (u + 1 < N) issue_dp(u + 1);
       }
       tc_commit(smem_u32(&sm.done));
       drain(smem_u32(&sm.done), 0, p.timeout_ns);
@@ -221,17 +248,19 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     if (p.km_bits) my_key = (__ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + (kv >> 5)) >> (kv & 31)) & 1u;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
-      const int s = u % BWD_NST;
+      const int s = u % DKDV_NST;
       const int qb = sm.list[u];
       const uint8_t f = sm.lflags[u];
       const int q0 = qb * 128 + 64 * w;   // first query of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-      if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
+      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
       uint32_t rr[64];
-      tmem_ld64(tS, rr);
+      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
+      // S^T(u) is in registers: the next S^T may be computed over it
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.sfree));
       const float* nl = &sm.lse2[s][64 * w];
       uint64_t chk = 0;
       if constexpr (MOD == MOD_CHECKER) {
@@ -265,14 +294,20 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       };
       if (causal) probs(std::true_type{});
       else probs(std::false_type{});
-      tmem_st32(tS, pk);
+      // dV(u-1) has finished reading the P^T region
+      if (u > 0) {
+        if (!wait_warp(smem_u32(&sm.dvdone), (u - 1) & 1, c)) { ok = false; break; }
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + C_P + 32 * w, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.pready));
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tP = tmem + lane_off + C_DP + 64 * w;
-      tmem_ld64(tP, rr);
+      tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.dpfree));
       const float* nd = &sm.delta[s][64 * w];
       uint32_t dsk[32];
 #pragma unroll
@@ -283,7 +318,12 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         unf2(fmul2(f2(pr[2 * i], pr[2 * i + 1]), dd), d0, d1);
         dsk[i] = pack2<BF16>(d0, d1);
       }
-      tmem_st32(tP, dsk);
+      // dK(u-1) has finished reading the dS^T region
+      if (u > 0) {
+        if (!wait_warp(smem_u32(&sm.dkdone), (u - 1) & 1, c)) { ok = false; break; }
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + C_DS + 32 * w, dsk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.dsready));
@@ -412,7 +452,8 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         tma_load_2d(smem_u32(sm.q), &p.tm_q, qbar, 0, bh * p.Sq + qb * 128);
         tma_load_2d(smem_u32(sm.dO), &p.tm_do, qbar, 0, bh * p.Sq + qb * 128);
       }
-      int last_u[BWD_NST] = {-1, -1, -1};
+      int last_u[BWD_NST];
+      for (int s = 0; s < BWD_NST; ++s) last_u[s] = -1;
       for (int u = 0; u < N; ++u) {
         const int s = u % BWD_NST;
         if (u >= BWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
@@ -599,7 +640,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
   static const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.B * p.H * (DKDV ? p.nkb : p.nqb));
-  kern<<<grid, BWD_T, smem, st>>>(p);
+  kern<<<grid, DKDV ? DKDV_T : BWD_T, smem, st>>>(p);
   return cudaGetLastError();
 }
 
