@@ -30,8 +30,7 @@ constexpr int BWD_NST = 3;    // dQ pass: K/V stages
 #define ATTN_DKDV_NST 4
 #endif
 constexpr int DKDV_NST = ATTN_DKDV_NST;   // dK/dV pass: Q/dO stages (deep enough to cover the copy latency)
-constexpr int DKDV_T = 352;   // dK/dV: warp 0 TMA, warps 1 and 10 MMA issue, warps 2-9 elementwise
-constexpr int BWD_T = 320;    // dQ: warp 0 TMA, warp 1 MMA issue, warps 2-9 elementwise
+constexpr int BWD_T = 352;   // warp 0 TMA, warps 1 and 10 MMA issue, warps 2-9 elementwise
 constexpr uint32_t BWD_TILE = 128 * 64 * 2;
 constexpr int BWD_MAXB = 2048;
 
@@ -49,9 +48,6 @@ DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
                : "memory");
 }
 
-// A operand of a K = 128 product whose 16-bit values sit in TMEM columns
-// [base, base+32) (k = 0..63) and [base+64, base+96) (k = 64..127).
-DEVI uint32_t split_a_col(uint32_t base, int kk) { return base + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); }
 
 // Byte offset of element (row r, column 0) in a 128-row x 64-column 16-bit tile
 // stored with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
@@ -73,7 +69,7 @@ struct __align__(1024) DkdvSmem {
 };
 
 template <bool BF16, int MOD>
-__global__ void __launch_bounds__(DKDV_T, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -372,7 +368,7 @@ struct __align__(1024) DqSmem {
   // column of ones, kaug[s] a column holding 0 or -inf per key (128B swizzle).
   uint8_t qaug[BWD_TILE];
   uint8_t kaug[BWD_NST][BWD_TILE];
-  uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull[2], dpfull, dsready, done;
+  uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, dsready, dqdone, fin, done;
   uint32_t tmem_base;
   int abort;
   int nlist;
@@ -397,10 +393,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 1);
     }
-    mbar_init(smem_u32(&sm.sfull[0]), 1);
-    mbar_init(smem_u32(&sm.sfull[1]), 1);
+    mbar_init(smem_u32(&sm.sfull), 1);
+    mbar_init(smem_u32(&sm.sfree), 256);
     mbar_init(smem_u32(&sm.dpfull), 1);
+    mbar_init(smem_u32(&sm.dpfree), 256);
     mbar_init(smem_u32(&sm.dsready), 256);
+    mbar_init(smem_u32(&sm.dqdone), 1);
+    mbar_init(smem_u32(&sm.fin), 1);
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     int n = 0;
@@ -437,7 +436,8 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const int N = sm.nlist;
-  constexpr uint32_t C_SB = 0, C_DP = 256, C_DQ = 384;
+  // TMEM columns: S 128, dP 128, dS (16-bit pairs) 64, dQ 64
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DS = 256, C_DQ = 320;
 
   if (warp == 0) {
     if (N > 0) {
@@ -487,25 +487,25 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---- MMA issue, thread A: S = Q K^T (+ key-padding bias) and dP = dO V^T, each
+    // issued as soon as the softmax warps hold the previous one in registers.
     if (lane == 0 && N > 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 22};
       constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
-      constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
-      const uint32_t qA = smem_u32(sm.q), dA = smem_u32(sm.dO);
-      auto issue_s = [&](int u) {   // S_u = Q K_u^T (+ key-padding bias) into buffer u & 1
-        const uint32_t kB = smem_u32(sm.k[u % BWD_NST]);
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + C_SB + 128 * (u & 1), sdesc_sw128(qA + 32 * kk, 16, 1024), sdesc_sw128(kB + 32 * kk, 16, 1024),
-                 ID_SS, kk > 0);
-        if (aug)
-          mma_ss(tmem + C_SB + 128 * (u & 1), sdesc_sw128(smem_u32(sm.qaug), 16, 1024),
-                 sdesc_sw128(smem_u32(sm.kaug[u % BWD_NST]), 16, 1024), ID_SS, 1u);
-        tc_commit(smem_u32(&sm.sfull[u & 1]));
+      const uint64_t qd = sdesc_sw128(smem_u32(sm.q), 16, 1024), od = sdesc_sw128(smem_u32(sm.dO), 16, 1024);
+      const uint64_t qad = sdesc_sw128(smem_u32(sm.qaug), 16, 1024);
+      auto issue_s = [&](int u) {   // S_u = Q K_u^T (+ key-padding bias)
+        const int s = u % BWD_NST;
+        const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_S, qd + 2 * kk, kd + 2 * kk, ID_SS, kk > 0);
+        if (aug) mma_ss(tmem + C_S, qad, sdesc_sw128(smem_u32(sm.kaug[s]), 16, 1024), ID_SS, 1u);
+        tc_commit(smem_u32(&sm.sfull));
       };
       auto issue_dp = [&](int u) {  // dP_u = dO V_u^T
-        const uint32_t vB = smem_u32(sm.v[u % BWD_NST]);
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + C_DP, sdesc_sw128(dA + 32 * kk, 16, 1024), sdesc_sw128(vB + 32 * kk, 16, 1024), ID_SS, kk > 0);
+        const uint64_t vd = sdesc_sw128(smem_u32(sm.v[u % BWD_NST]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_DP, od + 2 * kk, vd + 2 * kk, ID_SS, kk > 0);
         tc_commit(smem_u32(&sm.dpfull));
       };
       bool ok = wait_one(smem_u32(&sm.qfull), 0, c) && wait_one(smem_u32(&sm.full[0]), 0, c);
@@ -514,23 +514,37 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         issue_s(0);
         issue_dp(0);
       }
+      for (int u = 0; ok && u + 1 < N; ++u) {
+        if (!wait_one(smem_u32(&sm.full[(u + 1) % BWD_NST]), ((u + 1) / BWD_NST) & 1, c)) { ok = false; break; }
+        if (!wait_one(smem_u32(&sm.sfree), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        issue_s(u + 1);
+        if (!wait_one(smem_u32(&sm.dpfree), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        issue_dp(u + 1);
+      }
+      // every MMA issued by this thread completes before the CTA lets go of TMEM
+      tc_commit(smem_u32(&sm.fin));
+      drain(smem_u32(&sm.fin), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 10) {
+    // ---- MMA issue, thread B: dQ += dS K, A operand from TMEM where the softmax
+    // warps left dS.
+    if (lane == 0 && N > 0) {
+      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 24};
+      constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
+      bool ok = true;
       for (int u = 0; ok && u < N; ++u) {
         const int s = u % BWD_NST;
-        if (u + 1 < N) {
-          if (!wait_one(smem_u32(&sm.full[(u + 1) % BWD_NST]), ((u + 1) / BWD_NST) & 1, c)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(u + 1);
-        }
+        if (!wait_one(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
         if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
         tc_fence_after();
-        {   // dQ += dS_u K_u
-          const uint32_t a = tmem + C_SB + 128 * (u & 1);
-          const uint32_t kB = smem_u32(sm.k[s]);
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C_DQ, split_a_col(a, kk), sdesc_sw128(kB + 2048 * kk, 8192, 1024), ID_TS, (u > 0 || kk > 0));
-        }
+        const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 8192, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + C_DQ, tmem + C_DS + 8 * kk, kd + 128 * kk, ID_TS, (u > 0 || kk > 0));
+        tc_commit(smem_u32(&sm.dqdone));
         tc_commit(smem_u32(&sm.empty[s]));
-        if (u + 1 < N) issue_dp(u + 1);
       }
       tc_commit(smem_u32(&sm.done));
       drain(smem_u32(&sm.done), 0, p.timeout_ns);
@@ -554,11 +568,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       const int k0 = kb * 128 + 64 * w;   // first key of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-      if (!wait_warp(smem_u32(&sm.sfull[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
+      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tS = tmem + lane_off + C_SB + 128 * (u & 1) + 64 * w;
       uint32_t rr[64];
-      tmem_ld64(tS, rr);
+      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
+      // S(u) is in registers: the next S may be computed over it
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.sfree));
       uint64_t chk = 0;
       if constexpr (MOD == MOD_CHECKER) {
         const float hb = ((q + k0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
@@ -590,6 +606,8 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.dpfree));
       uint32_t dsk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -598,7 +616,12 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
              d0, d1);
         dsk[i] = pack2<BF16>(d0, d1);
       }
-      tmem_st32(tS, dsk);   // dS over this half's S columns [64 w, 64 w + 32)
+      // dQ(u-1) has finished reading the dS region
+      if (u > 0) {
+        if (!wait_warp(smem_u32(&sm.dqdone), (u - 1) & 1, c)) { ok = false; break; }
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + C_DS + 32 * w, dsk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.dsready));
@@ -640,7 +663,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
   static const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.B * p.H * (DKDV ? p.nkb : p.nqb));
-  kern<<<grid, DKDV ? DKDV_T : BWD_T, smem, st>>>(p);
+  kern<<<grid, BWD_T, smem, st>>>(p);
   return cudaGetLastError();
 }
 
