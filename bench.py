@@ -39,6 +39,13 @@ METRIC = "attention fwd+bwd TFLOP/s (fp16, B8 H8 S2048 D64, key-padding mask)"
 UNIT = "TFLOP/s"
 
 
+# DRAM bytes (read + write) of one bwd_dkdv_kernel launch at the bench workload, from
+# `ncu --set full` of `python bench.py --mode profile --batch 8 --steps 1`
+# (summary: profiles/step_kernels_keypad_fp16_b8h8s2048d64_ncu_full.md).  Set it
+# back to None when the kernel changes until it is captured again.
+DKDV_TRAFFIC_BYTES = 80.9e6
+
+
 def counted_flops(w, backward=True):
     f = 4.0 * w.B * w.H * w.Sq * w.Skv * w.D * (0.5 if w.causal else 1.0)
     return f * (3.5 if backward else 1.0)
@@ -443,7 +450,7 @@ def main():
             "decode": {"workload": dec["workload"], "us_per_call": dec["us_per_call"], "GB/s": dec["GB/s"],
                        "frac_of_hbm": dec["GB/s"] / hbm},
             "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": achieved, "peak": sustained,
-                         "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": DKDV_TRAFFIC_BYTES,
                          "peak_kind": f"bf16 sustained, {src}"},
             "e2e": {"value": fl / (e2e["ms"] * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"], "pipeline": e2e["pipeline"]},
