@@ -5,7 +5,9 @@
 // forward).  Here the backward is written out, recomputing P from the saved
 // lse instead of storing it (FlashAttention-2 style):
 //   P = 2^(S scale log2e + bias log2e - lse log2e),  dV = P^T dO,
-//   (the preprocess stores -lse log2e and -D, so P and dS cost one FFMA and one
+//   (the preprocess stores -lse log2e and -D; the dK/dV pass adds both to its
+//   score products on the tensor core as one more K step, so P and dS^T cost one
+//   FMUL per score; the dQ pass adds them per row, one FFMA and one
 //   FADD + FMUL per pair of scores with the packed f32x2 instructions),
 //   dP = dO V^T,  dS = P o (dP - D),  D_i = rowsum(dO o O),
 //   dQ = scale dS K,  dK = scale dS^T Q.
@@ -53,13 +55,39 @@ DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
 // stored with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
 DEVI uint32_t sw128_col0(int r) { return (uint32_t)r * 128u + (uint32_t)(r & 7) * 16u; }
 
+// One f32 value x as three 16-bit terms, x = t0 + t1 + 2048 t2, written to columns
+// 0..2 of row r of a K = 16 operand (no swizzle).  The 2048 t2 term keeps f16 in
+// range; t0 + t1 carry the rest to about 2^-22 relative.  -inf goes to t2 alone.
+template <bool BF16>
+DEVI void split3(float x, uint8_t* op, int r) {
+  float a2, a0, a1;
+  if (x == -INFINITY) {
+    a2 = -INFINITY;
+    a0 = a1 = 0.f;
+  } else {
+    a2 = from16<BF16>(to16<BF16>(x * (1.f / 2048.f)));
+    const float r1 = x - 2048.f * a2;
+    a0 = from16<BF16>(to16<BF16>(r1));
+    a1 = r1 - a0;
+  }
+  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 0)) = to16<BF16>(a0);
+  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 1)) = to16<BF16>(a1);
+  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 2)) = to16<BF16>(a2);
+}
+
 // ============================================================================
 // dK / dV pass
 // ============================================================================
 struct __align__(1024) DkdvSmem {
   uint8_t k[BWD_TILE], v[BWD_TILE];
   uint8_t q[DKDV_NST][BWD_TILE], dO[DKDV_NST][BWD_TILE];
-  float lse2[DKDV_NST][128], delta[DKDV_NST][128];
+  // Column terms folded into the score products as one more K = 16 step:
+  // ones holds (1, 1, 2048) in k = 0..2 for every kv row; qaug[s] / daug[s] hold,
+  // per q row, -lse log2(e) / (scale log2(e)) and -D split as t0 + t1 + 2048 t2
+  // (16-bit each; no swizzle, 4 KB per 128 x 16 operand).
+  __align__(128) uint8_t ones[4096];
+  __align__(128) uint8_t qaug[DKDV_NST][4096];
+  __align__(128) uint8_t daug[DKDV_NST][4096];
   uint64_t kvfull, full[DKDV_NST], empty[DKDV_NST], sfull, sfree, pready, dvdone, dpfull, dpfree, dsready, dkdone, fin, done;
   uint32_t tmem_base;
   int abort;
@@ -81,7 +109,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
   if (tid == 0) {
     mbar_init(smem_u32(&sm.kvfull), 1);
     for (int s = 0; s < DKDV_NST; ++s) {
-      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.full[s]), 2);   // the TMA arrival + the producer's column terms
       mbar_init(smem_u32(&sm.empty[s]), 1);
     }
     mbar_init(smem_u32(&sm.sfull), 1);
@@ -114,6 +142,18 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
   }
+  {
+    uint4* z = reinterpret_cast<uint4*>(sm.ones);
+    for (int i = tid; i < (int)((1 + 2 * DKDV_NST) * 4096 / 16); i += BWD_T) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < 128) {
+      const uint16_t one = to16<BF16>(1.f), big = to16<BF16>(2048.f);
+      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(tid, 0)) = one;
+      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(tid, 1)) = one;
+      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(tid, 2)) = big;
+    }
+    fence_async_smem();   // generic-proxy writes, read by the tensor core
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -123,32 +163,50 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
   constexpr uint32_t C_S = 0, C_P = 128, C_DP = 192, C_DS = 320, C_DV = 384, C_DK = 448;
 
   if (warp == 0) {
-    if (lane == 0 && N > 0) {
+    // ---- producer: lane 0 issues the TMA copies; all lanes write the stage's
+    // column terms (4 q rows each), then lane 0 adds the second arrival.
+    if (N > 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 11};
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      tma_prefetch_desc(&p.tm_do);
       const uint32_t kvb = smem_u32(&sm.kvfull);
-      mbar_expect_tx(kvb, 2 * BWD_TILE);
-      tma_load_2d(smem_u32(sm.k), &p.tm_k, kvb, 0, bh * p.Skv + kb * 128);
-      tma_load_2d(smem_u32(sm.v), &p.tm_v, kvb, 0, bh * p.Skv + kb * 128);
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+        mbar_expect_tx(kvb, 2 * BWD_TILE);
+        tma_load_2d(smem_u32(sm.k), &p.tm_k, kvb, 0, bh * p.Skv + kb * 128);
+        tma_load_2d(smem_u32(sm.v), &p.tm_v, kvb, 0, bh * p.Skv + kb * 128);
+      }
+      const float inv_sc = 1.f / p.sc;
       int last_u[DKDV_NST];
       for (int s = 0; s < DKDV_NST; ++s) last_u[s] = -1;
       for (int u = 0; u < N; ++u) {
         const int s = u % DKDV_NST;
-        if (u >= DKDV_NST && !wait_one(smem_u32(&sm.empty[s]), ((u / DKDV_NST) - 1) & 1, c)) break;
+        if (u >= DKDV_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / DKDV_NST) - 1) & 1, c)) break;
         const int qb = sm.list[u];
         const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_expect_tx(fb, 2 * BWD_TILE + 2 * 512);
         const int row = bh * p.Sq + qb * 128;
-        tma_load_2d(smem_u32(sm.q[s]), &p.tm_q, fb, 0, row);
-        tma_load_2d(smem_u32(sm.dO[s]), &p.tm_do, fb, 0, row);
-        bulk_load(smem_u32(sm.lse2[s]), p.lse2 + row, 512, fb);
-        bulk_load(smem_u32(sm.delta[s]), p.delta + row, 512, fb);
+        if (lane == 0) {
+          mbar_expect_tx(fb, 2 * BWD_TILE);
+          tma_load_2d(smem_u32(sm.q[s]), &p.tm_q, fb, 0, row);
+          tma_load_2d(smem_u32(sm.dO[s]), &p.tm_do, fb, 0, row);
+        }
+        const float4 nl = __ldg(reinterpret_cast<const float4*>(p.lse2 + row) + lane);
+        const float4 nd = __ldg(reinterpret_cast<const float4*>(p.delta + row) + lane);
+        const float xl[4] = {nl.x * inv_sc, nl.y * inv_sc, nl.z * inv_sc, nl.w * inv_sc};
+        const float xd[4] = {nd.x, nd.y, nd.z, nd.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 4 * lane + i;
+          split3<BF16>(xl[i], sm.qaug[s], r);
+          split3<BF16>(xd[i], sm.daug[s], r);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);
         last_u[s] = u;
       }
-      {   // every copy issued has landed before the CTA exits (instant unless aborted)
+      if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
         drain(kvb, 0, p.timeout_ns);
         for (int s = 0; s < DKDV_NST; ++s)
           if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / DKDV_NST) & 1, p.timeout_ns);
@@ -164,16 +222,21 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 12};
       constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
       const uint64_t kd = sdesc_sw128(smem_u32(sm.k), 16, 1024), vd = sdesc_sw128(smem_u32(sm.v), 16, 1024);
-      auto issue_s = [&](int u) {   // S^T_u = K Q_u^T
-        const uint64_t qd = sdesc_sw128(smem_u32(sm.q[u % DKDV_NST]), 16, 1024);
+      const uint64_t oned = sdesc_k16(smem_u32(sm.ones));
+      auto issue_s = [&](int u) {   // S^T_u = K Q_u^T - lse_q / scale
+        const int s = u % DKDV_NST;
+        const uint64_t qd = sdesc_sw128(smem_u32(sm.q[s]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_S, kd + 2 * kk, qd + 2 * kk, ID_SS, kk > 0);
+        mma_ss(tmem + C_S, oned, sdesc_k16(smem_u32(sm.qaug[s])), ID_SS, 1u);
         tc_commit(smem_u32(&sm.sfull));
       };
-      auto issue_dp = [&](int u) {  // dP^T_u = V dO_u^T
-        const uint64_t od = sdesc_sw128(smem_u32(sm.dO[u % DKDV_NST]), 16, 1024);
+      auto issue_dp = [&](int u) {  // dP^T_u = V dO_u^T - D_q
+        const int s = u % DKDV_NST;
+        const uint64_t od = sdesc_sw128(smem_u32(sm.dO[s]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_DP, vd + 2 * kk, od + 2 * kk, ID_SS, kk > 0);
+        mma_ss(tmem + C_DP, oned, sdesc_k16(smem_u32(sm.daug[s])), ID_SS, 1u);
         tc_commit(smem_u32(&sm.dpfull));
       };
       bool ok = wait_one(smem_u32(&sm.kvfull), 0, c) && wait_one(smem_u32(&sm.full[0]), 0, c);
@@ -244,7 +307,6 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     if (p.km_bits) my_key = (__ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + (kv >> 5)) >> (kv & 31)) & 1u;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
-      const int s = u % DKDV_NST;
       const int qb = sm.list[u];
       const uint8_t f = sm.lflags[u];
       const int q0 = qb * 128 + 64 * w;   // first query of this half
@@ -257,7 +319,6 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       // S^T(u) is in registers: the next S^T may be computed over it
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.sfree));
-      const float* nl = &sm.lse2[s][64 * w];
       uint64_t chk = 0;
       if constexpr (MOD == MOD_CHECKER) {
         const float hb = ((kv + q0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
@@ -271,8 +332,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         constexpr bool CAUSAL = decltype(causal_c)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          uint64_t xv = ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv,
-                              *reinterpret_cast<const uint64_t*>(nl + 2 * i));
+          uint64_t xv = fmul2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv);
           if constexpr (MOD == MOD_CHECKER) xv = fadd2(xv, chk);
           if constexpr (MOD == MOD_ALIBI)
             xv = fadd2(xv, f2(fmaf(-slope2, float(2 * i), abase), fmaf(-slope2, float(2 * i + 1), abase)));
@@ -304,12 +364,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.dpfree));
-      const float* nd = &sm.delta[s][64 * w];
       uint32_t dsk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint64_t dd = fadd2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])),
-                                  *reinterpret_cast<const uint64_t*>(nd + 2 * i));
+        const uint64_t dd = f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));   // dP - D
         float d0, d1;
         unf2(fmul2(f2(pr[2 * i], pr[2 * i + 1]), dd), d0, d1);
         dsk[i] = pack2<BF16>(d0, d1);

@@ -185,6 +185,22 @@ DEVI uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// Shared-memory descriptor of a K = 16 operand stored K-major without swizzle:
+// 8-row x 16-byte core matrices, the two along K 128 bytes apart (LBO), row
+// groups of 8 rows 256 bytes apart (SBO).  Element (row r, k c), c < 16, sits at
+// byte (r / 8) * 256 + (c / 8) * 128 + (r % 8) * 16 + (c % 8) * 2: 4 KB for 128 rows.
+DEVI uint32_t k16_offset(int r, int c) {
+  return (uint32_t)(r >> 3) * 256u + (uint32_t)(c >> 3) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(c & 7) * 2u;
+}
+DEVI uint64_t sdesc_k16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= 1ull << 46;   // descriptor version for tcgen05; layout type 0 = no swizzle
+  return d;
+}
+
 // tcgen05.ld 32x32b: each lane of the warp reads its own TMEM lane, 32 consecutive
 // 32-bit columns.  The wait is in the same statement, so the values are ready on return.
 DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -303,5 +319,11 @@ DEVI float2 unpack2(uint32_t w) {
   }
   return f;
 }
+
+// One value rounded to the 16-bit type (round to nearest even), and back.
+template <bool BF16>
+DEVI uint16_t to16(float x) { return static_cast<uint16_t>(pack2<BF16>(x, 0.f) & 0xFFFFu); }
+template <bool BF16>
+DEVI float from16(uint16_t v) { return unpack2<BF16>(static_cast<uint32_t>(v)).x; }
 
 }  // namespace attn
