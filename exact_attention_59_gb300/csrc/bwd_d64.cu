@@ -27,7 +27,10 @@
 
 namespace attn {
 
-constexpr int BWD_NST = 3;    // dQ pass: K/V stages
+#ifndef ATTN_DQ_NST
+#define ATTN_DQ_NST 4
+#endif
+constexpr int BWD_NST = ATTN_DQ_NST;   // dQ pass: K/V stages (deep enough to cover the copy latency)
 #ifndef ATTN_DKDV_NST
 #define ATTN_DKDV_NST 4
 #endif
@@ -50,10 +53,6 @@ DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
                : "memory");
 }
 
-
-// Byte offset of element (row r, column 0) in a 128-row x 64-column 16-bit tile
-// stored with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
-DEVI uint32_t sw128_col0(int r) { return (uint32_t)r * 128u + (uint32_t)(r & 7) * 16u; }
 
 // One f32 value x as three 16-bit terms, x = t0 + t1 + 2048 t2, written to columns
 // 0..2 of row r of a K = 16 operand (no swizzle).  The 2048 t2 term keeps f16 in
@@ -423,9 +422,10 @@ struct __align__(1024) DqSmem {
   uint8_t q[BWD_TILE], dO[BWD_TILE];
   uint8_t k[BWD_NST][BWD_TILE], v[BWD_NST][BWD_TILE];
   // Key-padding bias folded into S = Q K^T as one more K = 16 step: qaug has a
-  // column of ones, kaug[s] a column holding 0 or -inf per key (128B swizzle).
-  uint8_t qaug[BWD_TILE];
-  uint8_t kaug[BWD_NST][BWD_TILE];
+  // column of ones, kaug[s] a column holding 0 or -inf per key (K = 16 operands
+  // without swizzle, 4 KB each).
+  __align__(128) uint8_t qaug[4096];
+  __align__(128) uint8_t kaug[BWD_NST][4096];
   uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, dsready, dqdone, fin, done;
   uint32_t tmem_base;
   int abort;
@@ -480,13 +480,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   const bool aug = p.km_bits != nullptr;
   if (aug) {
     const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
-    uint4* qa = reinterpret_cast<uint4*>(sm.qaug);
-    for (int i = tid; i < (int)(BWD_TILE / 16); i += BWD_T) {
-      const int r = i >> 3, pos = i & 7;
-      qa[i] = make_uint4(pos == (r & 7) ? one : 0u, 0u, 0u, 0u);
-    }
-    uint4* ka = reinterpret_cast<uint4*>(sm.kaug[0]);
-    for (int i = tid; i < (int)(BWD_NST * BWD_TILE / 16); i += BWD_T) ka[i] = make_uint4(0u, 0u, 0u, 0u);
+    uint4* z = reinterpret_cast<uint4*>(sm.qaug);
+    for (int i = tid; i < (int)((1 + BWD_NST) * 4096 / 16); i += BWD_T) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < 128) *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(tid, 0)) = static_cast<uint16_t>(one);
     fence_async_smem();   // generic-proxy writes, read by the tensor core
   }
   tc_fence_before();
@@ -524,7 +521,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int col = 4 * lane + i;
-            *reinterpret_cast<uint16_t*>(sm.kaug[s] + sw128_col0(col)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+            *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, 0)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
           }
           fence_async_smem();
         }
@@ -551,13 +548,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 22};
       constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
       const uint64_t qd = sdesc_sw128(smem_u32(sm.q), 16, 1024), od = sdesc_sw128(smem_u32(sm.dO), 16, 1024);
-      const uint64_t qad = sdesc_sw128(smem_u32(sm.qaug), 16, 1024);
+      const uint64_t qad = sdesc_k16(smem_u32(sm.qaug));
       auto issue_s = [&](int u) {   // S_u = Q K_u^T (+ key-padding bias)
         const int s = u % BWD_NST;
         const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_S, qd + 2 * kk, kd + 2 * kk, ID_SS, kk > 0);
-        if (aug) mma_ss(tmem + C_S, qad, sdesc_sw128(smem_u32(sm.kaug[s]), 16, 1024), ID_SS, 1u);
+        if (aug) mma_ss(tmem + C_S, qad, sdesc_k16(smem_u32(sm.kaug[s])), ID_SS, 1u);
         tc_commit(smem_u32(&sm.sfull));
       };
       auto issue_dp = [&](int u) {  // dP_u = dO V_u^T
