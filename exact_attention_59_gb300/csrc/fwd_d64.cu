@@ -10,7 +10,7 @@
 // One CTA owns two 128-row query tiles of one (b, h) and streams the union of
 // their kv-block lists once:
 //   warp 0      TMA producer: both Q tiles once, then K and V tiles of each kv
-//               block into a 3-stage ring (128B swizzle, 16 KB per tile).
+//               block into a FWD_NST-stage ring (128B swizzle, 16 KB per tile).
 //   warps 1-2   warp 1 allocates 512 TMEM columns; lane 0 of warp 1 + t issues
 //               tile t's tcgen05.mma: S_t = Q_t K^T (128x128, f32 in TMEM) and
 //               O_t += P_t V with P_t read from TMEM.  Two issuing threads keep
@@ -32,9 +32,10 @@ struct __align__(1024) FwdSmem {
   uint8_t k[FWD_NST][FWD_TILE_BYTES];
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
   // Key-padding bias folded into S = Q K^T as one more K = 16 step: qaug has a
-  // column of ones, kaug[s] a column holding 0 or -inf per key (128B swizzle).
-  uint8_t qaug[FWD_TILE_BYTES];
-  uint8_t kaug[FWD_NST][FWD_TILE_BYTES];
+  // column of ones, kaug[s] a column holding 0 or -inf per key (K = 16 operands
+  // without swizzle, 4 KB each).
+  __align__(128) uint8_t qaug[4096];
+  __align__(128) uint8_t kaug[FWD_NST][4096];
   uint64_t full[FWD_NST], empty[FWD_NST];
   uint64_t qfull, sfull[2], sfree[2], pready[2], odone[2], fin[2];
   alignas(16) float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
@@ -45,10 +46,6 @@ struct __align__(1024) FwdSmem {
 
 // the bias table is read 16 bytes at a time
 static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
-
-// Byte offset of element (row r, column 0) in a 128-row x 64-column 16-bit tile
-// stored with the 128-byte swizzle (16-byte chunk index XOR row mod 8).
-DEVI uint32_t sw128_col0(int r) { return (uint32_t)r * 128u + (uint32_t)(r & 7) * 16u; }
 
 // Waits without honouring the abort flag: used on the way out to drain work in flight.
 DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -142,13 +139,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   const bool use_table = kTableMod;
   if (aug) {
     const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
-    uint4* qa = reinterpret_cast<uint4*>(sm.qaug);
-    for (int i = tid; i < FWD_TILE_BYTES / 16; i += FWD_THREADS) {
-      const int r = i >> 3, pos = i & 7;
-      qa[i] = make_uint4(pos == (r & 7) ? one : 0u, 0u, 0u, 0u);
-    }
-    uint4* ka = reinterpret_cast<uint4*>(sm.kaug[0]);
-    for (int i = tid; i < FWD_NST * FWD_TILE_BYTES / 16; i += FWD_THREADS) ka[i] = make_uint4(0u, 0u, 0u, 0u);
+    uint4* z = reinterpret_cast<uint4*>(sm.qaug);
+    for (int i = tid; i < (1 + FWD_NST) * 4096 / 16; i += FWD_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < 128) *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(tid, 0)) = static_cast<uint16_t>(one);
     fence_async_smem();   // generic-proxy writes, read by the tensor core
   }
   tc_fence_before();
@@ -185,7 +179,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int col = 4 * lane + i;
-          *reinterpret_cast<uint16_t*>(sm.kaug[s] + sw128_col0(col)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+          *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, 0)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
         }
         fence_async_smem();
       } else if (use_table) {
@@ -239,7 +233,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
       const uint32_t tS = tmem + 256 * t, tP = tS + 128, tO = tS + 192;
       const uint64_t qd = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
-      const uint64_t qad = sdesc_sw128(smem_u32(sm.qaug), 16, 1024);
+      const uint64_t qad = sdesc_k16(smem_u32(sm.qaug));
       uint64_t dk_[FWD_NST], dv_[FWD_NST];
       for (int s = 0; s < FWD_NST; ++s) {
         dk_[s] = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
@@ -279,7 +273,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const uint64_t kd = dk_[s];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_ss(tS, qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
-        if (aug) mma_ss(tS, qad, sdesc_sw128(smem_u32(sm.kaug[s]), 16, 1024), IDESC_S, 1u);
+        if (aug) mma_ss(tS, qad, sdesc_k16(smem_u32(sm.kaug[s])), IDESC_S, 1u);
         tc_commit(smem_u32(&sm.sfull[t]));
         if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
         s_pend = s;

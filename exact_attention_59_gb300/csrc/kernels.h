@@ -7,7 +7,10 @@
 namespace attn {
 
 // ---------------------------------------------------------------- forward, D = 64
-constexpr int FWD_NST = 3;
+#ifndef ATTN_FWD_NST
+#define ATTN_FWD_NST 3
+#endif
+constexpr int FWD_NST = ATTN_FWD_NST;   // forward K/V stages
 constexpr int FWD_THREADS = 352;   // warp 0 TMA, warps 1-2 MMA issue (one per tile), warps 3-10 softmax
 constexpr uint32_t FWD_TILE_BYTES = 128 * 64 * 2;
 constexpr int FWD_MAXKB = 2048;   // Skv <= 262144
