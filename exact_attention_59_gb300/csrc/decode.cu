@@ -4,14 +4,15 @@
 // lists "faster decoding attention" as a TODO.  It is a streaming read of K and
 // V (256 bytes per key at D = 64), so the kernel is shaped for bandwidth and
 // latency, not for the tensor core:
-//   grid (nsplit, B*H); each CTA owns a contiguous range of up to 64 keys of
+//   grid (nsplit, B*H); each CTA owns a contiguous range of up to 128 keys of
 //   one (b, h).  Its K and V rows are contiguous in HBM, so one thread issues
-//   two bulk copies (cp.async.bulk, 16-byte aligned, 8 KB each) into shared
+//   two bulk copies (cp.async.bulk, 16-byte aligned, 16 KB each) into shared
 //   memory completing on one mbarrier: a single round trip to HBM per CTA,
-//   with ~13 CTAs (208 KB of copies) in flight per SM.
-//   In shared memory: 2 lanes per key form the scores (32 dims each), the CTA
-//   takes the max and the exponentials, and thread d (and d + 64) sum p_j V_jd
-//   over half the keys each; the CTA's (m, l, o[64]) goes to the workspace.
+//   with 7 CTAs (224 KB of copies) in flight per SM, so the B8 H8 Skv 2048
+//   case (1024 CTAs) runs as one wave on 152 SMs.
+//   In shared memory: thread j forms the score of key j, the CTA takes the max
+//   and the exponentials, and thread d (and d + 64) sum p_j V_jd over half the
+//   keys each; the CTA's (m, l, o[64]) goes to the workspace.
 //   The last CTA of a (b, h) to finish (atomic ticket) merges the splits in a
 //   fixed order, writes out and lse, and re-arms the ticket for the next call.
 #include "kernels.h"
@@ -19,7 +20,7 @@
 namespace attn {
 
 constexpr int DEC_THREADS = 128;
-constexpr int DEC_KEYS = 64;   // keys per split (maximum)
+constexpr int DEC_KEYS = 128;   // keys per split (maximum): 32 KB of K and V per CTA
 
 int decode_num_splits(int B, int H, int Skv) {
   (void)B;
@@ -37,13 +38,13 @@ template <bool BF16, int MOD>
 __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecodeParams p) {
   const int split = blockIdx.x, bh = blockIdx.y;
   const int b = bh / p.H, h = bh % p.H;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k_lo = split * p.keys_per_split;
-  const int nk = min(p.Skv, k_lo + p.keys_per_split) - k_lo;   // 1 .. 64
+  const int nk = min(p.Skv, k_lo + p.keys_per_split) - k_lo;   // 1 .. 128
 
   __shared__ __align__(128) uint16_t ks[DEC_KEYS * 64], vs[DEC_KEYS * 64];
   __shared__ __align__(16) float qs[64];
-  __shared__ float sc_s[DEC_KEYS], red[4], o_part[64];
+  __shared__ float sc_s[DEC_KEYS], redm[4], reds[4], o_part[64];
   __shared__ __align__(8) uint64_t bar;
   __shared__ unsigned ticket;
 
@@ -80,56 +81,54 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecodeParams 
   }
   __syncthreads();
 
-  // ---- scores: lanes 2j and 2j+1 take halves of key j
+  // ---- scores: thread j owns key j (its 64 dims as eight 16-byte chunks, the
+  // start rotated by j so the lanes of a warp spread over the banks)
+  float x = -INFINITY;
   {
-    const int j = tid >> 1, hf = tid & 1;
-    float s = 0.f;
+    const int j = tid;
     if (j < nk) {
-      const uint4* kr = reinterpret_cast<const uint4*>(ks + j * 64 + hf * 32);
+      const uint4* kr = reinterpret_cast<const uint4*>(ks + j * 64);
+      float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = kr[(i + j) & 3];   // rotate the start to spread banks
-        const int d0 = hf * 32 + 8 * ((i + j) & 3);
+      for (int i = 0; i < 8; ++i) {
+        const int c = (i + j) & 7;
+        const uint4 u = kr[c];
         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = unpack2<BF16>(wd[e]);
-          s = fmaf(qs[d0 + 2 * e], f.x, s);
-          s = fmaf(qs[d0 + 2 * e + 1], f.y, s);
+          s = fmaf(qs[8 * c + 2 * e], f.x, s);
+          s = fmaf(qs[8 * c + 2 * e + 1], f.y, s);
         }
       }
-    }
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    if (hf == 0 && j < DEC_KEYS) {
       const int kv = k_lo + j;
-      float x = s;
-      if (j >= nk) x = -INFINITY;
+      x = s;
       if constexpr (MOD == MOD_ALIBI) x = fmaf(slope2, float(kv), x);   // q_idx = 0
       if constexpr (MOD == MOD_CHECKER) x += (kv & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;
       if constexpr (MOD == MOD_CAUSAL) if (kv > 0) x = -INFINITY;
-      if (p.key_mask && j < nk && p.key_mask[(size_t)b * p.Skv + kv] == 0) x = -INFINITY;
-      sc_s[j] = x;
+      if (p.key_mask && p.key_mask[(size_t)b * p.Skv + kv] == 0) x = -INFINITY;
     }
   }
-  __syncthreads();
-  // ---- max over the 64 scores (warp 0), exponentials, sum
-  float M = -INFINITY;
-  if (tid < 32) {
-    M = fmaxf(sc_s[tid], sc_s[tid + 32]);
+  // ---- max over the 128 scores, exponentials, their sum
+  float M = x;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (tid == 0) red[0] = M;
-  }
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) redm[warp] = M;
   __syncthreads();
-  M = red[0];
+  M = fmaxf(fmaxf(redm[0], redm[1]), fmaxf(redm[2], redm[3]));
   const float Mu = (M == -INFINITY) ? 0.f : M;
-  if (tid < DEC_KEYS) sc_s[tid] = ex2(sc_s[tid] - Mu);
+  const float pj = ex2(x - Mu);
+  sc_s[tid] = pj;
+  float ls = pj;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+  if (lane == 0) reds[warp] = ls;
   __syncthreads();
-  // ---- o[d] = sum_j p_j v_jd: thread d over keys [0, 32), thread d + 64 over [32, 64)
+  // ---- o[d] = sum_j p_j v_jd: thread d over keys [0, 64), thread d + 64 over [64, 128)
   {
     const int d = tid & 63, part = tid >> 6;
     float acc = 0.f;
-    const int j0 = part * 32, j1 = min(nk, j0 + 32);
+    const int j0 = part * 64, j1 = min(nk, j0 + 64);
     for (int j = j0; j < j1; ++j) {
       const uint16_t raw = vs[j * 64 + d];
       float vf;
@@ -143,16 +142,10 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecodeParams 
     __syncthreads();
     float* mine = p.partial + ((size_t)bh * p.nsplit + split) * (2 + 64);
     if (part == 0) {
-      acc += o_part[d];
-      mine[2 + d] = acc;
-      if (d < 32) {
-        float l = sc_s[d] + sc_s[d + 32];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-        if (d == 0) {
-          mine[0] = M;
-          mine[1] = l;
-        }
+      mine[2 + d] = acc + o_part[d];
+      if (d == 0) {
+        mine[0] = M;
+        mine[1] = (reds[0] + reds[1]) + (reds[2] + reds[3]);
       }
     }
   }
