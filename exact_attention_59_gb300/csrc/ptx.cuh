@@ -68,25 +68,27 @@ DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// One thread waits for phase `parity` of `bar` to complete.  False = gave up.
-DEVI bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& c) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The slow paths of the waits below: a bounded spin that gives up after
+// timeout_ns (raising the CTA's abort flag and recording `site` in the status
+// word) or as soon as another thread of the CTA has given up.  Kept out of line
+// so that the fast path (the phase has already completed) stays small.
+static __device__ __noinline__ bool wait_one_slow(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                           uint64_t timeout_ns, int site) {
   const uint64_t t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (global_timer_ns() - t0 > c.timeout_ns) {
-      raise_abort(c);
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      atomicCAS(status, 0, kStatusTimeout | (site << 8));
       return false;
     }
   }
 }
-
-// A whole warp waits; the outcome is warp-uniform (so .sync.aligned tcgen05
-// instructions that follow are executed by all 32 lanes together).
-DEVI bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                            uint64_t timeout_ns, int site) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
     const bool ok = mbar_try_wait(bar, parity);
@@ -96,16 +98,30 @@ DEVI bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& c) {
       if (lane_id() == 0) {
         const uint64_t t = global_timer_ns();
         if (t0 == 0) t0 = t;
-        if (*c.abort) {
+        if (*abort) {
           stop = 1;
-        } else if (t - t0 > c.timeout_ns) {
-          raise_abort(c);
+        } else if (t - t0 > timeout_ns) {
+          *abort = 1;
+          atomicCAS(status, 0, kStatusTimeout | (site << 8));
           stop = 1;
         }
       }
       if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
   }
+}
+
+// One thread waits for phase `parity` of `bar` to complete.  False = gave up.
+DEVI bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_one_slow(bar, parity, c.abort, c.status, c.timeout_ns, c.site);
+}
+
+// A whole warp waits; the outcome is warp-uniform (so .sync.aligned tcgen05
+// instructions that follow are executed by all 32 lanes together).
+DEVI bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return wait_warp_slow(bar, parity, c.abort, c.status, c.timeout_ns, c.site);
 }
 
 // ---------------------------------------------------------------------------
