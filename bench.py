@@ -454,7 +454,8 @@ def main():
                          "peak_kind": f"bf16 sustained, {src}"},
             "e2e": {"value": fl / (e2e["ms"] * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"], "pipeline": e2e["pipeline"]},
-            "gpu_launches": 6 * args.steps,
+            # per step: key-mask packing + forward, preprocess (packs the key mask too), dK/dV, dQ
+            "gpu_launches": 5 * args.steps,
             "clocks": res["clocks"],
         }
         if world == 1 and not args.no_cpu_baseline:

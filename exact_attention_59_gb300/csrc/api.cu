@@ -348,9 +348,10 @@ attn_status attn_bwd_preprocess(const attn_shape* s, const void* out, const floa
   ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout w = layout(ATTN_OP_BWD, s);
-  ATTN_TRY(run_keymask(s, key_mask, ws, st));
+  // the key mask is packed by the same launch (bits and block summary for the two passes)
   return cuda_status(launch_bwd_preprocess(out, dout, lse, (int)s->dtype, (long long)s->B * s->H * s->Sq, s->D,
-                                           at<float>(ws, w.delta), at<float>(ws, w.lse2), st));
+                                           at<float>(ws, w.delta), at<float>(ws, w.lse2), key_mask, s->B, s->Skv,
+                                           at<uint32_t>(ws, w.km_bits), at<uint8_t>(ws, w.km_sum), st));
 }
 
 attn_status attn_bwd_dkdv(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,

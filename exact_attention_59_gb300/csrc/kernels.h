@@ -79,8 +79,11 @@ cudaError_t launch_keymask_pack(const uint8_t* km, int B, int Skv, uint32_t* bit
 cudaError_t launch_build_block_mask(int mask_mod, int B, int H, int Sq, int Skv, int bq, int bkv, uint8_t* tiles,
                                     cudaStream_t st);
 // delta = -rowsum(dout * out) (f32), lse2 = -lse * log2(e) (-inf where lse = -inf)
+// -D and -lse log2(e) per row; with km, also packs the key mask (bits + block
+// summary) in the same launch.
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, int dtype, long long rows,
-                                  int D, float* delta, float* lse2, cudaStream_t st);
+                                  int D, float* delta, float* lse2, const uint8_t* km, int B, int Skv, uint32_t* bits,
+                                  uint8_t* summary, cudaStream_t st);
 
 // ---------------------------------------------------------------- decode (Sq = 1)
 struct DecodeParams {

@@ -100,41 +100,88 @@ DEVI void load8<b16>(const b16* p, float (&f)[8]) {
 }
 
 template <typename T>
-__global__ void bwd_preprocess_kernel(const T* __restrict__ out, const T* __restrict__ dout,
-                                      const float* __restrict__ lse, long long rows, int D,
-                                      float* __restrict__ delta, float* __restrict__ lse2) {
-  const int lpr = D / 8;   // lanes per row (8 elements per lane)
-  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long row = tid / lpr;
-  const int part = (int)(tid % lpr);
-  float acc = 0.f;
-  if (row < rows) {
-    float a[8], g[8];
-    load8<T>(out + row * D + part * 8, a);
-    load8<T>(dout + row * D + part * 8, g);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(a[i], g[i], acc);
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ out, const T* __restrict__ dout,
+                                                             const float* __restrict__ lse, long long rows, int D,
+                                                             float* __restrict__ delta, float* __restrict__ lse2,
+                                                             long long half_rows, unsigned pre_blocks,
+                                                             const uint8_t* __restrict__ km, int Skv,
+                                                             uint32_t* __restrict__ bits, uint8_t* __restrict__ summary) {
+  if (blockIdx.x >= pre_blocks) {
+    // key-mask packing, fused into the same launch: 128 threads per (b, kv block)
+    const int nkb = (Skv + 127) / 128, nkb2 = (nkb + 1) / 2;
+    const int idx = (int)(blockIdx.x - pre_blocks);
+    const int b = idx / nkb2, kb = (idx % nkb2) * 2 + (threadIdx.x >> 7);
+    const int t = threadIdx.x & 127;
+    const int kv = kb * 128 + t;
+    const bool keep = kb < nkb && kv < Skv && km[(size_t)b * Skv + kv] != 0;
+    const unsigned w = __ballot_sync(0xffffffffu, keep);
+    __shared__ int cnt[8];
+    const int words = (Skv + 31) >> 5;
+    const int wi = kb * 4 + (t >> 5);
+    if ((t & 31) == 0) {
+      if (kb < nkb && wi < words) bits[(size_t)b * words + wi] = w;
+      cnt[threadIdx.x >> 5] = __popc(w);
+    }
+    __syncthreads();
+    if (t == 0 && kb < nkb) {
+      const int g = (threadIdx.x >> 7) * 4;
+      const int valid = min(128, Skv - kb * 128);
+      const int c = cnt[g] + cnt[g + 1] + cnt[g + 2] + cnt[g + 3];
+      summary[(size_t)b * nkb + kb] = c == 0 ? 0 : (c == valid ? 2 : 1);
+    }
+    return;
   }
-  for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) {
-    delta[row] = -acc;
-    const float l = lse[row];
-    lse2[row] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+  // D_i = rowsum(dO o O) and -lse log2(e): 8 elements per lane, two rows per lane
+  // (row and row + half_rows) so that four 16-byte loads are in flight per thread
+  const int lpr = D / 8;   // lanes per row
+  const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long row0 = tid / lpr;
+  const int part = (int)(tid % lpr);
+  float acc[2] = {0.f, 0.f};
+  float a[2][8], g[2][8];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const long long row = row0 + k * half_rows;
+    if (row0 < half_rows && row < rows) {
+      load8<T>(out + row * D + part * 8, a[k]);
+      load8<T>(dout + row * D + part * 8, g[k]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[k][i] = g[k][i] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[k] = fmaf(a[k][i], g[k][i], acc[k]);
+    for (int off = lpr / 2; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+    const long long row = row0 + k * half_rows;
+    if (row0 < half_rows && row < rows && part == 0) {
+      delta[row] = -acc[k];
+      const float l = lse[row];
+      lse2[row] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+    }
   }
 }
 
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, int dtype, long long rows,
-                                  int D, float* delta, float* lse2, cudaStream_t st) {
-  const long long threads = rows * (D / 8);
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+                                  int D, float* delta, float* lse2, const uint8_t* km, int B, int Skv, uint32_t* bits,
+                                  uint8_t* summary, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
+  const long long half_rows = (rows + 1) / 2;
+  const long long threads = half_rows * (D / 8);
+  const unsigned pre_blocks = (unsigned)((threads + 255) / 256);
+  const unsigned pack_blocks = km ? (unsigned)(B * (((Skv + 127) / 128 + 1) / 2)) : 0u;
+  const unsigned grid = pre_blocks + pack_blocks;
   if (dtype == 0)
-    bwd_preprocess_kernel<float><<<blocks, 256, 0, st>>>((const float*)out, (const float*)dout, lse, rows, D, delta,
-                                                         lse2);
+    bwd_preprocess_kernel<float><<<grid, 256, 0, st>>>((const float*)out, (const float*)dout, lse, rows, D, delta,
+                                                         lse2, half_rows, pre_blocks, km, Skv, bits, summary);
   else if (dtype == 1)
-    bwd_preprocess_kernel<h16><<<blocks, 256, 0, st>>>((const h16*)out, (const h16*)dout, lse, rows, D, delta, lse2);
+    bwd_preprocess_kernel<h16><<<grid, 256, 0, st>>>((const h16*)out, (const h16*)dout, lse, rows, D, delta, lse2,
+                                                       half_rows, pre_blocks, km, Skv, bits, summary);
   else
-    bwd_preprocess_kernel<b16><<<blocks, 256, 0, st>>>((const b16*)out, (const b16*)dout, lse, rows, D, delta, lse2);
+    bwd_preprocess_kernel<b16><<<grid, 256, 0, st>>>((const b16*)out, (const b16*)dout, lse, rows, D, delta, lse2,
+                                                       half_rows, pre_blocks, km, Skv, bits, summary);
   return cudaGetLastError();
 }
 
