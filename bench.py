@@ -187,8 +187,11 @@ def run_ours(args, rank, world):
     # ---- end to end: pinned host buffers, copies inside the timed region
     e2e = bench_e2e(E, dev, args, w)
 
+    # ---- the other named workloads, for context (outside the timed region)
+    extras = None if args.no_extras else bench_extras(E, dev)
+
     res = {"ms": ms, "phases": {n: statistics.mean(v) for n, v in ph.items()}, "clocks": clk.summary(),
-           "decode": dec, "e2e": e2e}
+           "decode": dec, "e2e": e2e, "extras": extras}
     return res
 
 
@@ -300,6 +303,63 @@ def bench_e2e(E, dev, args, w):
     return {"ms": ms, "h2d": h2d, "d2h": d2h, "pipeline": "double-buffered, copies on separate streams"}
 
 
+def bench_extras(E, dev):
+    """Context timings of the other named workloads (not part of `value`): forward and
+    backward per call, CUDA events over repeated calls on two rotating input sets."""
+    res = {}
+
+    def timed(fn, n):
+        fn(0)
+        fn(1)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n):
+            fn(i)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    for w in (W.FLEX_CAUSAL_ALIBI_BF16, W.CHECKERBOARD_FP16):
+        sets = []
+        for i in range(2):
+            c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, seed=IN.SEED + 9000 + i, dout=w.dout)
+            d = {k: v.to(dev) for k, v in c.items() if v is not None}
+            d["out"] = torch.empty_like(d["q"])
+            d["lse"] = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
+            d["dq"], d["dk"], d["dv"] = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+            sets.append(d)
+        bm = E.create_block_mask(w.block_mask, 1, 1, w.Sq, w.Skv) if w.block_mask else None
+        mod = w.score_mod
+
+        def fwd(i, sets=sets, bm=bm, mod=mod):
+            d = sets[i % 2]
+            E.attn_fwd(d["q"], d["k"], d["v"], block_mask=bm, score_mod=mod, out=d["out"], lse=d["lse"])
+
+        def bwd(i, sets=sets, bm=bm, mod=mod):
+            d = sets[i % 2]
+            E.attn_bwd(d["q"], d["k"], d["v"], d["out"], d["lse"], d["dout"], block_mask=bm, score_mod=mod,
+                       dq=d["dq"], dk=d["dk"], dv=d["dv"])
+
+        f_ms = timed(fwd, 50)
+        b_ms = timed(bwd, 50)
+        half = 0.5 if w.causal else 1.0
+        f_fl = 4.0 * w.B * w.H * w.Sq * w.Skv * w.D * half
+        res[w.name] = {"fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_ms": b_ms,
+                       "bwd_tflops": 2.5 * f_fl / (b_ms * 1e-3) / 1e12}
+    w = W.LONG_CAUSAL_BF16
+    q = IN.randn((w.B, w.H, w.Sq, w.D), IN.SEED + 1, w.dtype).to(dev)
+    k = IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED, w.dtype).to(dev)
+    v = IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED + 2, w.dtype).to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    bm = E.create_block_mask("causal", 1, 1, w.Sq, w.Skv)
+    f_ms = timed(lambda i: E.attn_fwd(q, k, v, block_mask=bm, out=out, lse=lse), 3)
+    f_fl = 4.0 * w.B * w.H * w.Sq * w.Skv * w.D * 0.5
+    res[w.name] = {"fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12}
+    return res
+
+
 # ------------------------------------------------------------------ oracle (CPU) legs
 def oracle_sample(seconds=12.0, max_heads=64):
     """Times the oracle's fwd+bwd on whole heads of the workload until `seconds` pass."""
@@ -403,6 +463,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' context timings")
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
                     help="profile: a few untimed steps at --batch, for ncu captures")
     ap.add_argument("--batch", type=int, default=16)
@@ -458,6 +519,8 @@ def main():
             "gpu_launches": 5 * args.steps,
             "clocks": res["clocks"],
         }
+        if res["extras"] is not None:
+            line["extras"] = res["extras"]
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
