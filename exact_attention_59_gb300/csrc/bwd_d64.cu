@@ -39,13 +39,6 @@ constexpr int BWD_T = 352;   // warp 0 TMA, warps 1 and 10 MMA issue, warps 2-9 
 constexpr uint32_t BWD_TILE = 128 * 64 * 2;
 constexpr int BWD_MAXB = 2048;
 
-DEVI void drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return;
-  }
-}
-
 // 1-D bulk copy global -> shared, completion on an mbarrier (16-byte aligned, size % 16 == 0)
 DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -53,26 +46,6 @@ DEVI void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
                : "memory");
 }
 
-
-// One f32 value x as three 16-bit terms, x = t0 + t1 + 2048 t2, written to columns
-// 0..2 of row r of a K = 16 operand (no swizzle).  The 2048 t2 term keeps f16 in
-// range; t0 + t1 carry the rest to about 2^-22 relative.  -inf goes to t2 alone.
-template <bool BF16>
-DEVI void split3(float x, uint8_t* op, int r) {
-  float a2, a0, a1;
-  if (x == -INFINITY) {
-    a2 = -INFINITY;
-    a0 = a1 = 0.f;
-  } else {
-    a2 = from16<BF16>(to16<BF16>(x * (1.f / 2048.f)));
-    const float r1 = x - 2048.f * a2;
-    a0 = from16<BF16>(to16<BF16>(r1));
-    a1 = r1 - a0;
-  }
-  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 0)) = to16<BF16>(a0);
-  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 1)) = to16<BF16>(a1);
-  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 2)) = to16<BF16>(a2);
-}
 
 // ============================================================================
 // dK / dV pass
@@ -206,9 +179,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         last_u[s] = u;
       }
       if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-        drain(kvb, 0, p.timeout_ns);
+        drain_wait(kvb, 0, p.timeout_ns);
         for (int s = 0; s < DKDV_NST; ++s)
-          if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / DKDV_NST) & 1, p.timeout_ns);
+          if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / DKDV_NST) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -255,7 +228,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       }
       // every MMA issued by this thread completes before the CTA lets go of TMEM
       tc_commit(smem_u32(&sm.fin));
-      drain(smem_u32(&sm.fin), 0, p.timeout_ns);
+      drain_wait(smem_u32(&sm.fin), 0, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 10) {
@@ -287,7 +260,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         tc_commit(smem_u32(&sm.empty[s]));
       }
       tc_commit(smem_u32(&sm.done));
-      drain(smem_u32(&sm.done), 0, p.timeout_ns);
+      drain_wait(smem_u32(&sm.done), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
@@ -535,9 +508,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         last_u[s] = u;
       }
       if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-        drain(qbar, 0, p.timeout_ns);
+        drain_wait(qbar, 0, p.timeout_ns);
         for (int s = 0; s < BWD_NST; ++s)
-          if (last_u[s] >= 0) drain(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
+          if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -580,7 +553,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       }
       // every MMA issued by this thread completes before the CTA lets go of TMEM
       tc_commit(smem_u32(&sm.fin));
-      drain(smem_u32(&sm.fin), 0, p.timeout_ns);
+      drain_wait(smem_u32(&sm.fin), 0, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 10) {
@@ -602,7 +575,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         tc_commit(smem_u32(&sm.empty[s]));
       }
       tc_commit(smem_u32(&sm.done));
-      drain(smem_u32(&sm.done), 0, p.timeout_ns);
+      drain_wait(smem_u32(&sm.done), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {

@@ -40,13 +40,6 @@ struct __align__(1024) F5Smem {
   uint8_t lflags[F5_MAXKB];
 };
 
-DEVI void f5_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return;
-  }
-}
-
 template <bool BF16, int MOD>
 __global__ void __launch_bounds__(F5_THREADS, 1) fwd_d512_kernel(const __grid_constant__ FwdBigParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -128,9 +121,9 @@ __global__ void __launch_bounds__(F5_THREADS, 1) fwd_d512_kernel(const __grid_co
         for (int cc = 0; cc < 4 && ok; ++cc) ok = put(&p.tm_v, 256 * half + 64 * cc, krow0 + sm.list[j] * 128);
       }
       {   // every copy issued has landed before the CTA exits (instant unless aborted)
-        f5_drain(qbar, 0, p.timeout_ns);
+        drain_wait(qbar, 0, p.timeout_ns);
         for (int s = 0; s < F5_NST; ++s)
-          if (last_u[s] >= 0) f5_drain(smem_u32(&sm.full[s]), (last_u[s] / F5_NST) & 1, p.timeout_ns);
+          if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / F5_NST) & 1, p.timeout_ns);
       }
     }
     __syncwarp();
@@ -184,7 +177,7 @@ __global__ void __launch_bounds__(F5_THREADS, 1) fwd_d512_kernel(const __grid_co
       }
       if (ok) tc_commit(smem_u32(&sm.alldone));
       tc_commit(smem_u32(&sm.fin));
-      f5_drain(smem_u32(&sm.fin), 0, p.timeout_ns);
+      drain_wait(smem_u32(&sm.fin), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {

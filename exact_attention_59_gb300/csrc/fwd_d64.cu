@@ -47,14 +47,6 @@ struct __align__(1024) FwdSmem {
 // the bias table is read 16 bytes at a time
 static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 
-// Waits without honouring the abort flag: used on the way out to drain work in flight.
-DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > timeout_ns) return;
-  }
-}
-
 // Pass 1 over one row's 128 scores of a kv block: x = s * scale (+ column bias
 // from the stage's table), -inf where the causal rule drops column cc > lim,
 // and the running maximum in four independent chains.

@@ -111,6 +111,15 @@ static __device__ __noinline__ bool wait_warp_slow(uint32_t bar, uint32_t parity
   }
 }
 
+// Waits without honouring the abort flag (bounded by timeout_ns): used on the way
+// out, so that copies and MMAs in flight finish before the CTA exits.
+DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) return;
+  }
+}
+
 // One thread waits for phase `parity` of `bar` to complete.  False = gave up.
 DEVI bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& c) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -341,5 +350,25 @@ template <bool BF16>
 DEVI uint16_t to16(float x) { return static_cast<uint16_t>(pack2<BF16>(x, 0.f) & 0xFFFFu); }
 template <bool BF16>
 DEVI float from16(uint16_t v) { return unpack2<BF16>(static_cast<uint32_t>(v)).x; }
+
+// One f32 value x as three 16-bit terms, x = t0 + t1 + 2048 t2, written to columns
+// 0..2 of row r of a K = 16 operand (no swizzle).  The 2048 t2 term keeps f16 in
+// range; t0 + t1 carry the rest to about 2^-22 relative.  -inf goes to t2 alone.
+template <bool BF16>
+DEVI void split3(float x, uint8_t* op, int r) {
+  float a2, a0, a1;
+  if (x == -INFINITY) {
+    a2 = -INFINITY;
+    a0 = a1 = 0.f;
+  } else {
+    a2 = from16<BF16>(to16<BF16>(x * (1.f / 2048.f)));
+    const float r1 = x - 2048.f * a2;
+    a0 = from16<BF16>(to16<BF16>(r1));
+    a1 = r1 - a0;
+  }
+  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 0)) = to16<BF16>(a0);
+  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 1)) = to16<BF16>(a1);
+  *reinterpret_cast<uint16_t*>(op + k16_offset(r, 2)) = to16<BF16>(a2);
+}
 
 }  // namespace attn
