@@ -116,11 +116,17 @@ T* at(void* ws, size_t off) {
 
 attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// Checks shared by every prefill call.
+// 128-row tiles covering n rows (the last one may be partial)
+int tiles_of(int n) { return (n + 127) / 128; }
+
+// Checks shared by every prefill call.  Any Sq, Skv >= 1 on the f16/bf16
+// D = 64 path (the last q and kv tiles may be partial); multiples of 128 for
+// f32 and D = 512.
 attn_status check_prefill(const attn_shape* s, bool backward) {
   if (!shape_ok(s)) return ATTN_ERR_INVALID_ARG;
-  if (s->Sq % 128 != 0 || s->Skv % 128 != 0) return ATTN_ERR_SHAPE;
-  if (s->Skv / 128 > FWD_MAXKB || s->Sq / 128 > FWD_MAXKB) return ATTN_ERR_SHAPE;
+  const bool ragged_ok = s->D == 64 && s->dtype != ATTN_F32;
+  if (!ragged_ok && (s->Sq % 128 != 0 || s->Skv % 128 != 0)) return ATTN_ERR_SHAPE;
+  if (tiles_of(s->Skv) > FWD_MAXKB || tiles_of(s->Sq) > FWD_MAXKB) return ATTN_ERR_SHAPE;
   if (s->D == 64) return ATTN_OK;
   if (s->D == 512 && !backward && s->dtype != ATTN_F32) return ATTN_OK;
   return ATTN_ERR_UNSUPPORTED;
@@ -148,7 +154,7 @@ attn_status check_ws(attn_op op, const attn_shape* s, void* ws, size_t ws_bytes)
 }
 
 void bm_strides(const attn_shape* s, const attn_block_mask* bm, long long& sb, long long& sh) {
-  const long long tile = (long long)(s->Sq / 128) * (s->Skv / 128);
+  const long long tile = (long long)tiles_of(s->Sq) * tiles_of(s->Skv);
   sh = bm->bcast_h ? 0 : tile;
   sb = bm->bcast_b ? 0 : (bm->bcast_h ? 1 : s->H) * tile;
 }
@@ -200,8 +206,8 @@ BwdParams bwd_params(const attn_shape* s, const void* q, const void* k, const vo
   p.H = s->H;
   p.Sq = s->Sq;
   p.Skv = s->Skv;
-  p.nqb = s->Sq / 128;
-  p.nkb = s->Skv / 128;
+  p.nqb = tiles_of(s->Sq);
+  p.nkb = tiles_of(s->Skv);
   p.sc = scale * kLog2e;
   p.scale = scale;
   p.timeout_ns = timeout_ns();
@@ -223,8 +229,8 @@ SimtParams simt_params(const attn_shape* s, const void* q, const void* k, const 
   p.H = s->H;
   p.Sq = s->Sq;
   p.Skv = s->Skv;
-  p.nqb = s->Sq / 128;
-  p.nkb = s->Skv / 128;
+  p.nqb = tiles_of(s->Sq);
+  p.nkb = tiles_of(s->Skv);
   p.mod = (int)mod;
   p.sc = scale * kLog2e;
   p.scale = scale;
@@ -245,7 +251,7 @@ const char* attn_status_string(attn_status s) {
   switch (s) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_INVALID_ARG: return "invalid argument";
-    case ATTN_ERR_SHAPE: return "unsupported shape (prefill needs Sq, Skv multiples of 128; decode needs Sq == 1)";
+    case ATTN_ERR_SHAPE: return "unsupported shape (f32 and D=512 prefill need Sq, Skv multiples of 128; decode needs Sq == 1)";
     case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
     case ATTN_ERR_UNSUPPORTED: return "dtype / head dim / mod / block size combination not built";
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
@@ -295,8 +301,8 @@ attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const vo
     p.H = s->H;
     p.Sq = s->Sq;
     p.Skv = s->Skv;
-    p.nqb = s->Sq / 128;
-    p.nkb = s->Skv / 128;
+    p.nqb = tiles_of(s->Sq);
+    p.nkb = tiles_of(s->Skv);
     p.sc = scale * kLog2e;
     p.timeout_ns = timeout_ns();
     return cuda_status(launch_fwd_d512(p, s->dtype == ATTN_BF16, (int)mod, st));
@@ -329,8 +335,8 @@ attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const vo
   p.H = s->H;
   p.Sq = s->Sq;
   p.Skv = s->Skv;
-  p.nqb = s->Sq / 128;
-  p.nkb = s->Skv / 128;
+  p.nqb = tiles_of(s->Sq);
+  p.nkb = tiles_of(s->Skv);
   p.npairs = (p.nqb + 1) / 2;
   p.sc = scale * kLog2e;
   p.timeout_ns = timeout_ns();

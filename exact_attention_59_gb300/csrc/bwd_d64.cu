@@ -163,10 +163,20 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
           tma_load_2d(smem_u32(sm.q[s]), &p.tm_q, fb, 0, row);
           tma_load_2d(smem_u32(sm.dO[s]), &p.tm_do, fb, 0, row);
         }
-        const float4 nl = __ldg(reinterpret_cast<const float4*>(p.lse2 + row) + lane);
-        const float4 nd = __ldg(reinterpret_cast<const float4*>(p.delta + row) + lane);
-        const float xl[4] = {nl.x * inv_sc, nl.y * inv_sc, nl.z * inv_sc, nl.w * inv_sc};
-        const float xd[4] = {nd.x, nd.y, nd.z, nd.w};
+        float xl[4], xd[4];
+        if ((p.Sq & 3) == 0 && qb * 128 + 128 <= p.Sq) {   // whole block, 16-byte aligned rows
+          const float4 nl = __ldg(reinterpret_cast<const float4*>(p.lse2 + row) + lane);
+          const float4 nd = __ldg(reinterpret_cast<const float4*>(p.delta + row) + lane);
+          xl[0] = nl.x * inv_sc; xl[1] = nl.y * inv_sc; xl[2] = nl.z * inv_sc; xl[3] = nl.w * inv_sc;
+          xd[0] = nd.x; xd[1] = nd.y; xd[2] = nd.z; xd[3] = nd.w;
+        } else {   // rows past Sq (partial last q block) get P = 0
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const bool in = qb * 128 + 4 * lane + i < p.Sq;
+            xl[i] = in ? __ldg(p.lse2 + row + 4 * lane + i) * inv_sc : -INFINITY;
+            xd[i] = in ? __ldg(p.delta + row + 4 * lane + i) : 0.f;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 4 * lane + i;
@@ -275,8 +285,8 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     // A padded key's dK and dV rows are zero.  Its P^T and dS^T rows are not masked
     // here: row r of an MMA result depends on row r of its A operand only, so
     // those rows stay confined to the padded key and the epilogue writes zeros.
-    bool my_key = true;
-    if (p.km_bits) my_key = (__ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + (kv >> 5)) >> (kv & 31)) & 1u;
+    bool my_key = kv < p.Skv;   // rows past Skv (partial last kv block) are not written
+    if (p.km_bits && my_key) my_key = (km_word(p.km_bits, b, p.Skv, kv) >> (kv & 31)) & 1u;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
       const int qb = sm.list[u];
@@ -378,8 +388,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       }
       uint16_t* base = reinterpret_cast<uint16_t*>(w == 0 ? p.dv : p.dk);
       uint4* dst = reinterpret_cast<uint4*>(base + ((size_t)bh * p.Skv + kv) * 64);
+      if (kv < p.Skv) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      }
     }
   }
   tc_fence_before();
@@ -489,7 +501,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         if (aug) {   // lane owns keys 4 lane .. 4 lane + 3: column 0 of kaug[s]
           uint32_t bits = 0xffffffffu;
           if (sm.lflags[u] & KB_KEYMASK)
-            bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+            bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
           const uint16_t ninf = BF16 ? 0xFF80u : 0xFC00u;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -586,8 +598,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 23 + w};
     const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
-    const float nl2 = p.lse2[(size_t)bh * p.Sq + q];   // -lse log2(e)
-    const float nd = p.delta[(size_t)bh * p.Sq + q];   // -D
+    // rows past Sq (partial last q tile) get P = 0 and are not written
+    const float nl2 = q < p.Sq ? p.lse2[(size_t)bh * p.Sq + q] : -INFINITY;   // -lse log2(e)
+    const float nd = q < p.Sq ? p.delta[(size_t)bh * p.Sq + q] : 0.f;        // -D
     const uint64_t scv = f2(p.sc, p.sc), nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
     bool ok = true;
     for (int u = 0; u < N; ++u) {
@@ -596,6 +609,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       const int k0 = kb * 128 + 64 * w;   // first key of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+      // keep column cc of this half iff cc <= lim: the causal limit and, in a
+      // partial last kv block, the end of the keys
+      const int kvl = p.Skv - 1 - k0;
+      const bool limited = causal || kvl < 63;
+      const int lim = causal ? min(q - k0, kvl) : kvl;
       if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       uint32_t rr[64];
@@ -622,14 +640,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
           float x0, x1;
           unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
           if (CAUSAL) {
-            x0 = k0 + 2 * i > q ? -INFINITY : x0;
-            x1 = k0 + 2 * i + 1 > q ? -INFINITY : x1;
+            x0 = 2 * i > lim ? -INFINITY : x0;
+            x1 = 2 * i + 1 > lim ? -INFINITY : x1;
           }
           pr[2 * i] = ex2(x0);
           pr[2 * i + 1] = ex2(x1);
         }
       };
-      if (causal) probs(std::true_type{});
+      if (limited) probs(std::true_type{});
       else probs(std::false_type{});
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
@@ -672,8 +690,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         for (int i = 0; i < 32; ++i)
           o[i] = pack2<BF16>(__uint_as_float(rr[2 * i]) * p.scale, __uint_as_float(rr[2 * i + 1]) * p.scale);
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.dq) + ((size_t)bh * p.Sq + q) * 64);
+        if (q < p.Sq) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
       }
     }
   }

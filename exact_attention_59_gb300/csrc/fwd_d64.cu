@@ -48,9 +48,10 @@ struct __align__(1024) FwdSmem {
 static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 
 // Pass 1 over one row's 128 scores of a kv block: x = s * scale (+ column bias
-// from the stage's table), -inf where the causal rule drops column cc > lim,
-// and the running maximum in four independent chains.
-template <bool TABLE, bool CAUSAL>
+// from the stage's table), -inf for columns cc > lim (the causal rule, or keys
+// past the end in a partial last block), and the running maximum in four
+// independent chains.
+template <bool TABLE, bool LIMITED>
 DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, float (&mx)[4]) {
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
@@ -63,7 +64,7 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
       const uint64_t xv = TABLE ? ffma2(sv, scv, j ? f2(bias.z, bias.w) : f2(bias.x, bias.y)) : fmul2(sv, scv);
       float x0, x1;
       unf2(xv, x0, x1);
-      if (CAUSAL) {
+      if (LIMITED) {
         x0 = c > lim ? -INFINITY : x0;
         x1 = c + 1 > lim ? -INFINITY : x1;
       }
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       if (aug) {
         // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column 0 of kaug[s]
         uint32_t bits = 0xffffffffu;
-        if (fu & KB_KEYMASK) bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+        if (fu & KB_KEYMASK) bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
         const uint16_t ninf = BF16 ? 0xFF80u : 0xFC00u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       } else if (use_table) {
         // lane owns columns 4 lane .. 4 lane + 3 of this kv block
         uint32_t bits = 0xffffffffu;
-        if (p.km_bits && (fu & KB_KEYMASK)) bits = __ldg(p.km_bits + (size_t)b * (p.Skv >> 5) + ((kb * 128 + 4 * lane) >> 5));
+        if (p.km_bits && (fu & KB_KEYMASK)) bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int col = 4 * lane + i;
@@ -321,16 +322,20 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const int kv0 = kb * 128;
         const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128) ||
                             ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-        const int lim = q - kv0;   // keep column cc iff cc <= lim
+        // keep column cc iff cc <= lim: the causal limit and, in a partial last kv
+        // block, the end of the keys
+        const int kvlim = p.Skv - 1 - kv0;
+        const bool limited = causal || kvlim < 127;
+        const int lim = causal ? min(q - kv0, kvlim) : kvlim;
         const float* tb = sm.cb[s][parity];
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // one straight-line copy of the pass per (table, causal) pair: a runtime
         // test inside the unrolled loop would cost instructions on every score
         if (use_table) {
-          if (causal) scale_scores<true, true>(r, scv, tb, lim, mx);
+          if (limited) scale_scores<true, true>(r, scv, tb, lim, mx);
           else scale_scores<true, false>(r, scv, tb, lim, mx);
         } else {
-          if (causal) scale_scores<false, true>(r, scv, tb, lim, mx);
+          if (limited) scale_scores<false, true>(r, scv, tb, lim, mx);
           else scale_scores<false, false>(r, scv, tb, lim, mx);
         }
         // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
@@ -406,11 +411,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((size_t)bh * p.Sq + q) * 64);
+        // rows past Sq (partial last q tile) are computed, not written; the TMEM
+        // load above stays warp-wide (tcgen05.ld is .sync.aligned)
+        if (q < p.Sq) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((size_t)bh * p.Sq + q) * 64);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
-        p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (m_fin + lg2(l)) * kLn2 : -INFINITY;
+          for (int i = 0; i < 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
+          p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (m_fin + lg2(l)) * kLn2 : -INFINITY;
+        }
       }
     }
   }

@@ -351,6 +351,13 @@ DEVI uint16_t to16(float x) { return static_cast<uint16_t>(pack2<BF16>(x, 0.f) &
 template <bool BF16>
 DEVI float from16(uint16_t v) { return unpack2<BF16>(static_cast<uint32_t>(v)).x; }
 
+// Word of the packed key mask (bit j = key 32 w + j kept) holding key `key` of
+// batch b; words past the end of the row (a partial last kv block) read as 0.
+DEVI uint32_t km_word(const uint32_t* bits, int b, int Skv, int key) {
+  const int nw = (Skv + 31) >> 5, wi = key >> 5;
+  return wi < nw ? __ldg(bits + (size_t)b * nw + wi) : 0u;
+}
+
 // One f32 value x as three 16-bit terms, x = t0 + t1 + 2048 t2, written to columns
 // 0..2 of row r of a K = 16 operand (no swizzle).  The 2048 t2 term keeps f16 in
 // range; t0 + t1 carry the rest to about 2^-22 relative.  -inf goes to t2 alone.

@@ -77,8 +77,12 @@ def _fwd(lib, shape, q=FAKE, k=FAKE, v=FAKE, km=None, bm=None, mod=0, scale=0.12
 
 def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, None) == lib.ATTN_ERR_INVALID_ARG
-    assert _fwd(lib, _shape(lib, Sq=200)) == lib.ATTN_ERR_SHAPE
-    assert _fwd(lib, _shape(lib, Skv=130)) == lib.ATTN_ERR_SHAPE
+    # any lengths on the f16/bf16 D=64 path, multiples of 128 elsewhere
+    assert _fwd(lib, _shape(lib, Sq=200, dt=0)) == lib.ATTN_ERR_SHAPE
+    assert _fwd(lib, _shape(lib, Skv=130, D=512)) == lib.ATTN_ERR_SHAPE
+    assert _fwd(lib, _shape(lib, Sq=200, Skv=130), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE   # shape accepted
+    assert _fwd(lib, _shape(lib, Sq=1, Skv=1), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE
+    assert _fwd(lib, _shape(lib, Skv=2048 * 128 + 1)) == lib.ATTN_ERR_SHAPE   # more kv tiles than built
     assert _fwd(lib, _shape(lib, D=96)) == lib.ATTN_ERR_UNSUPPORTED
     assert _fwd(lib, _shape(lib, D=512, dt=0)) == lib.ATTN_ERR_UNSUPPORTED
     assert _fwd(lib, _shape(lib, dt=7)) == lib.ATTN_ERR_INVALID_ARG

@@ -43,7 +43,7 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
         d["key_mask"] = key_mask_override.cuda()
     bm = E.create_block_mask(bm_kind, 1, 1, Sq, Skv) if bm_kind else None
     tdt = d["q"].dtype
-    nqb, nkb = Sq // 128, Skv // 128
+    nqb, nkb = -(-Sq // 128), -(-Skv // 128)
     ob, out = guarded((B, H, Sq, D), tdt)
     lb, lse = guarded((B, H, Sq), torch.float32)
     vis = torch.full((B, H, nqb, nkb), 7, dtype=torch.uint8, device="cuda")
@@ -120,6 +120,36 @@ def test_rectangular_and_single_tile():
     run_and_check(2, 2, 512, 128, "f16", "checkerboard", False, None)
     run_and_check(1, 1, 128, 128, "bf16", "none", False, "causal")
     run_and_check(1, 3, 640, 640, "bf16", "none", False, "causal")   # odd number of q tiles
+
+
+# Lengths that are not multiples of 128 (f16/bf16, D=64): partial last q and kv
+# tiles, single rows and single keys, both sides of the causal diagonal.
+RAGGED = [
+    (1, 2, 200, 200, "bf16", "none", True, None),
+    (2, 1, 130, 333, "f16", "causal", False, None),
+    (1, 2, 1000, 77, "bf16", "alibi", True, None),
+    (1, 1, 77, 1000, "f16", "checkerboard", False, "causal"),
+    (2, 2, 300, 300, "bf16", "causal", True, "causal"),
+    (1, 2, 1, 129, "f16", "none", True, None),
+    (1, 2, 129, 1, "bf16", "alibi", False, None),
+    (1, 1, 255, 257, "f16", "alibi", True, "causal"),
+    (1, 3, 383, 129, "bf16", "checkerboard", True, None),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,dtype,mod,km,bm", RAGGED)
+def test_ragged_lengths(B, H, Sq, Skv, dtype, mod, km, bm):
+    run_and_check(B, H, Sq, Skv, dtype, mod, km, bm)
+
+
+def test_ragged_fully_masked():
+    """A batch with no key, and a partial last kv block whose kept keys are all masked."""
+    km = torch.ones((2, 333), dtype=torch.uint8)
+    km[1] = 0
+    km[0, 256:] = 0
+    for dt in ("bf16", "f16"):
+        run_and_check(2, 2, 150, 333, dt, "none", True, None, key_mask_override=km)
+        run_and_check(2, 1, 150, 333, dt, "causal", True, None, key_mask_override=km)
 
 
 def test_fully_masked_batches_and_blocks():
