@@ -25,8 +25,11 @@
  *  - key_mask is uint8 (B, Skv), nonzero = attend; NULL = no key mask.
  *  - Every pointer must be 16-byte aligned (the TMA engine needs it), else
  *    ATTN_ERR_ALIGN.
- *  - Prefill (attn_fwd / attn_bwd) needs Sq and Skv to be multiples of 128,
- *    as the attnax Pallas forward requires seq_q % block_q == 0 and
+ *  - Prefill (attn_fwd / attn_bwd) in f16/bf16 with D = 64 takes any
+ *    Sq, Skv >= 1 (up to 2048 tiles of 128): the last q and kv tiles may be
+ *    partial; keys past Skv get no weight and rows past Sq are not written.
+ *    float32 and D = 512 need Sq and Skv to be multiples of 128, as the
+ *    attnax Pallas forward requires seq_q % block_q == 0 and
  *    seq_kv % block_kv == 0 with block_q = block_kv = 128; else
  *    ATTN_ERR_SHAPE.  D must be 64 (all dtypes) or 512 (bf16/f16 forward).
  *  - The library allocates no memory and keeps no state.  Scratch space
@@ -60,7 +63,8 @@ typedef struct CUstream_st* attn_stream_t;
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, bad enum, bad scale */
-  ATTN_ERR_SHAPE = 2,       /* Sq/Skv not a multiple of 128 (prefill), Sq != 1 (decode), size overflow */
+  ATTN_ERR_SHAPE = 2,       /* Sq/Skv not a multiple of 128 (f32 or D=512 prefill), more than 2048 tiles,
+                               Sq != 1 (decode), size overflow */
   ATTN_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned (workspace: 256-byte) */
   ATTN_ERR_UNSUPPORTED = 4, /* dtype / D / mod / block-size combination not built */
   ATTN_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than attn_workspace_size() */
