@@ -13,7 +13,9 @@ online-softmax method reaches exactly (up to rounding order):
 * with the FlexAttention-style hooks of the flaxattention README ("Example
   usage": ``score_mod``, ``create_block_mask(causal_mask, ...)``,
   ``generate_alibi_bias``, ``checkerboard``), and the key-padding mask of shape
-  (batch, seq) from the flash-attention-jax docs ("3. Use flash_attention");
+  (batch, seq) from the flash-attention-jax docs ("3. Use flash_attention"),
+  and the dense boolean mask broadcastable to (batch, heads, seq_q, seq_kv) of
+  the attnax ``pallas_flash_attention`` arguments;
 * in the order of operations of the attnax Pallas kernel body
   (``_pallas_forward.kernel.body``): scale, then score_mod, then mask, then
   softmax, then the product with V.
@@ -21,7 +23,8 @@ online-softmax method reaches exactly (up to rounding order):
 Readings where the pages are silent (each one is listed in the design doc):
 
 * the key mask keeps a key where it is nonzero (``jnp.where(m, scores, neg)``
-  in the Pallas kernel body);
+  in the Pallas kernel body); so does the dense mask for a (query, key) pair,
+  given with batch and head extents of B or 1;
 * masked scores are -inf (not ``finfo.min``), so a fully masked row has
   O = 0, lse = -inf and zero gradients;
 * ALiBi adds ``slope_h * (kv_idx - q_idx)`` with ``slope_h = 2**(-8(h+1)/H)``
@@ -156,19 +159,29 @@ class BlockMask:
         return self.tiles[bb, hh]
 
 
+def dense_mask_head(dense_mask, b: int, h: int) -> np.ndarray:
+    """The (Sq, Skv) slice of a dense mask (Bm, Hm, Sq, Skv), Bm in {1, B}, Hm in {1, H}."""
+    dm = np.asarray(dense_mask)
+    assert dm.ndim == 4
+    return dm[0 if dm.shape[0] == 1 else b, 0 if dm.shape[1] == 1 else h]
+
+
 def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
-                block_mask: BlockMask | None = None, score_mod=MOD_NONE):
+                block_mask: BlockMask | None = None, score_mod=MOD_NONE, dense_mask=None):
     """Which (q, kv) entries take part in the softmax of head (b, h).
 
-    An entry is kept iff the key mask keeps kv (if given), the causal
-    score_mod keeps it (if selected), and its tile is not EMPTY and either FULL
-    or kept by the block mask's mask_mod (if a block mask is given).
+    An entry is kept iff the key mask keeps kv (if given), the dense mask keeps
+    (q, kv) (if given), the causal score_mod keeps it (if selected), and its
+    tile is not EMPTY and either FULL or kept by the block mask's mask_mod (if
+    a block mask is given).
     """
     q_idx = np.asarray(q_idx, dtype=np.int64)
     kv_idx = np.asarray(kv_idx, dtype=np.int64)
     _, keep = score_bias(score_mod, h, H, q_idx, kv_idx)
     if key_mask is not None:
         keep &= (np.asarray(key_mask)[b][kv_idx] != 0)[None, :]
+    if dense_mask is not None:
+        keep &= dense_mask_head(dense_mask, b, h)[q_idx[:, None], kv_idx[None, :]] != 0
     if block_mask is not None:
         st = block_mask.states(b, h)
         ts = st[(q_idx // block_mask.block_q)[:, None], (kv_idx // block_mask.block_kv)[None, :]]
@@ -178,12 +191,12 @@ def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
 
 
 def masked_logits(qbh, kbh, b, h, H, scale, q_idx, kv_idx, key_mask=None,
-                  block_mask=None, score_mod=MOD_NONE):
+                  block_mask=None, score_mod=MOD_NONE, dense_mask=None):
     """S = scale * q k^T + bias, with -inf where masked (float64)."""
     s = scale * (qbh @ kbh.T)
     bias, _ = score_bias(score_mod, h, H, q_idx, kv_idx)
     s = s + bias
-    keep = keep_matrix(b, h, H, q_idx, kv_idx, key_mask, block_mask, score_mod)
+    keep = keep_matrix(b, h, H, q_idx, kv_idx, key_mask, block_mask, score_mod, dense_mask)
     return np.where(keep, s, -np.inf), keep
 
 
@@ -214,10 +227,11 @@ def _default_scale(D, scale):
 # ---------------------------------------------------------------------------
 
 def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None,
-             score_mod=MOD_NONE, scale=None, heads=None, rows=None):
+             score_mod=MOD_NONE, scale=None, heads=None, rows=None, dense_mask=None):
     """O = softmax(mask(scale q k^T + bias)) v and lse, per (b, h), in float64.
 
-    q: (B, H, Sq, D); k, v: (B, H, Skv, D); key_mask: (B, Skv) or None.
+    q: (B, H, Sq, D); k, v: (B, H, Skv, D); key_mask: (B, Skv) or None;
+    dense_mask: (B|1, H|1, Sq, Skv) or None.
     ``heads``: optional list of (b, h) to compute (others stay NaN).
     ``rows``: optional 1-D array of query rows to compute (others stay NaN).
     Returns (o (B, H, Sq, D), lse (B, H, Sq)).
@@ -233,24 +247,24 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None,
     todo = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     for b, h in todo:
         s, _ = masked_logits(q[b, h, q_idx], k[b, h], b, h, H, scale, q_idx, kv_idx,
-                             key_mask, block_mask, score_mod)
+                             key_mask, block_mask, score_mod, dense_mask)
         p, l = softmax_rows(s)
         o[b, h, q_idx] = p @ v[b, h]
         lse[b, h, q_idx] = l
     return o, lse
 
 
-def attn_probs(q, k, b, h, key_mask=None, block_mask=None, score_mod=MOD_NONE, scale=None):
+def attn_probs(q, k, b, h, key_mask=None, block_mask=None, score_mod=MOD_NONE, scale=None, dense_mask=None):
     """P of one head (Sq, Skv), float64."""
     q, k = _f64(q), _f64(k)
     B, H, Sq, D = q.shape
     s, _ = masked_logits(q[b, h], k[b, h], b, h, H, _default_scale(D, scale),
-                         np.arange(Sq), np.arange(k.shape[2]), key_mask, block_mask, score_mod)
+                         np.arange(Sq), np.arange(k.shape[2]), key_mask, block_mask, score_mod, dense_mask)
     return softmax_rows(s)[0]
 
 
 def attn_bwd(q, k, v, dout, key_mask=None, block_mask: BlockMask | None = None,
-             score_mod=MOD_NONE, scale=None, heads=None):
+             score_mod=MOD_NONE, scale=None, heads=None, dense_mask=None):
     """Analytic gradients of sum(dout * O) with respect to q, k, v (float64).
 
     With P the attention weights:  dV = P^T dO;  dP = dO V^T;
@@ -268,7 +282,7 @@ def attn_bwd(q, k, v, dout, key_mask=None, block_mask: BlockMask | None = None,
     todo = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     for b, h in todo:
         s, _ = masked_logits(q[b, h], k[b, h], b, h, H, scale, np.arange(Sq), np.arange(Skv),
-                             key_mask, block_mask, score_mod)
+                             key_mask, block_mask, score_mod, dense_mask)
         p, _ = softmax_rows(s)
         do = dout[b, h]
         dv[b, h] = p.T @ do
@@ -287,8 +301,9 @@ def attn_decode(q, k, v, key_mask=None, score_mod=MOD_NONE, scale=None):
 
 
 def visited_tiles(B, H, Sq, Skv, key_mask=None, block_mask: BlockMask | None = None,
-                  block_q=128, block_kv=128):
-    """Tiles the method computes: not EMPTY in the block mask, and not all keys padded.
+                  block_q=128, block_kv=128, dense_mask=None):
+    """Tiles the method computes: not EMPTY in the block mask, not all keys
+    padded, and (with a dense mask) some pair of the tile kept by the dense mask.
 
     Returns uint8 (B, H, ceil(Sq/block_q), ceil(Skv/block_kv)), 1 = visited.
     """
@@ -302,6 +317,12 @@ def visited_tiles(B, H, Sq, Skv, key_mask=None, block_mask: BlockMask | None = N
                 km = np.asarray(key_mask)[b]
                 alive = np.array([km[kb * block_kv:(kb + 1) * block_kv].any() for kb in range(nkb)])
                 vis[b, h] &= alive[None, :].astype(np.uint8)
+            if dense_mask is not None:
+                dm = dense_mask_head(dense_mask, b, h) != 0
+                for qb in range(nqb):
+                    for kb in range(nkb):
+                        if not dm[qb * block_q:(qb + 1) * block_q, kb * block_kv:(kb + 1) * block_kv].any():
+                            vis[b, h, qb, kb] = 0
     return vis
 
 
@@ -310,7 +331,7 @@ def visited_tiles(B, H, Sq, Skv, key_mask=None, block_mask: BlockMask | None = N
 # ---------------------------------------------------------------------------
 
 def attn_fwd_online(q, k, v, key_mask=None, block_mask=None, score_mod=MOD_NONE,
-                    scale=None, block_q=128, block_kv=128):
+                    scale=None, block_q=128, block_kv=128, dense_mask=None):
     """The online-softmax forward of the Pallas kernel, step by step, in float64.
 
     Per q block: m = -inf, l = 0, acc = 0; per kv block: scores = q k^T scale,
@@ -325,7 +346,7 @@ def attn_fwd_online(q, k, v, key_mask=None, block_mask=None, score_mod=MOD_NONE,
     B, H, Sq, D = q.shape
     Skv = k.shape[2]
     scale = _default_scale(D, scale)
-    vis = visited_tiles(B, H, Sq, Skv, key_mask, block_mask, block_q, block_kv)
+    vis = visited_tiles(B, H, Sq, Skv, key_mask, block_mask, block_q, block_kv, dense_mask)
     o = np.zeros((B, H, Sq, v.shape[3]))
     lse = np.zeros((B, H, Sq))
     for b in range(B):
@@ -340,7 +361,7 @@ def attn_fwd_online(q, k, v, key_mask=None, block_mask=None, score_mod=MOD_NONE,
                         continue
                     kj = np.arange(kb * block_kv, min(Skv, (kb + 1) * block_kv))
                     s, _ = masked_logits(q[b, h, qi], k[b, h, kj], b, h, H, scale, qi, kj,
-                                         key_mask, block_mask, score_mod)
+                                         key_mask, block_mask, score_mod, dense_mask)
                     m_new = np.maximum(m, s.max(axis=1))
                     m_use = np.where(np.isfinite(m_new), m_new, 0.0)
                     alpha = np.exp(m - m_use)

@@ -234,7 +234,7 @@ def _fd_grad(f, x, h=1e-6):
 
 
 FD_CASES = [(S, D, mod, mask) for S, D in [(3, 2), (5, 4), (8, 2)] for mod in MODS
-            for mask in ("none", "key", "block")]
+            for mask in ("none", "key", "block", "dense")]
 
 
 @pytest.mark.parametrize("S,D,mod,mask", FD_CASES)
@@ -249,6 +249,10 @@ def test_finite_differences(S, D, mod, mask):
         kw["key_mask"] = km
     elif mask == "block":
         kw["block_mask"] = A.BlockMask(A.build_block_mask("causal", 1, H, S, S, 2, 2), "causal", 2, 2)
+    elif mask == "dense":
+        dm = (np.random.default_rng(77 + S).random((1, H, S, S)) > 0.4).astype(np.uint8)
+        dm[:, :, :, 0] = 1                # every row keeps a key
+        kw["dense_mask"] = dm
     dq, dk, dv = A.attn_bwd(q, k, v, do, **kw)
     for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
         def f(xx, name=name):
@@ -265,7 +269,7 @@ def test_finite_differences(S, D, mod, mask):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("mod", MODS)
-@pytest.mark.parametrize("mask", ["none", "key", "block", "key+block"])
+@pytest.mark.parametrize("mask", ["none", "key", "block", "key+block", "dense", "dense+key"])
 def test_online_recurrence_matches_plain(mod, mask):
     B, H, Sq, Skv, D, bq, bk = 2, 2, 24, 32, 5, 8, 8
     q, k, v = _rand(B, H, Sq, D, seed=80), _rand(B, H, Skv, D, seed=81), _rand(B, H, Skv, D, seed=82)
@@ -278,6 +282,11 @@ def test_online_recurrence_matches_plain(mod, mask):
         kw["key_mask"] = km
     if "block" in mask:
         kw["block_mask"] = A.BlockMask(A.build_block_mask("causal", 1, 1, Sq, Skv, bq, bk), "causal", bq, bk)
+    if "dense" in mask:
+        dm = (np.random.default_rng(84).random((1, H, Sq, Skv)) > 0.5).astype(np.uint8)
+        dm[0, 1, 8:16, 16:24] = 0         # one tile of head 1 with no kept pair (skipped)
+        dm[0, 0, 3, :] = 0                # a row with no kept key
+        kw["dense_mask"] = dm
     o1, l1 = A.attn_fwd(q, k, v, **kw)
     o2, l2 = A.attn_fwd_online(q, k, v, block_q=bq, block_kv=bk, **kw)
     fin = np.isfinite(l1)
@@ -331,3 +340,77 @@ def test_block_mask_full_tile_skips_mask_mod():
     tiles[:] = 0
     o_empty, l_empty = A.attn_fwd(q, k, v, block_mask=A.BlockMask(tiles, "causal", 4, 4))
     assert (o_empty == 0).all() and np.isneginf(l_empty).all()
+
+
+# ---------------------------------------------------------------------------
+# dense (query, key) mask: brute force, and the special cases it reduces to
+# ---------------------------------------------------------------------------
+
+def _brute_dense(q, k, v, dm, scale):
+    """Per row, softmax over the kept keys only, by explicit loops and math.exp."""
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    o = np.zeros((B, H, Sq, D))
+    lse = np.zeros((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            m = dm[b if dm.shape[0] > 1 else 0, h if dm.shape[1] > 1 else 0]
+            for i in range(Sq):
+                kept = [j for j in range(Skv) if m[i, j] != 0]
+                if not kept:
+                    lse[b, h, i] = -math.inf
+                    continue
+                z = [scale * sum(q[b, h, i, d] * k[b, h, j, d] for d in range(D)) for j in kept]
+                top = max(z)
+                w = [math.exp(x - top) for x in z]
+                tot = sum(w)
+                lse[b, h, i] = top + math.log(tot)
+                for wj, j in zip(w, kept):
+                    o[b, h, i] += (wj / tot) * v[b, h, j]
+    return o, lse
+
+
+@pytest.mark.parametrize("bshape", [(2, 3), (1, 3), (2, 1), (1, 1)])
+def test_dense_mask_brute_force(bshape):
+    """Non-square, non-symmetric masks with every broadcast form of the batch and head extents."""
+    B, H, Sq, Skv, D = 2, 3, 5, 7, 3
+    q, k, v = _rand(B, H, Sq, D, seed=100), _rand(B, H, Skv, D, seed=101), _rand(B, H, Skv, D, seed=102)
+    dm = (np.random.default_rng(103).random(bshape + (Sq, Skv)) > 0.5).astype(np.uint8)
+    dm[..., 2, :] = 0                     # a row with no kept key
+    dm[..., 4, :] = 3                     # any nonzero value keeps
+    o, lse = A.attn_fwd(q, k, v, dense_mask=dm, scale=0.6)
+    ob, lb = _brute_dense(q, k, v, dm, 0.6)
+    np.testing.assert_allclose(o, ob, rtol=1e-12, atol=1e-12)
+    assert (np.isneginf(lse) == np.isneginf(lb)).all()
+    fin = np.isfinite(lb)
+    np.testing.assert_allclose(lse[fin], lb[fin], rtol=1e-12, atol=1e-12)
+
+
+def test_dense_mask_reduces_to_key_mask_and_causal():
+    """A dense mask equal to the key mask broadcast over rows, or to the lower
+    triangle, gives exactly the key-mask or causal result (values and gradients)."""
+    B, H, S, D = 2, 2, 9, 4
+    q, k, v, do = (_rand(B, H, S, D, seed=s) for s in (110, 111, 112, 113))
+    km = (np.random.default_rng(114).random((B, S)) > 0.3).astype(np.uint8)
+    dm = np.broadcast_to(km[:, None, None, :], (B, 1, S, S)).astype(np.uint8)
+    for f in (A.attn_fwd, lambda *a, **kw: A.attn_bwd(*a, do, **kw)):
+        ra = f(q, k, v, key_mask=km)
+        rb = f(q, k, v, dense_mask=dm)
+        for x, y in zip(ra, rb):
+            np.testing.assert_array_equal(x, y)
+    tril = np.tril(np.ones((S, S), np.uint8))[None, None]
+    for f in (A.attn_fwd, lambda *a, **kw: A.attn_bwd(*a, do, **kw)):
+        ra = f(q, k, v, score_mod="causal")
+        rb = f(q, k, v, dense_mask=tril)
+        for x, y in zip(ra, rb):
+            np.testing.assert_array_equal(x, y)
+
+
+def test_visited_tiles_skip_empty_dense_tiles():
+    dm = np.ones((1, 2, 300, 260), np.uint8)
+    dm[0, 1, 128:256, 0:128] = 0          # tile (1, 0) of head 1 has no kept pair
+    dm[0, 0, 256:, 256:] = 0              # the partial corner tile of head 0
+    vis = A.visited_tiles(2, 2, 300, 260, dense_mask=dm)
+    assert vis.shape == (2, 2, 3, 3)
+    assert (vis[:, 1, 1, 0] == 0).all() and (vis[:, 0, 2, 2] == 0).all()
+    assert vis.sum() == 2 * (18 - 2)
