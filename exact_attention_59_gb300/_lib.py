@@ -25,7 +25,8 @@ MODS = {"none": 0, "alibi": 1, "checkerboard": 2, "causal": 3}
 MASK_MODS = {"none": 0, "causal": 1}
 
 SYMBOLS = ("attn_workspace_size", "attn_build_block_mask", "attn_fwd", "attn_bwd", "attn_bwd_preprocess",
-           "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_poll_status", "attn_status_string")
+           "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_poll_status", "attn_status_string",
+           "attn_dense_mask_bytes", "attn_pack_dense_mask", "attn_fwd_dense", "attn_bwd_dense")
 
 
 class AttnError(RuntimeError):
@@ -42,6 +43,11 @@ class Shape(ctypes.Structure):
 class BlockMaskC(ctypes.Structure):
     _fields_ = [("tiles", ctypes.c_void_p), ("bcast_b", ctypes.c_int), ("bcast_h", ctypes.c_int),
                 ("block_q", ctypes.c_int), ("block_kv", ctypes.c_int), ("mask_mod", ctypes.c_int)]
+
+
+class DenseMaskC(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("packed_bytes", ctypes.c_size_t), ("bcast_b", ctypes.c_int),
+                ("bcast_h", ctypes.c_int)]
 
 
 _lib = None
@@ -61,7 +67,7 @@ def load():
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m exact_attention_59_gb300.build`")
         lib = ctypes.CDLL(LIB_PATH)
-        sp, bp = ctypes.POINTER(Shape), ctypes.POINTER(BlockMaskC)
+        sp, bp, dp = ctypes.POINTER(Shape), ctypes.POINTER(BlockMaskC), ctypes.POINTER(DenseMaskC)
         sig = {
             "attn_workspace_size": (SZ, [I, sp]),
             "attn_build_block_mask": (I, [I, I, I, I, I, I, I, P, P]),
@@ -73,6 +79,10 @@ def load():
             "attn_decode": (I, [sp, P, P, P, P, I, F, P, P, P, SZ, P]),
             "attn_poll_status": (I, [P, P]),
             "attn_status_string": (ctypes.c_char_p, [I]),
+            "attn_dense_mask_bytes": (SZ, [sp, I, I]),
+            "attn_pack_dense_mask": (I, [sp, P, I, I, P, SZ, P]),
+            "attn_fwd_dense": (I, [sp, P, P, P, P, dp, bp, I, F, P, P, P, SZ, P, P]),
+            "attn_bwd_dense": (I, [sp, P, P, P, P, P, P, P, dp, bp, I, F, P, P, P, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -163,6 +173,43 @@ def create_block_mask(mask_mod, B, H, Sq, Skv, device="cuda", block_q=128, block
     return BlockMask(tiles, mm, block_q, block_kv)
 
 
+class DenseMask:
+    """A dense (query, key) mask packed on the device by attn_pack_dense_mask.
+
+    Built from a uint8 or bool tensor of shape (B|1, H|1, Sq, Skv), nonzero =
+    attend; reusable by every forward and backward call of that (B, H, Sq, Skv).
+    """
+
+    def __init__(self, packed: torch.Tensor, bcast_b: int, bcast_h: int):
+        self.packed, self.bcast_b, self.bcast_h = packed, int(bcast_b), int(bcast_h)
+
+    def c(self) -> DenseMaskC:
+        return DenseMaskC(self.packed.data_ptr(), self.packed.numel(), self.bcast_b, self.bcast_h)
+
+
+def pack_dense_mask(mask: torch.Tensor, B: int, H: int) -> DenseMask:
+    """Packs ``mask`` (B|1, H|1, Sq, Skv) for heads of batch B and H heads."""
+    _cuda(mask)
+    if mask.dim() != 4 or mask.shape[0] not in (1, B) or mask.shape[1] not in (1, H):
+        raise ValueError(f"dense mask of shape {tuple(mask.shape)} does not broadcast to ({B}, {H}, Sq, Skv)")
+    m = mask.to(torch.uint8).contiguous() if mask.dtype != torch.uint8 or not mask.is_contiguous() else mask
+    bb, bh = int(mask.shape[0] == 1 and B > 1), int(mask.shape[1] == 1 and H > 1)
+    shape = Shape(B, H, mask.shape[2], mask.shape[3], 64, ATTN_F16)
+    n = int(load().attn_dense_mask_bytes(ctypes.byref(shape), bb, bh))
+    if n == 0:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "attn_dense_mask_bytes")
+    packed = torch.empty(n, dtype=torch.uint8, device=mask.device)
+    _check(load().attn_pack_dense_mask(ctypes.byref(shape), _ptr(m), bb, bh, _ptr(packed), n,
+                                       _stream(mask.device)), "attn_pack_dense_mask")
+    dm = DenseMask(packed, bb, bh)
+    dm._source = m   # keeps a converted copy alive until the packing kernel has run
+    return dm
+
+
+def _dm(dm):
+    return None if dm is None else ctypes.byref(dm.c())
+
+
 def _mod(m) -> int:
     return MODS[m] if isinstance(m, str) else int(m)
 
@@ -172,7 +219,7 @@ def _bm(bm):
 
 
 def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_mod="none", scale=None,
-             out=None, lse=None, debug_visited=None, ws=None):
+             out=None, lse=None, debug_visited=None, ws=None, dense_mask: DenseMask | None = None):
     """(out, lse) of the forward pass on q's device and current stream."""
     _cuda(q, k, v, key_mask, out, lse)
     shape = make_shape(q, k)
@@ -180,15 +227,20 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
     ws = workspace(OP_FWD, shape, q.device) if ws is None else ws
-    code = load().attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _bm(block_mask),
-                           _mod(score_mod), scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device),
-                           _ptr(debug_visited))
+    if dense_mask is None:
+        code = load().attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _bm(block_mask),
+                               _mod(score_mod), scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                               _stream(q.device), _ptr(debug_visited))
+    else:
+        code = load().attn_fwd_dense(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _dm(dense_mask),
+                                     _bm(block_mask), _mod(score_mod), scale, _ptr(out), _ptr(lse), _ptr(ws),
+                                     ws.numel(), _stream(q.device), _ptr(debug_visited))
     _check(code, "attn_fwd")
     return out, lse
 
 
 def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod="none", scale=None,
-             dq=None, dk=None, dv=None, ws=None):
+             dq=None, dk=None, dv=None, ws=None, dense_mask: DenseMask | None = None):
     """(dq, dk, dv) of sum(dout * out)."""
     _cuda(q, k, v, out, lse, dout, key_mask)
     shape = make_shape(q, k)
@@ -197,9 +249,14 @@ def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod=
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
-    code = load().attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                           _ptr(key_mask), _bm(block_mask), _mod(score_mod), scale, _ptr(dq), _ptr(dk), _ptr(dv),
-                           _ptr(ws), ws.numel(), _stream(q.device))
+    if dense_mask is None:
+        code = load().attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(key_mask), _bm(block_mask), _mod(score_mod), scale, _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(ws), ws.numel(), _stream(q.device))
+    else:
+        code = load().attn_bwd_dense(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                     _ptr(dout), _ptr(key_mask), _dm(dense_mask), _bm(block_mask), _mod(score_mod),
+                                     scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(q.device))
     _check(code, "attn_bwd")
     return dq, dk, dv
 

@@ -237,6 +237,36 @@ SimtParams simt_params(const attn_shape* s, const void* q, const void* k, const 
   return p;
 }
 
+long long dense_mask_count(const attn_shape* s, int bcast_b, int bcast_h) {
+  return (long long)(bcast_b ? 1 : s->B) * (bcast_h ? 1 : s->H);
+}
+
+// A dense mask rides on the f16/bf16 D = 64 path only.
+attn_status check_dm(const attn_shape* s, const attn_dense_mask* dm) {
+  if (!dm) return ATTN_OK;
+  if (!dm->packed || (dm->bcast_b != 0 && dm->bcast_b != 1) || (dm->bcast_h != 0 && dm->bcast_h != 1))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(dm->packed, 256)) return ATTN_ERR_ALIGN;
+  if (s->D != 64 || s->dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+  if (dm->packed_bytes < dense_mask_layout(dense_mask_count(s, dm->bcast_b, dm->bcast_h), s->Sq, s->Skv).total)
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+DenseMaskView dm_view(const attn_shape* s, const attn_dense_mask* dm) {
+  DenseMaskView v;
+  std::memset(&v, 0, sizeof(v));
+  if (!dm) return v;
+  const DenseMaskLayout l = dense_mask_layout(dense_mask_count(s, dm->bcast_b, dm->bcast_h), s->Sq, s->Skv);
+  const uint8_t* base = static_cast<const uint8_t*>(dm->packed);
+  v.tiles = base + l.tiles;
+  v.rowbits = reinterpret_cast<const uint32_t*>(base + l.rowbits);
+  v.colbits = reinterpret_cast<const uint32_t*>(base + l.colbits);
+  v.mh = dm->bcast_h ? 0 : 1;
+  v.mb = dm->bcast_b ? 0 : (dm->bcast_h ? 1 : s->H);
+  return v;
+}
+
 }  // namespace
 
 extern "C" {
@@ -271,9 +301,17 @@ attn_status attn_build_block_mask(attn_mask_mod mask_mod, int B, int H, int Sq, 
 attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
                      const attn_block_mask* bm, attn_score_mod mod, float scale, void* out, float* lse, void* ws,
                      size_t ws_bytes, attn_stream_t stream, uint8_t* debug_visited) {
+  return attn_fwd_dense(s, q, k, v, key_mask, nullptr, bm, mod, scale, out, lse, ws, ws_bytes, stream, debug_visited);
+}
+
+attn_status attn_fwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                           const attn_dense_mask* dm, const attn_block_mask* bm, attn_score_mod mod, float scale,
+                           void* out, float* lse, void* ws, size_t ws_bytes, attn_stream_t stream,
+                           uint8_t* debug_visited) {
   ATTN_TRY(check_prefill(s, false));
   ATTN_TRY(check_mod(mod, scale));
   ATTN_TRY(check_bm(bm));
+  ATTN_TRY(check_dm(s, dm));
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -329,6 +367,7 @@ attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const vo
   p.bm_tiles = bm ? bm->tiles : nullptr;
   if (bm) bm_strides(s, bm, p.bm_sb, p.bm_sh);
   p.bm_mod = bm ? (int)bm->mask_mod : 0;
+  p.dm = dm_view(s, dm);
   p.visited = debug_visited;
   p.status = at<int>(ws, 0);
   p.B = s->B;
@@ -360,10 +399,16 @@ attn_status attn_bwd_preprocess(const attn_shape* s, const void* out, const floa
                                            at<uint32_t>(ws, w.km_bits), at<uint8_t>(ws, w.km_sum), st));
 }
 
-attn_status attn_bwd_dkdv(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
-                          const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale,
-                          void* dk, void* dv, void* ws, size_t ws_bytes, attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                          const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
+                          attn_score_mod mod, float scale, void* dk, void* dv, void* ws, size_t ws_bytes,
+                          attn_stream_t stream) {
   ATTN_TRY(check_prefill(s, true));
+  ATTN_TRY(check_dm(s, dm));
   ATTN_TRY(check_mod(mod, scale));
   ATTN_TRY(check_bm(bm));
   ATTN_PTR(q);
@@ -390,13 +435,15 @@ attn_status attn_bwd_dkdv(const attn_shape* s, const void* q, const void* k, con
   if (!ok) return ATTN_ERR_CUDA;
   p.dk = dk;
   p.dv = dv;
+  p.dm = dm_view(s, dm);
   return cuda_status(launch_bwd_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
-attn_status attn_bwd_dq(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
-                        const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq,
-                        void* ws, size_t ws_bytes, attn_stream_t stream) {
+attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                        const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
+                        attn_score_mod mod, float scale, void* dq, void* ws, size_t ws_bytes, attn_stream_t stream) {
   ATTN_TRY(check_prefill(s, true));
+  ATTN_TRY(check_dm(s, dm));
   ATTN_TRY(check_mod(mod, scale));
   ATTN_TRY(check_bm(bm));
   ATTN_PTR(q);
@@ -420,17 +467,43 @@ attn_status attn_bwd_dq(const attn_shape* s, const void* q, const void* k, const
   BwdParams p = bwd_params(s, q, k, v, dout, key_mask, bm, mod, scale, ws, ok);
   if (!ok) return ATTN_ERR_CUDA;
   p.dq = dq;
+  p.dm = dm_view(s, dm);
   return cuda_status(launch_bwd_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_dkdv(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                          const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale,
+                          void* dk, void* dv, void* ws, size_t ws_bytes, attn_stream_t stream) {
+  return bwd_dkdv_impl(s, q, k, v, dout, key_mask, nullptr, bm, mod, scale, dk, dv, ws, ws_bytes, stream);
+}
+
+attn_status attn_bwd_dq(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
+                        const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq,
+                        void* ws, size_t ws_bytes, attn_stream_t stream) {
+  return bwd_dq_impl(s, q, k, v, dout, key_mask, nullptr, bm, mod, scale, dq, ws, ws_bytes, stream);
 }
 
 attn_status attn_bwd(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
                      const float* lse, const void* dout, const uint8_t* key_mask, const attn_block_mask* bm,
                      attn_score_mod mod, float scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                      attn_stream_t stream) {
+  return attn_bwd_dense(s, q, k, v, out, lse, dout, key_mask, nullptr, bm, mod, scale, dq, dk, dv, ws, ws_bytes,
+                        stream);
+}
+
+attn_status attn_bwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
+                           const float* lse, const void* dout, const uint8_t* key_mask, const attn_dense_mask* dm,
+                           const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq, void* dk, void* dv,
+                           void* ws, size_t ws_bytes, attn_stream_t stream) {
   // validate everything before the first launch
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_mod(mod, scale));
   ATTN_TRY(check_bm(bm));
+  ATTN_TRY(check_dm(s, dm));
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -443,8 +516,28 @@ attn_status attn_bwd(const attn_shape* s, const void* q, const void* k, const vo
   ATTN_OPT_PTR(key_mask);
   ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
   ATTN_TRY(attn_bwd_preprocess(s, out, lse, dout, key_mask, ws, ws_bytes, stream));
-  ATTN_TRY(attn_bwd_dkdv(s, q, k, v, dout, key_mask, bm, mod, scale, dk, dv, ws, ws_bytes, stream));
-  return attn_bwd_dq(s, q, k, v, dout, key_mask, bm, mod, scale, dq, ws, ws_bytes, stream);
+  ATTN_TRY(bwd_dkdv_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dk, dv, ws, ws_bytes, stream));
+  return bwd_dq_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dq, ws, ws_bytes, stream);
+}
+
+size_t attn_dense_mask_bytes(const attn_shape* s, int bcast_b, int bcast_h) {
+  if (!shape_ok(s) || (bcast_b != 0 && bcast_b != 1) || (bcast_h != 0 && bcast_h != 1)) return 0;
+  return dense_mask_layout(dense_mask_count(s, bcast_b, bcast_h), s->Sq, s->Skv).total;
+}
+
+attn_status attn_pack_dense_mask(const attn_shape* s, const uint8_t* mask, int bcast_b, int bcast_h, void* packed,
+                                 size_t packed_bytes, attn_stream_t stream) {
+  if (!shape_ok(s) || !mask || !packed || (bcast_b != 0 && bcast_b != 1) || (bcast_h != 0 && bcast_h != 1))
+    return ATTN_ERR_INVALID_ARG;
+  if (tiles_of(s->Skv) > FWD_MAXKB || tiles_of(s->Sq) > FWD_MAXKB) return ATTN_ERR_SHAPE;
+  if (!aligned(packed, 256)) return ATTN_ERR_ALIGN;
+  const long long nmask = dense_mask_count(s, bcast_b, bcast_h);
+  const DenseMaskLayout l = dense_mask_layout(nmask, s->Sq, s->Skv);
+  if (packed_bytes < l.total) return ATTN_ERR_INVALID_ARG;
+  uint8_t* base = static_cast<uint8_t*>(packed);
+  return cuda_status(launch_dense_mask_pack(mask, nmask, s->Sq, s->Skv, base + l.tiles,
+                                            reinterpret_cast<uint32_t*>(base + l.rowbits),
+                                            reinterpret_cast<uint32_t*>(base + l.colbits), (cudaStream_t)stream));
 }
 
 attn_status attn_decode(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,

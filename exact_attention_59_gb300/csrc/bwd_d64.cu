@@ -68,7 +68,7 @@ struct __align__(1024) DkdvSmem {
   uint8_t lflags[BWD_MAXB];
 };
 
-template <bool BF16, int MOD>
+template <bool BF16, int MOD, bool DM>
 __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,13 +97,16 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     sm.abort = 0;
     // list of q blocks that see this kv block
     const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
+    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     int n = 0;
     if (ks != 0) {
       for (int qb = 0; qb < p.nqb; ++qb) {
         const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-        if (st == TILE_EMPTY) continue;
+        const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qb) * p.nkb + kb] : TILE_FULL;
+        if (st == TILE_EMPTY || ds == TILE_EMPTY) continue;
         sm.list[n] = (uint16_t)qb;
-        sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0);
+        sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
+                       (ds == TILE_PARTIAL ? KB_DENSE : 0);
         ++n;
       }
     }
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     // those rows stay confined to the padded key and the epilogue writes zeros.
     bool my_key = kv < p.Skv;   // rows past Skv (partial last kv block) are not written
     if (p.km_bits && my_key) my_key = (km_word(p.km_bits, b, p.Skv, kv) >> (kv & 31)) & 1u;
+    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
       const int qb = sm.list[u];
@@ -294,6 +298,15 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       const int q0 = qb * 128 + 64 * w;   // first query of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+      // this key's dense-mask bits for the half's 64 queries (column words)
+      const bool dense = DM && (f & KB_DENSE);
+      uint32_t dw[2] = {0u, 0u};
+      if (dense && kv < p.Skv) {
+        const uint2 d2 = __ldg(reinterpret_cast<const uint2*>(p.dm.colbits + (dmi * p.Skv + kv) * (4LL * p.nqb) +
+                                                              4 * qb + 2 * w));
+        dw[0] = d2.x;
+        dw[1] = d2.y;
+      }
       if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       uint32_t rr[64];
@@ -310,8 +323,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       float pr[64];
       uint32_t pk[32];
       // one straight-line copy per causal/not: no runtime test inside the unrolled loop
-      auto probs = [&](auto causal_c) {
+      auto probs = [&](auto causal_c, auto dense_c) {
         constexpr bool CAUSAL = decltype(causal_c)::value;
+        constexpr bool DENSE = decltype(dense_c)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           uint64_t xv = fmul2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv);
@@ -324,14 +338,23 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
             x0 = kv > q0 + 2 * i ? -INFINITY : x0;
             x1 = kv > q0 + 2 * i + 1 ? -INFINITY : x1;
           }
+          if (DENSE) {
+            x0 = (dw[(2 * i) >> 5] & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
+            x1 = (dw[(2 * i + 1) >> 5] & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
+          }
           const float p0 = ex2(x0), p1 = ex2(x1);
           pr[2 * i] = p0;
           pr[2 * i + 1] = p1;
           pk[i] = pack2<BF16>(p0, p1);
         }
       };
-      if (causal) probs(std::true_type{});
-      else probs(std::false_type{});
+      if (dense) {
+        if (causal) probs(std::true_type{}, std::true_type{});
+        else probs(std::false_type{}, std::true_type{});
+      } else {
+        if (causal) probs(std::true_type{}, std::false_type{});
+        else probs(std::false_type{}, std::false_type{});
+      }
       // dV(u-1) has finished reading the P^T region
       if (u > 0) {
         if (!wait_warp(smem_u32(&sm.dvdone), (u - 1) & 1, c)) { ok = false; break; }
@@ -419,7 +442,7 @@ struct __align__(1024) DqSmem {
   uint8_t lflags[BWD_MAXB];
 };
 
-template <bool BF16, int MOD>
+template <bool BF16, int MOD, bool DM>
 __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -446,13 +469,16 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     int n = 0;
+    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     for (int kb = 0; kb < p.nkb; ++kb) {
       const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
       if (ks == 0) continue;
       const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-      if (st == TILE_EMPTY) continue;
+      const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qb) * p.nkb + kb] : TILE_FULL;
+      if (st == TILE_EMPTY || ds == TILE_EMPTY) continue;
       sm.list[n] = (uint16_t)kb;
-      sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0);
+      sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
+                     (ds == TILE_PARTIAL ? KB_DENSE : 0);
       ++n;
     }
     sm.nlist = n;
@@ -601,6 +627,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     // rows past Sq (partial last q tile) get P = 0 and are not written
     const float nl2 = q < p.Sq ? p.lse2[(size_t)bh * p.Sq + q] : -INFINITY;   // -lse log2(e)
     const float nd = q < p.Sq ? p.delta[(size_t)bh * p.Sq + q] : 0.f;        // -D
+    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     const uint64_t scv = f2(p.sc, p.sc), nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
     bool ok = true;
     for (int u = 0; u < N; ++u) {
@@ -614,6 +641,15 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       const int kvl = p.Skv - 1 - k0;
       const bool limited = causal || kvl < 63;
       const int lim = causal ? min(q - k0, kvl) : kvl;
+      // this row's dense-mask bits for the half's 64 keys
+      const bool dense = DM && (f & KB_DENSE);
+      uint32_t dw[2] = {0u, 0u};
+      if (dense && q < p.Sq) {
+        const uint2 d2 = __ldg(reinterpret_cast<const uint2*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) +
+                                                              4 * kb + 2 * w));
+        dw[0] = d2.x;
+        dw[1] = d2.y;
+      }
       if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       uint32_t rr[64];
@@ -629,8 +665,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
       float pr[64];
       // one straight-line copy per causal/not: no runtime test inside the unrolled loop
-      auto probs = [&](auto causal_c) {
+      auto probs = [&](auto causal_c, auto dense_c) {
         constexpr bool CAUSAL = decltype(causal_c)::value;
+        constexpr bool DENSE = decltype(dense_c)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           uint64_t add = nl2v;
@@ -643,12 +680,17 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
             x0 = 2 * i > lim ? -INFINITY : x0;
             x1 = 2 * i + 1 > lim ? -INFINITY : x1;
           }
+          if (DENSE) {
+            x0 = (dw[(2 * i) >> 5] & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
+            x1 = (dw[(2 * i + 1) >> 5] & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
+          }
           pr[2 * i] = ex2(x0);
           pr[2 * i + 1] = ex2(x1);
         }
       };
-      if (limited) probs(std::true_type{});
-      else probs(std::false_type{});
+      if (dense) probs(std::true_type{}, std::true_type{});   // with dense bits, the limited copy too
+      else if (limited) probs(std::true_type{}, std::false_type{});
+      else probs(std::false_type{}, std::false_type{});
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
@@ -706,9 +748,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 template <typename Smem, bool BF16, int MOD, bool DKDV>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
-  auto kern = DKDV ? bwd_dkdv_kernel<BF16, MOD> : bwd_dq_kernel<BF16, MOD>;
+  // DM: the build with the dense-mask path, used only when a dense mask is given
+  auto plain = DKDV ? bwd_dkdv_kernel<BF16, MOD, false> : bwd_dq_kernel<BF16, MOD, false>;
+  auto masked = DKDV ? bwd_dkdv_kernel<BF16, MOD, true> : bwd_dq_kernel<BF16, MOD, true>;
+  auto kern = p.dm.tiles ? masked : plain;
   const size_t smem = sizeof(Smem) + 1024;
-  static const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static const cudaError_t e0 = cudaFuncSetAttribute(plain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static const cudaError_t e1 = cudaFuncSetAttribute(masked, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = p.dm.tiles ? e1 : e0;
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(p.B * p.H * (DKDV ? p.nkb : p.nqb));
   kern<<<grid, BWD_T, smem, st>>>(p);

@@ -21,6 +21,7 @@ constexpr int TILE_EMPTY = 0, TILE_PARTIAL = 1, TILE_FULL = 2;
 constexpr uint8_t KB_VISIT = 1;    // the tile is computed
 constexpr uint8_t KB_MASKMOD = 2;  // partial tile: evaluate the mask_mod per entry
 constexpr uint8_t KB_KEYMASK = 4;  // some keys of the kv block are padding: test the key bits
+constexpr uint8_t KB_DENSE = 8;    // the dense mask keeps only some pairs of the tile: test its bits
 
 // Workspace layout (offsets in bytes; every region 256-byte aligned).
 //   [0, 256)            status word (int32 at offset 0) + reserved

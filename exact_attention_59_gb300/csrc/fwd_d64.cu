@@ -49,10 +49,12 @@ static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 
 // Pass 1 over one row's 128 scores of a kv block: x = s * scale (+ column bias
 // from the stage's table), -inf for columns cc > lim (the causal rule, or keys
-// past the end in a partial last block), and the running maximum in four
+// past the end in a partial last block) and, with DENSE, for columns whose bit
+// in the row's dense-mask words dw is 0; and the running maximum in four
 // independent chains.
-template <bool TABLE, bool LIMITED>
-DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, float (&mx)[4]) {
+template <bool TABLE, bool LIMITED, bool DENSE>
+DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, const uint32_t (&dw)[4],
+                       float (&mx)[4]) {
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
     float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -68,6 +70,10 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
         x0 = c > lim ? -INFINITY : x0;
         x1 = c + 1 > lim ? -INFINITY : x1;
       }
+      if (DENSE) {
+        x0 = (dw[c >> 5] & (1u << (c & 31))) ? x0 : -INFINITY;
+        x1 = (dw[(c + 1) >> 5] & (1u << ((c + 1) & 31))) ? x1 : -INFINITY;
+      }
       r[c] = __float_as_uint(x0);
       r[c + 1] = __float_as_uint(x1);
       mx[(i + j) & 3] = fmax3(mx[(i + j) & 3], x0, x1);
@@ -75,7 +81,8 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
   }
 }
 
-template <bool BF16, int MOD>
+// DM: built with the dense-mask path (the kernels without it are unchanged by it)
+template <bool BF16, int MOD, bool DM>
 __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,6 +117,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
   }
+  const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;   // dense-mask index of (b, h)
   for (int kb = tid; kb < p.nkb; kb += FWD_THREADS) {
     const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
     for (int t = 0; t < 2; ++t) {
@@ -117,9 +125,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       uint8_t f = 0;
       if (qt < p.nqb && ks != 0) {
         const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qt * p.nkb + kb] : TILE_FULL;
-        if (st != TILE_EMPTY)
+        const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb] : TILE_FULL;
+        if (st != TILE_EMPTY && ds != TILE_EMPTY)
           f = KB_VISIT | (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) |
-              (ks == 1 ? KB_KEYMASK : 0);
+              (ks == 1 ? KB_KEYMASK : 0) | (ds == TILE_PARTIAL ? KB_DENSE : 0);
       }
       sm.flags[t][kb] = f;
     }
@@ -310,6 +319,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         }
         const int s = u % FWD_NST;
         ++u;
+        // this row's dense-mask bits for the block, fetched before the wait hides the load
+        const bool dense = DM && (f & KB_DENSE);
+        uint32_t dw[4] = {0u, 0u, 0u, 0u};
+        if (dense && q < p.Sq) {
+          const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb)) + kb);
+          dw[0] = d4.x; dw[1] = d4.y; dw[2] = d4.z; dw[3] = d4.w;
+        }
         if (!wait_warp(smem_u32(&sm.sfull[t]), n & 1, c)) { ok = false; break; }
         // the stage's bias table was written before its full barrier was armed
         if (use_table && !wait_warp(smem_u32(&sm.full[s]), ((u - 1) / FWD_NST) & 1, c)) { ok = false; break; }
@@ -331,12 +347,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // one straight-line copy of the pass per (table, causal) pair: a runtime
         // test inside the unrolled loop would cost instructions on every score
+        // (a block with dense-mask bits always takes the limited copy too)
         if (use_table) {
-          if (limited) scale_scores<true, true>(r, scv, tb, lim, mx);
-          else scale_scores<true, false>(r, scv, tb, lim, mx);
+          if (dense) scale_scores<true, true, true>(r, scv, tb, lim, dw, mx);
+          else if (limited) scale_scores<true, true, false>(r, scv, tb, lim, dw, mx);
+          else scale_scores<true, false, false>(r, scv, tb, lim, dw, mx);
         } else {
-          if (limited) scale_scores<false, true>(r, scv, tb, lim, mx);
-          else scale_scores<false, false>(r, scv, tb, lim, mx);
+          if (dense) scale_scores<false, true, true>(r, scv, tb, lim, dw, mx);
+          else if (limited) scale_scores<false, true, false>(r, scv, tb, lim, dw, mx);
+          else scale_scores<false, false, false>(r, scv, tb, lim, dw, mx);
         }
         // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
         // per-score work: scores here are x' = x - base
@@ -438,7 +457,7 @@ size_t fwd_d64_smem_bytes() { return sizeof(FwdSmem) + 1024; }
 
 template <bool BF16, int MOD>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
-  auto kern = fwd_d64_kernel<BF16, MOD>;
+  auto kern = p.dm.tiles ? fwd_d64_kernel<BF16, MOD, true> : fwd_d64_kernel<BF16, MOD, false>;
   const size_t smem = fwd_d64_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -6,6 +6,37 @@
 
 namespace attn {
 
+// ---------------------------------------------------------------- dense mask
+// A dense (Bm, Hm, Sq, Skv) uint8 mask (Bm in {1, B}, Hm in {1, H}, nonzero =
+// keep) packed once by launch_dense_mask_pack into caller memory:
+//   tiles   (Bm, Hm, nqb, nkb) uint8: TILE_EMPTY (no kept pair), TILE_PARTIAL,
+//           TILE_FULL (every in-range pair kept)
+//   rowbits (Bm, Hm, Sq, 4 nkb) u32: bit j of word 4 kb + w = pair (q, 128 kb + 32 w + j)
+//   colbits (Bm, Hm, Skv, 4 nqb) u32: bit j of word 4 qb + w = pair (128 qb + 32 w + j, kv)
+// Bits of positions past Sq or Skv are 0.  Head (b, h) uses mask index
+// b * mb + h * mh.
+struct DenseMaskLayout {
+  size_t tiles, rowbits, colbits, total;   // byte offsets and size, 256-byte aligned
+};
+inline DenseMaskLayout dense_mask_layout(long long nmask, int Sq, int Skv) {
+  const long long nqb = (Sq + 127) / 128, nkb = (Skv + 127) / 128;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  DenseMaskLayout l;
+  l.tiles = 0;
+  l.rowbits = up((size_t)(nmask * nqb * nkb));
+  l.colbits = l.rowbits + up((size_t)(nmask * Sq * nkb * 16));
+  l.total = l.colbits + up((size_t)(nmask * Skv * nqb * 16));
+  return l;
+}
+struct DenseMaskView {
+  const uint8_t* tiles;      // nullptr = no dense mask
+  const uint32_t* rowbits;
+  const uint32_t* colbits;
+  int mb, mh;                // mask index of head (b, h) = b * mb + h * mh
+};
+cudaError_t launch_dense_mask_pack(const uint8_t* mask, long long nmask, int Sq, int Skv, uint8_t* tiles,
+                                   uint32_t* rowbits, uint32_t* colbits, cudaStream_t st);
+
 // ---------------------------------------------------------------- forward, D = 64
 #ifndef ATTN_FWD_NST
 #define ATTN_FWD_NST 3
@@ -24,6 +55,7 @@ struct FwdParams {
   const uint8_t* bm_tiles;        // block-mask states or nullptr
   long long bm_sb, bm_sh;         // element strides of b and h in bm_tiles (0 = broadcast)
   int bm_mod;
+  DenseMaskView dm;               // dense (query, key) mask, dm.tiles = nullptr if none
   uint8_t* visited;               // (B, H, nqb, nkb) or nullptr
   int* status;
   int B, H, Sq, Skv, nqb, nkb, npairs;
@@ -63,6 +95,7 @@ struct BwdParams {
   const uint8_t* bm_tiles;
   long long bm_sb, bm_sh;
   int bm_mod;
+  DenseMaskView dm;
   int* status;
   int B, H, Sq, Skv, nqb, nkb;
   float sc;               // scale * log2(e)

@@ -3,6 +3,8 @@
 //     kv block) summary that lets whole 128-key blocks be skipped or kept;
 //   * the block-mask builder (the analogue of create_block_mask(mask_mod, B, H,
 //     Sq, Skv) in the flaxattention README "Example usage");
+//   * dense-mask packing: the (query, key) mask of the attnax
+//     pallas_flash_attention arguments as row bits, column bits and tile states;
 //   * the backward preprocess: -D_i = -sum_d dO_id O_id and -lse_i log2(e)
 //     (-inf for rows with no kept key), negated so the passes use one FFMA.
 #include "kernels.h"
@@ -35,6 +37,83 @@ cudaError_t launch_keymask_pack(const uint8_t* km, int B, int Skv, uint32_t* bit
                                 cudaStream_t st) {
   dim3 grid((Skv + 127) / 128, B);
   keymask_pack_kernel<<<grid, 128, 0, st>>>(km, Skv, bits, summary);
+  return cudaGetLastError();
+}
+
+// Dense mask packing: one CTA of 256 threads per (mask, q tile, kv tile).  The
+// tile's 128 x 128 bytes go to shared memory as 0/1 (rows padded to 132 bytes
+// so that a warp reading one column touches 32 banks); a ballot over 32 lanes
+// then gives each 32-bit word: along a row for rowbits, down a column for
+// colbits.
+__global__ void __launch_bounds__(256) dense_mask_pack_kernel(const uint8_t* __restrict__ mask, int Sq, int Skv,
+                                                              int nqb, int nkb, uint8_t* __restrict__ tiles,
+                                                              uint32_t* __restrict__ rowbits,
+                                                              uint32_t* __restrict__ colbits) {
+  __shared__ __align__(16) uint8_t t[128][132];
+  __shared__ int kept;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long mi = blockIdx.x / ((long long)nqb * nkb);
+  const int rem = (int)(blockIdx.x % ((long long)nqb * nkb));
+  const int qb = rem / nkb, kb = rem % nkb;
+  const uint8_t* src = mask + (size_t)mi * Sq * Skv;
+  if (tid == 0) kept = 0;
+  if ((Skv & 15) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15) == 0) {
+    // 16 bytes per load; Skv % 16 == 0 keeps each 16-byte group inside one row
+    for (int i = tid; i < 128 * 8; i += 256) {
+      const int r = i >> 3, c = (i & 7) * 16;
+      const int q = qb * 128 + r, kv = kb * 128 + c;
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (q < Sq && kv < Skv) x = __ldg(reinterpret_cast<const uint4*>(src + (size_t)q * Skv + kv));
+      uint32_t* d = reinterpret_cast<uint32_t*>(&t[r][c]);
+      d[0] = __vcmpne4(x.x, 0u) & 0x01010101u;
+      d[1] = __vcmpne4(x.y, 0u) & 0x01010101u;
+      d[2] = __vcmpne4(x.z, 0u) & 0x01010101u;
+      d[3] = __vcmpne4(x.w, 0u) & 0x01010101u;
+    }
+  } else {
+    for (int i = tid; i < 128 * 128; i += 256) {
+      const int r = i >> 7, c = i & 127;
+      const int q = qb * 128 + r, kv = kb * 128 + c;
+      t[r][c] = (q < Sq && kv < Skv && src[(size_t)q * Skv + kv] != 0) ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  // rows: warp w packs rows 16 w .. 16 w + 15, one ballot per 32 columns
+  int cnt = 0;
+  for (int rr = 0; rr < 16; ++rr) {
+    const int r = warp * 16 + rr, q = qb * 128 + r;
+    uint32_t w4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w4[j] = __ballot_sync(0xffffffffu, t[r][32 * j + lane] != 0);
+    cnt += __popc(w4[0]) + __popc(w4[1]) + __popc(w4[2]) + __popc(w4[3]);
+    if (lane == 0 && q < Sq)
+      *reinterpret_cast<uint4*>(rowbits + ((size_t)mi * Sq + q) * (4 * nkb) + 4 * kb) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+  // columns: warp w packs columns 16 w .. 16 w + 15, one ballot per 32 rows
+  for (int cc = 0; cc < 16; ++cc) {
+    const int c = warp * 16 + cc, kv = kb * 128 + c;
+    uint32_t w4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w4[j] = __ballot_sync(0xffffffffu, t[32 * j + lane][c] != 0);
+    if (lane == 0 && kv < Skv)
+      *reinterpret_cast<uint4*>(colbits + ((size_t)mi * Skv + kv) * (4 * nqb) + 4 * qb) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+  if (lane == 0) atomicAdd(&kept, cnt);
+  __syncthreads();
+  if (tid == 0) {
+    const long long valid = (long long)min(128, Sq - qb * 128) * min(128, Skv - kb * 128);
+    tiles[blockIdx.x] = kept == 0 ? TILE_EMPTY : (kept == valid ? TILE_FULL : TILE_PARTIAL);
+  }
+}
+
+cudaError_t launch_dense_mask_pack(const uint8_t* mask, long long nmask, int Sq, int Skv, uint8_t* tiles,
+                                   uint32_t* rowbits, uint32_t* colbits, cudaStream_t st) {
+  const int nqb = (Sq + 127) / 128, nkb = (Skv + 127) / 128;
+  const long long grid = nmask * nqb * nkb;
+  if (grid == 0) return cudaSuccess;
+  dense_mask_pack_kernel<<<(unsigned)grid, 256, 0, st>>>(mask, Sq, Skv, nqb, nkb, tiles, rowbits, colbits);
   return cudaGetLastError();
 }
 

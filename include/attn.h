@@ -113,6 +113,22 @@ typedef struct {
   attn_mask_mod mask_mod;
 } attn_block_mask;
 
+/* Dense (query, key) mask, as the attnax pallas_flash_attention arguments
+ * take it: a boolean mask broadcastable to (batch, heads, seq_q, seq_kv).
+ * Here: uint8 (bcast_b ? 1 : B, bcast_h ? 1 : H, Sq, Skv), row-major device
+ * memory, nonzero = attend; it is combined (AND) with the key mask, the
+ * score_mod and the block mask.  attn_pack_dense_mask turns it once into
+ * the packed form the kernels read (row bits, column bits and one state
+ * per 128 x 128 tile; tiles with no kept pair are skipped, tiles with every
+ * pair kept are not tested per entry); the packed form can be reused by any
+ * number of forward and backward calls of the same shape.  Taken on the
+ * f16/bf16 D = 64 path (ATTN_ERR_UNSUPPORTED elsewhere). */
+typedef struct {
+  const void* packed;    /* device, 256-byte aligned, written by attn_pack_dense_mask */
+  size_t packed_bytes;   /* its size: at least attn_dense_mask_bytes() */
+  int bcast_b, bcast_h;  /* 0 or 1, as given to attn_pack_dense_mask */
+} attn_dense_mask;
+
 /* Bytes of workspace that `op` needs for `shape` (0 if the shape is invalid).
  * Monotonic non-decreasing in every dimension of the shape. */
 size_t attn_workspace_size(attn_op op, const attn_shape* shape);
@@ -123,6 +139,20 @@ size_t attn_workspace_size(attn_op op, const attn_shape* shape);
  * when mask_mod keeps all its entries, EMPTY when it keeps none, else PARTIAL. */
 attn_status attn_build_block_mask(attn_mask_mod mask_mod, int B, int H, int Sq, int Skv, int bq,
                                   int bkv, uint8_t* tiles, attn_stream_t stream);
+
+/* Bytes of the packed form of a dense mask for `shape` (B, H, Sq, Skv are
+ * used) with the given broadcast flags; 0 if an argument is invalid. */
+size_t attn_dense_mask_bytes(const attn_shape* shape, int bcast_b, int bcast_h);
+
+/* Packs a dense uint8 mask (layout in attn_dense_mask) into `packed`
+ * (caller-owned device memory, 256-byte aligned, at least
+ * attn_dense_mask_bytes() bytes), asynchronously on `stream`.  The mask
+ * itself needs no alignment (16-byte aligned rows with Skv % 16 == 0 are
+ * read 16 bytes at a time).  Errors: ATTN_ERR_INVALID_ARG (NULL pointer,
+ * flag not 0/1, packed too small), ATTN_ERR_SHAPE (more than 2048 tiles of
+ * 128 along Sq or Skv), ATTN_ERR_ALIGN (packed). */
+attn_status attn_pack_dense_mask(const attn_shape* shape, const uint8_t* mask, int bcast_b, int bcast_h,
+                                 void* packed, size_t packed_bytes, attn_stream_t stream);
 
 /* Forward: out = softmax(mask(scale q k^T + mod)) v and lse (attnax Pallas
  * kernel body, online softmax with exp2/log2 arithmetic as in the
@@ -136,6 +166,16 @@ attn_status attn_fwd(const attn_shape* shape, const void* q, const void* k, cons
                      float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                      attn_stream_t stream, uint8_t* debug_visited);
 
+/* attn_fwd with a dense (query, key) mask `dm` (nullable; NULL = attn_fwd).
+ * The visited map also leaves out tiles with no pair kept by dm.  Errors as
+ * attn_fwd, plus ATTN_ERR_INVALID_ARG (dm->packed NULL, flag not 0/1,
+ * packed_bytes too small), ATTN_ERR_ALIGN (dm->packed) and
+ * ATTN_ERR_UNSUPPORTED (f32 or D = 512). */
+attn_status attn_fwd_dense(const attn_shape* shape, const void* q, const void* k, const void* v,
+                           const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
+                           attn_score_mod mod, float scale, void* out, float* lse, void* ws,
+                           size_t ws_bytes, attn_stream_t stream, uint8_t* debug_visited);
+
 /* Backward of sum(dout * out): dq, dk, dv (same shapes and dtype as q, k, v).
  * Takes the forward's out and lse and the same key_mask, bm, mod and scale.
  * Runs three kernels: a preprocess (D_i = rowsum(dout * out)), a dK/dV pass
@@ -146,6 +186,14 @@ attn_status attn_bwd(const attn_shape* shape, const void* q, const void* k, cons
                      const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod,
                      float scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                      attn_stream_t stream);
+
+/* attn_bwd with the forward's dense mask `dm` (nullable; NULL = attn_bwd);
+ * errors as attn_fwd_dense. */
+attn_status attn_bwd_dense(const attn_shape* shape, const void* q, const void* k, const void* v,
+                           const void* out, const float* lse, const void* dout, const uint8_t* key_mask,
+                           const attn_dense_mask* dm, const attn_block_mask* bm, attn_score_mod mod,
+                           float scale, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                           attn_stream_t stream);
 
 /* The three phases of attn_bwd as separate calls, in this order, on one
  * workspace (for timing a phase alone).  Same arguments as attn_bwd. */

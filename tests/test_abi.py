@@ -133,3 +133,47 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         E.attn_fwd(q, q, q)
+
+
+def test_dense_mask_sizes_and_validation(lib):
+    """Packing and dense-mask calls validate before launching (FAKE pointers are never touched)."""
+    L = lib.load()
+    s = _shape(lib, B=2, H=4, Sq=300, Skv=200)
+    full = L.attn_dense_mask_bytes(ctypes.byref(s), 0, 0)
+    assert full > 0 and full % 256 == 0
+    assert L.attn_dense_mask_bytes(ctypes.byref(s), 1, 0) < full
+    assert L.attn_dense_mask_bytes(ctypes.byref(s), 1, 1) < L.attn_dense_mask_bytes(ctypes.byref(s), 0, 1) < full
+    assert L.attn_dense_mask_bytes(ctypes.byref(s), 2, 0) == 0
+    assert L.attn_dense_mask_bytes(ctypes.byref(_shape(lib, B=0)), 0, 0) == 0
+    big = _shape(lib, B=2, H=4, Sq=600, Skv=200)
+    assert L.attn_dense_mask_bytes(ctypes.byref(big), 0, 0) > full
+
+    def pack(shape=s, mask=FAKE, bb=0, bh=0, packed=FAKE, n=1 << 30):
+        return L.attn_pack_dense_mask(ctypes.byref(shape), mask, bb, bh, packed, n, None)
+    assert pack(mask=None) == lib.ATTN_ERR_INVALID_ARG
+    assert pack(packed=None) == lib.ATTN_ERR_INVALID_ARG
+    assert pack(bh=3) == lib.ATTN_ERR_INVALID_ARG
+    assert pack(packed=FAKE + 16) == lib.ATTN_ERR_ALIGN
+    assert pack(n=full - 1) == lib.ATTN_ERR_INVALID_ARG
+    assert pack(shape=_shape(lib, Skv=2048 * 128 + 1)) == lib.ATTN_ERR_SHAPE
+
+    def fwd(shape=s, dm=None):
+        return L.attn_fwd_dense(ctypes.byref(shape), FAKE, FAKE, FAKE, None,
+                                ctypes.byref(dm) if dm is not None else None, None, 0, 0.125, FAKE, FAKE, FAKE,
+                                1 << 30, None, None)
+
+    def bwd(shape=s, dm=None):
+        return L.attn_bwd_dense(ctypes.byref(shape), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                ctypes.byref(dm) if dm is not None else None, None, 0, 0.125, FAKE, FAKE, FAKE,
+                                FAKE, 1 << 30, None)
+    ok = lib.DenseMaskC(FAKE, full, 0, 0)
+    for call in (fwd, bwd):
+        assert call(dm=lib.DenseMaskC(None, full, 0, 0)) == lib.ATTN_ERR_INVALID_ARG
+        assert call(dm=lib.DenseMaskC(FAKE, full, 0, 2)) == lib.ATTN_ERR_INVALID_ARG
+        assert call(dm=lib.DenseMaskC(FAKE + 64, full, 0, 0)) == lib.ATTN_ERR_ALIGN
+        assert call(dm=lib.DenseMaskC(FAKE, full - 256, 0, 0)) == lib.ATTN_ERR_INVALID_ARG
+        assert call(shape=_shape(lib, B=2, H=4, Sq=256, Skv=256, dt=0), dm=ok) == lib.ATTN_ERR_UNSUPPORTED
+        assert call(shape=_shape(lib, Sq=300, dt=0), dm=ok) == lib.ATTN_ERR_SHAPE
+    assert fwd(shape=_shape(lib, B=2, H=4, Sq=256, Skv=256, D=512), dm=ok) == lib.ATTN_ERR_UNSUPPORTED
+    # with no dense mask the calls are attn_fwd / attn_bwd (same validation)
+    assert fwd(shape=_shape(lib, D=96)) == _fwd(lib, _shape(lib, D=96)) == lib.ATTN_ERR_UNSUPPORTED

@@ -36,24 +36,27 @@ def _oracle_bm(bm_kind, B, H, Sq, Skv):
 
 
 def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", backward=True, heads=None,
-                  check_det=True, key_mask_override=None, strict=False, D=64):
+                  check_det=True, key_mask_override=None, strict=False, D=64, dense=None):
+    """``dense``: optional uint8 CPU tensor (B|1, H|1, Sq, Skv), the dense (query, key) mask."""
     c, d = make_dev(B, H, Sq, Skv, D, dtype, key_mask=key_mask, dout=dout)
     if key_mask_override is not None:
         c["key_mask"] = key_mask_override.clone()
         d["key_mask"] = key_mask_override.cuda()
     bm = E.create_block_mask(bm_kind, 1, 1, Sq, Skv) if bm_kind else None
+    dm = E.pack_dense_mask(dense.cuda(), B, H) if dense is not None else None
+    dn = None if dense is None else dense.numpy()
     tdt = d["q"].dtype
     nqb, nkb = -(-Sq // 128), -(-Skv // 128)
     ob, out = guarded((B, H, Sq, D), tdt)
     lb, lse = guarded((B, H, Sq), torch.float32)
     vis = torch.full((B, H, nqb, nkb), 7, dtype=torch.uint8, device="cuda")
     E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod, out=out, lse=lse,
-               debug_visited=vis)
+               debug_visited=vis, dense_mask=dm)
     grads = None
     if backward:
         gb = [guarded(d[n].shape, tdt) for n in ("q", "k", "v")]
         E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
-                   score_mod=mod, dq=gb[0][1], dk=gb[1][1], dv=gb[2][1])
+                   score_mod=mod, dq=gb[0][1], dk=gb[1][1], dv=gb[2][1], dense_mask=dm)
         grads = gb
     shp = E.make_shape(d["q"], d["k"])
     assert E.poll_status(E.workspace(E.OP_FWD, shp, d["q"].device)) == E.ATTN_OK
@@ -64,7 +67,8 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
     km = None if c["key_mask"] is None else c["key_mask"].numpy()
     obm = _oracle_bm(bm_kind, B, H, Sq, Skv)
     q64, k64, v64 = f64(c["q"]), f64(c["k"]), f64(c["v"])
-    o_ref, lse_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, block_mask=obm, score_mod=mod, heads=heads)
+    o_ref, lse_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, block_mask=obm, score_mod=mod, heads=heads,
+                                 dense_mask=dn)
     sel = (slice(None),) if heads is None else tuple(np.array(x) for x in zip(*heads))
     tol = TOL[dtype]
     compare("out", f64(out)[sel], o_ref[sel], tol["o_max"], tol["o_mean"], scaled=not strict)
@@ -76,22 +80,23 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
     dead = ~fin
     if dead.any():
         assert (f64(out)[sel][dead] == 0).all()
-    vis_ref = OR.visited_tiles(B, H, Sq, Skv, key_mask=km, block_mask=obm)
+    vis_ref = OR.visited_tiles(B, H, Sq, Skv, key_mask=km, block_mask=obm, dense_mask=dn)
     np.testing.assert_array_equal(vis.cpu().numpy(), vis_ref)
     if backward:
         dq_r, dk_r, dv_r = OR.attn_bwd(q64, k64, v64, f64(c["dout"]), key_mask=km, block_mask=obm, score_mod=mod,
-                                       heads=heads)
+                                       heads=heads, dense_mask=dn)
         for name, (buf, g), ref, shp in zip(("dq", "dk", "dv"), grads, (dq_r, dk_r, dv_r),
                                             ((B, H, Sq, D), (B, H, Skv, D), (B, H, Skv, D))):
             assert canary_ok(buf, shp), f"{name}: canary overwritten"
             compare(name, f64(g)[sel], ref[sel], tol["g_max"], tol["g_mean"], scaled=not strict)
     if check_det:
-        out2, lse2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod)
+        out2, lse2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod,
+                                dense_mask=dm)
         assert torch.equal(out2.view(torch.uint8), out.view(torch.uint8)), "forward not bitwise reproducible"
         assert torch.equal(lse2.view(torch.uint8), lse.view(torch.uint8)), "lse not bitwise reproducible"
         if backward and D == 64:
             g2 = E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
-                            score_mod=mod)
+                            score_mod=mod, dense_mask=dm)
             for a, (_, b_) in zip(g2, grads):
                 assert torch.equal(a.view(torch.uint8), b_.view(torch.uint8)), "backward not bitwise reproducible"
 
@@ -150,6 +155,60 @@ def test_ragged_fully_masked():
     for dt in ("bf16", "f16"):
         run_and_check(2, 2, 150, 333, dt, "none", True, None, key_mask_override=km)
         run_and_check(2, 1, 150, 333, dt, "causal", True, None, key_mask_override=km)
+
+
+# Dense (query, key) masks (f16/bf16, D=64), seeded: random pairs, a sliding
+# window (tiles far from the diagonal are skipped), whole tiles kept or
+# dropped, every broadcast form, and combinations with the other hooks.
+def _dense(kind, Bm, Hm, Sq, Skv, seed=11):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "random":
+        m = (torch.rand((Bm, Hm, Sq, Skv), generator=g) < 0.5).to(torch.uint8)
+    elif kind == "window":
+        qi = torch.arange(Sq)[:, None]
+        kj = torch.arange(Skv)[None, :]
+        m = ((qi - kj).abs() < 100).to(torch.uint8).expand(Bm, Hm, Sq, Skv).clone()
+    elif kind == "tiles":
+        m = (torch.rand((Bm, Hm, Sq, Skv), generator=g) < 0.7).to(torch.uint8)
+        m[..., :128, 128:256] = 0          # tile (0, 1): nothing kept, skipped
+        m[..., 128:256, :128] = 1          # tile (1, 0): everything kept, no per-entry test
+        m[..., 5, :] = 0                   # a query row with no kept key
+        m[..., :, 7] = 0                   # a key kept by no query
+    else:
+        raise ValueError(kind)
+    return m
+
+
+DENSE = [
+    # (B, H, Sq, Skv, dtype, mod, km, bm, kind, Bm, Hm)
+    (2, 2, 256, 256, "bf16", "none", False, None, "random", 2, 2),
+    (2, 2, 256, 384, "f16", "alibi", False, None, "tiles", 1, 1),
+    (2, 3, 384, 256, "bf16", "checkerboard", True, None, "tiles", 2, 1),
+    (1, 2, 640, 640, "f16", "none", False, None, "window", 1, 2),
+    (2, 1, 300, 200, "bf16", "causal", True, "causal", "random", 1, 1),
+    (1, 2, 333, 129, "f16", "alibi", True, "causal", "tiles", 1, 2),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,dtype,mod,km,bm,kind,Bm,Hm", DENSE)
+def test_dense_mask(B, H, Sq, Skv, dtype, mod, km, bm, kind, Bm, Hm):
+    run_and_check(B, H, Sq, Skv, dtype, mod, km, bm, dense=_dense(kind, Bm, Hm, Sq, Skv))
+
+
+def test_dense_mask_packed_once_reused():
+    """One packed mask serves several calls; an all-ones mask equals no mask bit for bit."""
+    B, H, S = 2, 2, 256
+    _, d = make_dev(B, H, S, S, 64, "bf16")
+    ones = E.pack_dense_mask(torch.ones((1, 1, S, S), dtype=torch.uint8, device="cuda"), B, H)
+    o0, l0 = E.attn_fwd(d["q"], d["k"], d["v"])
+    for _ in range(2):
+        o1, l1 = E.attn_fwd(d["q"], d["k"], d["v"], dense_mask=ones)
+        assert torch.equal(o0.view(torch.uint8), o1.view(torch.uint8))
+        assert torch.equal(l0.view(torch.uint8), l1.view(torch.uint8))
+    g0 = E.attn_bwd(d["q"], d["k"], d["v"], o0, l0, d["dout"])
+    g1 = E.attn_bwd(d["q"], d["k"], d["v"], o0, l0, d["dout"], dense_mask=ones)
+    for a, b_ in zip(g0, g1):
+        assert torch.equal(a.view(torch.uint8), b_.view(torch.uint8))
 
 
 def test_fully_masked_batches_and_blocks():
