@@ -347,6 +347,44 @@ def bench_extras(E, dev):
         f_fl = 4.0 * w.B * w.H * w.Sq * w.Skv * w.D * half
         res[w.name] = {"fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_ms": b_ms,
                        "bwd_tflops": 2.5 * f_fl / (b_ms * 1e-3) / 1e12}
+    # dense (query, key) mask: a sliding window |q - k| < 256 shared by every head,
+    # on the key-padding workload's shape (fp16, B8 H8 S2048 D64); tiles with no
+    # kept pair are skipped, so the rate is quoted over kept pairs and visited tiles
+    w = WL
+    S, win = w.Sq, 256
+    sets = []
+    for i in range(2):
+        c = IN.make_case(w.B, w.H, S, S, w.D, w.dtype, seed=IN.SEED + 9100 + i)
+        d = {k: v.to(dev) for k, v in c.items() if v is not None}
+        d["out"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
+        d["dq"], d["dk"], d["dv"] = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+        sets.append(d)
+    qi = torch.arange(S, device=dev)[:, None]
+    mask = ((qi - torch.arange(S, device=dev)[None, :]).abs() < win).to(torch.uint8)[None, None]
+    p_ms = timed(lambda i: E.pack_dense_mask(mask, w.B, w.H), 5)
+    dm = E.pack_dense_mask(mask, w.B, w.H)
+
+    def dfwd(i):
+        d = sets[i % 2]
+        E.attn_fwd(d["q"], d["k"], d["v"], dense_mask=dm, out=d["out"], lse=d["lse"])
+
+    def dbwd(i):
+        d = sets[i % 2]
+        E.attn_bwd(d["q"], d["k"], d["v"], d["out"], d["lse"], d["dout"], dense_mask=dm, dq=d["dq"], dk=d["dk"],
+                   dv=d["dv"])
+
+    f_ms = timed(dfwd, 50)
+    b_ms = timed(dbwd, 50)
+    kept = int(mask.sum().item()) * w.B * w.H
+    nt = -(-S // 128)
+    vt = sum(1 for a in range(nt) for b in range(nt) if abs(a - b) * 128 < win + 127) * w.B * w.H
+    f_kept = 4.0 * w.D * kept
+    f_vis = 4.0 * w.D * vt * 128 * 128
+    res[f"window{win}_dense_fp16_b8h8s2048d64"] = {
+        "pack_ms": p_ms, "fwd_ms": f_ms, "bwd_ms": b_ms, "kept_pairs": kept, "visited_tiles": vt,
+        "fwd_tflops_kept": f_kept / (f_ms * 1e-3) / 1e12, "fwd_tflops_visited": f_vis / (f_ms * 1e-3) / 1e12,
+        "bwd_tflops_visited": 2.5 * f_vis / (b_ms * 1e-3) / 1e12}
     w = W.LONG_CAUSAL_BF16
     q = IN.randn((w.B, w.H, w.Sq, w.D), IN.SEED + 1, w.dtype).to(dev)
     k = IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED, w.dtype).to(dev)
