@@ -167,7 +167,7 @@ def dense_mask_head(dense_mask, b: int, h: int) -> np.ndarray:
 
 
 def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
-                block_mask: BlockMask | None = None, score_mod=MOD_NONE, dense_mask=None):
+                block_mask: BlockMask | None = None, score_mod=MOD_NONE, dense_mask=None, row_idx=None):
     """Which (q, kv) entries take part in the softmax of head (b, h).
 
     An entry is kept iff the key mask keeps kv (if given), the dense mask keeps
@@ -181,7 +181,8 @@ def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
     if key_mask is not None:
         keep &= (np.asarray(key_mask)[b][kv_idx] != 0)[None, :]
     if dense_mask is not None:
-        keep &= dense_mask_head(dense_mask, b, h)[q_idx[:, None], kv_idx[None, :]] != 0
+        ri = q_idx if row_idx is None else np.asarray(row_idx, dtype=np.int64)
+        keep &= dense_mask_head(dense_mask, b, h)[ri[:, None], kv_idx[None, :]] != 0
     if block_mask is not None:
         st = block_mask.states(b, h)
         ts = st[(q_idx // block_mask.block_q)[:, None], (kv_idx // block_mask.block_kv)[None, :]]
@@ -191,12 +192,15 @@ def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
 
 
 def masked_logits(qbh, kbh, b, h, H, scale, q_idx, kv_idx, key_mask=None,
-                  block_mask=None, score_mod=MOD_NONE, dense_mask=None):
-    """S = scale * q k^T + bias, with -inf where masked (float64)."""
+                  block_mask=None, score_mod=MOD_NONE, dense_mask=None, row_idx=None):
+    """S = scale * q k^T + bias, with -inf where masked (float64).
+
+    q_idx are the query positions; row_idx (default q_idx) the rows of the
+    dense mask they read."""
     s = scale * (qbh @ kbh.T)
     bias, _ = score_bias(score_mod, h, H, q_idx, kv_idx)
     s = s + bias
-    keep = keep_matrix(b, h, H, q_idx, kv_idx, key_mask, block_mask, score_mod, dense_mask)
+    keep = keep_matrix(b, h, H, q_idx, kv_idx, key_mask, block_mask, score_mod, dense_mask, row_idx)
     return np.where(keep, s, -np.inf), keep
 
 
@@ -227,11 +231,14 @@ def _default_scale(D, scale):
 # ---------------------------------------------------------------------------
 
 def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None,
-             score_mod=MOD_NONE, scale=None, heads=None, rows=None, dense_mask=None):
+             score_mod=MOD_NONE, scale=None, heads=None, rows=None, dense_mask=None, q_offset=0):
     """O = softmax(mask(scale q k^T + bias)) v and lse, per (b, h), in float64.
 
     q: (B, H, Sq, D); k, v: (B, H, Skv, D); key_mask: (B, Skv) or None;
     dense_mask: (B|1, H|1, Sq, Skv) or None.
+    ``q_offset``: position of query row 0 in the key sequence (a KV cache that
+    already holds earlier tokens): row i has q_idx = q_offset + i in every
+    score_mod, mask_mod and block-mask lookup (the dense mask is indexed by row).
     ``heads``: optional list of (b, h) to compute (others stay NaN).
     ``rows``: optional 1-D array of query rows to compute (others stay NaN).
     Returns (o (B, H, Sq, D), lse (B, H, Sq)).
@@ -246,8 +253,8 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None,
     kv_idx = np.arange(Skv)
     todo = [(b, h) for b in range(B) for h in range(H)] if heads is None else heads
     for b, h in todo:
-        s, _ = masked_logits(q[b, h, q_idx], k[b, h], b, h, H, scale, q_idx, kv_idx,
-                             key_mask, block_mask, score_mod, dense_mask)
+        s, _ = masked_logits(q[b, h, q_idx], k[b, h], b, h, H, scale, q_idx + int(q_offset), kv_idx,
+                             key_mask, block_mask, score_mod, dense_mask, row_idx=q_idx)
         p, l = softmax_rows(s)
         o[b, h, q_idx] = p @ v[b, h]
         lse[b, h, q_idx] = l
@@ -294,10 +301,10 @@ def attn_bwd(q, k, v, dout, key_mask=None, block_mask: BlockMask | None = None,
     return dq, dk, dv
 
 
-def attn_decode(q, k, v, key_mask=None, score_mod=MOD_NONE, scale=None):
-    """Single-query decode: the forward with Sq = 1 and q_idx = 0."""
-    assert np.asarray(q).shape[2] == 1
-    return attn_fwd(q, k, v, key_mask=key_mask, score_mod=score_mod, scale=scale)
+def attn_decode(q, k, v, key_mask=None, score_mod=MOD_NONE, scale=None, q_offset=0):
+    """Decode: the forward for a few queries (Sq = 1 in the single-query case)
+    at positions q_offset .. q_offset + Sq - 1 of the key sequence."""
+    return attn_fwd(q, k, v, key_mask=key_mask, score_mod=score_mod, scale=scale, q_offset=q_offset)
 
 
 def visited_tiles(B, H, Sq, Skv, key_mask=None, block_mask: BlockMask | None = None,

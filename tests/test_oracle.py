@@ -414,3 +414,27 @@ def test_visited_tiles_skip_empty_dense_tiles():
     assert vis.shape == (2, 2, 3, 3)
     assert (vis[:, 1, 1, 0] == 0).all() and (vis[:, 0, 2, 2] == 0).all()
     assert vis.sum() == 2 * (18 - 2)
+
+
+# ---------------------------------------------------------------------------
+# query position offset (decode against a KV cache that holds earlier tokens)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mod", MODS)
+def test_query_offset_equals_rows_of_full(mod):
+    """nq queries at positions off .. off+nq-1 give exactly the last rows of the
+    full square computation over the same keys, for every score_mod, with and
+    without a key mask (the positions, not the row numbers, enter the mods)."""
+    B, H, S, D, nq = 2, 2, 11, 3, 4
+    off = S - nq
+    q, k, v = _rand(B, H, S, D, seed=120), _rand(B, H, S, D, seed=121), _rand(B, H, S, D, seed=122)
+    km = (np.random.default_rng(123).random((B, S)) > 0.3).astype(np.uint8)
+    for kmask in (None, km):
+        of, lf = A.attn_fwd(q, k, v, key_mask=kmask, score_mod=mod)
+        oc, lc = A.attn_decode(q[:, :, off:], k, v, key_mask=kmask, score_mod=mod, q_offset=off)
+        np.testing.assert_array_equal(oc, of[:, :, off:])
+        np.testing.assert_array_equal(lc, lf[:, :, off:])
+    # an offset past the last key keeps every key under the causal rule
+    o1, _ = A.attn_decode(q[:, :, :2], k, v, score_mod="causal", q_offset=S + 5)
+    o2, _ = A.attn_fwd(q[:, :, :2], k, v)
+    np.testing.assert_array_equal(o1, o2)

@@ -30,10 +30,12 @@ MUTANTS = {
     "lse_log2": ("m_safe[:, 0] + np.log(", "m_safe[:, 0] + np.log2("),
     "keymask_polarity": ("keep &= (np.asarray(key_mask)[b][kv_idx] != 0)[None, :]",
                          "keep &= (np.asarray(key_mask)[b][kv_idx] == 0)[None, :]"),
-    "dense_polarity": ("keep &= dense_mask_head(dense_mask, b, h)[q_idx[:, None], kv_idx[None, :]] != 0",
-                       "keep &= dense_mask_head(dense_mask, b, h)[q_idx[:, None], kv_idx[None, :]] == 0"),
-    "dense_transposed": ("keep &= dense_mask_head(dense_mask, b, h)[q_idx[:, None], kv_idx[None, :]] != 0",
-                         "keep &= dense_mask_head(dense_mask, b, h).T[kv_idx[None, :] % len(q_idx), q_idx[:, None] % len(kv_idx)] != 0"),
+    "dense_polarity": ("keep &= dense_mask_head(dense_mask, b, h)[ri[:, None], kv_idx[None, :]] != 0",
+                       "keep &= dense_mask_head(dense_mask, b, h)[ri[:, None], kv_idx[None, :]] == 0"),
+    "dense_transposed": ("keep &= dense_mask_head(dense_mask, b, h)[ri[:, None], kv_idx[None, :]] != 0",
+                         "keep &= dense_mask_head(dense_mask, b, h).T[kv_idx[None, :] % len(ri), ri[:, None] % len(kv_idx)] != 0"),
+    "offset_ignored": ("q_idx + int(q_offset), kv_idx,", "q_idx, kv_idx,"),
+    "offset_sign": ("q_idx + int(q_offset), kv_idx,", "q_idx - int(q_offset), kv_idx,"),
     "dense_bcast_b": ("return dm[0 if dm.shape[0] == 1 else b, 0 if dm.shape[1] == 1 else h]",
                       "return dm[0, 0 if dm.shape[1] == 1 else h]"),
     "dense_bcast_h": ("return dm[0 if dm.shape[0] == 1 else b, 0 if dm.shape[1] == 1 else h]",
@@ -63,6 +65,7 @@ PINS = [
     lambda: [T.test_finite_differences(5, 4, m, mk) for m in ("none", "causal") for mk in ("none", "key")],
     lambda: T.test_alibi_row_constant_only_shifts_lse(),
     lambda: [T.test_dense_mask_brute_force(bs) for bs in [(2, 3), (1, 3), (2, 1)]],
+    lambda: [T.test_query_offset_equals_rows_of_full(m) for m in T.MODS],
 ]
 
 
