@@ -205,36 +205,55 @@ def bench_decode(E, dev, args):
     for i in range(nsets):
         ks.append(IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED + 3000 + i, w.dtype).to(dev))
         vs.append(IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED + 5000 + i, w.dtype).to(dev))
+    reps = nsets * 8
+
+    def graph_us(call, ws):
+        """Median time per call of `reps` calls captured in one CUDA graph, K/V rotating."""
+        for i in range(3):
+            call(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(reps):
+                    call(i)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / reps)
+        assert E.poll_status(ws) == 0
+        return statistics.median(times) * 1e3
+
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, 1), dtype=torch.float32, device=dev)
-    shape = E.make_shape(q, ks[0])
-    ws = E.workspace(E.OP_DECODE, shape, dev)
-    for i in range(3):
-        E.attn_decode(q, ks[i], vs[i], score_mod=w.score_mod, out=out, lse=lse, ws=ws)
-    torch.cuda.synchronize()
-    reps = nsets * 8
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream(dev)
-    s.wait_stream(torch.cuda.current_stream(dev))
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            for i in range(reps):
-                E.attn_decode(q, ks[i % nsets], vs[i % nsets], score_mod=w.score_mod, out=out, lse=lse, ws=ws)
-    torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(5):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b) / reps)
-    us = statistics.median(times) * 1e3
-    assert E.poll_status(ws) == 0
-    return {"workload": w.name, "us_per_call": us, "bytes_per_call": per + 2 * w.B * w.H * w.D * 2,
-            "GB/s": (per + 2 * w.B * w.H * w.D * 2) / (us * 1e-6) / 1e9, "rotating_sets": nsets}
+    ws = E.workspace(E.OP_DECODE, E.make_shape(q, ks[0]), dev)
+    us = graph_us(lambda i: E.attn_decode(q, ks[i % nsets], vs[i % nsets], score_mod=w.score_mod, out=out, lse=lse,
+                                          ws=ws), ws)
+    res = {"workload": w.name, "us_per_call": us, "bytes_per_call": per + 2 * w.B * w.H * w.D * 2,
+           "GB/s": (per + 2 * w.B * w.H * w.D * 2) / (us * 1e-6) / 1e9, "rotating_sets": nsets}
+    # chunked decode: nq queries at the last nq positions of the same KV cache, causal
+    # (speculative / chunked decoding); the K/V bytes bound it as for one query
+    chunk = []
+    for nq in (4, 16, 64):
+        qc = IN.randn((w.B, w.H, nq, w.D), IN.SEED + 7 + nq, w.dtype).to(dev)
+        oc = torch.empty_like(qc)
+        lc = torch.empty((w.B, w.H, nq), dtype=torch.float32, device=dev)
+        wsc = E.workspace(E.OP_DECODE_CHUNK, E.make_shape(qc, ks[0]), dev)
+        usc = graph_us(lambda i: E.attn_decode_chunk(qc, ks[i % nsets], vs[i % nsets], w.Skv - nq, score_mod="causal",
+                                                     out=oc, lse=lc, ws=wsc), wsc)
+        byt = per + 2 * w.B * w.H * nq * w.D * 2
+        chunk.append({"nq": nq, "us_per_call": usc, "GB/s": byt / (usc * 1e-6) / 1e9})
+    res["chunk_causal_fp16_b8h8kv2048d64"] = chunk
+    return res
 
 
 def bench_e2e(E, dev, args, w):
@@ -547,7 +566,9 @@ def main():
             "phase_ms": ph,
             "frac_of_peak": {"burst": value / burst, "sustained": value / sustained, "peak_source": src},
             "decode": {"workload": dec["workload"], "us_per_call": dec["us_per_call"], "GB/s": dec["GB/s"],
-                       "frac_of_hbm": dec["GB/s"] / hbm},
+                       "frac_of_hbm": dec["GB/s"] / hbm,
+                       "chunk_causal_fp16_b8h8kv2048d64": [dict(c, frac_of_hbm=c["GB/s"] / hbm)
+                                                           for c in dec["chunk_causal_fp16_b8h8kv2048d64"]]},
             "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": achieved, "peak": sustained,
                          "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": DKDV_TRAFFIC_BYTES,
                          "peak_kind": f"bf16 sustained, {src}"},

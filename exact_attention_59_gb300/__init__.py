@@ -7,15 +7,16 @@ not load the library; the first call does, and raises if it is not built.
 """
 
 from ._lib import (ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_SHAPE, ATTN_ERR_TIMEOUT,
-                   ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_OK, LIB_PATH, MODS, OP_BWD, OP_DECODE, OP_FWD,
+                   ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_OK, LIB_PATH, MODS, OP_BWD, OP_DECODE,
+                   OP_DECODE_CHUNK, OP_FWD,
                    SYMBOLS, AttnError, BlockMask, DenseMask, Shape, attn_bwd, attn_bwd_dkdv, attn_bwd_dq,
-                   attn_bwd_preprocess, attn_decode, attn_fwd, create_block_mask, load, make_shape,
+                   attn_bwd_preprocess, attn_decode, attn_decode_chunk, attn_fwd, create_block_mask, load, make_shape,
                    pack_dense_mask, poll_status, status_string, workspace, workspace_size)
 
 __all__ = [
-    "attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode",
+    "attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_decode_chunk",
     "create_block_mask", "BlockMask", "pack_dense_mask", "DenseMask", "workspace", "workspace_size",
     "poll_status", "status_string", "load", "AttnError", "Shape", "make_shape", "LIB_PATH", "SYMBOLS", "MODS",
-    "OP_FWD", "OP_BWD", "OP_DECODE", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_SHAPE", "ATTN_ERR_ALIGN",
+    "OP_FWD", "OP_BWD", "OP_DECODE", "OP_DECODE_CHUNK", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_SHAPE", "ATTN_ERR_ALIGN",
     "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT",
 ]

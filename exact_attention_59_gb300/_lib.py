@@ -20,13 +20,14 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn_gb3
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_SHAPE, ATTN_ERR_ALIGN = 0, 1, 2, 3
 ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 4, 5, 6, 7
 ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
-OP_FWD, OP_BWD, OP_DECODE = 0, 1, 2
+OP_FWD, OP_BWD, OP_DECODE, OP_DECODE_CHUNK = 0, 1, 2, 3
 MODS = {"none": 0, "alibi": 1, "checkerboard": 2, "causal": 3}
 MASK_MODS = {"none": 0, "causal": 1}
 
 SYMBOLS = ("attn_workspace_size", "attn_build_block_mask", "attn_fwd", "attn_bwd", "attn_bwd_preprocess",
            "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_poll_status", "attn_status_string",
-           "attn_dense_mask_bytes", "attn_pack_dense_mask", "attn_fwd_dense", "attn_bwd_dense")
+           "attn_dense_mask_bytes", "attn_pack_dense_mask", "attn_fwd_dense", "attn_bwd_dense",
+           "attn_decode_chunk")
 
 
 class AttnError(RuntimeError):
@@ -83,6 +84,7 @@ def load():
             "attn_pack_dense_mask": (I, [sp, P, I, I, P, SZ, P]),
             "attn_fwd_dense": (I, [sp, P, P, P, P, dp, bp, I, F, P, P, P, SZ, P, P]),
             "attn_bwd_dense": (I, [sp, P, P, P, P, P, P, P, dp, bp, I, F, P, P, P, P, SZ, P]),
+            "attn_decode_chunk": (I, [sp, P, P, P, P, I, F, I, P, P, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -298,6 +300,23 @@ def attn_decode(q, k, v, key_mask=None, score_mod="none", scale=None, out=None, 
     code = load().attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _mod(score_mod),
                               scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
     _check(code, "attn_decode")
+    return out, lse
+
+
+def attn_decode_chunk(q, k, v, q_offset: int, key_mask=None, score_mod="none", scale=None, out=None, lse=None,
+                      ws=None):
+    """(out, lse) for a chunk of queries q (B, H, nq, D) at positions
+    q_offset .. q_offset + nq - 1 of the keys k, v (B, H, Skv, D)."""
+    _cuda(q, k, v, key_mask, out, lse)
+    shape = make_shape(q, k)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(OP_DECODE_CHUNK, shape, q.device) if ws is None else ws
+    code = load().attn_decode_chunk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask),
+                                    _mod(score_mod), scale, int(q_offset), _ptr(out), _ptr(lse), _ptr(ws),
+                                    ws.numel(), _stream(q.device))
+    _check(code, "attn_decode_chunk")
     return out, lse
 
 

@@ -84,6 +84,23 @@ DecodeSplit decode_split(const attn_shape* s) {
   return {ns, kps};
 }
 
+// 128-row tiles covering n rows (the last one may be partial)
+int tiles_of(int n) { return (n + 127) / 128; }
+
+// Split of a query chunk's kv blocks over CTAs: about one CTA per SM in total
+// (152 SMs; the forward kernel runs one CTA per SM), at least one kv block each.
+struct ChunkSplit {
+  int nsplit, kps;
+};
+constexpr long long kSms = 152;
+ChunkSplit chunk_split(const attn_shape* s) {
+  const long long nkb = tiles_of(s->Skv), items = (long long)s->B * s->H * ((tiles_of(s->Sq) + 1) / 2);
+  int ns = (int)std::max<long long>(1, std::min<long long>(nkb, kSms / std::max<long long>(1, items)));
+  const int kps = (int)((nkb + ns - 1) / ns);
+  ns = (int)((nkb + kps - 1) / kps);
+  return {ns, kps};
+}
+
 WsLayout layout(attn_op op, const attn_shape* s) {
   WsLayout w;
   size_t off = 256;
@@ -105,6 +122,14 @@ WsLayout layout(attn_op op, const attn_shape* s) {
     w.counter = off;
     off = align256(off + BH * 4);
   }
+  if (op == ATTN_OP_DECODE_CHUNK) {
+    // partial rows of the split: sized for min(max(items, SMs), items * nkb) CTAs,
+    // a bound on items * nsplit that grows with every dimension of the shape
+    const long long items = (long long)BH * ((tiles_of(s->Sq) + 1) / 2), nkb = tiles_of(s->Skv);
+    const long long ctas = std::min(std::max(items, kSms), items * nkb);
+    w.partial = off;
+    off = align256(off + (size_t)ctas * 256 * FWD_PART * 4);
+  }
   w.total = off;
   return w;
 }
@@ -115,9 +140,6 @@ T* at(void* ws, size_t off) {
 }
 
 attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
-
-// 128-row tiles covering n rows (the last one may be partial)
-int tiles_of(int n) { return (n + 127) / 128; }
 
 // Checks shared by every prefill call.  Any Sq, Skv >= 1 on the f16/bf16
 // D = 64 path (the last q and kv tiles may be partial); multiples of 128 for
@@ -273,7 +295,7 @@ extern "C" {
 
 size_t attn_workspace_size(attn_op op, const attn_shape* shape) {
   if (!shape_ok(shape)) return 0;
-  if ((int)op < 0 || (int)op > 2) return 0;
+  if ((int)op < 0 || (int)op > 3) return 0;
   return layout(op, shape).total;
 }
 
@@ -380,6 +402,7 @@ attn_status attn_fwd_dense(const attn_shape* s, const void* q, const void* k, co
   p.sc = scale * kLog2e;
   p.timeout_ns = timeout_ns();
   p.inject_stall = inject_stall();
+  p.nsplit = 1;   // whole kv range per CTA, q_off = 0
   return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
@@ -575,6 +598,54 @@ attn_status attn_decode(const attn_shape* s, const void* q, const void* k, const
   p.sc = scale * kLog2e;
   p.mod = (int)mod;
   return cuda_status(launch_decode(p, s->dtype == ATTN_BF16, (cudaStream_t)stream));
+}
+
+attn_status attn_decode_chunk(const attn_shape* s, const void* q, const void* k, const void* v,
+                              const uint8_t* key_mask, attn_score_mod mod, float scale, int q_offset, void* out,
+                              float* lse, void* ws, size_t ws_bytes, attn_stream_t stream) {
+  if (!shape_ok(s) || q_offset < 0) return ATTN_ERR_INVALID_ARG;
+  if (s->D != 64 || s->dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+  if (tiles_of(s->Skv) > FWD_MAXKB || tiles_of(s->Sq) > FWD_MAXKB) return ATTN_ERR_SHAPE;
+  ATTN_TRY(check_mod(mod, scale));
+  ATTN_PTR(q);
+  ATTN_PTR(k);
+  ATTN_PTR(v);
+  ATTN_PTR(out);
+  ATTN_PTR(lse);
+  ATTN_OPT_PTR(key_mask);
+  ATTN_TRY(check_ws(ATTN_OP_DECODE_CHUNK, s, ws, ws_bytes));
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout w = layout(ATTN_OP_DECODE_CHUNK, s);
+  const ChunkSplit cs = chunk_split(s);
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const long long rq = (long long)s->B * s->H * s->Sq, rk = (long long)s->B * s->H * s->Skv;
+  if (!make_tmap(&p.tm_q, q, rq, 64, s->dtype) || !make_tmap(&p.tm_k, k, rk, 64, s->dtype) ||
+      !make_tmap(&p.tm_v, v, rk, 64, s->dtype))
+    return ATTN_ERR_CUDA;
+  ATTN_TRY(run_keymask(s, key_mask, ws, st));
+  p.out = out;
+  p.lse = lse;
+  p.km_bits = key_mask ? at<uint32_t>(ws, w.km_bits) : nullptr;
+  p.km_sum = key_mask ? at<uint8_t>(ws, w.km_sum) : nullptr;
+  p.status = at<int>(ws, 0);
+  p.B = s->B;
+  p.H = s->H;
+  p.Sq = s->Sq;
+  p.Skv = s->Skv;
+  p.nqb = tiles_of(s->Sq);
+  p.nkb = tiles_of(s->Skv);
+  p.npairs = (p.nqb + 1) / 2;
+  p.sc = scale * kLog2e;
+  p.timeout_ns = timeout_ns();
+  p.q_off = q_offset;
+  p.nsplit = cs.nsplit;
+  p.kps = cs.kps;
+  p.part = cs.nsplit > 1 ? at<float>(ws, w.partial) : nullptr;
+  const bool bf16 = s->dtype == ATTN_BF16;
+  ATTN_TRY(cuda_status(launch_fwd_d64(p, bf16, (int)mod, st)));
+  if (cs.nsplit == 1) return ATTN_OK;   // one kv range: the kernel wrote out and lse itself
+  return cuda_status(launch_split_merge(p.part, cs.nsplit, rq, s->Sq, out, lse, bf16, st));
 }
 
 attn_status attn_poll_status(void* ws, attn_stream_t stream) {

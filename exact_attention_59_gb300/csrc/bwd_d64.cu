@@ -97,12 +97,15 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     sm.abort = 0;
     // list of q blocks that see this kv block
     const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
-    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     int n = 0;
     if (ks != 0) {
       for (int qb = 0; qb < p.nqb; ++qb) {
         const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-        const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qb) * p.nkb + kb] : TILE_FULL;
+        // the dense tile state, only in the dense build: a runtime test here, in the
+        // one thread that builds the list while the CTA waits, cost ~4% of the pass
+        int ds = TILE_FULL;
+        if constexpr (DM)
+          ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
         if (st == TILE_EMPTY || ds == TILE_EMPTY) continue;
         sm.list[n] = (uint16_t)qb;
         sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
@@ -290,7 +293,6 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     // those rows stay confined to the padded key and the epilogue writes zeros.
     bool my_key = kv < p.Skv;   // rows past Skv (partial last kv block) are not written
     if (p.km_bits && my_key) my_key = (km_word(p.km_bits, b, p.Skv, kv) >> (kv & 31)) & 1u;
-    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     bool ok = true;
     for (int u = 0; u < N; ++u) {
       const int qb = sm.list[u];
@@ -299,13 +301,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
       // this key's dense-mask bits for the half's 64 queries (column words)
-      const bool dense = DM && (f & KB_DENSE);
-      uint32_t dw[2] = {0u, 0u};
-      if (dense && kv < p.Skv) {
-        const uint2 d2 = __ldg(reinterpret_cast<const uint2*>(p.dm.colbits + (dmi * p.Skv + kv) * (4LL * p.nqb) +
-                                                              4 * qb + 2 * w));
-        dw[0] = d2.x;
-        dw[1] = d2.y;
+      bool dense = false;
+      uint2 dwv = make_uint2(0u, 0u);
+      if constexpr (DM) {
+        dense = f & KB_DENSE;
+        const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
+        if (dense && kv < p.Skv)
+          dwv = __ldg(reinterpret_cast<const uint2*>(p.dm.colbits + (dmi * p.Skv + kv) * (4LL * p.nqb) + 4 * qb +
+                                                     2 * w));
       }
       if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
@@ -338,9 +341,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
             x0 = kv > q0 + 2 * i ? -INFINITY : x0;
             x1 = kv > q0 + 2 * i + 1 ? -INFINITY : x1;
           }
-          if (DENSE) {
-            x0 = (dw[(2 * i) >> 5] & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
-            x1 = (dw[(2 * i + 1) >> 5] & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
+          if constexpr (DENSE) {
+            const uint32_t dwi = i < 16 ? dwv.x : dwv.y;
+            x0 = (dwi & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
+            x1 = (dwi & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
           }
           const float p0 = ex2(x0), p1 = ex2(x1);
           pr[2 * i] = p0;
@@ -348,9 +352,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
           pk[i] = pack2<BF16>(p0, p1);
         }
       };
-      if (dense) {
-        if (causal) probs(std::true_type{}, std::true_type{});
-        else probs(std::false_type{}, std::true_type{});
+      if (dense) {   // never with DM = false
+        if constexpr (DM) {
+          if (causal) probs(std::true_type{}, std::true_type{});
+          else probs(std::false_type{}, std::true_type{});
+        }
       } else {
         if (causal) probs(std::true_type{}, std::false_type{});
         else probs(std::false_type{}, std::false_type{});
@@ -469,12 +475,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     int n = 0;
-    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     for (int kb = 0; kb < p.nkb; ++kb) {
       const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
       if (ks == 0) continue;
       const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-      const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qb) * p.nkb + kb] : TILE_FULL;
+      int ds = TILE_FULL;   // dense tile state: dense build only (as in the dK/dV list)
+      if constexpr (DM)
+        ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
       if (st == TILE_EMPTY || ds == TILE_EMPTY) continue;
       sm.list[n] = (uint16_t)kb;
       sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
@@ -627,7 +634,6 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     // rows past Sq (partial last q tile) get P = 0 and are not written
     const float nl2 = q < p.Sq ? p.lse2[(size_t)bh * p.Sq + q] : -INFINITY;   // -lse log2(e)
     const float nd = q < p.Sq ? p.delta[(size_t)bh * p.Sq + q] : 0.f;        // -D
-    const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
     const uint64_t scv = f2(p.sc, p.sc), nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
     bool ok = true;
     for (int u = 0; u < N; ++u) {
@@ -642,13 +648,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       const bool limited = causal || kvl < 63;
       const int lim = causal ? min(q - k0, kvl) : kvl;
       // this row's dense-mask bits for the half's 64 keys
-      const bool dense = DM && (f & KB_DENSE);
-      uint32_t dw[2] = {0u, 0u};
-      if (dense && q < p.Sq) {
-        const uint2 d2 = __ldg(reinterpret_cast<const uint2*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) +
-                                                              4 * kb + 2 * w));
-        dw[0] = d2.x;
-        dw[1] = d2.y;
+      bool dense = false;
+      uint2 dwv = make_uint2(0u, 0u);
+      if constexpr (DM) {
+        dense = f & KB_DENSE;
+        const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
+        if (dense && q < p.Sq)
+          dwv = __ldg(reinterpret_cast<const uint2*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) + 4 * kb +
+                                                     2 * w));
       }
       if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
@@ -680,17 +687,22 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
             x0 = 2 * i > lim ? -INFINITY : x0;
             x1 = 2 * i + 1 > lim ? -INFINITY : x1;
           }
-          if (DENSE) {
-            x0 = (dw[(2 * i) >> 5] & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
-            x1 = (dw[(2 * i + 1) >> 5] & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
+          if constexpr (DENSE) {
+            const uint32_t dwi = i < 16 ? dwv.x : dwv.y;
+            x0 = (dwi & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
+            x1 = (dwi & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
           }
           pr[2 * i] = ex2(x0);
           pr[2 * i + 1] = ex2(x1);
         }
       };
-      if (dense) probs(std::true_type{}, std::true_type{});   // with dense bits, the limited copy too
-      else if (limited) probs(std::true_type{}, std::false_type{});
-      else probs(std::false_type{}, std::false_type{});
+      if (dense) {   // with dense bits, the limited copy too (never with DM = false)
+        if constexpr (DM) probs(std::true_type{}, std::true_type{});
+      } else if (limited) {
+        probs(std::true_type{}, std::false_type{});
+      } else {
+        probs(std::false_type{}, std::false_type{});
+      }
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
       tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);

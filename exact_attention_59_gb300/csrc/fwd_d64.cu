@@ -53,8 +53,7 @@ static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 // in the row's dense-mask words dw is 0; and the running maximum in four
 // independent chains.
 template <bool TABLE, bool LIMITED, bool DENSE>
-DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, const uint32_t (&dw)[4],
-                       float (&mx)[4]) {
+DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4]) {
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
     float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -70,9 +69,10 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
         x0 = c > lim ? -INFINITY : x0;
         x1 = c + 1 > lim ? -INFINITY : x1;
       }
-      if (DENSE) {
-        x0 = (dw[c >> 5] & (1u << (c & 31))) ? x0 : -INFINITY;
-        x1 = (dw[(c + 1) >> 5] & (1u << ((c + 1) & 31))) ? x1 : -INFINITY;
+      if constexpr (DENSE) {
+        const uint32_t w = c < 32 ? dw.x : (c < 64 ? dw.y : (c < 96 ? dw.z : dw.w));
+        x0 = (w & (1u << (c & 31))) ? x0 : -INFINITY;
+        x1 = (w & (1u << ((c + 1) & 31))) ? x1 : -INFINITY;
       }
       r[c] = __float_as_uint(x0);
       r[c + 1] = __float_as_uint(x1);
@@ -81,15 +81,25 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
   }
 }
 
-// DM: built with the dense-mask path (the kernels without it are unchanged by it)
-template <bool BF16, int MOD, bool DM>
+// Kernel variants, so that each path costs the others nothing:
+//   FWD_PLAIN  the forward;
+//   FWD_DENSE  with the dense-mask path;
+//   FWD_CHUNK  queries at a position offset, kv blocks split over CTAs (decode).
+constexpr int FWD_PLAIN = 0, FWD_DENSE = 1, FWD_CHUNK = 2;
+
+template <bool BF16, int MOD, int VAR>
 __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr bool DM = VAR == FWD_DENSE, CHUNK = VAR == FWD_CHUNK;
   const int BH = p.B * p.H;
-  const int L = blockIdx.x;
+  const int L = CHUNK ? blockIdx.x % (p.npairs * BH) : blockIdx.x;
+  const int split = CHUNK ? blockIdx.x / (p.npairs * BH) : 0;   // kv-block range of this CTA
+  const int kb_lo = CHUNK ? split * p.kps : 0;
+  const int kb_hi = CHUNK && p.nsplit > 1 ? min(p.nkb, kb_lo + p.kps) : p.nkb;
+  const int q_off = CHUNK ? p.q_off : 0;
   const int pair = p.npairs - 1 - L / BH;   // longest causal pairs first
   const int bh = L % BH;
   const int b = bh / p.H, h = bh % p.H;
@@ -123,9 +133,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     for (int t = 0; t < 2; ++t) {
       const int qt = qt0 + t;
       uint8_t f = 0;
-      if (qt < p.nqb && ks != 0) {
+      if (qt < p.nqb && ks != 0 && (!CHUNK || (kb >= kb_lo && kb < kb_hi))) {
         const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qt * p.nkb + kb] : TILE_FULL;
-        const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb] : TILE_FULL;
+        int ds = TILE_FULL;   // dense tile state: dense build only
+        if constexpr (DM) ds = p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb];
         if (st != TILE_EMPTY && ds != TILE_EMPTY)
           f = KB_VISIT | (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) |
               (ks == 1 ? KB_KEYMASK : 0) | (ds == TILE_PARTIAL ? KB_DENSE : 0);
@@ -300,10 +311,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       const uint32_t tP = tS + 128, tO = tS + 192;
       const int row = 32 * quad + lane;
       const int q = qt * 128 + row;
+      const int qpos = q + q_off;   // the row's position among the keys (score mods, causal rule)
       const bool writer = quad == 3 && lane == 0;   // first warp of the group (warp 3 or 7)
       const uint64_t scv = f2(p.sc, p.sc);
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
-      const int parity = (MOD == MOD_CHECKER) ? (q & 1) : 0;
+      const int parity = (MOD == MOD_CHECKER) ? (qpos & 1) : 0;
       float m_run = -INFINITY, l = 0.f;
       uint32_t n = 0;
       int u = 0;
@@ -320,11 +332,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const int s = u % FWD_NST;
         ++u;
         // this row's dense-mask bits for the block, fetched before the wait hides the load
-        const bool dense = DM && (f & KB_DENSE);
-        uint32_t dw[4] = {0u, 0u, 0u, 0u};
-        if (dense && q < p.Sq) {
-          const uint4 d4 = __ldg(reinterpret_cast<const uint4*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb)) + kb);
-          dw[0] = d4.x; dw[1] = d4.y; dw[2] = d4.z; dw[3] = d4.w;
+        bool dense = false;
+        uint4 dw = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (DM) {
+          dense = f & KB_DENSE;
+          if (dense && q < p.Sq)
+            dw = __ldg(reinterpret_cast<const uint4*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb)) + kb);
         }
         if (!wait_warp(smem_u32(&sm.sfull[t]), n & 1, c)) { ok = false; break; }
         // the stage's bias table was written before its full barrier was armed
@@ -336,30 +349,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.sfree[t]));
         const int kv0 = kb * 128;
-        const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128) ||
+        const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128 + q_off) ||
                             ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
         // keep column cc iff cc <= lim: the causal limit and, in a partial last kv
         // block, the end of the keys
         const int kvlim = p.Skv - 1 - kv0;
         const bool limited = causal || kvlim < 127;
-        const int lim = causal ? min(q - kv0, kvlim) : kvlim;
+        const int lim = causal ? min(qpos - kv0, kvlim) : kvlim;
         const float* tb = sm.cb[s][parity];
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // one straight-line copy of the pass per (table, causal) pair: a runtime
         // test inside the unrolled loop would cost instructions on every score
         // (a block with dense-mask bits always takes the limited copy too)
         if (use_table) {
-          if (dense) scale_scores<true, true, true>(r, scv, tb, lim, dw, mx);
+          if (DM && dense) scale_scores<true, true, DM>(r, scv, tb, lim, dw, mx);
           else if (limited) scale_scores<true, true, false>(r, scv, tb, lim, dw, mx);
           else scale_scores<true, false, false>(r, scv, tb, lim, dw, mx);
         } else {
-          if (dense) scale_scores<false, true, true>(r, scv, tb, lim, dw, mx);
+          if (DM && dense) scale_scores<false, true, DM>(r, scv, tb, lim, dw, mx);
           else if (limited) scale_scores<false, true, false>(r, scv, tb, lim, dw, mx);
           else scale_scores<false, false, false>(r, scv, tb, lim, dw, mx);
         }
         // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
         // per-score work: scores here are x' = x - base
-        const float base = (MOD == MOD_ALIBI) ? slope2 * float(kv0 - q) : 0.f;
+        const float base = (MOD == MOD_ALIBI) ? slope2 * float(kv0 - qpos) : 0.f;
         const float rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) + base;
         // stale running max: rescale O only when the max grows by more than 2^8
         float alpha = 1.f;
@@ -432,7 +445,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
         // rows past Sq (partial last q tile) are computed, not written; the TMEM
         // load above stays warp-wide (tcgen05.ld is .sync.aligned)
-        if (q < p.Sq) {
+        if (CHUNK && p.part && q < p.Sq) {
+          // one kv range of a split: the unnormalised row, merged by launch_split_merge
+          float* dst = p.part + (((size_t)bh * p.nsplit + split) * p.Sq + q) * FWD_PART;
+          *reinterpret_cast<float4*>(dst) = make_float4(l > 0.f ? m_run : -INFINITY, l, 0.f, 0.f);
+          uint4* od = reinterpret_cast<uint4*>(dst + 4);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) od[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        } else if (q < p.Sq) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + ((size_t)bh * p.Sq + q) * 64);
 #pragma unroll
           for (int i = 0; i < 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -457,12 +477,57 @@ size_t fwd_d64_smem_bytes() { return sizeof(FwdSmem) + 1024; }
 
 template <bool BF16, int MOD>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
-  auto kern = p.dm.tiles ? fwd_d64_kernel<BF16, MOD, true> : fwd_d64_kernel<BF16, MOD, false>;
+  auto kern = p.nsplit > 1 || p.q_off != 0 ? fwd_d64_kernel<BF16, MOD, FWD_CHUNK>
+              : p.dm.tiles             ? fwd_d64_kernel<BF16, MOD, FWD_DENSE>
+                                       : fwd_d64_kernel<BF16, MOD, FWD_PLAIN>;
   const size_t smem = fwd_d64_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.npairs * p.B * p.H);
+  const unsigned grid = (unsigned)(p.npairs * p.B * p.H * p.nsplit);
   kern<<<grid, FWD_THREADS, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+// One warp per row: M = max_s m_s, L = sum_s l_s 2^(m_s - M),
+// O = sum_s O_s 2^(m_s - M) / L, lse = (M + log2 L) ln 2 (O = 0, lse = -inf
+// when no split kept a key).  Lane j owns columns 2 j, 2 j + 1.
+template <bool BF16>
+__global__ void __launch_bounds__(256) split_merge_kernel(const float* __restrict__ part, int nsplit, long long rows,
+                                                          int Sq, void* __restrict__ out, float* __restrict__ lse) {
+  const long long r = blockIdx.x * 8LL + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const long long bh = r / Sq, q = r % Sq;
+  const float* base = part + ((size_t)bh * nsplit * Sq + q) * FWD_PART;
+  const size_t stride = (size_t)Sq * FWD_PART;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, base[s * stride]);
+  float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < nsplit; ++s) {
+      const float* ps = base + s * stride;
+      const float m = ps[0];
+      if (m == -INFINITY) continue;
+      const float w = ex2(m - M);
+      Lsum = fmaf(w, ps[1], Lsum);
+      const float2 ov = *reinterpret_cast<const float2*>(ps + 4 + 2 * lane);
+      o0 = fmaf(w, ov.x, o0);
+      o1 = fmaf(w, ov.y, o1);
+    }
+  }
+  const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+  reinterpret_cast<uint32_t*>(out)[r * 32 + lane] = pack2<BF16>(o0 * inv, o1 * inv);
+  if (lane == 0) lse[r] = Lsum > 0.f ? (M + lg2(Lsum)) * kLn2 : -INFINITY;
+}
+
+cudaError_t launch_split_merge(const float* part, int nsplit, long long rows, int Sq, void* out, float* lse, bool bf16,
+                               cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (bf16)
+    split_merge_kernel<true><<<grid, 256, 0, st>>>(part, nsplit, rows, Sq, out, lse);
+  else
+    split_merge_kernel<false><<<grid, 256, 0, st>>>(part, nsplit, rows, Sq, out, lse);
   return cudaGetLastError();
 }
 

@@ -62,9 +62,19 @@ struct FwdParams {
   float sc;                       // scale * log2(e)
   unsigned long long timeout_ns;
   int inject_stall;               // test hook: the producer withholds the first K/V copy
+  int q_off;                      // position of query row 0 among the keys (0 for prefill)
+  // split over kv blocks: CTA split s takes blocks [s kps, (s + 1) kps) and writes
+  // part (B*H, nsplit, Sq, FWD_PART) f32 rows {m (log2 units), l, 0, 0, O[64]
+  // unnormalised} instead of out and lse; nsplit = 1 and part = nullptr otherwise
+  int nsplit, kps;
+  float* part;
 };
+constexpr int FWD_PART = 68;      // floats per partial row (16-byte aligned O)
 size_t fwd_d64_smem_bytes();
 cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t st);
+// out, lse of each row from its nsplit partial rows (part as in FwdParams)
+cudaError_t launch_split_merge(const float* part, int nsplit, long long rows, int Sq, void* out, float* lse, bool bf16,
+                               cudaStream_t st);
 
 // ---------------------------------------------------------------- forward, D = 512
 struct FwdBigParams {

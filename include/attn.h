@@ -94,7 +94,7 @@ typedef enum { ATTN_MASKMOD_NONE = 0, ATTN_MASKMOD_CAUSAL = 1 } attn_mask_mod;
 /* Block-mask tile states. */
 enum { ATTN_TILE_EMPTY = 0, ATTN_TILE_PARTIAL = 1, ATTN_TILE_FULL = 2 };
 
-typedef enum { ATTN_OP_FWD = 0, ATTN_OP_BWD = 1, ATTN_OP_DECODE = 2 } attn_op;
+typedef enum { ATTN_OP_FWD = 0, ATTN_OP_BWD = 1, ATTN_OP_DECODE = 2, ATTN_OP_DECODE_CHUNK = 3 } attn_op;
 
 typedef struct {
   int B, H, Sq, Skv, D;
@@ -243,6 +243,24 @@ attn_status attn_decode_noalloc(const attn_shape* shape, const void* q, const vo
 /* Synchronises `stream`, then reads and clears the workspace status word.
  * Returns ATTN_OK, ATTN_ERR_TIMEOUT (a device wait ran out), or
  * ATTN_ERR_CUDA (the stream reported an error). */
+/* Decode of a chunk of shape->Sq >= 1 queries against a KV cache of Skv keys
+ * that already holds earlier tokens: query row i sits at position
+ * q_offset + i, the position every score_mod uses (the causal rule keeps
+ * keys kv <= q_offset + i; ALiBi and checkerboard see the position).  The
+ * flaxattention README's "Decoding" benchmark and its "faster decoding"
+ * item cover q_len = 1; this is the same computation for a few queries
+ * (speculative or chunked decoding), run on the tensor cores: the kv blocks
+ * are split over about one CTA per SM and a second launch merges the
+ * per-split rows.  f16/bf16, D = 64, any Sq and Skv (ATTN_ERR_SHAPE past
+ * 2048 tiles of 128), optional key_mask; no block or dense mask.
+ * Workspace: attn_workspace_size(ATTN_OP_DECODE_CHUNK, shape).
+ * Errors: ATTN_ERR_INVALID_ARG (q_offset < 0, NULL pointer, bad mod or
+ * scale), ATTN_ERR_UNSUPPORTED (f32 or D != 64), ATTN_ERR_ALIGN,
+ * ATTN_ERR_WORKSPACE. */
+attn_status attn_decode_chunk(const attn_shape* shape, const void* q, const void* k, const void* v,
+                              const uint8_t* key_mask, attn_score_mod mod, float scale, int q_offset, void* out,
+                              float* lse, void* ws, size_t ws_bytes, attn_stream_t stream);
+
 attn_status attn_poll_status(void* ws, attn_stream_t stream);
 
 /* Static text for a status code. */

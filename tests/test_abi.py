@@ -52,7 +52,7 @@ def _shape(lib, B=1, H=2, Sq=256, Skv=256, D=64, dt=2):
 
 def test_workspace_size_monotonic(lib):
     base = dict(B=2, H=2, Sq=256, Skv=256, D=64, dt=2)
-    for op in (0, 1, 2):
+    for op in (0, 1, 2, 3):
         prev = lib.workspace_size(op, _shape(lib, **base))
         assert prev > 0
         for key in ("B", "H", "Sq", "Skv"):
@@ -177,3 +177,21 @@ def test_dense_mask_sizes_and_validation(lib):
     assert fwd(shape=_shape(lib, B=2, H=4, Sq=256, Skv=256, D=512), dm=ok) == lib.ATTN_ERR_UNSUPPORTED
     # with no dense mask the calls are attn_fwd / attn_bwd (same validation)
     assert fwd(shape=_shape(lib, D=96)) == _fwd(lib, _shape(lib, D=96)) == lib.ATTN_ERR_UNSUPPORTED
+
+
+def test_decode_chunk_validation(lib):
+    L = lib.load()
+
+    def call(shape, q_offset=0, mod=0, scale=0.125, ws=FAKE, n=1 << 30, out=FAKE):
+        return L.attn_decode_chunk(ctypes.byref(shape), FAKE, FAKE, FAKE, None, mod, scale, q_offset, out, FAKE,
+                                   ws, n, None)
+    s = _shape(lib, B=2, H=3, Sq=4, Skv=1000)
+    assert call(s, q_offset=-1) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, B=2, H=3, Sq=4, Skv=1000, dt=0)) == lib.ATTN_ERR_UNSUPPORTED
+    assert call(_shape(lib, B=2, H=3, Sq=4, Skv=1000, D=128)) == lib.ATTN_ERR_UNSUPPORTED
+    assert call(_shape(lib, Skv=2048 * 128 + 1)) == lib.ATTN_ERR_SHAPE
+    assert call(s, mod=7) == lib.ATTN_ERR_INVALID_ARG
+    assert call(s, out=FAKE + 4) == lib.ATTN_ERR_ALIGN
+    assert call(s, ws=None) == lib.ATTN_ERR_WORKSPACE
+    assert call(s, n=lib.workspace_size(3, s) - 1) == lib.ATTN_ERR_WORKSPACE
+    assert lib.workspace_size(3, s) > lib.workspace_size(0, s)

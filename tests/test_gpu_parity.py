@@ -211,6 +211,64 @@ def test_dense_mask_packed_once_reused():
         assert torch.equal(a.view(torch.uint8), b_.view(torch.uint8))
 
 
+# Chunked decode: nq queries at positions off .. off + nq - 1 against Skv keys
+# (off = Skv - nq, the usual KV-cache case, unless given), split over kv blocks
+# and merged.
+CHUNK = [
+    # (B, H, nq, Skv, dtype, mod, key_mask, off)
+    (2, 3, 1, 2048, "f16", "causal", False, None),
+    (2, 3, 4, 2048, "bf16", "causal", True, None),
+    (1, 2, 16, 1000, "f16", "alibi", False, None),
+    (2, 2, 64, 777, "bf16", "checkerboard", True, None),
+    (1, 1, 100, 300, "f16", "none", True, 17),
+    (1, 2, 128, 4096 + 40, "bf16", "causal", False, None),
+    (2, 1, 200, 640, "f16", "causal", False, 440),
+    (1, 2, 3, 129, "bf16", "alibi", False, 1000),
+    (8, 8, 4, 2048, "f16", "causal", False, None),
+]
+
+
+@pytest.mark.parametrize("B,H,nq,Skv,dtype,mod,km,off", CHUNK)
+def test_decode_chunk(B, H, nq, Skv, dtype, mod, km, off):
+    off = Skv - nq if off is None else off
+    c, d = make_dev(B, H, nq, Skv, 64, dtype, key_mask=km)
+    tdt = d["q"].dtype
+    ob, out = guarded((B, H, nq, 64), tdt)
+    lb, lse = guarded((B, H, nq), torch.float32)
+    E.attn_decode_chunk(d["q"], d["k"], d["v"], off, key_mask=d["key_mask"], score_mod=mod, out=out, lse=lse)
+    shp = E.make_shape(d["q"], d["k"])
+    assert E.poll_status(E.workspace(E.OP_DECODE_CHUNK, shp, d["q"].device)) == E.ATTN_OK
+    assert canary_ok(ob, (B, H, nq, 64)) and canary_ok(lb, (B, H, nq))
+    kmn = None if c["key_mask"] is None else c["key_mask"].numpy()
+    o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=kmn, score_mod=mod, q_offset=off)
+    tol = TOL[dtype]
+    compare("out", f64(out), o_ref, tol["o_max"], tol["o_mean"])
+    fin = np.isfinite(l_ref)
+    assert (np.isneginf(f64(lse)) == np.isneginf(l_ref)).all(), "lse -inf pattern differs"
+    compare("lse", f64(lse), l_ref, tol["lse_max"], mask=fin)
+    if (~fin).any():
+        assert (f64(out)[~fin] == 0).all()
+    out2, lse2 = E.attn_decode_chunk(d["q"], d["k"], d["v"], off, key_mask=d["key_mask"], score_mod=mod)
+    assert torch.equal(out2.view(torch.uint8), out.view(torch.uint8)), "decode chunk not bitwise reproducible"
+    assert torch.equal(lse2.view(torch.uint8), lse.view(torch.uint8))
+
+
+def test_decode_chunk_matches_forward_rows():
+    """With off = 0 and nq = Sq the chunk call is the forward; with off = Skv - nq its
+    rows are the forward's last rows over the same keys.  The split path merges f32
+    partial rows in another order, so a bf16 output may differ by one step (2^-8 near
+    1): 1e-2 bounds that."""
+    B, H, S = 2, 2, 384
+    _, d = make_dev(B, H, S, S, 64, "bf16")
+    of, lf = E.attn_fwd(d["q"], d["k"], d["v"], score_mod="causal")
+    oc, lc = E.attn_decode_chunk(d["q"], d["k"], d["v"], 0, score_mod="causal")
+    torch.testing.assert_close(oc.float(), of.float(), atol=1e-2, rtol=0)
+    nq = 5
+    ot, lt = E.attn_decode_chunk(d["q"][:, :, S - nq:].contiguous(), d["k"], d["v"], S - nq, score_mod="causal")
+    torch.testing.assert_close(ot.float(), of[:, :, S - nq:].float(), atol=1e-2, rtol=0)
+    torch.testing.assert_close(lt, lf[:, :, S - nq:], atol=1e-4, rtol=0)
+
+
 def test_fully_masked_batches_and_blocks():
     """Batch 1 has no key at all; batch 0 has whole 128-key blocks padded (skipped tiles)."""
     km = torch.ones((2, 512), dtype=torch.uint8)
