@@ -95,26 +95,37 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     mbar_init(smem_u32(&sm.fin), 1);
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
-    // list of q blocks that see this kv block
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    // list of q blocks that see this kv block, in ascending order, 32 candidates
+    // per ballot (the whole CTA waits for it: it is kept off any single thread)
     const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
     int n = 0;
     if (ks != 0) {
-      for (int qb = 0; qb < p.nqb; ++qb) {
-        const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-        // the dense tile state, only in the dense build: a runtime test here, in the
-        // one thread that builds the list while the CTA waits, cost ~4% of the pass
-        int ds = TILE_FULL;
-        if constexpr (DM)
-          ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
-        if (st == TILE_EMPTY || ds == TILE_EMPTY) continue;
-        sm.list[n] = (uint16_t)qb;
-        sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
-                       (ds == TILE_PARTIAL ? KB_DENSE : 0);
-        ++n;
+      for (int q0 = 0; q0 < p.nqb; q0 += 32) {
+        const int qb = q0 + lane;
+        bool keep = false;
+        uint8_t fl = 0;
+        if (qb < p.nqb) {
+          const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
+          int ds = TILE_FULL;   // the dense tile state: dense build only
+          if constexpr (DM)
+            ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
+          keep = st != TILE_EMPTY && ds != TILE_EMPTY;
+          fl = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
+               (ds == TILE_PARTIAL ? KB_DENSE : 0);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int pos = n + __popc(m & ((1u << lane) - 1u));
+          sm.list[pos] = (uint16_t)qb;
+          sm.lflags[pos] = fl;
+        }
+        n += __popc(m);
       }
     }
-    sm.nlist = n;
-    fence_mbar_init();
+    if (lane == 0) sm.nlist = n;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -474,22 +485,35 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     mbar_init(smem_u32(&sm.fin), 1);
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
-    int n = 0;
-    for (int kb = 0; kb < p.nkb; ++kb) {
-      const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
-      if (ks == 0) continue;
-      const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-      int ds = TILE_FULL;   // dense tile state: dense build only (as in the dK/dV list)
-      if constexpr (DM)
-        ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
-      if (st == TILE_EMPTY || ds == TILE_EMPTY) continue;
-      sm.list[n] = (uint16_t)kb;
-      sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
-                     (ds == TILE_PARTIAL ? KB_DENSE : 0);
-      ++n;
-    }
-    sm.nlist = n;
     fence_mbar_init();
+  }
+  if (warp == 2) {
+    // list of kv blocks this q block sees, in ascending order, 32 candidates per
+    // ballot (as in the dK/dV pass)
+    int n = 0;
+    for (int k0 = 0; k0 < p.nkb; k0 += 32) {
+      const int kb = k0 + lane;
+      bool keep = false;
+      uint8_t fl = 0;
+      if (kb < p.nkb) {
+        const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
+        const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
+        int ds = TILE_FULL;   // the dense tile state: dense build only
+        if constexpr (DM)
+          ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
+        keep = ks != 0 && st != TILE_EMPTY && ds != TILE_EMPTY;
+        fl = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
+             (ds == TILE_PARTIAL ? KB_DENSE : 0);
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
+        const int pos = n + __popc(m & ((1u << lane) - 1u));
+        sm.list[pos] = (uint16_t)kb;
+        sm.lflags[pos] = fl;
+      }
+      n += __popc(m);
+    }
+    if (lane == 0) sm.nlist = n;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
