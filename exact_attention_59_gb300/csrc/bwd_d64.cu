@@ -96,6 +96,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     fence_mbar_init();
+    fence_async_smem();
+    // K and V of this kv block do not depend on the work list: their copy goes
+    // out now and lands under the rest of the set-up
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+    mbar_expect_tx(smem_u32(&sm.kvfull), 2 * BWD_TILE);
+    tma_load_2d(smem_u32(sm.k), &p.tm_k, smem_u32(&sm.kvfull), 0, bh * p.Skv + kb * 128);
+    tma_load_2d(smem_u32(sm.v), &p.tm_v, smem_u32(&sm.kvfull), 0, bh * p.Skv + kb * 128);
   }
   if (warp == 2) {
     // list of q blocks that see this kv block, in ascending order, 32 candidates
@@ -156,15 +164,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     // column terms (4 q rows each), then lane 0 adds the second arrival.
     if (N > 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 11};
-      const uint32_t kvb = smem_u32(&sm.kvfull);
-      if (lane == 0) {
+      if (lane == 0) {   // K and V went out in the set-up
         tma_prefetch_desc(&p.tm_q);
-        tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_do);
-        mbar_expect_tx(kvb, 2 * BWD_TILE);
-        tma_load_2d(smem_u32(sm.k), &p.tm_k, kvb, 0, bh * p.Skv + kb * 128);
-        tma_load_2d(smem_u32(sm.v), &p.tm_v, kvb, 0, bh * p.Skv + kb * 128);
       }
       const float inv_sc = 1.f / p.sc;
       int last_u[DKDV_NST];
@@ -206,11 +208,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         last_u[s] = u;
       }
       if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-        drain_wait(kvb, 0, p.timeout_ns);
         for (int s = 0; s < DKDV_NST; ++s)
           if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / DKDV_NST) & 1, p.timeout_ns);
       }
     }
+    if (lane == 0) drain_wait(smem_u32(&sm.kvfull), 0, p.timeout_ns);   // issued in the set-up, even for N = 0
     __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issue, thread A: the score products S^T = K Q^T and dP^T = V dO^T.
@@ -486,6 +488,14 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     fence_mbar_init();
+    fence_async_smem();
+    // Q and dO of this q block do not depend on the work list: their copy goes
+    // out now and lands under the rest of the set-up
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_do);
+    mbar_expect_tx(smem_u32(&sm.qfull), 2 * BWD_TILE);
+    tma_load_2d(smem_u32(sm.q), &p.tm_q, smem_u32(&sm.qfull), 0, bh * p.Sq + qb * 128);
+    tma_load_2d(smem_u32(sm.dO), &p.tm_do, smem_u32(&sm.qfull), 0, bh * p.Sq + qb * 128);
   }
   if (warp == 2) {
     // list of kv blocks this q block sees, in ascending order, 32 candidates per
@@ -539,15 +549,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   if (warp == 0) {
     if (N > 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 21};
-      const uint32_t qbar = smem_u32(&sm.qfull);
-      if (lane == 0) {
-        tma_prefetch_desc(&p.tm_q);
+      if (lane == 0) {   // Q and dO went out in the set-up
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
-        tma_prefetch_desc(&p.tm_do);
-        mbar_expect_tx(qbar, 2 * BWD_TILE);
-        tma_load_2d(smem_u32(sm.q), &p.tm_q, qbar, 0, bh * p.Sq + qb * 128);
-        tma_load_2d(smem_u32(sm.dO), &p.tm_do, qbar, 0, bh * p.Sq + qb * 128);
       }
       int last_u[BWD_NST];
       for (int s = 0; s < BWD_NST; ++s) last_u[s] = -1;
@@ -577,11 +581,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         last_u[s] = u;
       }
       if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-        drain_wait(qbar, 0, p.timeout_ns);
         for (int s = 0; s < BWD_NST; ++s)
           if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
       }
     }
+    if (lane == 0) drain_wait(smem_u32(&sm.qfull), 0, p.timeout_ns);   // issued in the set-up, even for N = 0
     __syncwarp();
   } else if (warp == 1) {
     // ---- MMA issue, thread A: S = Q K^T (+ key-padding bias) and dP = dO V^T, each

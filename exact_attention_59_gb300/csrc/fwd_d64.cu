@@ -122,6 +122,13 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     }
     sm.abort = 0;
     fence_mbar_init();
+    fence_async_smem();
+    // the CTA's query tiles do not depend on the flags: their copy goes out now
+    // and lands under the rest of the set-up
+    tma_prefetch_desc(&p.tm_q);
+    mbar_expect_tx(smem_u32(&sm.qfull), (valid1 ? 2 : 1) * FWD_TILE_BYTES);
+    tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, smem_u32(&sm.qfull), 0, bh * p.Sq + qt0 * 128);
+    if (valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, smem_u32(&sm.qfull), 0, bh * p.Sq + qt1 * 128);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -167,13 +174,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     // ======================= TMA producer (lane 0) + bias tables (all lanes) =======================
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
     const uint32_t qbar = smem_u32(&sm.qfull);
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
+    if (lane == 0) {   // the query tiles went out in the set-up
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_expect_tx(qbar, (valid1 ? 2 : 1) * FWD_TILE_BYTES);
-      tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, qbar, 0, bh * p.Sq + qt0 * 128);
-      if (valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, qbar, 0, bh * p.Sq + qt1 * 128);
     }
     const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
     int last_u[FWD_NST];
