@@ -43,7 +43,7 @@ UNIT = "TFLOP/s"
 # `ncu --set full` of `python bench.py --mode profile --batch 8 --steps 1`
 # (summary: profiles/step_kernels_keypad_fp16_b8h8s2048d64_ncu_full.md).  Set it
 # back to None when the kernel changes until it is captured again.
-DKDV_TRAFFIC_BYTES = 81.0e6
+DKDV_TRAFFIC_BYTES = 80.8e6
 
 
 def counted_flops(w, backward=True):
