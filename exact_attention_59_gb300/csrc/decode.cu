@@ -7,9 +7,12 @@
 //   grid (nsplit, B*H); each CTA owns a contiguous range of up to 128 keys of
 //   one (b, h).  Its K and V rows are contiguous in HBM, so one thread issues
 //   two bulk copies (cp.async.bulk, 16-byte aligned, 16 KB each) into shared
-//   memory completing on one mbarrier: a single round trip to HBM per CTA,
-//   with 7 CTAs (224 KB of copies) in flight per SM, so the B8 H8 Skv 2048
-//   case (1024 CTAs) runs as one wave on 152 SMs.
+//   memory completing on one mbarrier: a single round trip to HBM per CTA.
+//   At 33 KB of shared memory a CTA, 6 fit on an SM, so the B8 H8 Skv 2048
+//   case runs 912 of its 1024 CTAs in the first wave (all of K and V, 33.5
+//   MB, is more than the GPU's shared memory); streaming each split through a
+//   two-stage ring instead, to fit one wave, was slower (a second round trip
+//   per CTA).
 //   In shared memory: thread j forms the score of key j, the CTA takes the max
 //   and the exponentials, and thread d (and d + 64) sum p_j V_jd over half the
 //   keys each; the CTA's (m, l, o[64]) goes to the workspace.
