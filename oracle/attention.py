@@ -76,18 +76,25 @@ def alibi_slope(h: int, H: int) -> float:
     return 2.0 ** (-8.0 * (h + 1) / H)
 
 
-def score_bias(mod, h: int, H: int, q_idx: np.ndarray, kv_idx: np.ndarray):
+def score_bias(mod, h: int, H: int, q_idx: np.ndarray, kv_idx: np.ndarray, b: int = 0):
     """Additive bias and keep-mask of a score_mod on a (len(q_idx), len(kv_idx)) block.
 
     Indices are global positions (attnax Pallas kernel body: ``q_idx`` and
     ``kv_idx`` are offset by the block starts).  Returns (bias float64, keep
     bool).  The causal score_mod masks ``kv_idx > q_idx``; the other mods only
-    add a bias.
+    add a bias.  A user score_mod is a callable ``f(b, h, q_idx, kv_idx)`` of
+    integer arrays (q_idx a column, kv_idx a row) giving the additive bias,
+    -inf where the pair is masked: score' = score + f (the mods on the pages
+    are all of this form, so d score' / d score = 1).
     """
-    mod = _mod_id(mod)
     qi = np.asarray(q_idx, dtype=np.int64)[:, None]
     kj = np.asarray(kv_idx, dtype=np.int64)[None, :]
     shape = (qi.shape[0], kj.shape[1])
+    if callable(mod):
+        raw = np.broadcast_to(np.asarray(mod(b, h, qi, kj), dtype=np.float64), shape)
+        keep = raw != -np.inf
+        return np.where(keep, raw, 0.0), keep.copy()
+    mod = _mod_id(mod)
     bias = np.zeros(shape, dtype=np.float64)
     keep = np.ones(shape, dtype=bool)
     if mod == MOD_NONE:
@@ -177,7 +184,7 @@ def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
     """
     q_idx = np.asarray(q_idx, dtype=np.int64)
     kv_idx = np.asarray(kv_idx, dtype=np.int64)
-    _, keep = score_bias(score_mod, h, H, q_idx, kv_idx)
+    _, keep = score_bias(score_mod, h, H, q_idx, kv_idx, b)
     if key_mask is not None:
         keep &= (np.asarray(key_mask)[b][kv_idx] != 0)[None, :]
     if dense_mask is not None:
@@ -198,7 +205,7 @@ def masked_logits(qbh, kbh, b, h, H, scale, q_idx, kv_idx, key_mask=None,
     q_idx are the query positions; row_idx (default q_idx) the rows of the
     dense mask they read."""
     s = scale * (qbh @ kbh.T)
-    bias, _ = score_bias(score_mod, h, H, q_idx, kv_idx)
+    bias, _ = score_bias(score_mod, h, H, q_idx, kv_idx, b)
     s = s + bias
     keep = keep_matrix(b, h, H, q_idx, kv_idx, key_mask, block_mask, score_mod, dense_mask, row_idx)
     return np.where(keep, s, -np.inf), keep

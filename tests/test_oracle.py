@@ -438,3 +438,77 @@ def test_query_offset_equals_rows_of_full(mod):
     o1, _ = A.attn_decode(q[:, :, :2], k, v, score_mod="causal", q_offset=S + 5)
     o2, _ = A.attn_fwd(q[:, :, :2], k, v)
     np.testing.assert_array_equal(o1, o2)
+
+
+# ---------------------------------------------------------------------------
+# user score_mod (an additive bias of (b, h, q_idx, kv_idx), -inf to mask)
+# ---------------------------------------------------------------------------
+
+def _user_alibi(H):
+    return lambda b, h, q, kv: 2.0 ** (-8.0 * (h + 1) / H) * (kv - q)
+
+
+def _user_checker(b, h, q, kv):
+    return np.where((q + kv) % 2 == 0, 0.5, -0.5)
+
+
+def _user_causal(b, h, q, kv):
+    return np.where(kv <= q, 0.0, -np.inf)
+
+
+@pytest.mark.parametrize("name", ["alibi", "checkerboard", "causal"])
+def test_user_mod_reproduces_builtin_mods(name):
+    """The user-mod hook given the closed forms of the built-in mods gives exactly
+    their results, forward and backward (the built-ins are pinned above)."""
+    B, H, Sq, Skv, D = 2, 3, 7, 9, 4
+    q, k, v, do = _rand(B, H, Sq, D, seed=130), _rand(B, H, Skv, D, seed=131), _rand(B, H, Skv, D, seed=132), \
+        _rand(B, H, Sq, D, seed=133)
+    user = {"alibi": _user_alibi(H), "checkerboard": _user_checker, "causal": _user_causal}[name]
+    for off in (0, 2):
+        ob, lb = A.attn_fwd(q, k, v, score_mod=name, q_offset=off)
+        ou, lu = A.attn_fwd(q, k, v, score_mod=user, q_offset=off)
+        np.testing.assert_array_equal(ou, ob)
+        np.testing.assert_array_equal(lu, lb)
+    for x, y in zip(A.attn_bwd(q, k, v, do, score_mod=name), A.attn_bwd(q, k, v, do, score_mod=user)):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_user_mod_brute_force():
+    """A bias that depends on b, h, q and kv (not symmetric in q and kv), with a
+    masked band, against loops."""
+    B, H, S, D = 2, 2, 6, 3
+    q, k, v = _rand(B, H, S, D, seed=140), _rand(B, H, S, D, seed=141), _rand(B, H, S, D, seed=142)
+
+    def f(b, h, qq, kk):
+        base = 0.25 * b - 0.5 * h + 0.1 * (qq * kk % 5) + 0.05 * (qq - 2 * kk)
+        return np.where(np.abs(qq - kk) == 2, -np.inf, base)
+    o, lse = A.attn_fwd(q, k, v, score_mod=f, scale=0.8)
+    for b in range(B):
+        for h in range(H):
+            for i in range(S):
+                z = {}
+                for j in range(S):
+                    if abs(i - j) == 2:
+                        continue
+                    z[j] = 0.8 * sum(q[b, h, i, d] * k[b, h, j, d] for d in range(D)) + \
+                        0.25 * b - 0.5 * h + 0.1 * ((i * j) % 5) + 0.05 * (i - 2 * j)
+                top = max(z.values())
+                tot = sum(math.exp(x - top) for x in z.values())
+                assert abs(lse[b, h, i] - (top + math.log(tot))) < 1e-12
+                ref = sum(math.exp(x - top) / tot * v[b, h, j] for j, x in z.items())
+                np.testing.assert_allclose(o[b, h, i], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_user_mod_finite_differences():
+    B, H, S, D = 1, 2, 5, 3
+    q, k, v, do = (_rand(B, H, S, D, seed=s) for s in (150, 151, 152, 153))
+    f = lambda b, h, qq, kk: np.where(kk > qq + 1, -np.inf, 0.3 * h - 0.2 * np.abs(qq - kk))
+    kw = {"score_mod": f, "scale": 0.7}
+    dq, dk, dv = A.attn_bwd(q, k, v, do, **kw)
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        def fn(xx, name=name):
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xx
+            return _loss(args["q"], args["k"], args["v"], do, **kw)
+        gfd = _fd_grad(fn, x)
+        assert np.abs(gfd - g).max() / max(1e-12, np.abs(g).max()) < 1e-6, name

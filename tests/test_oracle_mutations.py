@@ -34,6 +34,10 @@ MUTANTS = {
                        "keep &= dense_mask_head(dense_mask, b, h)[ri[:, None], kv_idx[None, :]] == 0"),
     "dense_transposed": ("keep &= dense_mask_head(dense_mask, b, h)[ri[:, None], kv_idx[None, :]] != 0",
                          "keep &= dense_mask_head(dense_mask, b, h).T[kv_idx[None, :] % len(ri), ri[:, None] % len(kv_idx)] != 0"),
+    "user_bias_sign": ("raw = np.broadcast_to(np.asarray(mod(b, h, qi, kj), dtype=np.float64), shape)",
+                       "raw = -np.broadcast_to(np.asarray(mod(b, h, qi, kj), dtype=np.float64), shape)"),
+    "user_bias_swapped": ("raw = np.broadcast_to(np.asarray(mod(b, h, qi, kj), dtype=np.float64), shape)",
+                          "raw = np.broadcast_to(np.asarray(mod(b, h, kj, qi), dtype=np.float64), shape)"),
     "offset_ignored": ("q_idx + int(q_offset), kv_idx,", "q_idx, kv_idx,"),
     "offset_sign": ("q_idx + int(q_offset), kv_idx,", "q_idx - int(q_offset), kv_idx,"),
     "dense_bcast_b": ("return dm[0 if dm.shape[0] == 1 else b, 0 if dm.shape[1] == 1 else h]",
@@ -66,6 +70,7 @@ PINS = [
     lambda: T.test_alibi_row_constant_only_shifts_lse(),
     lambda: [T.test_dense_mask_brute_force(bs) for bs in [(2, 3), (1, 3), (2, 1)]],
     lambda: [T.test_query_offset_equals_rows_of_full(m) for m in T.MODS],
+    lambda: T.test_user_mod_brute_force(),
 ]
 
 
