@@ -423,6 +423,25 @@ def bench_extras(E, dev):
         "pack_ms": p_ms, "fwd_ms": f_ms, "bwd_ms": b_ms, "kept_pairs": kept, "visited_tiles": vt,
         "fwd_tflops_kept": f_kept / (f_ms * 1e-3) / 1e12, "fwd_tflops_visited": f_vis / (f_ms * 1e-3) / 1e12,
         "bwd_tflops_visited": 2.5 * f_vis / (b_ms * 1e-3) / 1e12}
+    # a score_mod compiled at run time: a relative-position bias on the same shape
+    try:
+        um = E.compile_score_mod("0.05f * (float)(kv - q)", dtype=torch.float16)
+
+        def ufwd(i):
+            d = sets[i % 2]
+            E.attn_fwd(d["q"], d["k"], d["v"], score_mod=um, out=d["out"], lse=d["lse"])
+
+        def ubwd(i):
+            d = sets[i % 2]
+            E.attn_bwd(d["q"], d["k"], d["v"], d["out"], d["lse"], d["dout"], score_mod=um, dq=d["dq"], dk=d["dk"],
+                       dv=d["dv"])
+        f_ms, b_ms = timed(ufwd, 50), timed(ubwd, 50)
+        f_fl = 4.0 * w.D * S * S * w.B * w.H
+        res["user_relative_bias_fp16_b8h8s2048d64"] = {
+            "expr": um.bias_expr, "fwd_ms": f_ms, "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_ms": b_ms,
+            "bwd_tflops": 2.5 * f_fl / (b_ms * 1e-3) / 1e12}
+    except Exception as e:   # noqa: BLE001 - context only: report, do not fail the bench
+        res["user_relative_bias_fp16_b8h8s2048d64"] = {"error": str(e)[:300]}
     w = W.LONG_CAUSAL_BF16
     q = IN.randn((w.B, w.H, w.Sq, w.D), IN.SEED + 1, w.dtype).to(dev)
     k = IN.randn((w.B, w.H, w.Skv, w.D), IN.SEED, w.dtype).to(dev)

@@ -27,7 +27,7 @@ MASK_MODS = {"none": 0, "causal": 1}
 SYMBOLS = ("attn_workspace_size", "attn_build_block_mask", "attn_fwd", "attn_bwd", "attn_bwd_preprocess",
            "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_poll_status", "attn_status_string",
            "attn_dense_mask_bytes", "attn_pack_dense_mask", "attn_fwd_dense", "attn_bwd_dense",
-           "attn_decode_chunk")
+           "attn_decode_chunk", "attn_user_mod_create", "attn_user_mod_destroy", "attn_fwd_user", "attn_bwd_user")
 
 
 class AttnError(RuntimeError):
@@ -85,6 +85,10 @@ def load():
             "attn_fwd_dense": (I, [sp, P, P, P, P, dp, bp, I, F, P, P, P, SZ, P, P]),
             "attn_bwd_dense": (I, [sp, P, P, P, P, P, P, P, dp, bp, I, F, P, P, P, P, SZ, P]),
             "attn_decode_chunk": (I, [sp, P, P, P, P, I, F, I, P, P, P, SZ, P]),
+            "attn_user_mod_create": (I, [ctypes.c_char_p, I, ctypes.POINTER(P), ctypes.c_char_p, SZ]),
+            "attn_user_mod_destroy": (None, [P]),
+            "attn_fwd_user": (I, [sp, P, P, P, P, P, bp, F, P, P, P, SZ, P, P]),
+            "attn_bwd_user": (I, [sp, P, P, P, P, P, P, P, P, bp, F, P, P, P, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -212,6 +216,38 @@ def _dm(dm):
     return None if dm is None else ctypes.byref(dm.c())
 
 
+class UserScoreMod:
+    """A score_mod compiled at run time: score + bias, where ``bias_expr`` is a C
+    expression in the int variables b, h, q, kv (q and kv are positions) that
+    gives a float, or -INFINITY to mask the pair.  Built for one 16-bit dtype."""
+
+    def __init__(self, bias_expr: str, dtype=torch.bfloat16):
+        self.bias_expr = bias_expr
+        self.dtype = dtype
+        self.log = ""
+        self._h = ctypes.c_void_p()
+        buf = ctypes.create_string_buffer(1 << 16)
+        code = load().attn_user_mod_create(bias_expr.encode(), _dtype_id(dtype), ctypes.byref(self._h), buf,
+                                           len(buf))
+        self.log = buf.value.decode(errors="replace")
+        if code != ATTN_OK:
+            raise AttnError(code, "attn_user_mod_create: " + self.log.strip()[:2000])
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        if getattr(self, "_h", None) and self._h.value and _lib is not None:
+            _lib.attn_user_mod_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+
+def compile_score_mod(bias_expr: str, dtype=torch.bfloat16) -> UserScoreMod:
+    """Compiles ``bias_expr`` (see UserScoreMod) into the D = 64 kernels for ``dtype``."""
+    return UserScoreMod(bias_expr, dtype)
+
+
 def _mod(m) -> int:
     return MODS[m] if isinstance(m, str) else int(m)
 
@@ -229,7 +265,13 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
     ws = workspace(OP_FWD, shape, q.device) if ws is None else ws
-    if dense_mask is None:
+    if isinstance(score_mod, UserScoreMod):
+        if dense_mask is not None:
+            raise ValueError("a user score_mod runs without a dense mask")
+        code = load().attn_fwd_user(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), score_mod.handle,
+                                    _bm(block_mask), scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                    _stream(q.device), _ptr(debug_visited))
+    elif dense_mask is None:
         code = load().attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _bm(block_mask),
                                _mod(score_mod), scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                                _stream(q.device), _ptr(debug_visited))
@@ -251,7 +293,13 @@ def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod=
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
-    if dense_mask is None:
+    if isinstance(score_mod, UserScoreMod):
+        if dense_mask is not None:
+            raise ValueError("a user score_mod runs without a dense mask")
+        code = load().attn_bwd_user(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                    _ptr(dout), _ptr(key_mask), score_mod.handle, _bm(block_mask), scale, _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(q.device))
+    elif dense_mask is None:
         code = load().attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
                                _ptr(key_mask), _bm(block_mask), _mod(score_mod), scale, _ptr(dq), _ptr(dk),
                                _ptr(dv), _ptr(ws), ws.numel(), _stream(q.device))

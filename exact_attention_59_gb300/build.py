@@ -59,7 +59,8 @@ def build(force: bool = False, jobs: int | None = None) -> str:
         objs = list(ex.map(lambda s: _compile(s, force, hdr_t), srcs))
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + ".tmp"
-        r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lnvrtc", "-ldl"], capture_output=True,
+                           text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr[-6000:]}")
         os.replace(tmp, LIB)

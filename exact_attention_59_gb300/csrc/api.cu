@@ -11,6 +11,7 @@
 
 #include "../../include/attn.h"
 #include "kernels.h"
+#include "usermod.h"
 
 using namespace attn;
 
@@ -326,14 +327,21 @@ attn_status attn_fwd(const attn_shape* s, const void* q, const void* k, const vo
   return attn_fwd_dense(s, q, k, v, key_mask, nullptr, bm, mod, scale, out, lse, ws, ws_bytes, stream, debug_visited);
 }
 
-attn_status attn_fwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
-                           const attn_dense_mask* dm, const attn_block_mask* bm, attn_score_mod mod, float scale,
-                           void* out, float* lse, void* ws, size_t ws_bytes, attn_stream_t stream,
-                           uint8_t* debug_visited) {
+// The forward behind attn_fwd, attn_fwd_dense and attn_fwd_user (um: a
+// run-time-compiled score_mod in place of `mod`, or NULL).
+static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                            const attn_dense_mask* dm, const attn_block_mask* bm, attn_score_mod mod, float scale,
+                            void* out, float* lse, void* ws, size_t ws_bytes, attn_stream_t stream,
+                            uint8_t* debug_visited, attn_user_mod um) {
   ATTN_TRY(check_prefill(s, false));
   ATTN_TRY(check_mod(mod, scale));
   ATTN_TRY(check_bm(bm));
   ATTN_TRY(check_dm(s, dm));
+  const void* uk[3] = {nullptr, nullptr, nullptr};
+  if (um) {   // the user kernels: D = 64, the 16-bit dtype they were built for, no dense mask
+    if (s->D != 64 || s->dtype == ATTN_F32 || dm) return ATTN_ERR_UNSUPPORTED;
+    ATTN_TRY(user_mod_kernels(um, s->dtype, uk));
+  }
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -403,7 +411,23 @@ attn_status attn_fwd_dense(const attn_shape* s, const void* q, const void* k, co
   p.timeout_ns = timeout_ns();
   p.inject_stall = inject_stall();
   p.nsplit = 1;   // whole kv range per CTA, q_off = 0
+  if (um) return cuda_status(launch_fwd_d64_kernel(p, uk[0], st));
   return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
+}
+
+attn_status attn_fwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                           const attn_dense_mask* dm, const attn_block_mask* bm, attn_score_mod mod, float scale,
+                           void* out, float* lse, void* ws, size_t ws_bytes, attn_stream_t stream,
+                           uint8_t* debug_visited) {
+  return fwd_impl(s, q, k, v, key_mask, dm, bm, mod, scale, out, lse, ws, ws_bytes, stream, debug_visited, nullptr);
+}
+
+attn_status attn_fwd_user(const attn_shape* s, const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                          attn_user_mod um, const attn_block_mask* bm, float scale, void* out, float* lse, void* ws,
+                          size_t ws_bytes, attn_stream_t stream, uint8_t* debug_visited) {
+  if (!um) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(s, q, k, v, key_mask, nullptr, bm, ATTN_MOD_NONE, scale, out, lse, ws, ws_bytes, stream,
+                  debug_visited, um);
 }
 
 attn_status attn_bwd_preprocess(const attn_shape* s, const void* out, const float* lse, const void* dout,
@@ -429,7 +453,7 @@ namespace {
 attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
                           const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
                           attn_score_mod mod, float scale, void* dk, void* dv, void* ws, size_t ws_bytes,
-                          attn_stream_t stream) {
+                          attn_stream_t stream, const void* ukern = nullptr) {
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_dm(s, dm));
   ATTN_TRY(check_mod(mod, scale));
@@ -459,12 +483,14 @@ attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, con
   p.dk = dk;
   p.dv = dv;
   p.dm = dm_view(s, dm);
+  if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, true, st));
   return cuda_status(launch_bwd_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
 attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
                         const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
-                        attn_score_mod mod, float scale, void* dq, void* ws, size_t ws_bytes, attn_stream_t stream) {
+                        attn_score_mod mod, float scale, void* dq, void* ws, size_t ws_bytes, attn_stream_t stream,
+                        const void* ukern = nullptr) {
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_dm(s, dm));
   ATTN_TRY(check_mod(mod, scale));
@@ -491,6 +517,7 @@ attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const
   if (!ok) return ATTN_ERR_CUDA;
   p.dq = dq;
   p.dm = dm_view(s, dm);
+  if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, false, st));
   return cuda_status(launch_bwd_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
@@ -518,15 +545,21 @@ attn_status attn_bwd(const attn_shape* s, const void* q, const void* k, const vo
                         stream);
 }
 
-attn_status attn_bwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
+// The backward behind attn_bwd, attn_bwd_dense and attn_bwd_user.
+static attn_status bwd_all(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
                            const float* lse, const void* dout, const uint8_t* key_mask, const attn_dense_mask* dm,
                            const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq, void* dk, void* dv,
-                           void* ws, size_t ws_bytes, attn_stream_t stream) {
+                           void* ws, size_t ws_bytes, attn_stream_t stream, attn_user_mod um) {
   // validate everything before the first launch
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_mod(mod, scale));
   ATTN_TRY(check_bm(bm));
   ATTN_TRY(check_dm(s, dm));
+  const void* uk[3] = {nullptr, nullptr, nullptr};
+  if (um) {
+    if (s->D != 64 || s->dtype == ATTN_F32 || dm) return ATTN_ERR_UNSUPPORTED;
+    ATTN_TRY(user_mod_kernels(um, s->dtype, uk));
+  }
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -539,8 +572,24 @@ attn_status attn_bwd_dense(const attn_shape* s, const void* q, const void* k, co
   ATTN_OPT_PTR(key_mask);
   ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
   ATTN_TRY(attn_bwd_preprocess(s, out, lse, dout, key_mask, ws, ws_bytes, stream));
-  ATTN_TRY(bwd_dkdv_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dk, dv, ws, ws_bytes, stream));
-  return bwd_dq_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dq, ws, ws_bytes, stream);
+  ATTN_TRY(bwd_dkdv_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dk, dv, ws, ws_bytes, stream, uk[1]));
+  return bwd_dq_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dq, ws, ws_bytes, stream, uk[2]);
+}
+
+attn_status attn_bwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
+                           const float* lse, const void* dout, const uint8_t* key_mask, const attn_dense_mask* dm,
+                           const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq, void* dk, void* dv,
+                           void* ws, size_t ws_bytes, attn_stream_t stream) {
+  return bwd_all(s, q, k, v, out, lse, dout, key_mask, dm, bm, mod, scale, dq, dk, dv, ws, ws_bytes, stream, nullptr);
+}
+
+attn_status attn_bwd_user(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* dout, const uint8_t* key_mask, attn_user_mod um,
+                          const attn_block_mask* bm, float scale, void* dq, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, attn_stream_t stream) {
+  if (!um) return ATTN_ERR_INVALID_ARG;
+  return bwd_all(s, q, k, v, out, lse, dout, key_mask, nullptr, bm, ATTN_MOD_NONE, scale, dq, dk, dv, ws, ws_bytes,
+                 stream, um);
 }
 
 size_t attn_dense_mask_bytes(const attn_shape* s, int bcast_b, int bcast_h) {

@@ -21,8 +21,6 @@
 // 6-9 split the 128 columns of each 128x128 score tile in two halves of 64.
 // S is double-buffered in TMEM so the next S product overlaps this tile's
 // elementwise work.
-#include <type_traits>
-
 #include "kernels.h"
 
 namespace attn {
@@ -350,6 +348,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
             xv = fadd2(xv, f2(fmaf(-slope2, float(2 * i), abase), fmaf(-slope2, float(2 * i + 1), abase)));
           float x0, x1;
           unf2(xv, x0, x1);
+          if constexpr (MOD == MOD_USER) {
+            x0 = fmaf(user_bias(b, h, q0 + 2 * i, kv), kLog2e, x0);
+            x1 = fmaf(user_bias(b, h, q0 + 2 * i + 1, kv), kLog2e, x1);
+          }
           if (CAUSAL) {
             x0 = kv > q0 + 2 * i ? -INFINITY : x0;
             x1 = kv > q0 + 2 * i + 1 ? -INFINITY : x1;
@@ -367,12 +369,12 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       };
       if (dense) {   // never with DM = false
         if constexpr (DM) {
-          if (causal) probs(std::true_type{}, std::true_type{});
-          else probs(std::false_type{}, std::true_type{});
+          if (causal) probs(bconst<true>{}, bconst<true>{});
+          else probs(bconst<false>{}, bconst<true>{});
         }
       } else {
-        if (causal) probs(std::true_type{}, std::false_type{});
-        else probs(std::false_type{}, std::false_type{});
+        if (causal) probs(bconst<true>{}, bconst<false>{});
+        else probs(bconst<false>{}, bconst<false>{});
       }
       // dV(u-1) has finished reading the P^T region
       if (u > 0) {
@@ -711,6 +713,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
             add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
           float x0, x1;
           unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
+          if constexpr (MOD == MOD_USER) {
+            x0 = fmaf(user_bias(b, h, q, k0 + 2 * i), kLog2e, x0);
+            x1 = fmaf(user_bias(b, h, q, k0 + 2 * i + 1), kLog2e, x1);
+          }
           if (CAUSAL) {
             x0 = 2 * i > lim ? -INFINITY : x0;
             x1 = 2 * i + 1 > lim ? -INFINITY : x1;
@@ -725,11 +731,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         }
       };
       if (dense) {   // with dense bits, the limited copy too (never with DM = false)
-        if constexpr (DM) probs(std::true_type{}, std::true_type{});
+        if constexpr (DM) probs(bconst<true>{}, bconst<true>{});
       } else if (limited) {
-        probs(std::true_type{}, std::false_type{});
+        probs(bconst<true>{}, bconst<false>{});
       } else {
-        probs(std::false_type{}, std::false_type{});
+        probs(bconst<false>{}, bconst<false>{});
       }
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();
@@ -786,6 +792,18 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
+#ifndef __CUDACC_RTC__
+// Backward kernels of these layouts built elsewhere (a run-time-compiled
+// score_mod): the same shared memory, grid and block as the built-in variants.
+cudaError_t launch_bwd_kernel(const BwdParams& p, const void* kern, bool dkdv, cudaStream_t st) {
+  const size_t smem = (dkdv ? sizeof(DkdvSmem) : sizeof(DqSmem)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(p.B * p.H * (dkdv ? p.nkb : p.nqb));
+  void* args[] = {const_cast<BwdParams*>(&p)};
+  return cudaLaunchKernel(kern, dim3(grid), dim3(BWD_T), args, smem, st);
+}
+
 template <typename Smem, bool BF16, int MOD, bool DKDV>
 static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
   // DM: the build with the dense-mask path, used only when a dense mask is given
@@ -826,5 +844,7 @@ cudaError_t launch_bwd_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t
 cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, int mod, cudaStream_t st) {
   return launch_bwd_any<DqSmem, false>(p, bf16, mod, st);
 }
+
+#endif  // host
 
 }  // namespace attn

@@ -1,9 +1,11 @@
 // common.cuh - definitions shared by the attention kernels and their launchers.
 #pragma once
 
+#ifndef __CUDACC_RTC__
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#endif
 
 #include "ptx.cuh"
 
@@ -12,10 +14,26 @@ namespace attn {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// score_mod ids (same values as attn_score_mod in attn.h)
-constexpr int MOD_NONE = 0, MOD_ALIBI = 1, MOD_CHECKER = 2, MOD_CAUSAL = 3;
+// score_mod ids (same values as attn_score_mod in attn.h); MOD_USER is a
+// score_mod compiled at run time: score + user_bias(b, h, q_idx, kv_idx)
+constexpr int MOD_NONE = 0, MOD_ALIBI = 1, MOD_CHECKER = 2, MOD_CAUSAL = 3, MOD_USER = 4;
 constexpr int MASKMOD_NONE = 0, MASKMOD_CAUSAL = 1;
 constexpr int TILE_EMPTY = 0, TILE_PARTIAL = 1, TILE_FULL = 2;
+
+// The user's bias expression, in the variables b, h, q (the query position) and
+// kv (the key position); only a run-time compilation defines ATTN_USER_BIAS_EXPR
+// (and only it instantiates the MOD_USER kernels).
+#ifdef ATTN_USER_BIAS_EXPR
+__device__ __forceinline__ float user_bias(int b, int h, int q, int kv) { return (float)(ATTN_USER_BIAS_EXPR); }
+#else
+__device__ __forceinline__ float user_bias(int, int, int, int) { return 0.f; }
+#endif
+
+// A compile-time bool as a type: selects one straight-line copy of a loop.
+template <bool V>
+struct bconst {
+  static constexpr bool value = V;
+};
 
 // Per-(q tile, kv block) work flags staged in shared memory by the prefill kernels.
 constexpr uint8_t KB_VISIT = 1;    // the tile is computed

@@ -45,15 +45,19 @@ struct __align__(1024) FwdSmem {
 };
 
 // the bias table is read 16 bytes at a time
+#ifndef __CUDACC_RTC__   // (the offline build checks the same layout)
 static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
+#endif
 
 // Pass 1 over one row's 128 scores of a kv block: x = s * scale (+ column bias
 // from the stage's table), -inf for columns cc > lim (the causal rule, or keys
 // past the end in a partial last block) and, with DENSE, for columns whose bit
 // in the row's dense-mask words dw is 0; and the running maximum in four
 // independent chains.
-template <bool TABLE, bool LIMITED, bool DENSE>
-DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4]) {
+// With USER, x += user_bias(b, h, q, kv0 + cc) log2(e) (a run-time-compiled score_mod).
+template <bool TABLE, bool LIMITED, bool DENSE, bool USER = false>
+DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4],
+                       int ub = 0, int uh = 0, int uq = 0, int ukv0 = 0) {
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
     float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -65,6 +69,10 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
       const uint64_t xv = TABLE ? ffma2(sv, scv, j ? f2(bias.z, bias.w) : f2(bias.x, bias.y)) : fmul2(sv, scv);
       float x0, x1;
       unf2(xv, x0, x1);
+      if constexpr (USER) {
+        x0 = fmaf(user_bias(ub, uh, uq, ukv0 + c), kLog2e, x0);
+        x1 = fmaf(user_bias(ub, uh, uq, ukv0 + c + 1), kLog2e, x1);
+      }
       if (LIMITED) {
         x0 = c > lim ? -INFINITY : x0;
         x1 = c + 1 > lim ? -INFINITY : x1;
@@ -368,6 +376,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           if (DM && dense) scale_scores<true, true, DM>(r, scv, tb, lim, dw, mx);
           else if (limited) scale_scores<true, true, false>(r, scv, tb, lim, dw, mx);
           else scale_scores<true, false, false>(r, scv, tb, lim, dw, mx);
+        } else if constexpr (MOD == MOD_USER) {
+          if (DM && dense) scale_scores<false, true, DM, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          else if (limited) scale_scores<false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          else scale_scores<false, false, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
         } else {
           if (DM && dense) scale_scores<false, true, DM>(r, scv, tb, lim, dw, mx);
           else if (limited) scale_scores<false, true, false>(r, scv, tb, lim, dw, mx);
@@ -476,7 +488,19 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
 // ---------------------------------------------------------------------------
 // host-side launcher
 // ---------------------------------------------------------------------------
+#ifndef __CUDACC_RTC__
 size_t fwd_d64_smem_bytes() { return sizeof(FwdSmem) + 1024; }
+
+// A forward kernel of this layout built elsewhere (a run-time-compiled score_mod):
+// the same shared memory, grid and block as the built-in variants.
+cudaError_t launch_fwd_d64_kernel(const FwdParams& p, const void* kern, cudaStream_t st) {
+  const size_t smem = fwd_d64_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(p.npairs * p.B * p.H * p.nsplit);
+  void* args[] = {const_cast<FwdParams*>(&p)};
+  return cudaLaunchKernel(kern, dim3(grid), dim3(FWD_THREADS), args, smem, st);
+}
 
 template <bool BF16, int MOD>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
@@ -490,6 +514,7 @@ static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
   kern<<<grid, FWD_THREADS, smem, st>>>(p);
   return cudaGetLastError();
 }
+#endif  // host
 
 // One warp per row: M = max_s m_s, L = sum_s l_s 2^(m_s - M),
 // O = sum_s O_s 2^(m_s - M) / L, lse = (M + log2 L) ln 2 (O = 0, lse = -inf
@@ -523,6 +548,7 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const float* __restric
   if (lane == 0) lse[r] = Lsum > 0.f ? (M + lg2(Lsum)) * kLn2 : -INFINITY;
 }
 
+#ifndef __CUDACC_RTC__
 cudaError_t launch_split_merge(const float* part, int nsplit, long long rows, int Sq, void* out, float* lse, bool bf16,
                                cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
@@ -550,5 +576,7 @@ cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t 
     default: return launch_fwd_t<false, MOD_CAUSAL>(p, st);
   }
 }
+
+#endif  // host
 
 }  // namespace attn

@@ -18,6 +18,7 @@ namespace attn {
 struct DenseMaskLayout {
   size_t tiles, rowbits, colbits, total;   // byte offsets and size, 256-byte aligned
 };
+#ifndef __CUDACC_RTC__
 inline DenseMaskLayout dense_mask_layout(long long nmask, int Sq, int Skv) {
   const long long nqb = (Sq + 127) / 128, nkb = (Skv + 127) / 128;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -28,14 +29,17 @@ inline DenseMaskLayout dense_mask_layout(long long nmask, int Sq, int Skv) {
   l.total = l.colbits + up((size_t)(nmask * Skv * nqb * 16));
   return l;
 }
+#endif  // host
 struct DenseMaskView {
   const uint8_t* tiles;      // nullptr = no dense mask
   const uint32_t* rowbits;
   const uint32_t* colbits;
   int mb, mh;                // mask index of head (b, h) = b * mb + h * mh
 };
+#ifndef __CUDACC_RTC__
 cudaError_t launch_dense_mask_pack(const uint8_t* mask, long long nmask, int Sq, int Skv, uint8_t* tiles,
                                    uint32_t* rowbits, uint32_t* colbits, cudaStream_t st);
+#endif  // host
 
 // ---------------------------------------------------------------- forward, D = 64
 #ifndef ATTN_FWD_NST
@@ -70,11 +74,16 @@ struct FwdParams {
   float* part;
 };
 constexpr int FWD_PART = 68;      // floats per partial row (16-byte aligned O)
+#ifndef __CUDACC_RTC__
 size_t fwd_d64_smem_bytes();
 cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t st);
+cudaError_t launch_fwd_d64_kernel(const FwdParams& p, const void* kern, cudaStream_t st);
+#endif  // host
 // out, lse of each row from its nsplit partial rows (part as in FwdParams)
+#ifndef __CUDACC_RTC__
 cudaError_t launch_split_merge(const float* part, int nsplit, long long rows, int Sq, void* out, float* lse, bool bf16,
                                cudaStream_t st);
+#endif  // host
 
 // ---------------------------------------------------------------- forward, D = 512
 struct FwdBigParams {
@@ -90,7 +99,9 @@ struct FwdBigParams {
   float sc;
   unsigned long long timeout_ns;
 };
+#ifndef __CUDACC_RTC__
 cudaError_t launch_fwd_d512(const FwdBigParams& p, bool bf16, int mod, cudaStream_t st);
+#endif  // host
 
 // ---------------------------------------------------------------- backward, D = 64
 struct BwdParams {
@@ -112,21 +123,28 @@ struct BwdParams {
   float scale;
   unsigned long long timeout_ns;
 };
+#ifndef __CUDACC_RTC__
 cudaError_t launch_bwd_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
+cudaError_t launch_bwd_kernel(const BwdParams& p, const void* kern, bool dkdv, cudaStream_t st);
+#endif  // host
 
 // ---------------------------------------------------------------- small kernels
 // key mask (B, Skv) uint8 -> bits (B, Skv/32) + summary (B, ceil(Skv/128))
+#ifndef __CUDACC_RTC__
 cudaError_t launch_keymask_pack(const uint8_t* km, int B, int Skv, uint32_t* bits, uint8_t* summary,
                                 cudaStream_t st);
 cudaError_t launch_build_block_mask(int mask_mod, int B, int H, int Sq, int Skv, int bq, int bkv, uint8_t* tiles,
                                     cudaStream_t st);
+#endif  // host
 // delta = -rowsum(dout * out) (f32), lse2 = -lse * log2(e) (-inf where lse = -inf)
 // -D and -lse log2(e) per row; with km, also packs the key mask (bits + block
 // summary) in the same launch.
+#ifndef __CUDACC_RTC__
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float* lse, int dtype, long long rows,
                                   int D, float* delta, float* lse2, const uint8_t* km, int B, int Skv, uint32_t* bits,
                                   uint8_t* summary, cudaStream_t st);
+#endif  // host
 
 // ---------------------------------------------------------------- decode (Sq = 1)
 struct DecodeParams {
@@ -143,8 +161,10 @@ struct DecodeParams {
   float sc;
   int mod;
 };
+#ifndef __CUDACC_RTC__
 int decode_num_splits(int B, int H, int Skv);
 cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t st);
+#endif  // host
 
 // ---------------------------------------------------------------- f32 path (SIMT FMA)
 struct SimtParams {
@@ -168,8 +188,10 @@ struct SimtParams {
   int B, H, Sq, Skv, nqb, nkb, mod;
   float sc, scale;
 };
+#ifndef __CUDACC_RTC__
 cudaError_t launch_simt_fwd(const SimtParams& p, cudaStream_t st);
 cudaError_t launch_simt_bwd_dkdv(const SimtParams& p, cudaStream_t st);
 cudaError_t launch_simt_bwd_dq(const SimtParams& p, cudaStream_t st);
+#endif  // host
 
 }  // namespace attn

@@ -6,8 +6,24 @@
 // all roles of the CTA leave their loops, release tensor memory and return.
 #pragma once
 
+#ifdef __CUDACC_RTC__
+// Runtime compilation (a user score_mod): no host headers; the fixed-width
+// integers and the tensor-map layout that <cstdint> and <cuda.h> give.
+typedef unsigned char uint8_t;
+typedef unsigned short uint16_t;
+typedef unsigned int uint32_t;
+typedef unsigned long long uint64_t;
+typedef int int32_t;
+typedef long long int64_t;
+typedef unsigned long long uintptr_t;
+typedef struct CUtensorMap_st {
+  alignas(64) unsigned long long opaque[16];
+} CUtensorMap;
+#define INFINITY (__int_as_float(0x7f800000))
+#else
 #include <cuda.h>
 #include <cstdint>
+#endif
 
 #define DEVI __device__ __forceinline__
 

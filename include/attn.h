@@ -261,6 +261,38 @@ attn_status attn_decode_chunk(const attn_shape* shape, const void* q, const void
                               const uint8_t* key_mask, attn_score_mod mod, float scale, int q_offset, void* out,
                               float* lse, void* ws, size_t ws_bytes, attn_stream_t stream);
 
+/* A score_mod compiled at run time (NVRTC): the flaxattention README's hooks
+ * take arbitrary callables, the enum above covers the ones it names.  Here a
+ * user score_mod is a C expression for an additive bias in the int
+ * variables b, h, q, kv (q and kv are positions; -INFINITY masks the pair):
+ * score' = score + bias, the form of every mod the pages name, so the
+ * backward needs no derivative of it.  It is compiled into the D = 64
+ * forward, dK/dV and dQ kernels for one 16-bit dtype (about 2 s, no GPU
+ * needed); the result is loaded on a device when a call first uses it there.
+ * The expression runs as device code in the caller's process.
+ *   log: nullable buffer for the compiler's messages (also on success).
+ * Errors: ATTN_ERR_INVALID_ARG (NULL, empty or over 4096 characters, or the
+ * expression does not compile: see log), ATTN_ERR_UNSUPPORTED (f32, or the
+ * kernel sources are not beside the library). */
+typedef struct attn_user_mod_st* attn_user_mod;
+attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dtype, attn_user_mod* mod, char* log,
+                                 size_t log_bytes);
+/* Frees a user score_mod (NULL is ignored); no call may be using it. */
+void attn_user_mod_destroy(attn_user_mod mod);
+
+/* attn_fwd / attn_bwd with a user score_mod in place of the enum (f16/bf16,
+ * D = 64, the dtype the mod was built for, else ATTN_ERR_UNSUPPORTED); the
+ * key mask, block mask and debug_visited work as in attn_fwd.  Errors as
+ * attn_fwd. */
+attn_status attn_fwd_user(const attn_shape* shape, const void* q, const void* k, const void* v,
+                          const uint8_t* key_mask, attn_user_mod mod, const attn_block_mask* bm, float scale,
+                          void* out, float* lse, void* ws, size_t ws_bytes, attn_stream_t stream,
+                          uint8_t* debug_visited);
+attn_status attn_bwd_user(const attn_shape* shape, const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* dout, const uint8_t* key_mask, attn_user_mod mod,
+                          const attn_block_mask* bm, float scale, void* dq, void* dk, void* dv, void* ws,
+                          size_t ws_bytes, attn_stream_t stream);
+
 attn_status attn_poll_status(void* ws, attn_stream_t stream);
 
 /* Static text for a status code. */

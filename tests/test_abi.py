@@ -195,3 +195,27 @@ def test_decode_chunk_validation(lib):
     assert call(s, ws=None) == lib.ATTN_ERR_WORKSPACE
     assert call(s, n=lib.workspace_size(3, s) - 1) == lib.ATTN_ERR_WORKSPACE
     assert lib.workspace_size(3, s) > lib.workspace_size(0, s)
+
+
+def test_user_score_mod_compiles_without_a_gpu(lib):
+    """The run-time compile of a bias expression into the kernels needs no GPU:
+    a valid expression gives a handle, a broken one a compiler log and an error."""
+    import torch
+    L = lib.load()
+    h = ctypes.c_void_p()
+    buf = ctypes.create_string_buffer(1 << 16)
+    assert L.attn_user_mod_create(b"0.05f * (float)(kv - q) + (h == 1 ? -INFINITY : 0.0f)", lib.ATTN_BF16,
+                                  ctypes.byref(h), buf, len(buf)) == lib.ATTN_OK
+    assert h.value
+    L.attn_user_mod_destroy(h)
+    assert L.attn_user_mod_create(b"kv +* q", lib.ATTN_F16, ctypes.byref(h), buf, len(buf)) == lib.ATTN_ERR_INVALID_ARG
+    assert b"error" in buf.value
+    assert L.attn_user_mod_create(b"0.0f", lib.ATTN_F32, ctypes.byref(h), buf, len(buf)) == lib.ATTN_ERR_UNSUPPORTED
+    assert L.attn_user_mod_create(b"", lib.ATTN_F16, ctypes.byref(h), buf, len(buf)) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_user_mod_create(None, lib.ATTN_F16, ctypes.byref(h), buf, len(buf)) == lib.ATTN_ERR_INVALID_ARG
+    L.attn_user_mod_destroy(None)
+    m = lib.compile_score_mod("(kv > q) ? -INFINITY : 0.0f", dtype=torch.float16)
+    assert m.handle.value
+    # a call with no handle is refused before anything is launched
+    assert L.attn_fwd_user(ctypes.byref(_shape(lib)), FAKE, FAKE, FAKE, None, None, None, 0.125, FAKE, FAKE, FAKE,
+                           1 << 30, None, None) == lib.ATTN_ERR_INVALID_ARG

@@ -36,8 +36,10 @@ def _oracle_bm(bm_kind, B, H, Sq, Skv):
 
 
 def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", backward=True, heads=None,
-                  check_det=True, key_mask_override=None, strict=False, D=64, dense=None):
-    """``dense``: optional uint8 CPU tensor (B|1, H|1, Sq, Skv), the dense (query, key) mask."""
+                  check_det=True, key_mask_override=None, strict=False, D=64, dense=None, oracle_mod=None):
+    """``dense``: optional uint8 CPU tensor (B|1, H|1, Sq, Skv), the dense (query, key) mask.
+    ``oracle_mod``: the oracle's form of ``mod`` when it differs (a user score_mod)."""
+    omod = mod if oracle_mod is None else oracle_mod
     c, d = make_dev(B, H, Sq, Skv, D, dtype, key_mask=key_mask, dout=dout)
     if key_mask_override is not None:
         c["key_mask"] = key_mask_override.clone()
@@ -67,7 +69,7 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
     km = None if c["key_mask"] is None else c["key_mask"].numpy()
     obm = _oracle_bm(bm_kind, B, H, Sq, Skv)
     q64, k64, v64 = f64(c["q"]), f64(c["k"]), f64(c["v"])
-    o_ref, lse_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, block_mask=obm, score_mod=mod, heads=heads,
+    o_ref, lse_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, block_mask=obm, score_mod=omod, heads=heads,
                                  dense_mask=dn)
     sel = (slice(None),) if heads is None else tuple(np.array(x) for x in zip(*heads))
     tol = TOL[dtype]
@@ -83,7 +85,7 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
     vis_ref = OR.visited_tiles(B, H, Sq, Skv, key_mask=km, block_mask=obm, dense_mask=dn)
     np.testing.assert_array_equal(vis.cpu().numpy(), vis_ref)
     if backward:
-        dq_r, dk_r, dv_r = OR.attn_bwd(q64, k64, v64, f64(c["dout"]), key_mask=km, block_mask=obm, score_mod=mod,
+        dq_r, dk_r, dv_r = OR.attn_bwd(q64, k64, v64, f64(c["dout"]), key_mask=km, block_mask=obm, score_mod=omod,
                                        heads=heads, dense_mask=dn)
         for name, (buf, g), ref, shp in zip(("dq", "dk", "dv"), grads, (dq_r, dk_r, dv_r),
                                             ((B, H, Sq, D), (B, H, Skv, D), (B, H, Skv, D))):
@@ -306,6 +308,43 @@ def test_graph_replay_matches_direct_launches():
             assert torch.equal(t.view(torch.uint8), ref[n].view(torch.uint8)), n
         assert torch.equal(lse.view(torch.uint8), ref_lse.view(torch.uint8))
     assert E.poll_status(wf) == E.ATTN_OK and E.poll_status(wb) == E.ATTN_OK
+
+
+# Score_mods compiled at run time: C bias expressions and their oracle forms.
+USER_MODS = {
+    "relative": ("0.05f * (float)(kv - q)", lambda b, h, q, kv: 0.05 * (kv - q)),
+    "window": ("(kv > q || q - kv >= 200) ? -INFINITY : 0.0f",
+               lambda b, h, q, kv: np.where((kv > q) | (q - kv >= 200), -np.inf, 0.0)),
+    "document": ("(q / 100 == kv / 100) ? 0.1f * (float)h : -INFINITY",
+                 lambda b, h, q, kv: np.where(q // 100 == kv // 100, 0.1 * h, -np.inf)),
+    "batch_parity": ("0.25f * (float)b - 0.5f * (float)((q + kv) & 1)",
+                     lambda b, h, q, kv: 0.25 * b - 0.5 * ((q + kv) & 1)),
+}
+
+
+@pytest.mark.parametrize("name,km,bm,Sq,Skv", [("relative", False, None, 384, 300), ("window", True, None, 512, 512),
+                                               ("document", False, "causal", 300, 300),
+                                               ("batch_parity", True, None, 256, 640)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_user_score_mod(name, km, bm, Sq, Skv, dtype):
+    expr, f = USER_MODS[name]
+    m = E.compile_score_mod(expr, dtype=torch.bfloat16 if dtype == "bf16" else torch.float16)
+    run_and_check(2, 2, Sq, Skv, dtype, m, km, bm, oracle_mod=f)
+
+
+def test_user_score_mod_matches_builtin_alibi():
+    """ALiBi written as a user expression gives the built-in ALiBi's result to rounding."""
+    B, H, S = 2, 4, 384
+    _, d = make_dev(B, H, S, S, 64, "bf16")
+    m = E.compile_score_mod("exp2f(-8.0f * (float)(h + 1) / 4.0f) * (float)(kv - q)", dtype=torch.bfloat16)
+    ob, lb = E.attn_fwd(d["q"], d["k"], d["v"], score_mod="alibi")
+    ou, lu = E.attn_fwd(d["q"], d["k"], d["v"], score_mod=m)
+    torch.testing.assert_close(ou.float(), ob.float(), atol=1e-2, rtol=0)
+    torch.testing.assert_close(lu, lb, atol=1e-3, rtol=0)
+    gb = E.attn_bwd(d["q"], d["k"], d["v"], ob, lb, d["dout"], score_mod="alibi")
+    gu = E.attn_bwd(d["q"], d["k"], d["v"], ob, lb, d["dout"], score_mod=m)
+    for a, b_ in zip(gu, gb):
+        torch.testing.assert_close(a.float(), b_.float(), atol=2e-2, rtol=0)
 
 
 def test_fully_masked_batches_and_blocks():
