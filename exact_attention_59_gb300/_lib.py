@@ -368,6 +368,31 @@ def attn_decode_chunk(q, k, v, q_offset: int, key_mask=None, score_mod="none", s
     return out, lse
 
 
+def flash_attention(q, k, v, mask=None):
+    """The flash-attention-jax entry point ("3. Use flash_attention"): q, k, v
+    (batch, heads, seq, dim), an optional key mask (batch, seq) (nonzero keeps
+    a key); returns (out, lse), the second value being the row log-sum-exp."""
+    km = None
+    if mask is not None:
+        km = mask if mask.dtype == torch.uint8 and mask.is_contiguous() else (mask != 0).to(torch.uint8).contiguous()
+    return attn_fwd(q, k, v, key_mask=km)
+
+
+def causal_flash_attention(q, k, v):
+    """The flash-attention-jax causal entry point ("4. Use causal_flash_attention"):
+    q, k, v (seq, dim) without batch or head dimensions; returns (out (seq, dim),
+    lse (seq,)).  Causal top-left (key kv kept for query q iff kv <= q), with
+    the tiles above the diagonal skipped by a causal block mask."""
+    if q.dim() != 2 or k.dim() != 2 or v.dim() != 2:
+        raise ValueError("causal_flash_attention takes (seq, dim) tensors")
+    Sq, D = q.shape
+    Skv = k.shape[0]
+    q4, k4, v4 = (t.reshape(1, 1, t.shape[0], D) for t in (q, k, v))
+    bm = create_block_mask("causal", 1, 1, Sq, Skv, device=q.device)
+    out, lse = attn_fwd(q4, k4, v4, block_mask=bm)
+    return out.reshape(Sq, D), lse.reshape(Sq)
+
+
 def poll_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream and returns (and clears) the workspace status code."""
     return int(load().attn_poll_status(_ptr(ws), _stream(ws.device)))

@@ -351,13 +351,16 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   ATTN_TRY(check_ws(ATTN_OP_FWD, s, ws, ws_bytes));
   cudaStream_t st = (cudaStream_t)stream;
   if (s->D == 512) {
-    if (key_mask) return ATTN_ERR_UNSUPPORTED;   // the 512-wide kernel is built without a key mask
     FwdBigParams p;
     std::memset(&p, 0, sizeof(p));
     const long long rq = (long long)s->B * s->H * s->Sq, rk = (long long)s->B * s->H * s->Skv;
     if (!make_tmap(&p.tm_q, q, rq, 512, s->dtype) || !make_tmap(&p.tm_k, k, rk, 512, s->dtype) ||
         !make_tmap(&p.tm_v, v, rk, 512, s->dtype))
       return ATTN_ERR_CUDA;
+    ATTN_TRY(run_keymask(s, key_mask, ws, st));
+    const WsLayout wl = layout(ATTN_OP_FWD, s);
+    p.km_bits = key_mask ? at<uint32_t>(ws, wl.km_bits) : nullptr;
+    p.km_sum = key_mask ? at<uint8_t>(ws, wl.km_sum) : nullptr;
     p.out = out;
     p.lse = lse;
     p.bm_tiles = bm ? bm->tiles : nullptr;

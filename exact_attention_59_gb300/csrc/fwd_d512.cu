@@ -69,10 +69,12 @@ __global__ void __launch_bounds__(F5_THREADS, 1) fwd_d512_kernel(const __grid_co
     int n = 0;
     for (int kb = 0; kb < p.nkb; ++kb) {
       const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qt * p.nkb + kb] : TILE_FULL;
-      if (p.visited && half == 0) p.visited[((size_t)bh * p.nqb + qt) * p.nkb + kb] = st != TILE_EMPTY ? 1 : 0;
-      if (st == TILE_EMPTY) continue;
+      const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;   // key-padding summary of the block
+      const bool visit = st != TILE_EMPTY && ks != 0;
+      if (p.visited && half == 0) p.visited[((size_t)bh * p.nqb + qt) * p.nkb + kb] = visit ? 1 : 0;
+      if (!visit) continue;
       sm.list[n] = (uint16_t)kb;
-      sm.lflags[n] = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE) ? KB_MASKMOD : 0;
+      sm.lflags[n] = ((st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE) ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0);
       ++n;
     }
     sm.nlist = n;
@@ -210,18 +212,34 @@ __global__ void __launch_bounds__(F5_THREADS, 1) fwd_d512_kernel(const __grid_co
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      // one straight-line copy of the pass for blocks that mix kept and padded
+      // keys (a bit test per score) and one for the rest
+      auto pass = [&](auto keymask_c, uint4 kw) {
+        constexpr bool KM = decltype(keymask_c)::value;
 #pragma unroll
-      for (int cc = 0; cc < 128; ++cc) {
-        float x;
-        if constexpr (MOD == MOD_ALIBI)
-          x = fmaf(s[cc], sc, slope2 * float(kv0 - q + cc));
-        else if constexpr (MOD == MOD_CHECKER)
-          x = fmaf(s[cc], sc, (cc & 1) ? -cb_even : cb_even);
-        else
-          x = s[cc] * sc;
-        if (causal && cc > lim) x = -INFINITY;
-        s[cc] = x;
-        mx[cc & 7] = fmaxf(mx[cc & 7], x);
+        for (int cc = 0; cc < 128; ++cc) {
+          float x;
+          if constexpr (MOD == MOD_ALIBI)
+            x = fmaf(s[cc], sc, slope2 * float(kv0 - q + cc));
+          else if constexpr (MOD == MOD_CHECKER)
+            x = fmaf(s[cc], sc, (cc & 1) ? -cb_even : cb_even);
+          else
+            x = s[cc] * sc;
+          if (causal && cc > lim) x = -INFINITY;
+          if constexpr (KM) {
+            const uint32_t w = cc < 32 ? kw.x : (cc < 64 ? kw.y : (cc < 96 ? kw.z : kw.w));
+            if (!(w & (1u << (cc & 31)))) x = -INFINITY;
+          }
+          s[cc] = x;
+          mx[cc & 7] = fmaxf(mx[cc & 7], x);
+        }
+      };
+      if (sm.lflags[j] & KB_KEYMASK) {
+        const uint4 kw = make_uint4(km_word(p.km_bits, b, p.Skv, kv0), km_word(p.km_bits, b, p.Skv, kv0 + 32),
+                                    km_word(p.km_bits, b, p.Skv, kv0 + 64), km_word(p.km_bits, b, p.Skv, kv0 + 96));
+        pass(bconst<true>{}, kw);
+      } else {
+        pass(bconst<false>{}, make_uint4(0u, 0u, 0u, 0u));
       }
       const float rowmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));

@@ -90,6 +90,8 @@ struct FwdBigParams {
   CUtensorMap tm_q, tm_k, tm_v;   // 2-D views (rows = B*H*S, cols = 512), box {64, 128}, 128B swizzle
   void* out;
   float* lse;
+  const uint32_t* km_bits;        // key mask as bits (B, ceil(Skv/32)), or nullptr
+  const uint8_t* km_sum;          // (B, nkb): 0 no key kept, 1 some, 2 all
   const uint8_t* bm_tiles;
   long long bm_sb, bm_sh;
   int bm_mod;

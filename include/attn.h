@@ -160,7 +160,8 @@ attn_status attn_pack_dense_mask(const attn_shape* shape, const uint8_t* mask, i
  *   key_mask: nullable; bm: nullable (NULL = no block mask);
  *   debug_visited: nullable uint8 (B, H, Sq/128, Skv/128); when given, each
  *   entry is set to 1 if the kernel computed that tile and 0 if it skipped it.
- *   D = 512 is built for f16/bf16 without key mask. */
+ *   D = 512 is built for f16/bf16 (key mask, block mask and the built-in
+ *   mods; Sq, Skv multiples of 128). */
 attn_status attn_fwd(const attn_shape* shape, const void* q, const void* k, const void* v,
                      const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod,
                      float scale, void* out, float* lse, void* ws, size_t ws_bytes,

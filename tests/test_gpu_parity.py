@@ -433,6 +433,57 @@ def test_d512_forward_variants(B, H, S, dtype, mod, bm):
     run_and_check(B, H, S, S, dtype, mod, False, bm, backward=False, D=512)
 
 
+@pytest.mark.parametrize("mod,bm", [("none", None), ("alibi", "causal"), ("checkerboard", None), ("causal", None)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_d512_key_mask(mod, bm, dtype):
+    """Head dim 512 with the key-padding mask (flash-attention-jax's (batch, seq) mask)."""
+    run_and_check(2, 1, 384, 512, dtype, mod, True, bm, backward=False, D=512)
+
+
+def test_d512_key_mask_padded_blocks():
+    """Batch 1 keeps no key; batch 0 has whole 128-key blocks padded (skipped)."""
+    km = torch.ones((2, 512), dtype=torch.uint8)
+    km[1] = 0
+    km[0, 128:256] = 0
+    km[0, 384:] = 0
+    run_and_check(2, 2, 256, 512, "bf16", "none", True, None, backward=False, D=512, key_mask_override=km)
+
+
+def test_flash_attention_entry_points():
+    """flash_attention(q, k, v, mask) and causal_flash_attention on (seq, dim) tensors."""
+    c, d = make_dev(2, 2, 256, 256, 64, "bf16", key_mask=True)
+    o1, l1 = E.flash_attention(d["q"], d["k"], d["v"], d["key_mask"].bool())
+    o2, l2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"])
+    assert torch.equal(o1.view(torch.uint8), o2.view(torch.uint8)) and torch.equal(l1, l2)
+    for S, D in ((300, 64), (384, 512)):
+        c, d = make_dev(1, 1, S, S, D, "bf16")
+        out, lse = E.causal_flash_attention(d["q"][0, 0], d["k"][0, 0], d["v"][0, 0])
+        assert out.shape == (S, D) and lse.shape == (S,)
+        o_ref, l_ref = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod="causal")
+        compare("out", f64(out)[None, None], o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"])
+        compare("lse", f64(lse)[None, None], l_ref, TOL["bf16"]["lse_max"])
+
+
+@pytest.mark.slow
+def test_flash_attention_page_example_sampled_rows():
+    """The flash-attention-jax example at its size: q, k, v (1, 2, 131072, 512), a
+    (1, 131072) key mask drawn from {0, 1}; 16 seeded rows per head against the oracle."""
+    w = W.LONG_CAUSAL_BF16
+    c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, dout=None, with_key_mask=True)
+    d = {k: v.cuda() for k, v in c.items() if v is not None}
+    out, lse = E.flash_attention(d["q"], d["k"], d["v"], d["key_mask"])
+    torch.cuda.synchronize()
+    km = c["key_mask"].numpy()
+    tol = TOL["bf16"]
+    for h in range(w.H):
+        rows = IN.sample_rows(w.Sq, 16, seed=IN.SEED + 7 + h).numpy()
+        q64 = f64(c["q"][:, h:h + 1])
+        k64, v64 = f64(c["k"][:, h:h + 1]), f64(c["v"][:, h:h + 1])
+        o_ref, l_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, rows=rows)
+        compare(f"out h{h}", f64(out[:, h:h + 1, rows]), o_ref[:, :, rows], tol["o_max"], tol["o_mean"])
+        compare(f"lse h{h}", f64(lse[:, h:h + 1, rows]), l_ref[:, :, rows], tol["lse_max"])
+
+
 def test_d512_rectangular():
     run_and_check(1, 2, 128, 1024, "bf16", "alibi", False, None, backward=False, D=512)
     run_and_check(1, 1, 384, 128, "bf16", "none", False, None, backward=False, D=512)
