@@ -111,7 +111,15 @@ extern "C" attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dt
 
 extern "C" void attn_user_mod_destroy(attn_user_mod mod) {
   if (!mod) return;
-  for (auto& kv : mod->per_device) cudaLibraryUnload(kv.second.lib);
+  // Kernels of this mod may still be queued (calls are asynchronous): each
+  // device it was loaded on finishes its work before the code is unloaded.
+  int cur = 0;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : mod->per_device) {
+    if (cudaSetDevice(kv.first) == cudaSuccess) cudaDeviceSynchronize();
+    cudaLibraryUnload(kv.second.lib);
+  }
+  if (have_cur) cudaSetDevice(cur);
   delete mod;
 }
 

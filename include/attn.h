@@ -278,7 +278,9 @@ attn_status attn_decode_chunk(const attn_shape* shape, const void* q, const void
 typedef struct attn_user_mod_st* attn_user_mod;
 attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dtype, attn_user_mod* mod, char* log,
                                  size_t log_bytes);
-/* Frees a user score_mod (NULL is ignored); no call may be using it. */
+/* Frees a user score_mod (NULL is ignored).  Waits for all work on each
+ * device the mod was loaded on before unloading its code, so a call still
+ * queued on a stream finishes first; it must not race with a new call. */
 void attn_user_mod_destroy(attn_user_mod mod);
 
 /* attn_fwd / attn_bwd with a user score_mod in place of the enum (f16/bf16,

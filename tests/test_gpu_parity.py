@@ -347,6 +347,43 @@ def test_user_score_mod_matches_builtin_alibi():
         torch.testing.assert_close(a.float(), b_.float(), atol=2e-2, rtol=0)
 
 
+def _random_configs(n=14, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 4))
+        Sq, Skv = int(rng.integers(1, 700)), int(rng.integers(1, 700))
+        out.append((B, H, Sq, Skv, str(rng.choice(["bf16", "f16"])),
+                    str(rng.choice(["none", "alibi", "checkerboard", "causal"])), bool(rng.integers(0, 2)),
+                    None if rng.integers(0, 2) else "causal", bool(rng.integers(0, 3) == 0)))
+    return out
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,dtype,mod,km,bm,dense", _random_configs())
+def test_random_configurations(B, H, Sq, Skv, dtype, mod, km, bm, dense):
+    """Seeded random mixes of lengths (any, ragged), dtypes, mods, key/block/dense masks."""
+    dn = None
+    if dense:
+        g = torch.Generator().manual_seed(Sq * 1000 + Skv)
+        dn = (torch.rand((1, H, Sq, Skv), generator=g) < 0.6).to(torch.uint8)
+    run_and_check(B, H, Sq, Skv, dtype, mod, km, bm, dense=dn)
+
+
+def test_user_score_mod_dropped_while_queued():
+    """A user mod that goes out of scope right after an asynchronous call: its
+    destruction waits for the queued kernels before unloading their code."""
+    B, H, S = 2, 2, 512
+    c, d = make_dev(B, H, S, S, 64, "bf16")
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    E.attn_fwd(d["q"], d["k"], d["v"], score_mod=E.compile_score_mod("0.05f * (float)(kv - q)"), out=out, lse=lse)
+    import gc
+    gc.collect()
+    torch.cuda.synchronize()
+    o_ref, _ = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod=USER_MODS["relative"][1])
+    compare("out", f64(out), o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"], scaled=True)
+
+
 def test_fully_masked_batches_and_blocks():
     """Batch 1 has no key at all; batch 0 has whole 128-key blocks padded (skipped tiles)."""
     km = torch.ones((2, 512), dtype=torch.uint8)
