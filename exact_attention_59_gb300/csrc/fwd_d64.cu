@@ -55,7 +55,10 @@ static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 // in the row's dense-mask words dw is 0; and the running maximum in four
 // independent chains.
 // With USER, x += user_bias(b, h, q, kv0 + cc) log2(e) (a run-time-compiled score_mod).
-template <bool TABLE, bool LIMITED, bool DENSE, bool USER = false>
+// With RAW (no table, no user bias, scale > 0) the scores stay unscaled: the
+// masks and the maximum work on s itself (max of s * scale = scale * max of s),
+// and the exponential pass applies the scale in its one FFMA.
+template <bool TABLE, bool LIMITED, bool DENSE, bool USER = false, bool RAW = false>
 DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4],
                        int ub = 0, int uh = 0, int uq = 0, int ukv0 = 0) {
 #pragma unroll
@@ -66,7 +69,8 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
     for (int j = 0; j < 2; ++j) {
       const int c = 2 * (i + j);
       const uint64_t sv = f2(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-      const uint64_t xv = TABLE ? ffma2(sv, scv, j ? f2(bias.z, bias.w) : f2(bias.x, bias.y)) : fmul2(sv, scv);
+      const uint64_t xv = TABLE ? ffma2(sv, scv, j ? f2(bias.z, bias.w) : f2(bias.x, bias.y))
+                                : (RAW ? sv : fmul2(sv, scv));
       float x0, x1;
       unf2(xv, x0, x1);
       if constexpr (USER) {
@@ -327,6 +331,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       const uint64_t scv = f2(p.sc, p.sc);
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
       const int parity = (MOD == MOD_CHECKER) ? (qpos & 1) : 0;
+      // unscaled scores in the max pass (scale > 0 keeps the order of the maximum)
+      const bool raw = !kTableMod && MOD != MOD_USER && p.sc > 0.f;
       float m_run = -INFINITY, l = 0.f;
       uint32_t n = 0;
       int u = 0;
@@ -380,6 +386,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           if (DM && dense) scale_scores<false, true, DM, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
           else if (limited) scale_scores<false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
           else scale_scores<false, false, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+        } else if (raw) {
+          if (DM && dense) scale_scores<false, true, DM, false, true>(r, scv, tb, lim, dw, mx);
+          else if (limited) scale_scores<false, true, false, false, true>(r, scv, tb, lim, dw, mx);
+          else scale_scores<false, false, false, false, true>(r, scv, tb, lim, dw, mx);
         } else {
           if (DM && dense) scale_scores<false, true, DM>(r, scv, tb, lim, dw, mx);
           else if (limited) scale_scores<false, true, false>(r, scv, tb, lim, dw, mx);
@@ -388,7 +398,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
         // per-score work: scores here are x' = x - base
         const float base = (MOD == MOD_ALIBI) ? slope2 * float(kv0 - qpos) : 0.f;
-        const float rowmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) + base;
+        const float mxs = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        const float rowmax = (raw ? mxs * p.sc : mxs) + base;
         // stale running max: rescale O only when the max grows by more than 2^8
         float alpha = 1.f;
         bool resc = false;
@@ -401,12 +412,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         const uint64_t negm = f2(base - m_use, base - m_use);
+        // x = s scale - m on the raw path; x' - m (exactly x' + negm) otherwise
+        const uint64_t mulv = raw ? scv : f2(1.f, 1.f);
         uint64_t sumv[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
         uint32_t pk[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           float d0, d1;
-          unf2(fadd2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), negm), d0, d1);
+          unf2(ffma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), mulv, negm), d0, d1);
           const float p0 = ex2(d0), p1 = ex2(d1);
           sumv[i & 1] = fadd2(sumv[i & 1], f2(p0, p1));
           pk[i] = pack2<BF16>(p0, p1);
