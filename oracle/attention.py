@@ -37,7 +37,14 @@ Readings where the pages are silent (each one is listed in the design doc):
   elementwise), 2 = full (the mask_mod is not evaluated);
 * the second return value of ``flash_attention`` is the row log-sum-exp in
   natural log;
-* the decode entry is the forward with Sq = 1 and q_idx = 0.
+* the decode entry is the forward with Sq = 1 and q_idx = 0; a chunk of
+  queries decoded against a KV cache sits at positions q_offset + i, and the
+  position is what the mods and the causal rule see;
+* sequence lengths need not be multiples of the block size: the last blocks
+  are partial (the plain formula has no block size at all);
+* a user score_mod (the README's hooks take arbitrary callables) is an
+  additive bias f(b, h, q_idx, kv_idx), -inf to mask, the form of every mod
+  the pages name.
 
 Parity unpinned: the ALiBi and checkerboard definitions themselves (no page
 defines them; they are pinned only against their own closed forms), and the
