@@ -1,7 +1,7 @@
 // api.cu - the C ABI declared in include/attn.h: validation, workspace
 // layout, TMA descriptor encoding and kernel dispatch.  No allocation, no
 // synchronisation (except attn_poll_status), no state beyond one cached
-// process-wide value (the driver's tensor-map encoder).
+// process-wide value (the CUDA driver's tensor-map encoder).
 #include <cudaTypedefs.h>
 
 #include <cmath>

@@ -20,7 +20,7 @@ online-softmax method reaches exactly (up to rounding order):
   (``_pallas_forward.kernel.body``): scale, then score_mod, then mask, then
   softmax, then the product with V.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the sources above are silent:
 
 * the key mask keeps a key where it is nonzero (``jnp.where(m, scores, neg)``
   in the Pallas kernel body); so does the dense mask for a (query, key) pair,
