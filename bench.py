@@ -42,8 +42,7 @@ UNIT = "TFLOP/s"
 
 
 # DRAM bytes (read + write) of one bwd_dkdv_kernel launch at the bench workload, from
-# `ncu --set full` of `python bench.py --mode profile --batch 8 --steps 1`
-# (summary: profiles/step_kernels_keypad_fp16_b8h8s2048d64_ncu_full.md).  Set it
+# `ncu --set full` of `python bench.py --mode profile --batch 8 --steps 1`.  Set it
 # back to None when the kernel changes until it is captured again.
 DKDV_TRAFFIC_BYTES = 80.8e6
 
@@ -69,14 +68,15 @@ class Clocks:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_ms=10):
         self.idx = gpu_index
+        self.period_ms = period_ms
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -180,21 +180,23 @@ def run_ours(args, rank, world):
     t_end = torch.cuda.Event(enable_timing=True)
     DIST.barrier()
     torch.cuda.synchronize()
+    # The clock sampler (every 10 ms) runs across the timed replay and the phase
+    # pass that follows it (the same kernels launched directly), so its samples
+    # see the GPU under this load even when the timed region itself is short.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     with Clocks(dev.index) as clk:
         t_start.record(stream)
         graph.replay()
         t_end.record(stream)
         torch.cuda.synchronize()
-    DIST.barrier()
+        DIST.barrier()
+        # per-kernel phase times: the same steps launched directly, CUDA events between the calls
+        for i in range(args.steps):
+            step(sets[i % nsets], evs[i])
+        torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
-    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout in the timed region"
     ms = DIST.max_over_ranks(total_ms, device=dev) / args.steps   # the slowest rank sets the time
-    # per-kernel phase times: the same steps launched directly, CUDA events between the calls
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        step(sets[i % nsets], evs[i])
-    torch.cuda.synchronize()
-    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout in the phase pass"
+    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout in the timed region"
     ph = {n: [] for n in ("fwd", "pre", "dkdv", "dq")}
     for e in evs:
         for j, n in enumerate(ph):
@@ -203,14 +205,16 @@ def run_ours(args, rank, world):
     # ---- decode (config: checkerboard fp16, q 8x8x1x64, K/V 8x8x2048x64), CUDA graph, rotating K/V
     dec = bench_decode(E, dev, args)
 
-    # ---- end to end: pinned host buffers, copies inside the timed region
+    # ---- end to end: pinned host buffers, copies inside the timed region; every
+    # output comes back (and, as an extra figure, the run that reads back lse alone)
     e2e = bench_e2e(E, dev, args, w)
+    e2e_lse = bench_e2e(E, dev, args, w, results=("lse",))
 
     # ---- the other named workloads, for context (outside the timed region)
     extras = None if args.no_extras else bench_extras(E, dev)
 
     res = {"ms": ms, "phases": {n: statistics.mean(v) for n, v in ph.items()}, "clocks": clk.summary(),
-           "decode": dec, "e2e": e2e, "extras": extras}
+           "decode": dec, "e2e": e2e, "e2e_lse": e2e_lse, "extras": extras}
     return res
 
 
@@ -275,19 +279,24 @@ def bench_decode(E, dev, args):
     return res
 
 
-def bench_e2e(E, dev, args, w):
+E2E_ALL = ("out", "lse", "dq", "dk", "dv")
+
+
+def bench_e2e(E, dev, args, w, results=E2E_ALL):
     """fwd+bwd through the public API with host buffers: every step copies its inputs
-    (q, k, v, dout, key mask) from pinned host memory and reads back its result
-    metric, the forward's row log-sum-exp, inside the timed region; out and the
-    gradients stay on the device for whatever consumes them, as in a training
-    step whose loss alone comes back.  Copies run on their own streams,
-    double-buffered, so step i+1's upload and step i-1's download overlap step
-    i's kernels (as a training input pipeline would)."""
+    (q, k, v, dout, key mask) from pinned host memory into the device and reads
+    back the step's `results` (by default every output: out, lse, dq, dk, dv)
+    into pinned host memory, inside the timed region.  Copies run on their own
+    streams, double-buffered, so step i+1's upload and step i-1's download
+    overlap step i's kernels (as a training input pipeline would)."""
     hosts = []
     for j in range(2):
         c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, seed=IN.SEED + 7000 + j, with_key_mask=True)
         hosts.append({k: v.pin_memory() for k, v in c.items()})
-    outs_h = [{"lse": torch.empty(hosts[0]["q"].shape[:3], dtype=torch.float32).pin_memory()} for _ in range(2)]
+    shapes = {"out": hosts[0]["q"].shape, "lse": hosts[0]["q"].shape[:3], "dq": hosts[0]["q"].shape,
+              "dk": hosts[0]["k"].shape, "dv": hosts[0]["v"].shape}
+    dts = {n: (torch.float32 if n == "lse" else hosts[0]["q"].dtype) for n in shapes}
+    outs_h = [{n: torch.empty(shapes[n], dtype=dts[n]).pin_memory() for n in results} for _ in range(2)]
     ins_d = [{k: torch.empty_like(v, device=dev) for k, v in hosts[0].items()} for _ in range(2)]
     outs_d = [{"lse": torch.empty(hosts[0]["q"].shape[:3], dtype=torch.float32, device=dev),
                "out": torch.empty_like(hosts[0]["q"], device=dev), "dq": torch.empty_like(hosts[0]["q"], device=dev),
@@ -336,7 +345,7 @@ def bench_e2e(E, dev, args, w):
             cmp_done[j].record(s_cmp)
         with torch.cuda.stream(s_down):
             s_down.wait_event(cmp_done[j])
-            for k in ho:   # the result metric only
+            for k in ho:
                 ho[k].copy_(do[k], non_blocking=True)
             down_done[j].record(s_down)
         first[j] = False
@@ -357,9 +366,9 @@ def bench_e2e(E, dev, args, w):
     assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0
     h2d = sum(v.numel() * v.element_size() for v in hosts[0].values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h[0].values())
-    return {"ms": ms, "h2d": h2d, "d2h": d2h,
-            "pipeline": "double-buffered, copies on separate streams, kernels replayed as a CUDA graph; lse read back, "
-                        "out and gradients stay on the device"}
+    return {"ms": ms, "h2d": h2d, "d2h": d2h, "results": list(results),
+            "pipeline": "double-buffered, copies on separate streams, kernels replayed as a CUDA graph; "
+                        f"read back: {', '.join(results)}"}
 
 
 def bench_extras(E, dev):
@@ -477,24 +486,33 @@ def bench_extras(E, dev):
 
 
 # ------------------------------------------------------------------ oracle (CPU) legs
-def oracle_sample(seconds=12.0, max_heads=64):
-    """Times the oracle's fwd+bwd on whole heads of the workload until `seconds` pass."""
-    import numpy as np
-    import oracle.attention as OR
+def oracle_case():
+    """The bench workload's inputs as float64 arrays, built once (outside any timing)."""
+    import numpy as np  # noqa: F401
     w = WL
     c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=True)
     q, k, v, do = (c[n].float().double().numpy() for n in ("q", "k", "v", "dout"))
-    km = c["key_mask"].numpy()
+    return {"q": q, "k": k, "v": v, "dout": do, "key_mask": c["key_mask"].numpy()}
+
+
+def oracle_head(case, idx):
+    """The oracle's forward and backward of head `idx` (b = idx // H, h = idx % H)."""
+    import oracle.attention as OR
+    b, h = divmod(idx % (WL.B * WL.H), WL.H)
+    OR.attn_fwd(case["q"], case["k"], case["v"], key_mask=case["key_mask"], heads=[(b, h)])
+    OR.attn_bwd(case["q"], case["k"], case["v"], case["dout"], key_mask=case["key_mask"], heads=[(b, h)])
+
+
+def oracle_sample(case, seconds=12.0, max_heads=64):
+    """Times the oracle's fwd+bwd on whole heads of the workload until `seconds` pass."""
     done, t0 = 0, time.perf_counter()
     while done < max_heads:
-        b, h = divmod(done, w.H)
-        OR.attn_fwd(q, k, v, key_mask=km, heads=[(b, h)])
-        OR.attn_bwd(q, k, v, do, key_mask=km, heads=[(b, h)])
+        oracle_head(case, done)
         done += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    flops = 3.5 * 4.0 * w.Sq * w.Skv * w.D * done
+    flops = 3.5 * 4.0 * WL.Sq * WL.Skv * WL.D * done
     return flops / dt / 1e12, done, dt
 
 
@@ -506,24 +524,33 @@ def blas_threads():
             return int(max(n))
     except Exception:
         pass
-    return os.cpu_count()
+    return None
+
+
+def host_cores():
+    """Threads the oracle's BLAS uses (its `cores`) and the host's CPU count, separately."""
+    bt = blas_threads()
+    return {"cores": bt if bt is not None else os.cpu_count(), "blas_threads": bt, "host_cpus": os.cpu_count()}
 
 
 def cpu_baseline(seconds=12.0):
-    v, heads, dt = oracle_sample(seconds)
-    return {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"float64 NumPy fwd+bwd of {heads} of {WL.B * WL.H} (b,h) heads of the workload in {dt:.1f} s"}
+    case = oracle_case()
+    v, heads, dt = oracle_sample(case, seconds)
+    return {"value": v, "unit": UNIT, **host_cores(), "kind": "oracle",
+            "sample": f"float64 NumPy fwd+bwd of {heads} of {WL.B * WL.H} (b,h) heads of the workload in {dt:.1f} s "
+                      "(inputs built before the timing)"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        oracle_sample(seconds=0.0, max_heads=1)
+    case = oracle_case()   # inputs once, outside the timed steps
+    for i in range(args.warmup):
+        oracle_head(case, i)
     times = []
-    for _ in range(args.steps):
+    for i in range(args.steps):
         t0 = time.perf_counter()
-        oracle_sample(seconds=0.0, max_heads=1)
+        oracle_head(case, i)
         times.append(time.perf_counter() - t0)
     ms = statistics.mean(times) * 1e3
     val = 3.5 * 4.0 * WL.Sq * WL.Skv * WL.D / (ms * 1e-3) / 1e12
@@ -532,8 +559,9 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WL.name, "B": WL.B, "H": WL.H, "Sq": WL.Sq, "Skv": WL.Skv, "D": WL.D,
                        "step": "oracle fwd+bwd of one (b, h) head per step (bounded sample)"},
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": "one (b, h) head of the workload per step, float64 NumPy"},
+            "cpu_baseline": {"value": val, "unit": UNIT, **host_cores(), "kind": "oracle",
+                             "sample": "one (b, h) head of the workload per step, float64 NumPy, inputs built once "
+                                       "before the timed steps"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -629,11 +657,16 @@ def main():
                        "frac_of_hbm": dec["GB/s"] / hbm,
                        "chunk_causal_fp16_b8h8kv2048d64": [dict(c, frac_of_hbm=c["GB/s"] / hbm)
                                                            for c in dec["chunk_causal_fp16_b8h8kv2048d64"]]},
-            "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": achieved, "peak": sustained,
-                         "unit": "TFLOP/s", "frac": achieved / sustained, "traffic": DKDV_TRAFFIC_BYTES,
-                         "peak_kind": f"bf16 sustained, {src}"},
+            "roofline": {"kernel": "bwd_dkdv_kernel", "bound": "tensor", "achieved": achieved, "peak": burst,
+                         "unit": "TFLOP/s", "frac": achieved / burst, "traffic": DKDV_TRAFFIC_BYTES,
+                         "peak_kind": f"bf16 burst, {src} (the kernel is timed in a ms-scale region)",
+                         "frac_of_sustained": achieved / sustained},
             "e2e": {"value": fl / (e2e["ms"] * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                     "d2h_bytes_per_step": e2e["d2h"], "pipeline": e2e["pipeline"]},
+            "e2e_lse_only": {"value": fl / (res["e2e_lse"]["ms"] * 1e-3) / 1e12, "unit": UNIT,
+                             "h2d_bytes_per_step": res["e2e_lse"]["h2d"],
+                             "d2h_bytes_per_step": res["e2e_lse"]["d2h"],
+                             "pipeline": res["e2e_lse"]["pipeline"]},
             # per step: key-mask packing + forward, preprocess (packs the key mask too), dK/dV, dQ
             "gpu_launches": 5 * args.steps,
             "clocks": res["clocks"],

@@ -4,26 +4,32 @@
 // lists "faster decoding attention" as a TODO.  It is a streaming read of K and
 // V (256 bytes per key at D = 64), so the kernel is shaped for bandwidth and
 // latency, not for the tensor core:
-//   grid (nsplit, B*H); each CTA owns a contiguous range of up to 128 keys of
-//   one (b, h).  Its K and V rows are contiguous in HBM, so one thread issues
-//   two bulk copies (cp.async.bulk, 16-byte aligned, 16 KB each) into shared
-//   memory completing on one mbarrier: a single round trip to HBM per CTA.
-//   At 33 KB of shared memory a CTA, 6 fit on an SM, so the B8 H8 Skv 2048
-//   case runs 912 of its 1024 CTAs in the first wave (all of K and V, 33.5
-//   MB, is more than the GPU's shared memory); streaming each split through a
-//   two-stage ring instead, to fit one wave, was slower (a second round trip
-//   per CTA).
-//   In shared memory: thread j forms the score of key j, the CTA takes the max
-//   and the exponentials, and thread d (and d + 64) sum p_j V_jd over half the
-//   keys each; the CTA's (m, l, o[64]) goes to the workspace.
-//   The last CTA of a (b, h) to finish (atomic ticket) merges the splits in a
-//   fixed order, writes out and lse, and re-arms the ticket for the next call.
+//   one CTA per (b, h, split), the splits of a head adjacent; each CTA owns a contiguous range of up to DEC_KEYS keys
+//   of one (b, h), DEC_WARP_KEYS per warp.  Inside a warp, lane = 8 g + c: the
+//   lane group g (0..3) owns keys 4 u + g (u < DEC_U) of the warp's range and
+//   lane c of the group owns head dimensions 8 c .. 8 c + 7.  Every lane issues
+//   all of its 16-byte K and V loads (ld.global.nc, no L1 allocation) before it
+//   uses any of them, so each CTA has 32 KB in flight at once and the HBM
+//   latency is paid once per CTA; consecutive lanes read consecutive 16-byte
+//   pieces of the key rows, so every load instruction reads 512 contiguous
+//   bytes.  No shared-memory staging and no barrier wait: nothing can stall.
+//   Per lane group: the score of each key (an 8-wide dot product, summed over
+//   the 8 lanes by three xor shuffles), the mods and masks, a local max, the
+//   exponentials and p-weighted sums of V rows; the groups and then the warps
+//   are merged with the usual rescaling by 2^(m_i - M).  The CTA's (m, l, o[64])
+//   goes to the workspace.
+//   The last CTA of a (b, h) to finish (atomic ticket, no spin) merges the
+//   splits in a fixed order, writes out and lse, and re-arms the ticket.
+// Arithmetic in base 2 (scale and biases carry log2(e)), as in the prefill.
 #include "kernels.h"
 
 namespace attn {
 
-constexpr int DEC_THREADS = 128;
-constexpr int DEC_KEYS = 128;   // keys per split (maximum): 32 KB of K and V per CTA
+constexpr int DEC_WARPS = 8;
+constexpr int DEC_THREADS = 32 * DEC_WARPS;
+constexpr int DEC_U = 4;                           // keys per lane group
+constexpr int DEC_WARP_KEYS = 4 * DEC_U;           // 16
+constexpr int DEC_KEYS = DEC_WARPS * DEC_WARP_KEYS;   // 128 keys per CTA at most
 
 int decode_num_splits(int B, int H, int Skv) {
   (void)B;
@@ -31,128 +37,157 @@ int decode_num_splits(int B, int H, int Skv) {
   return (Skv + DEC_KEYS - 1) / DEC_KEYS;
 }
 
-DEVI void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
+// 16-byte read-only load that does not allocate in L1 (each byte is read once).
+DEVI uint4 ldg_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Merges the running (m, l, o) of this lane with the one `off` lanes away.
+DEVI void merge_xor(float& m, float& l, float (&o)[8], int off) {
+  const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+  const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+  const float M = fmaxf(m, m2);
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  const float a = ex2(m - Mu), b = ex2(m2 - Mu);   // 2^-inf = 0 for an empty side
+  l = l * a + l2 * b;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = o[e] * a + __shfl_xor_sync(0xffffffffu, o[e], off) * b;
+  m = M;
 }
 
 template <bool BF16, int MOD>
-__global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecodeParams p) {
-  const int split = blockIdx.x, bh = blockIdx.y;
+__global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(const DecodeParams p) {
+  const int split = blockIdx.x % p.nsplit, bh = blockIdx.x / p.nsplit;
   const int b = bh / p.H, h = bh % p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 3, c = lane & 7;
   const int k_lo = split * p.keys_per_split;
-  const int nk = min(p.Skv, k_lo + p.keys_per_split) - k_lo;   // 1 .. 128
+  const int k_hi = min(p.Skv, k_lo + p.keys_per_split);
+  const int kw = k_lo + DEC_WARP_KEYS * warp;   // first key of this warp
 
-  __shared__ __align__(128) uint16_t ks[DEC_KEYS * 64], vs[DEC_KEYS * 64];
-  __shared__ __align__(16) float qs[64];
-  __shared__ float sc_s[DEC_KEYS], redm[4], reds[4], o_part[64];
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ float sm_m[DEC_WARPS], sm_l[DEC_WARPS], sm_o[DEC_WARPS][64];
   __shared__ unsigned ticket;
 
-  const uint32_t barp = smem_u32(&bar);
-  if (tid == 0) {
-    mbar_init(barp, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t bytes = (uint32_t)nk * 128u;
-    mbar_expect_tx(barp, 2 * bytes);
-    const uint16_t* kg = reinterpret_cast<const uint16_t*>(p.k) + ((size_t)bh * p.Skv + k_lo) * 64;
-    const uint16_t* vg = reinterpret_cast<const uint16_t*>(p.v) + ((size_t)bh * p.Skv + k_lo) * 64;
-    bulk_g2s(smem_u32(ks), kg, bytes, barp);
-    bulk_g2s(smem_u32(vs), vg, bytes, barp);
-  }
-  // q (scaled by scale * log2 e) while the copies fly
-  if (tid < 32) {
-    const uint32_t w = reinterpret_cast<const uint32_t*>(p.q)[(size_t)bh * 32 + tid];
-    const float2 f = unpack2<BF16>(w);
-    qs[2 * tid] = f.x * p.sc;
-    qs[2 * tid + 1] = f.y * p.sc;
-  }
+  // (before the loads: the slope's exp2 then needs no registers beside them)
   const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
-  // The copies complete in well under a millisecond; a generous bounded spin
-  // keeps a lost completion from hanging the GPU (the status word records it).
-  bool ok = true;
-  {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(barp, 0)) {
-      if (global_timer_ns() - t0 > 2000000000ull) { ok = false; break; }
+  // ---- every K and V load of this lane goes out first
+  const uint4* kg = reinterpret_cast<const uint4*>(p.k) + (size_t)bh * p.Skv * 8 + c;
+  const uint4* vg = reinterpret_cast<const uint4*>(p.v) + (size_t)bh * p.Skv * 8 + c;
+  uint4 kr[DEC_U], vr[DEC_U];
+#pragma unroll
+  for (int u = 0; u < DEC_U; ++u) {
+    const int key = kw + 4 * u + g;
+    if (key < k_hi) {
+      kr[u] = ldg_stream(kg + (size_t)key * 8);
+      vr[u] = ldg_stream(vg + (size_t)key * 8);
+    } else {
+      kr[u] = make_uint4(0u, 0u, 0u, 0u);
+      vr[u] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  __syncthreads();
+  uint32_t keep = 0;   // bit u: key 4 u + g of the warp's range is in range and kept
+#pragma unroll
+  for (int u = 0; u < DEC_U; ++u) {
+    const int key = kw + 4 * u + g;
+    const bool in = key < k_hi && (!p.key_mask || __ldg(p.key_mask + (size_t)b * p.Skv + key) != 0);
+    keep |= (in ? 1u : 0u) << u;
+  }
+  // q (this lane's 8 dimensions), scaled by scale * log2(e)
+  float qf[8];
+  {
+    const uint4 qw = __ldg(reinterpret_cast<const uint4*>(p.q) + (size_t)bh * 8 + c);
+    const uint32_t w4[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack2<BF16>(w4[e]);
+      qf[2 * e] = f.x * p.sc;
+      qf[2 * e + 1] = f.y * p.sc;
+    }
+  }
 
-  // ---- scores: thread j owns key j (its 64 dims as eight 16-byte chunks, the
-  // start rotated by j so the lanes of a warp spread over the banks)
-  float x = -INFINITY;
-  {
-    const int j = tid;
-    if (j < nk) {
-      const uint4* kr = reinterpret_cast<const uint4*>(ks + j * 64);
-      float s = 0.f;
+  // ---- scores of the group's keys (partial dot over 8 dims, then over the 8 lanes)
+  float s[DEC_U];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = (i + j) & 7;
-        const uint4 u = kr[c];
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = unpack2<BF16>(wd[e]);
-          s = fmaf(qs[8 * c + 2 * e], f.x, s);
-          s = fmaf(qs[8 * c + 2 * e + 1], f.y, s);
-        }
-      }
-      const int kv = k_lo + j;
-      x = s;
-      if constexpr (MOD == MOD_ALIBI) x = fmaf(slope2, float(kv), x);   // q_idx = 0
-      if constexpr (MOD == MOD_CHECKER) x += (kv & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;
-      if constexpr (MOD == MOD_CAUSAL) if (kv > 0) x = -INFINITY;
-      if (p.key_mask && p.key_mask[(size_t)b * p.Skv + kv] == 0) x = -INFINITY;
-    }
-  }
-  // ---- max over the 128 scores, exponentials, their sum
-  float M = x;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) redm[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(redm[0], redm[1]), fmaxf(redm[2], redm[3]));
-  const float Mu = (M == -INFINITY) ? 0.f : M;
-  const float pj = ex2(x - Mu);
-  sc_s[tid] = pj;
-  float ls = pj;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-  if (lane == 0) reds[warp] = ls;
-  __syncthreads();
-  // ---- o[d] = sum_j p_j v_jd: thread d over keys [0, 64), thread d + 64 over [64, 128)
-  {
-    const int d = tid & 63, part = tid >> 6;
+  for (int u = 0; u < DEC_U; ++u) {
+    const uint32_t w4[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
     float acc = 0.f;
-    const int j0 = part * 64, j1 = min(nk, j0 + 64);
-    for (int j = j0; j < j1; ++j) {
-      const uint16_t raw = vs[j * 64 + d];
-      float vf;
-      if constexpr (BF16)
-        vf = __uint_as_float(static_cast<uint32_t>(raw) << 16);
-      else
-        asm("cvt.f32.f16 %0, %1;" : "=f"(vf) : "h"(raw));
-      acc = fmaf(sc_s[j], vf, acc);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack2<BF16>(w4[e]);
+      acc = fmaf(qf[2 * e], f.x, acc);
+      acc = fmaf(qf[2 * e + 1], f.y, acc);
     }
-    if (part == 1) o_part[d] = acc;
-    __syncthreads();
-    float* mine = p.partial + ((size_t)bh * p.nsplit + split) * (2 + 64);
-    if (part == 0) {
-      mine[2 + d] = acc + o_part[d];
-      if (d == 0) {
-        mine[0] = M;
-        mine[1] = (reds[0] + reds[1]) + (reds[2] + reds[3]);
-      }
+    s[u] = acc;
+  }
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) {
+#pragma unroll
+    for (int u = 0; u < DEC_U; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < DEC_U; ++u) {
+    const int kv = kw + 4 * u + g;   // q_idx = 0
+    float x = s[u];
+    if constexpr (MOD == MOD_ALIBI) x = fmaf(slope2, float(kv), x);
+    if constexpr (MOD == MOD_CHECKER) x += (kv & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;
+    if constexpr (MOD == MOD_CAUSAL) x = kv > 0 ? -INFINITY : x;
+    x = ((keep >> u) & 1u) ? x : -INFINITY;
+    s[u] = x;
+    m = fmaxf(m, x);
+  }
+  // ---- exponentials and the p-weighted sum of V rows (this lane's 8 dims)
+  const float mu = (m == -INFINITY) ? 0.f : m;
+  float l = 0.f, o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
+#pragma unroll
+  for (int u = 0; u < DEC_U; ++u) {
+    const float pu = ex2(s[u] - mu);
+    l += pu;
+    const uint32_t w4[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack2<BF16>(w4[e]);
+      o[2 * e] = fmaf(pu, f.x, o[2 * e]);
+      o[2 * e + 1] = fmaf(pu, f.y, o[2 * e + 1]);
     }
   }
-  if (!ok && tid == 0 && p.status) atomicCAS(p.status, 0, kStatusTimeout | (41 << 8));
+  // ---- the four lane groups of the warp, then the four warps of the CTA
+  merge_xor(m, l, o, 8);
+  merge_xor(m, l, o, 16);
+  if (g == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sm_o[warp][8 * c + e] = o[e];
+    if (c == 0) {
+      sm_m[warp] = m;
+      sm_l[warp] = l;
+    }
+  }
+  __syncthreads();
+  if (tid < 64) {
+    float M = sm_m[0];
+#pragma unroll
+    for (int w = 1; w < DEC_WARPS; ++w) M = fmaxf(M, sm_m[w]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) {
+      const float a = ex2(sm_m[w] - Mu);
+      L = fmaf(sm_l[w], a, L);
+      O = fmaf(sm_o[w][tid], a, O);
+    }
+    float* mine = p.partial + ((size_t)bh * p.nsplit + split) * (2 + 64);
+    mine[2 + tid] = O;
+    if (tid == 0) {
+      mine[0] = M;
+      mine[1] = L;
+    }
+  }
   // ---- the last CTA of this (b, h) merges all splits
   __threadfence();
   __syncthreads();
@@ -160,25 +195,47 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecodeParams 
   __syncthreads();
   if (ticket != (unsigned)(p.nsplit - 1)) return;
   __threadfence();
-  if (tid < 64) {
-    const float* all = p.partial + (size_t)bh * p.nsplit * (2 + 64);
-    float Mx = -INFINITY;
-    for (int s = 0; s < p.nsplit; ++s) Mx = fmaxf(Mx, __ldcg(all + s * 66));
-    const float Mxu = (Mx == -INFINITY) ? 0.f : Mx;
-    float Lsum = 0.f, acc = 0.f;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float w = ex2(__ldcg(all + s * 66) - Mxu);
-      Lsum = fmaf(__ldcg(all + s * 66 + 1), w, Lsum);
-      acc = fmaf(__ldcg(all + s * 66 + 2 + tid), w, acc);
+  // max over the splits: threads stride over them, then a CTA reduction
+  const float* all = p.partial + (size_t)bh * p.nsplit * (2 + 64);
+  float Mx = -INFINITY;
+  for (int sidx = tid; sidx < p.nsplit; sidx += DEC_THREADS) Mx = fmaxf(Mx, __ldcg(all + (size_t)sidx * 66));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+  if (lane == 0) sm_m[warp] = Mx;
+  __syncthreads();
+  Mx = sm_m[0];
+#pragma unroll
+  for (int w = 1; w < DEC_WARPS; ++w) Mx = fmaxf(Mx, sm_m[w]);
+  const float Mxu = (Mx == -INFINITY) ? 0.f : Mx;
+  // thread (part, d) sums dimension d over the splits congruent to part mod 4
+  const int d = tid & 63, part = tid >> 6;
+  float Lsum = 0.f, acc = 0.f;
+  for (int sidx = part; sidx < p.nsplit; sidx += DEC_THREADS / 64) {
+    const float* ps = all + (size_t)sidx * 66;
+    const float w = ex2(__ldcg(ps) - Mxu);
+    Lsum = fmaf(__ldcg(ps + 1), w, Lsum);
+    acc = fmaf(__ldcg(ps + 2 + d), w, acc);
+  }
+  __syncthreads();   // sm_o and sm_l are reused below
+  if (part > 0) {
+    sm_o[part][d] = acc;
+    if (d == 0) sm_l[part] = Lsum;
+  }
+  __syncthreads();
+  if (part == 0) {
+#pragma unroll
+    for (int j = 1; j < DEC_THREADS / 64; ++j) {   // fixed order
+      acc += sm_o[j][d];
+      Lsum += sm_l[j];
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     const float val = acc * inv;
     const float nb = __shfl_down_sync(0xffffffffu, val, 1);
-    if ((tid & 1) == 0) {
-      uint32_t* op = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + (size_t)bh * 64 + tid);
+    if ((d & 1) == 0) {
+      uint32_t* op = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + (size_t)bh * 64 + d);
       *op = pack2<BF16>(val, nb);
     }
-    if (tid == 0) {
+    if (d == 0) {
       p.lse[bh] = Lsum > 0.f ? (Mxu + lg2(Lsum)) * kLn2 : -INFINITY;
       p.counter[bh] = 0u;   // re-arm for the next call
     }
@@ -187,7 +244,9 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(const DecodeParams 
 
 template <bool BF16>
 static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
-  dim3 grid(p.nsplit, p.B * p.H);
+  const long long n = (long long)p.nsplit * p.B * p.H;   // one CTA per (b, h, split), splits of a head adjacent
+  if (n > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)n;
   switch (p.mod) {
     case MOD_NONE: decode_kernel<BF16, MOD_NONE><<<grid, DEC_THREADS, 0, st>>>(p); break;
     case MOD_ALIBI: decode_kernel<BF16, MOD_ALIBI><<<grid, DEC_THREADS, 0, st>>>(p); break;

@@ -11,11 +11,13 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds kDecodeScratchBytes of it until the process exits.  Host code
-// cannot use the array's name as a device address, so the first call on each
-// device looks the address up with cudaGetSymbolAddress (with that device
-// current) and caches it.
+// cannot use the array's name as a device address, so each call looks the
+// address up with cudaGetSymbolAddress on the current device.  The first call
+// on a device also loads this library's device code there (set-up work that
+// belongs before any stream capture); later look-ups are cheap, and a fresh
+// look-up stays right after cudaDeviceReset or under another context, where a
+// remembered address would point at memory that is no longer mapped.
 #include <cmath>
-#include <mutex>
 
 #include "../../include/attn.h"
 #include "kernels.h"
@@ -23,25 +25,17 @@
 namespace {
 
 constexpr size_t kDecodeScratchBytes = size_t(4) << 20;   // 4 MiB per device
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBytes];
 
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the built-in scratch on the current device (looked up once per device).
+// Device address of the built-in scratch on the current device.
 attn_status scratch_address(void** addr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();
+    return ATTN_ERR_CUDA;
   }
-  *addr = g_scratch_addr[dev];
+  *addr = p;
   return ATTN_OK;
 }
 

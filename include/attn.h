@@ -211,9 +211,10 @@ attn_status attn_bwd_dq(const attn_shape* shape, const void* q, const void* k, c
                         attn_stream_t stream);
 
 /* Single-query decode (shape->Sq must be 1; q_idx = 0): split-KV partial
- * softmax per (b, h, split) streamed with 16-byte loads, combined in the same
- * launch by the last split to finish (flaxattention README "Decoding").
- * f16/bf16, D = 64. */
+ * softmax per (b, h, split of up to 128 keys), K and V streamed straight into
+ * registers with 16-byte loads, combined in the same launch by the last split
+ * to finish (flaxattention README "Decoding").  f16/bf16, D = 64.  The kernel
+ * has no device-side wait, so it has no timeout to report. */
 attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, const void* v,
                         const uint8_t* key_mask, attn_score_mod mod, float scale, void* out,
                         float* lse, void* ws, size_t ws_bytes, attn_stream_t stream);
@@ -230,9 +231,12 @@ attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, c
  *     library holds until the process exits.
  *   - Shapes whose scratch (B*H*nsplit*(D+2)*4 bytes of partials plus B*H*4
  *     bytes of tickets) exceeds 4 MiB are rejected with ATTN_ERR_WORKSPACE.
- *   - It runs on the CURRENT device; `stream` must belong to it.  The first
- *     call on each device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - It runs on the CURRENT device; `stream` must belong to it.  Every call
+ *     looks up the array's device address there (cudaGetSymbolAddress); the
+ *     first call on a device also loads the library's device code on it, so
+ *     make that first call before any stream capture.
+ *   - Like attn_decode, its kernel has no device-side wait, so there is no
+ *     timeout to report and no status word.
  *   - Every call on a device shares the one array.  Each call zeroes the
  *     tickets it uses (an asynchronous memset on `stream`) before its kernel.
  *     Calls that overlap in time on the GPU (other streams, other threads)
@@ -241,9 +245,6 @@ attn_status attn_decode_noalloc(const attn_shape* shape, const void* q, const vo
                                 const uint8_t* key_mask, attn_score_mod mod, float scale, void* out,
                                 float* lse, attn_stream_t stream);
 
-/* Synchronises `stream`, then reads and clears the workspace status word.
- * Returns ATTN_OK, ATTN_ERR_TIMEOUT (a device wait ran out), or
- * ATTN_ERR_CUDA (the stream reported an error). */
 /* Decode of a chunk of shape->Sq >= 1 queries against a KV cache of Skv keys
  * that already holds earlier tokens: query row i sits at position
  * q_offset + i, the position every score_mod uses (the causal rule keeps
@@ -296,6 +297,9 @@ attn_status attn_bwd_user(const attn_shape* shape, const void* q, const void* k,
                           const attn_block_mask* bm, float scale, void* dq, void* dk, void* dv, void* ws,
                           size_t ws_bytes, attn_stream_t stream);
 
+/* Synchronises `stream`, then reads and clears the workspace status word.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT (a device wait ran out), or
+ * ATTN_ERR_CUDA (the stream reported an error). */
 attn_status attn_poll_status(void* ws, attn_stream_t stream);
 
 /* Static text for a status code. */

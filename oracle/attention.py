@@ -397,8 +397,3 @@ def attn_fwd_online(q, k, v, key_mask=None, block_mask=None, score_mod=MOD_NONE,
                                              + np.log(np.where(dead, 1.0, l)))
     return o, lse
 
-
-def flops_fwd(B, H, Sq, Skv, D, causal=False):
-    """Counted forward FLOPs: 4 B H Sq Skv D, halved for causal."""
-    f = 4.0 * B * H * Sq * Skv * D
-    return f / 2 if causal else f

@@ -36,5 +36,5 @@ def test_stalled_wait_reports_timeout_and_context_survives(monkeypatch):
     out, lse = E.attn_fwd(d["q"], d["k"], d["v"], ws=ws)
     assert E.poll_status(ws) == E.ATTN_OK
     o_ref, l_ref = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]))
-    compare("out after recovery", f64(out), o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"])
-    compare("lse after recovery", f64(lse), l_ref, TOL["bf16"]["lse_max"])
+    compare("out after recovery", f64(out), o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"], dtype="bf16", kind="out")
+    compare("lse after recovery", f64(lse), l_ref, TOL["bf16"]["lse_max"], dtype="bf16", kind="lse")

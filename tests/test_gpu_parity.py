@@ -73,11 +73,12 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
                                  dense_mask=dn)
     sel = (slice(None),) if heads is None else tuple(np.array(x) for x in zip(*heads))
     tol = TOL[dtype]
-    compare("out", f64(out)[sel], o_ref[sel], tol["o_max"], tol["o_mean"], scaled=not strict)
+    compare("out", f64(out)[sel], o_ref[sel], tol["o_max"], tol["o_mean"], dtype=dtype, kind="out",
+            relative=not strict)
     lg, lr = f64(lse)[sel], lse_ref[sel]
     fin = np.isfinite(lr)
     assert (np.isneginf(lg) == np.isneginf(lr)).all(), "lse -inf pattern differs"
-    compare("lse", lg, lr, tol["lse_max"], mask=fin)
+    compare("lse", lg, lr, tol["lse_max"], mask=fin, dtype=dtype, kind="lse")
     # mask exactness: rows with no kept key are exactly zero
     dead = ~fin
     if dead.any():
@@ -90,7 +91,8 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
         for name, (buf, g), ref, shp in zip(("dq", "dk", "dv"), grads, (dq_r, dk_r, dv_r),
                                             ((B, H, Sq, D), (B, H, Skv, D), (B, H, Skv, D))):
             assert canary_ok(buf, shp), f"{name}: canary overwritten"
-            compare(name, f64(g)[sel], ref[sel], tol["g_max"], tol["g_mean"], scaled=not strict)
+            compare(name, f64(g)[sel], ref[sel], tol["g_max"], tol["g_mean"], dtype=dtype, kind="grad",
+                    relative=not strict)
     if check_det:
         out2, lse2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod,
                                 dense_mask=dm)
@@ -244,10 +246,10 @@ def test_decode_chunk(B, H, nq, Skv, dtype, mod, km, off):
     kmn = None if c["key_mask"] is None else c["key_mask"].numpy()
     o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=kmn, score_mod=mod, q_offset=off)
     tol = TOL[dtype]
-    compare("out", f64(out), o_ref, tol["o_max"], tol["o_mean"])
+    compare("out", f64(out), o_ref, tol["o_max"], tol["o_mean"], dtype=dtype, kind="out")
     fin = np.isfinite(l_ref)
     assert (np.isneginf(f64(lse)) == np.isneginf(l_ref)).all(), "lse -inf pattern differs"
-    compare("lse", f64(lse), l_ref, tol["lse_max"], mask=fin)
+    compare("lse", f64(lse), l_ref, tol["lse_max"], mask=fin, dtype=dtype, kind="lse")
     if (~fin).any():
         assert (f64(out)[~fin] == 0).all()
     out2, lse2 = E.attn_decode_chunk(d["q"], d["k"], d["v"], off, key_mask=d["key_mask"], score_mod=mod)
@@ -381,7 +383,7 @@ def test_user_score_mod_dropped_while_queued():
     gc.collect()
     torch.cuda.synchronize()
     o_ref, _ = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod=USER_MODS["relative"][1])
-    compare("out", f64(out), o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"], scaled=True)
+    compare("out", f64(out), o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"], dtype="bf16", kind="out")
 
 
 def test_fully_masked_batches_and_blocks():
@@ -428,9 +430,9 @@ def test_decode(mod, dtype, Skv, km):
     kmn = None if c["key_mask"] is None else c["key_mask"].numpy()
     o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=kmn, score_mod=mod)
     tol = TOL[dtype]
-    compare("decode out", f64(out), o_ref, tol["o_max"], tol["o_mean"])
+    compare("decode out", f64(out), o_ref, tol["o_max"], tol["o_mean"], dtype=dtype, kind="out")
     fin = np.isfinite(l_ref)
-    compare("decode lse", f64(lse), l_ref, tol["lse_max"], mask=fin)
+    compare("decode lse", f64(lse), l_ref, tol["lse_max"], mask=fin, dtype=dtype, kind="lse")
     assert (np.isneginf(f64(lse)) == ~fin).all()
 
 
@@ -442,8 +444,8 @@ def test_decode_workload_full_size():
     out2, lse2 = E.attn_decode(d["q"], d["k"], d["v"], score_mod=w.score_mod)
     assert torch.equal(out.view(torch.uint8), out2.view(torch.uint8)) and torch.equal(lse, lse2)
     o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod=w.score_mod)
-    compare("decode out", f64(out), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"])
-    compare("decode lse", f64(lse), l_ref, TOL["f16"]["lse_max"])
+    compare("decode out", f64(out), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+    compare("decode lse", f64(lse), l_ref, TOL["f16"]["lse_max"], dtype="f16", kind="lse")
 
 
 # ---------------------------------------------------------------- block-mask builder
@@ -497,8 +499,9 @@ def test_flash_attention_entry_points():
         out, lse = E.causal_flash_attention(d["q"][0, 0], d["k"][0, 0], d["v"][0, 0])
         assert out.shape == (S, D) and lse.shape == (S,)
         o_ref, l_ref = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod="causal")
-        compare("out", f64(out)[None, None], o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"])
-        compare("lse", f64(lse)[None, None], l_ref, TOL["bf16"]["lse_max"])
+        compare("out", f64(out)[None, None], o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"], dtype="bf16",
+                kind="out")
+        compare("lse", f64(lse)[None, None], l_ref, TOL["bf16"]["lse_max"], dtype="bf16", kind="lse")
 
 
 @pytest.mark.slow
@@ -517,8 +520,10 @@ def test_flash_attention_page_example_sampled_rows():
         q64 = f64(c["q"][:, h:h + 1])
         k64, v64 = f64(c["k"][:, h:h + 1]), f64(c["v"][:, h:h + 1])
         o_ref, l_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, rows=rows)
-        compare(f"out h{h}", f64(out[:, h:h + 1, rows]), o_ref[:, :, rows], tol["o_max"], tol["o_mean"])
-        compare(f"lse h{h}", f64(lse[:, h:h + 1, rows]), l_ref[:, :, rows], tol["lse_max"])
+        compare(f"out h{h}", f64(out[:, h:h + 1, rows]), o_ref[:, :, rows], tol["o_max"], tol["o_mean"],
+                dtype="bf16", kind="out")
+        compare(f"lse h{h}", f64(lse[:, h:h + 1, rows]), l_ref[:, :, rows], tol["lse_max"], dtype="bf16",
+                kind="lse")
 
 
 def test_d512_rectangular():
@@ -543,8 +548,10 @@ def test_long_context_d512_sampled_rows():
         k64, v64 = f64(c["k"][:, h:h + 1]), f64(c["v"][:, h:h + 1])
         # the oracle computes just these rows over all keys (q_idx = the sampled positions)
         o_ref, l_ref = _rows_oracle(q64, k64, v64, rows, obm)
-        compare(f"out h{h}", f64(out[:, h:h + 1, rows]), o_ref, tol["o_max"], tol["o_mean"])
-        compare(f"lse h{h}", f64(lse[:, h:h + 1, rows]), l_ref, tol["lse_max"])
+        compare(f"out h{h}", f64(out[:, h:h + 1, rows]), o_ref, tol["o_max"], tol["o_mean"], dtype="bf16",
+                kind="out")
+        compare(f"lse h{h}", f64(lse[:, h:h + 1, rows]), l_ref, tol["lse_max"], dtype="bf16",
+                kind="lse")
 
 
 def _rows_oracle(q_rows, k, v, rows, obm):
@@ -583,7 +590,7 @@ def run_two_pass(B, H, S, dtype, mod, km, bm_kind):
                        score_mod=mod)
     tol = TOL[dtype]
     for name, g, ref in zip(("dq", "dk", "dv"), g1, refs):
-        compare(name, f64(g), ref, tol["g_max"], tol["g_mean"], scaled=True)
+        compare(name, f64(g), ref, tol["g_max"], tol["g_mean"], dtype=dtype, kind="grad")
 
 
 @pytest.mark.parametrize("mod,km,bm", [("none", True, None), ("alibi", False, "causal"), ("checkerboard", True, None),
