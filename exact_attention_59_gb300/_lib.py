@@ -22,12 +22,13 @@ ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 4, 5
 ATTN_F32, ATTN_F16, ATTN_BF16 = 0, 1, 2
 OP_FWD, OP_BWD, OP_DECODE, OP_DECODE_CHUNK = 0, 1, 2, 3
 MODS = {"none": 0, "alibi": 1, "checkerboard": 2, "causal": 3}
-MASK_MODS = {"none": 0, "causal": 1}
+MASK_MODS = {"none": 0, "causal": 1, "user": 2}
 
 SYMBOLS = ("attn_workspace_size", "attn_build_block_mask", "attn_fwd", "attn_bwd", "attn_bwd_preprocess",
            "attn_bwd_dkdv", "attn_bwd_dq", "attn_decode", "attn_poll_status", "attn_status_string",
            "attn_dense_mask_bytes", "attn_pack_dense_mask", "attn_fwd_dense", "attn_bwd_dense",
-           "attn_decode_chunk", "attn_user_mod_create", "attn_user_mod_destroy", "attn_fwd_user", "attn_bwd_user")
+           "attn_decode_chunk", "attn_user_mod_create", "attn_user_mod_destroy", "attn_fwd_user", "attn_bwd_user",
+           "attn_user_mod_create_masked", "attn_build_block_mask_user")
 
 
 class AttnError(RuntimeError):
@@ -87,6 +88,9 @@ def load():
             "attn_decode_chunk": (I, [sp, P, P, P, P, I, F, I, P, P, P, SZ, P]),
             "attn_user_mod_create": (I, [ctypes.c_char_p, I, ctypes.POINTER(P), ctypes.c_char_p, SZ]),
             "attn_user_mod_destroy": (None, [P]),
+            "attn_user_mod_create_masked": (I, [ctypes.c_char_p, ctypes.c_char_p, I, ctypes.POINTER(P),
+                                                ctypes.c_char_p, SZ]),
+            "attn_build_block_mask_user": (I, [P, I, I, I, I, I, I, P, P]),
             "attn_fwd_user": (I, [sp, P, P, P, P, P, bp, F, P, P, P, SZ, P, P]),
             "attn_bwd_user": (I, [sp, P, P, P, P, P, P, P, P, bp, F, P, P, P, P, SZ, P]),
         }
@@ -171,7 +175,18 @@ class BlockMask:
 
 
 def create_block_mask(mask_mod, B, H, Sq, Skv, device="cuda", block_q=128, block_kv=128) -> BlockMask:
-    """Tile states built on the device by attn_build_block_mask."""
+    """Tile states built on the device: attn_build_block_mask for a built-in
+    mask_mod ("none", "causal"), attn_build_block_mask_user for a UserScoreMod
+    compiled with a mask expression (its tiles go with that mod's calls)."""
+    if isinstance(mask_mod, UserScoreMod):
+        if not mask_mod.mask_expr:
+            raise ValueError("this user mod has no mask expression")
+        tiles = torch.empty((B, H, -(-Sq // block_q), -(-Skv // block_kv)), dtype=torch.uint8, device=device)
+        _check(load().attn_build_block_mask_user(mask_mod.handle, B, H, Sq, Skv, block_q, block_kv, _ptr(tiles),
+                                                 _stream(tiles.device)), "attn_build_block_mask_user")
+        bm = BlockMask(tiles, MASK_MODS["user"], block_q, block_kv)
+        bm.user_mod = mask_mod
+        return bm
     mm = MASK_MODS[mask_mod] if isinstance(mask_mod, str) else int(mask_mod)
     tiles = torch.empty((B, H, -(-Sq // block_q), -(-Skv // block_kv)), dtype=torch.uint8, device=device)
     _check(load().attn_build_block_mask(mm, B, H, Sq, Skv, block_q, block_kv, _ptr(tiles), _stream(tiles.device)),
@@ -219,19 +234,23 @@ def _dm(dm):
 class UserScoreMod:
     """A score_mod compiled at run time: score + bias, where ``bias_expr`` is a C
     expression in the int variables b, h, q, kv (q and kv are positions) that
-    gives a float, or -INFINITY to mask the pair.  Built for one 16-bit dtype."""
+    gives a float, or -INFINITY to mask the pair; optionally with a mask_mod,
+    ``mask_expr``, a C expression in the same variables, nonzero = keep, whose
+    block mask (create_block_mask(mod, ...)) skips the tiles it empties.  Built
+    for one 16-bit dtype."""
 
-    def __init__(self, bias_expr: str, dtype=torch.bfloat16):
-        self.bias_expr = bias_expr
+    def __init__(self, bias_expr: str | None, dtype=torch.bfloat16, mask_expr: str | None = None):
+        self.bias_expr = bias_expr or ""
+        self.mask_expr = mask_expr or ""
         self.dtype = dtype
         self.log = ""
         self._h = ctypes.c_void_p()
         buf = ctypes.create_string_buffer(1 << 16)
-        code = load().attn_user_mod_create(bias_expr.encode(), _dtype_id(dtype), ctypes.byref(self._h), buf,
-                                           len(buf))
+        code = load().attn_user_mod_create_masked(self.bias_expr.encode(), self.mask_expr.encode(), _dtype_id(dtype),
+                                                  ctypes.byref(self._h), buf, len(buf))
         self.log = buf.value.decode(errors="replace")
         if code != ATTN_OK:
-            raise AttnError(code, "attn_user_mod_create: " + self.log.strip()[:2000])
+            raise AttnError(code, "attn_user_mod_create_masked: " + self.log.strip()[:2000])
 
     @property
     def handle(self):
@@ -246,6 +265,14 @@ class UserScoreMod:
 def compile_score_mod(bias_expr: str, dtype=torch.bfloat16) -> UserScoreMod:
     """Compiles ``bias_expr`` (see UserScoreMod) into the D = 64 kernels for ``dtype``."""
     return UserScoreMod(bias_expr, dtype)
+
+
+def compile_mask_mod(mask_expr: str, bias_expr: str | None = None, dtype=torch.bfloat16) -> UserScoreMod:
+    """Compiles a mask_mod ``mask_expr`` (nonzero = keep; see UserScoreMod), with an
+    optional additive ``bias_expr``, into the D = 64 kernels and a block-mask
+    builder for ``dtype``.  Use it as the score_mod of the calls and build their
+    block mask with create_block_mask(mod, B, H, Sq, Skv)."""
+    return UserScoreMod(bias_expr, dtype, mask_expr=mask_expr)
 
 
 def _mod(m) -> int:

@@ -88,15 +88,27 @@ DecodeSplit decode_split(const attn_shape* s) {
 // 128-row tiles covering n rows (the last one may be partial)
 int tiles_of(int n) { return (n + 127) / 128; }
 
+// Streaming multiprocessors of the current device (152 on a GB300; the same
+// number is assumed when no device can be queried, e.g. for a size query on a
+// machine without a GPU).
+long long sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0) {
+    (void)cudaGetLastError();   // leave no stale error for a later launch check
+    return 152;
+  }
+  return n;
+}
+
 // Split of a query chunk's kv blocks over CTAs: about one CTA per SM in total
-// (152 SMs; the forward kernel runs one CTA per SM), at least one kv block each.
+// (the forward kernel runs one CTA per SM), at least one kv block each.
 struct ChunkSplit {
   int nsplit, kps;
 };
-constexpr long long kSms = 152;
 ChunkSplit chunk_split(const attn_shape* s) {
   const long long nkb = tiles_of(s->Skv), items = (long long)s->B * s->H * ((tiles_of(s->Sq) + 1) / 2);
-  int ns = (int)std::max<long long>(1, std::min<long long>(nkb, kSms / std::max<long long>(1, items)));
+  int ns = (int)std::max<long long>(1, std::min<long long>(nkb, sm_count() / std::max<long long>(1, items)));
   const int kps = (int)((nkb + ns - 1) / ns);
   ns = (int)((nkb + kps - 1) / kps);
   return {ns, kps};
@@ -127,7 +139,7 @@ WsLayout layout(attn_op op, const attn_shape* s) {
     // partial rows of the split: sized for min(max(items, SMs), items * nkb) CTAs,
     // a bound on items * nsplit that grows with every dimension of the shape
     const long long items = (long long)BH * ((tiles_of(s->Sq) + 1) / 2), nkb = tiles_of(s->Skv);
-    const long long ctas = std::min(std::max(items, kSms), items * nkb);
+    const long long ctas = std::min(std::max(items, sm_count()), items * nkb);
     w.partial = off;
     off = align256(off + (size_t)ctas * 256 * FWD_PART * 4);
   }
@@ -150,21 +162,41 @@ attn_status check_prefill(const attn_shape* s, bool backward) {
   const bool ragged_ok = s->D == 64 && s->dtype != ATTN_F32;
   if (!ragged_ok && (s->Sq % 128 != 0 || s->Skv % 128 != 0)) return ATTN_ERR_SHAPE;
   if (tiles_of(s->Skv) > FWD_MAXKB || tiles_of(s->Sq) > FWD_MAXKB) return ATTN_ERR_SHAPE;
+  (void)backward;   // D = 512 has a forward and a backward, f16/bf16
   if (s->D == 64) return ATTN_OK;
-  if (s->D == 512 && !backward && s->dtype != ATTN_F32) return ATTN_OK;
+  if (s->D == 512 && s->dtype != ATTN_F32) return ATTN_OK;
   return ATTN_ERR_UNSUPPORTED;
 }
 
+// Whether the ALiBi / checkerboard bias rides on the score products (three 16-bit
+// terms of bias / scale in one more K = 16 MMA step): needs scale != 0 and a
+// term of at most 2^12, where the f32 sum of S and the term keeps S to about
+// 2^-11 of its scale-free units (1/sqrt(D) scales give 4 for the checkerboard
+// and 2^(-8/H) 127 / scale <= 1016 for ALiBi at D <= 64).  Otherwise the
+// kernels add the bias per score.
+int mod_fold_ok(attn_score_mod mod, float scale, int H) {
+  if (scale == 0.f || !std::isfinite(scale)) return 0;
+  const float inv = 1.f / std::fabs(scale);
+  if (mod == ATTN_MOD_CHECKERBOARD) return 0.5f * inv <= 4096.f ? 1 : 0;
+  if (mod == ATTN_MOD_ALIBI) return std::exp2(-8.0f / float(H)) * 127.f * inv <= 4096.f ? 1 : 0;
+  return 0;
+}
+
+// The scale must be finite and nonzero: the D = 64 kernels carry masks and the
+// dK/dV pass's -lse / scale as terms of their score products, which the scale
+// multiplies afterwards (the pages' scale is 1/sqrt(D), never 0).
 attn_status check_mod(attn_score_mod mod, float scale) {
   if ((int)mod < 0 || (int)mod > 3) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale == 0.f) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
-attn_status check_bm(const attn_block_mask* bm) {
+// A block mask; mask_mod ATTN_MASKMOD_USER only with a user mod that has a mask
+// expression (`user_mask`).
+attn_status check_bm(const attn_block_mask* bm, bool user_mask = false) {
   if (!bm) return ATTN_OK;
   if (!bm->tiles) return ATTN_ERR_INVALID_ARG;
-  if ((int)bm->mask_mod < 0 || (int)bm->mask_mod > 1) return ATTN_ERR_INVALID_ARG;
+  if ((int)bm->mask_mod < 0 || (int)bm->mask_mod > (user_mask ? 2 : 1)) return ATTN_ERR_INVALID_ARG;
   if (bm->block_q != 128 || bm->block_kv != 128) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -234,6 +266,8 @@ BwdParams bwd_params(const attn_shape* s, const void* q, const void* k, const vo
   p.sc = scale * kLog2e;
   p.scale = scale;
   p.timeout_ns = timeout_ns();
+  p.fold = mod_fold_ok(mod, scale, s->H);
+  p.inv_scale = scale != 0.f ? 1.f / scale : 0.f;
   return p;
 }
 
@@ -335,13 +369,10 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
                             uint8_t* debug_visited, attn_user_mod um) {
   ATTN_TRY(check_prefill(s, false));
   ATTN_TRY(check_mod(mod, scale));
-  ATTN_TRY(check_bm(bm));
+  ATTN_TRY(check_bm(bm, um && user_mod_has_mask(um)));
   ATTN_TRY(check_dm(s, dm));
-  const void* uk[3] = {nullptr, nullptr, nullptr};
-  if (um) {   // the user kernels: D = 64, the 16-bit dtype they were built for, no dense mask
-    if (s->D != 64 || s->dtype == ATTN_F32 || dm) return ATTN_ERR_UNSUPPORTED;
-    ATTN_TRY(user_mod_kernels(um, s->dtype, uk));
-  }
+  // the user kernels: D = 64, the 16-bit dtype they were built for, no dense mask
+  if (um && (s->D != 64 || s->dtype == ATTN_F32 || dm)) return ATTN_ERR_UNSUPPORTED;
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -349,6 +380,8 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   ATTN_PTR(lse);
   ATTN_OPT_PTR(key_mask);
   ATTN_TRY(check_ws(ATTN_OP_FWD, s, ws, ws_bytes));
+  const void* uk[3] = {nullptr, nullptr, nullptr};
+  if (um) ATTN_TRY(user_mod_kernels(um, s->dtype, uk));   // loads the mod's code on this device (first use)
   cudaStream_t st = (cudaStream_t)stream;
   if (s->D == 512) {
     FwdBigParams p;
@@ -413,6 +446,8 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   p.sc = scale * kLog2e;
   p.timeout_ns = timeout_ns();
   p.inject_stall = inject_stall();
+  p.fold = um ? 0 : mod_fold_ok(mod, scale, s->H);
+  p.inv_scale = scale != 0.f ? 1.f / scale : 0.f;
   p.nsplit = 1;   // whole kv range per CTA, q_off = 0
   if (um) return cuda_status(launch_fwd_d64_kernel(p, uk[0], st));
   return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
@@ -456,11 +491,11 @@ namespace {
 attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
                           const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
                           attn_score_mod mod, float scale, void* dk, void* dv, void* ws, size_t ws_bytes,
-                          attn_stream_t stream, const void* ukern = nullptr) {
+                          attn_stream_t stream, const void* ukern = nullptr, bool user_mask = false) {
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_dm(s, dm));
   ATTN_TRY(check_mod(mod, scale));
-  ATTN_TRY(check_bm(bm));
+  ATTN_TRY(check_bm(bm, user_mask));
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -487,17 +522,18 @@ attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, con
   p.dv = dv;
   p.dm = dm_view(s, dm);
   if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, true, st));
+  if (s->D == 512) return cuda_status(launch_bwd512_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
   return cuda_status(launch_bwd_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
 attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const void* v, const void* dout,
                         const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
                         attn_score_mod mod, float scale, void* dq, void* ws, size_t ws_bytes, attn_stream_t stream,
-                        const void* ukern = nullptr) {
+                        const void* ukern = nullptr, bool user_mask = false) {
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_dm(s, dm));
   ATTN_TRY(check_mod(mod, scale));
-  ATTN_TRY(check_bm(bm));
+  ATTN_TRY(check_bm(bm, user_mask));
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -521,6 +557,7 @@ attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const
   p.dq = dq;
   p.dm = dm_view(s, dm);
   if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, false, st));
+  if (s->D == 512) return cuda_status(launch_bwd512_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
   return cuda_status(launch_bwd_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 
@@ -554,15 +591,12 @@ static attn_status bwd_all(const attn_shape* s, const void* q, const void* k, co
                            const attn_block_mask* bm, attn_score_mod mod, float scale, void* dq, void* dk, void* dv,
                            void* ws, size_t ws_bytes, attn_stream_t stream, attn_user_mod um) {
   // validate everything before the first launch
+  const bool umask = um && user_mod_has_mask(um);
   ATTN_TRY(check_prefill(s, true));
   ATTN_TRY(check_mod(mod, scale));
-  ATTN_TRY(check_bm(bm));
+  ATTN_TRY(check_bm(bm, umask));
   ATTN_TRY(check_dm(s, dm));
-  const void* uk[3] = {nullptr, nullptr, nullptr};
-  if (um) {
-    if (s->D != 64 || s->dtype == ATTN_F32 || dm) return ATTN_ERR_UNSUPPORTED;
-    ATTN_TRY(user_mod_kernels(um, s->dtype, uk));
-  }
+  if (um && (s->D != 64 || s->dtype == ATTN_F32 || dm)) return ATTN_ERR_UNSUPPORTED;
   ATTN_PTR(q);
   ATTN_PTR(k);
   ATTN_PTR(v);
@@ -574,9 +608,11 @@ static attn_status bwd_all(const attn_shape* s, const void* q, const void* k, co
   ATTN_PTR(dv);
   ATTN_OPT_PTR(key_mask);
   ATTN_TRY(check_ws(ATTN_OP_BWD, s, ws, ws_bytes));
+  const void* uk[3] = {nullptr, nullptr, nullptr};
+  if (um) ATTN_TRY(user_mod_kernels(um, s->dtype, uk));   // loads the mod's code on this device (first use)
   ATTN_TRY(attn_bwd_preprocess(s, out, lse, dout, key_mask, ws, ws_bytes, stream));
-  ATTN_TRY(bwd_dkdv_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dk, dv, ws, ws_bytes, stream, uk[1]));
-  return bwd_dq_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dq, ws, ws_bytes, stream, uk[2]);
+  ATTN_TRY(bwd_dkdv_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dk, dv, ws, ws_bytes, stream, uk[1], umask));
+  return bwd_dq_impl(s, q, k, v, dout, key_mask, dm, bm, mod, scale, dq, ws, ws_bytes, stream, uk[2], umask);
 }
 
 attn_status attn_bwd_dense(const attn_shape* s, const void* q, const void* k, const void* v, const void* out,
@@ -641,7 +677,6 @@ attn_status attn_decode(const attn_shape* s, const void* q, const void* k, const
   p.key_mask = key_mask;
   p.partial = at<float>(ws, w.partial);
   p.counter = at<unsigned>(ws, w.counter);
-  p.status = at<int>(ws, 0);
   p.B = s->B;
   p.H = s->H;
   p.Skv = s->Skv;
@@ -691,6 +726,8 @@ attn_status attn_decode_chunk(const attn_shape* s, const void* q, const void* k,
   p.sc = scale * kLog2e;
   p.timeout_ns = timeout_ns();
   p.q_off = q_offset;
+  p.fold = mod_fold_ok(mod, scale, s->H);
+  p.inv_scale = scale != 0.f ? 1.f / scale : 0.f;
   p.nsplit = cs.nsplit;
   p.kps = cs.kps;
   p.part = cs.nsplit > 1 ? at<float>(ws, w.partial) : nullptr;

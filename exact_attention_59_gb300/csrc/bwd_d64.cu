@@ -54,7 +54,9 @@ struct __align__(1024) DkdvSmem {
   // Column terms folded into the score products as one more K = 16 step:
   // ones holds (1, 1, 2048) in k = 0..2 for every kv row; qaug[s] / daug[s] hold,
   // per q row, -lse log2(e) / (scale log2(e)) and -D split as t0 + t1 + 2048 t2
-  // (16-bit each; no swizzle, 4 KB per 128 x 16 operand).
+  // (16-bit each; no swizzle, 4 KB per 128 x 16 operand).  With a folded
+  // ALiBi / checkerboard bias, columns AUG_BMOD.. and AUG_MOD2.. of ones and of
+  // every qaug[s] carry it too (constant over the q blocks; daug's stay 0).
   __align__(128) uint8_t ones[4096];
   __align__(128) uint8_t qaug[DKDV_NST][4096];
   __align__(128) uint8_t daug[DKDV_NST][4096];
@@ -137,15 +139,52 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
   }
+  // With `fold`, the ALiBi / checkerboard bias over scale rides on S^T = K Q^T
+  // (rows = keys, columns = queries), as three 16-bit terms per part:
+  //   checkerboard  ones: (-1)^r  x  qaug: (-1)^c t_i          (t = 0.5 / scale)
+  //   ALiBi         ones: t_i(r)  x  qaug: 1                   (t(r) = slope_h r / scale)
+  //                 ones: 1       x  qaug: t_i(-c)             (t(-c) = -slope_h c / scale)
+  // r = key row of the block, c = query column of a q block (both blocks start at
+  // multiples of 128, so parities are those of r and c); ALiBi's remaining
+  // slope_h (kv0 - q0) is one constant per (kv block, q block).
+  constexpr bool kModTerm = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
+  const bool fold = kModTerm && p.fold;
   {
     uint4* z = reinterpret_cast<uint4*>(sm.ones);
     for (int i = tid; i < (int)((1 + 2 * DKDV_NST) * 4096 / 16); i += BWD_T) z[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     if (tid < 128) {
+      const int r = tid;
       const uint16_t one = to16<BF16>(1.f), big = to16<BF16>(2048.f);
-      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(tid, 0)) = one;
-      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(tid, 1)) = one;
-      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(tid, 2)) = big;
+      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(r, 0)) = one;
+      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(r, 1)) = one;
+      *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(r, 2)) = big;
+      if (fold) {
+        uint16_t a3[3], b3[3];      // columns AUG_BMOD..: key side, query side
+        uint16_t a3b[3], b3b[3];    // columns AUG_MOD2.. (ALiBi only)
+        if constexpr (MOD == MOD_CHECKER) {
+          uint16_t t[3];
+          split3_plain<BF16>(0.5f * p.inv_scale, t);
+          for (int i = 0; i < 3; ++i) {
+            a3[i] = (r & 1) ? to16<BF16>(-1.f) : one;
+            b3[i] = (r & 1) ? uint16_t(t[i] ^ 0x8000u) : t[i];   // r as the query column here
+            a3b[i] = b3b[i] = 0;
+          }
+        } else {
+          const float slope = exp2f(-8.0f * float(h + 1) / float(p.H));
+          split3_plain<BF16>(slope * float(r) * p.inv_scale, a3);
+          split3_plain<BF16>(-slope * float(r) * p.inv_scale, b3b);
+          for (int i = 0; i < 3; ++i) b3[i] = a3b[i] = one;
+        }
+        for (int i = 0; i < 3; ++i) {
+          *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(r, AUG_BMOD + i)) = a3[i];
+          *reinterpret_cast<uint16_t*>(sm.ones + k16_offset(r, AUG_MOD2 + i)) = a3b[i];
+          for (int st = 0; st < DKDV_NST; ++st) {
+            *reinterpret_cast<uint16_t*>(sm.qaug[st] + k16_offset(r, AUG_BMOD + i)) = b3[i];
+            *reinterpret_cast<uint16_t*>(sm.qaug[st] + k16_offset(r, AUG_MOD2 + i)) = b3b[i];
+          }
+        }
+      }
     }
     fence_async_smem();   // generic-proxy writes, read by the tensor core
   }
@@ -186,11 +225,12 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
           const float4 nd = __ldg(reinterpret_cast<const float4*>(p.delta + row) + lane);
           xl[0] = nl.x * inv_sc; xl[1] = nl.y * inv_sc; xl[2] = nl.z * inv_sc; xl[3] = nl.w * inv_sc;
           xd[0] = nd.x; xd[1] = nd.y; xd[2] = nd.z; xd[3] = nd.w;
-        } else {   // rows past Sq (partial last q block) get P = 0
+        } else {   // rows past Sq (partial last q block) get P = 0: the infinity that the scale turns into -inf
+          const float pad = p.sc < 0.f ? INFINITY : -INFINITY;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const bool in = qb * 128 + 4 * lane + i < p.Sq;
-            xl[i] = in ? __ldg(p.lse2 + row + 4 * lane + i) * inv_sc : -INFINITY;
+            xl[i] = in ? __ldg(p.lse2 + row + 4 * lane + i) * inv_sc : pad;
             xd[i] = in ? __ldg(p.delta + row + 4 * lane + i) : 0.f;
           }
         }
@@ -311,6 +351,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       const int q0 = qb * 128 + 64 * w;   // first query of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+      const bool umask = MOD == MOD_USER && (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
       // this key's dense-mask bits for the half's 64 queries (column words)
       bool dense = false;
       uint2 dwv = make_uint2(0u, 0u);
@@ -334,23 +375,32 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
         chk = f2(hb, -hb);
       }
       const float abase = (MOD == MOD_ALIBI) ? slope2 * float(kv - q0) : 0.f;
+      // with the bias folded into S^T, one constant per (kv block, q block) is left
+      const float fb = (MOD == MOD_ALIBI) ? slope2 * float(kb * 128 - qb * 128) : 0.f;
+      const uint64_t fbv = f2(fb, fb);
       float pr[64];
       uint32_t pk[32];
       // one straight-line copy per causal/not: no runtime test inside the unrolled loop
-      auto probs = [&](auto causal_c, auto dense_c) {
+      auto probs = [&](auto causal_c, auto dense_c, auto fold_c) {
         constexpr bool CAUSAL = decltype(causal_c)::value;
         constexpr bool DENSE = decltype(dense_c)::value;
+        constexpr bool FOLD = decltype(fold_c)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          uint64_t xv = fmul2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv);
-          if constexpr (MOD == MOD_CHECKER) xv = fadd2(xv, chk);
-          if constexpr (MOD == MOD_ALIBI)
+          const uint64_t sv = f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+          uint64_t xv = FOLD ? ffma2(sv, scv, fbv) : fmul2(sv, scv);
+          if constexpr (MOD == MOD_CHECKER && !FOLD) xv = fadd2(xv, chk);
+          if constexpr (MOD == MOD_ALIBI && !FOLD)
             xv = fadd2(xv, f2(fmaf(-slope2, float(2 * i), abase), fmaf(-slope2, float(2 * i + 1), abase)));
           float x0, x1;
           unf2(xv, x0, x1);
           if constexpr (MOD == MOD_USER) {
             x0 = fmaf(user_bias(b, h, q0 + 2 * i, kv), kLog2e, x0);
             x1 = fmaf(user_bias(b, h, q0 + 2 * i + 1, kv), kLog2e, x1);
+            if (umask) {   // a PARTIAL tile of a user mask_mod's block mask
+              x0 = user_keep(b, h, q0 + 2 * i, kv) ? x0 : -INFINITY;
+              x1 = user_keep(b, h, q0 + 2 * i + 1, kv) ? x1 : -INFINITY;
+            }
           }
           if (CAUSAL) {
             x0 = kv > q0 + 2 * i ? -INFINITY : x0;
@@ -367,14 +417,22 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
           pk[i] = pack2<BF16>(p0, p1);
         }
       };
-      if (dense) {   // never with DM = false
-        if constexpr (DM) {
-          if (causal) probs(bconst<true>{}, bconst<true>{});
-          else probs(bconst<false>{}, bconst<true>{});
+      auto probs_any = [&](auto fold_c) {
+        if (dense) {   // never with DM = false
+          if constexpr (DM) {
+            if (causal) probs(bconst<true>{}, bconst<true>{}, fold_c);
+            else probs(bconst<false>{}, bconst<true>{}, fold_c);
+          }
+        } else {
+          if (causal) probs(bconst<true>{}, bconst<false>{}, fold_c);
+          else probs(bconst<false>{}, bconst<false>{}, fold_c);
         }
+      };
+      if constexpr (kModTerm) {
+        if (fold) probs_any(bconst<true>{});
+        else probs_any(bconst<false>{});
       } else {
-        if (causal) probs(bconst<true>{}, bconst<false>{});
-        else probs(bconst<false>{}, bconst<false>{});
+        probs_any(bconst<false>{});
       }
       // dV(u-1) has finished reading the P^T region
       if (u > 0) {
@@ -450,9 +508,9 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
 struct __align__(1024) DqSmem {
   uint8_t q[BWD_TILE], dO[BWD_TILE];
   uint8_t k[BWD_NST][BWD_TILE], v[BWD_NST][BWD_TILE];
-  // Key-padding bias folded into S = Q K^T as one more K = 16 step: qaug has a
-  // column of ones, kaug[s] a column holding 0 or -inf per key (K = 16 operands
-  // without swizzle, 4 KB each).
+  // Column terms folded into S = Q K^T as one more K = 16 step, as in the
+  // forward (columns AUG_MOD / AUG_KEY): qaug per query row (resident), kaug[s]
+  // per key of stage s (K = 16 operands without swizzle, 4 KB each).
   __align__(128) uint8_t qaug[4096];
   __align__(128) uint8_t kaug[BWD_NST][4096];
   uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, dsready, dqdone, fin, done;
@@ -531,13 +589,41 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
   }
-  const bool aug = p.km_bits != nullptr;
+  // The key-padding mask and (with `fold`) the ALiBi / checkerboard bias ride on
+  // the S product, with the operands of the forward (fwd_d64.cu): checkerboard
+  // (-1)^q t_i x (-1)^c, ALiBi 1 x t_i(c), t = bias / scale in three 16-bit
+  // terms; ALiBi's slope_h (kv0 - q) is a per-row constant of each block.
+  constexpr bool kModTerm = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
+  const bool fold = kModTerm && p.fold;
+  const bool aug = fold || p.km_bits != nullptr;
   if (aug) {
-    const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
     uint4* z = reinterpret_cast<uint4*>(sm.qaug);
     for (int i = tid; i < (int)((1 + BWD_NST) * 4096 / 16); i += BWD_T) z[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    if (tid < 128) *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(tid, 0)) = static_cast<uint16_t>(one);
+    if (tid < 128) {
+      const int r = tid;   // query row of the block, and key column of a kv block
+      const uint16_t one = to16<BF16>(1.f);
+      *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_KEY)) = one;
+      if (fold) {
+        uint16_t qt3[3], kt3[3];
+        if constexpr (MOD == MOD_CHECKER) {
+          uint16_t t[3];
+          split3_plain<BF16>(0.5f * p.inv_scale, t);
+          for (int i = 0; i < 3; ++i) {
+            qt3[i] = (r & 1) ? uint16_t(t[i] ^ 0x8000u) : t[i];   // q block starts at a multiple of 128
+            kt3[i] = (r & 1) ? to16<BF16>(-1.f) : one;
+          }
+        } else {
+          split3_plain<BF16>(exp2f(-8.0f * float(h + 1) / float(p.H)) * float(r) * p.inv_scale, kt3);
+          for (int i = 0; i < 3; ++i) qt3[i] = one;
+        }
+        for (int i = 0; i < 3; ++i) {
+          *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_MOD + i)) = qt3[i];
+          for (int st = 0; st < BWD_NST; ++st)
+            *reinterpret_cast<uint16_t*>(sm.kaug[st] + k16_offset(r, AUG_MOD + i)) = kt3[i];
+        }
+      }
+    }
     fence_async_smem();   // generic-proxy writes, read by the tensor core
   }
   tc_fence_before();
@@ -561,15 +647,17 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         const int s = u % BWD_NST;
         if (u >= BWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
         const int kb = sm.list[u];
-        if (aug) {   // lane owns keys 4 lane .. 4 lane + 3: column 0 of kaug[s]
+        if (aug && p.km_bits) {   // lane owns keys 4 lane .. 4 lane + 3: column AUG_KEY of kaug[s]
           uint32_t bits = 0xffffffffu;
           if (sm.lflags[u] & KB_KEYMASK)
             bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
-          const uint16_t ninf = BF16 ? 0xFF80u : 0xFC00u;
+          // the infinity whose product with the scale is -inf (scale != 0)
+          const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int col = 4 * lane + i;
-            *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, 0)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+            *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, AUG_KEY)) =
+                ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
           }
           fence_async_smem();
         }
@@ -672,6 +760,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       const int k0 = kb * 128 + 64 * w;   // first key of this half
       const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
                           ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+      const bool umask = MOD == MOD_USER && (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
       // keep column cc of this half iff cc <= lim: the causal limit and, in a
       // partial last kv block, the end of the keys
       const int kvl = p.Skv - 1 - k0;
@@ -700,22 +789,30 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         chk = f2(hb, -hb);
       }
       const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
+      // with the bias folded into S, all that is left per pair is this row's constant
+      const float fb = (MOD == MOD_ALIBI) ? slope2 * float(kb * 128 - q) : 0.f;
+      const uint64_t addf = fadd2(nl2v, f2(fb, fb));
       float pr[64];
       // one straight-line copy per causal/not: no runtime test inside the unrolled loop
-      auto probs = [&](auto causal_c, auto dense_c) {
+      auto probs = [&](auto causal_c, auto dense_c, auto fold_c) {
         constexpr bool CAUSAL = decltype(causal_c)::value;
         constexpr bool DENSE = decltype(dense_c)::value;
+        constexpr bool FOLD = decltype(fold_c)::value;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          uint64_t add = nl2v;
-          if constexpr (MOD == MOD_CHECKER) add = fadd2(add, chk);
-          if constexpr (MOD == MOD_ALIBI)
+          uint64_t add = FOLD ? addf : nl2v;
+          if constexpr (MOD == MOD_CHECKER && !FOLD) add = fadd2(add, chk);
+          if constexpr (MOD == MOD_ALIBI && !FOLD)
             add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
           float x0, x1;
           unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
           if constexpr (MOD == MOD_USER) {
             x0 = fmaf(user_bias(b, h, q, k0 + 2 * i), kLog2e, x0);
             x1 = fmaf(user_bias(b, h, q, k0 + 2 * i + 1), kLog2e, x1);
+            if (umask) {   // a PARTIAL tile of a user mask_mod's block mask
+              x0 = user_keep(b, h, q, k0 + 2 * i) ? x0 : -INFINITY;
+              x1 = user_keep(b, h, q, k0 + 2 * i + 1) ? x1 : -INFINITY;
+            }
           }
           if (CAUSAL) {
             x0 = 2 * i > lim ? -INFINITY : x0;
@@ -730,12 +827,20 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
           pr[2 * i + 1] = ex2(x1);
         }
       };
-      if (dense) {   // with dense bits, the limited copy too (never with DM = false)
-        if constexpr (DM) probs(bconst<true>{}, bconst<true>{});
-      } else if (limited) {
-        probs(bconst<true>{}, bconst<false>{});
+      auto probs_any = [&](auto fold_c) {
+        if (dense) {   // with dense bits, the limited copy too (never with DM = false)
+          if constexpr (DM) probs(bconst<true>{}, bconst<true>{}, fold_c);
+        } else if (limited) {
+          probs(bconst<true>{}, bconst<false>{}, fold_c);
+        } else {
+          probs(bconst<false>{}, bconst<false>{}, fold_c);
+        }
+      };
+      if constexpr (kModTerm) {
+        if (fold) probs_any(bconst<true>{});
+        else probs_any(bconst<false>{});
       } else {
-        probs(bconst<false>{}, bconst<false>{});
+        probs_any(bconst<false>{});
       }
       if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
       tc_fence_after();

@@ -17,7 +17,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // score_mod ids (same values as attn_score_mod in attn.h); MOD_USER is a
 // score_mod compiled at run time: score + user_bias(b, h, q_idx, kv_idx)
 constexpr int MOD_NONE = 0, MOD_ALIBI = 1, MOD_CHECKER = 2, MOD_CAUSAL = 3, MOD_USER = 4;
-constexpr int MASKMOD_NONE = 0, MASKMOD_CAUSAL = 1;
+constexpr int MASKMOD_NONE = 0, MASKMOD_CAUSAL = 1, MASKMOD_USER = 2;
 constexpr int TILE_EMPTY = 0, TILE_PARTIAL = 1, TILE_FULL = 2;
 
 // The user's bias expression, in the variables b, h, q (the query position) and
@@ -28,12 +28,30 @@ __device__ __forceinline__ float user_bias(int b, int h, int q, int kv) { return
 #else
 __device__ __forceinline__ float user_bias(int, int, int, int) { return 0.f; }
 #endif
+// The user's mask expression (a run-time compilation defines ATTN_USER_MASK_EXPR):
+// nonzero = query position q attends to key position kv.
+#ifdef ATTN_USER_MASK_EXPR
+__device__ __forceinline__ bool user_keep(int b, int h, int q, int kv) { return (ATTN_USER_MASK_EXPR) != 0; }
+#else
+__device__ __forceinline__ bool user_keep(int, int, int, int) { return true; }
+#endif
 
 // A compile-time bool as a type: selects one straight-line copy of a loop.
 template <bool V>
 struct bconst {
   static constexpr bool value = V;
 };
+
+// Columns of the K = 16 augmented operands that ride on the score products
+// (one more K = 16 step of S = Q K^T in the D = 64 kernels; see fwd_d64.cu):
+//   forward and dQ pass: AUG_MOD .. AUG_MOD + 2 the ALiBi / checkerboard bias
+//   (three 16-bit terms), AUG_KEY the key-padding mask (1 on the query side,
+//   0 or -inf on the key side);
+//   dK/dV pass: columns 0-2 hold the -lse terms, AUG_BMOD .. AUG_BMOD + 2 the
+//   bias (the key-position part of ALiBi, or the checkerboard), AUG_MOD2 ..
+//   AUG_MOD2 + 2 the query-position part of ALiBi.
+constexpr int AUG_MOD = 0, AUG_KEY = 3;
+constexpr int AUG_BMOD = 3, AUG_MOD2 = 6;
 
 // Per-(q tile, kv block) work flags staged in shared memory by the prefill kernels.
 constexpr uint8_t KB_VISIT = 1;    // the tile is computed

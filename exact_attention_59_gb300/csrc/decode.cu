@@ -25,9 +25,15 @@
 
 namespace attn {
 
-constexpr int DEC_WARPS = 8;
+#ifndef ATTN_DEC_WARPS
+#define ATTN_DEC_WARPS 8
+#endif
+#ifndef ATTN_DEC_U
+#define ATTN_DEC_U 4
+#endif
+constexpr int DEC_WARPS = ATTN_DEC_WARPS;
 constexpr int DEC_THREADS = 32 * DEC_WARPS;
-constexpr int DEC_U = 4;                           // keys per lane group
+constexpr int DEC_U = ATTN_DEC_U;                  // keys per lane group
 constexpr int DEC_WARP_KEYS = 4 * DEC_U;           // 16
 constexpr int DEC_KEYS = DEC_WARPS * DEC_WARP_KEYS;   // 128 keys per CTA at most
 
@@ -60,7 +66,7 @@ DEVI void merge_xor(float& m, float& l, float (&o)[8], int off) {
 }
 
 template <bool BF16, int MOD>
-__global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DEC_THREADS, (1024 / DEC_THREADS > 0 ? 1024 / DEC_THREADS : 1)) decode_kernel(const DecodeParams p) {
   const int split = blockIdx.x % p.nsplit, bh = blockIdx.x / p.nsplit;
   const int b = bh / p.H, h = bh % p.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -51,7 +51,7 @@ extern "C" attn_status attn_decode_noalloc(const attn_shape* s, const void* q, c
   if (s->dtype != ATTN_F16 && s->dtype != ATTN_BF16 && s->dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (s->Sq != 1) return ATTN_ERR_SHAPE;
   if (s->D != 64 || s->dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
-  if ((int)mod < 0 || (int)mod > 3 || !std::isfinite(scale))
+  if ((int)mod < 0 || (int)mod > 3 || !std::isfinite(scale) || scale == 0.f)
     return ATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !out || !lse) return ATTN_ERR_INVALID_ARG;
   if (!is_aligned16(q) || !is_aligned16(k) || !is_aligned16(v) || !is_aligned16(out) || !is_aligned16(lse) ||

@@ -31,9 +31,9 @@ struct __align__(1024) FwdSmem {
   uint8_t q[2][FWD_TILE_BYTES];
   uint8_t k[FWD_NST][FWD_TILE_BYTES];
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
-  // Key-padding bias folded into S = Q K^T as one more K = 16 step: qaug has a
-  // column of ones, kaug[s] a column holding 0 or -inf per key (K = 16 operands
-  // without swizzle, 4 KB each).
+  // Column terms folded into S = Q K^T as one more K = 16 step (K = 16 operands
+  // without swizzle, 4 KB each; columns as AUG_MOD / AUG_KEY in common.cuh):
+  // qaug (per query row, resident) x kaug[s] (per key of stage s).
   __align__(128) uint8_t qaug[4096];
   __align__(128) uint8_t kaug[FWD_NST][4096];
   uint64_t full[FWD_NST], empty[FWD_NST];
@@ -54,11 +54,13 @@ static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 // past the end in a partial last block) and, with DENSE, for columns whose bit
 // in the row's dense-mask words dw is 0; and the running maximum in four
 // independent chains.
-// With USER, x += user_bias(b, h, q, kv0 + cc) log2(e) (a run-time-compiled score_mod).
+// With USER, x += user_bias(b, h, q, kv0 + cc) log2(e) (a run-time-compiled score_mod)
+// and, with UMASK (a PARTIAL tile of a user mask_mod's block mask), -inf where
+// user_keep(b, h, q, kv0 + cc) is false.
 // With RAW (no table, no user bias, scale > 0) the scores stay unscaled: the
 // masks and the maximum work on s itself (max of s * scale = scale * max of s),
 // and the exponential pass applies the scale in its one FFMA.
-template <bool TABLE, bool LIMITED, bool DENSE, bool USER = false, bool RAW = false>
+template <bool TABLE, bool LIMITED, bool DENSE, bool USER = false, bool RAW = false, bool UMASK = false>
 DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4],
                        int ub = 0, int uh = 0, int uq = 0, int ukv0 = 0) {
 #pragma unroll
@@ -76,6 +78,10 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
       if constexpr (USER) {
         x0 = fmaf(user_bias(ub, uh, uq, ukv0 + c), kLog2e, x0);
         x1 = fmaf(user_bias(ub, uh, uq, ukv0 + c + 1), kLog2e, x1);
+      }
+      if constexpr (UMASK) {
+        x0 = user_keep(ub, uh, uq, ukv0 + c) ? x0 : -INFINITY;
+        x1 = user_keep(ub, uh, uq, ukv0 + c + 1) ? x1 : -INFINITY;
       }
       if (LIMITED) {
         x0 = c > lim ? -INFINITY : x0;
@@ -164,17 +170,52 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     }
   }
   constexpr bool kTableMod = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
-  // Without ALiBi / checkerboard the key-padding mask rides on the S product
-  // (exact: the extra step adds +0 or -inf to each f32 score); with them the
-  // producer's per-column table carries it.
-  const bool aug = !kTableMod && p.km_bits != nullptr;
-  const bool use_table = kTableMod;
+  // Terms that depend on the query row or the key column alone ride on the S
+  // product as one more K = 16 step (the tensor core adds them; the softmax warps
+  // do no per-score work for them):
+  //   key-padding mask: 1 x (0 or -inf) in column AUG_KEY (exact: +0 or -inf);
+  //   with `fold`, the mod's bias over scale in columns AUG_MOD .. +2, as three
+  //   16-bit terms of one f32 value:
+  //     checkerboard  (-1)^q_pos t_i  x  (-1)^c        (t = 0.5 / scale)
+  //     ALiBi         1               x  t_i(c)        (t(c) = slope_h c / scale)
+  //   c = key column in the block (a kv block starts at a multiple of 128, so
+  //   (-1)^kv = (-1)^c); ALiBi's remaining slope_h (kv0 - q_pos) is a constant per
+  //   row and block, added to the row maximum (below).  Without `fold` (scale 0,
+  //   or a bias too large for three 16-bit terms) the producer's per-column table
+  //   carries the mod and the mask instead.
+  const bool fold = kTableMod && p.fold;
+  const bool use_table = kTableMod && !fold;   // the table then carries the key mask too
+  const bool aug = !use_table && (fold || p.km_bits != nullptr);
   if (aug) {
-    const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
     uint4* z = reinterpret_cast<uint4*>(sm.qaug);
     for (int i = tid; i < (1 + FWD_NST) * 4096 / 16; i += FWD_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    if (tid < 128) *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(tid, 0)) = static_cast<uint16_t>(one);
+    if (tid < 128) {
+      const int r = tid;   // query row of the tile, and key column of a block
+      const uint16_t one = to16<BF16>(1.f);
+      *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_KEY)) = one;
+      if (fold) {
+        uint16_t qt3[3], kt3[3];
+        if constexpr (MOD == MOD_CHECKER) {
+          uint16_t t[3];
+          split3_plain<BF16>(0.5f * p.inv_scale, t);
+          const bool qodd = (r + q_off) & 1;   // both query tiles start at a multiple of 128
+          for (int i = 0; i < 3; ++i) {
+            qt3[i] = qodd ? uint16_t(t[i] ^ 0x8000u) : t[i];   // the sign bit of f16 and bf16
+            kt3[i] = (r & 1) ? to16<BF16>(-1.f) : one;
+          }
+        } else {
+          const float slope = exp2f(-8.0f * float(h + 1) / float(p.H));
+          split3_plain<BF16>(slope * float(r) * p.inv_scale, kt3);
+          for (int i = 0; i < 3; ++i) qt3[i] = one;
+        }
+        for (int i = 0; i < 3; ++i) {
+          *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_MOD + i)) = qt3[i];
+          for (int st = 0; st < FWD_NST; ++st)
+            *reinterpret_cast<uint16_t*>(sm.kaug[st] + k16_offset(r, AUG_MOD + i)) = kt3[i];
+        }
+      }
+    }
     fence_async_smem();   // generic-proxy writes, read by the tensor core
   }
   tc_fence_before();
@@ -199,15 +240,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       if (!(fu & KB_VISIT)) continue;
       const int s = u % FWD_NST;
       if (u >= FWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) break;
-      if (aug) {
-        // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column 0 of kaug[s]
+      if (aug && p.km_bits) {
+        // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column AUG_KEY of kaug[s]
         uint32_t bits = 0xffffffffu;
         if (fu & KB_KEYMASK) bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
-        const uint16_t ninf = BF16 ? 0xFF80u : 0xFC00u;
+        // the infinity whose product with the scale is -inf (scale != 0)
+        const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int col = 4 * lane + i;
-          *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, 0)) = ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+          *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, AUG_KEY)) =
+              ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
         }
         fence_async_smem();
       } else if (use_table) {
@@ -332,7 +375,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
       const int parity = (MOD == MOD_CHECKER) ? (qpos & 1) : 0;
       // unscaled scores in the max pass (scale > 0 keeps the order of the maximum)
-      const bool raw = !kTableMod && MOD != MOD_USER && p.sc > 0.f;
+      const bool raw = !use_table && MOD != MOD_USER && p.sc > 0.f;
       float m_run = -INFINITY, l = 0.f;
       uint32_t n = 0;
       int u = 0;
@@ -383,9 +426,18 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           else if (limited) scale_scores<true, true, false>(r, scv, tb, lim, dw, mx);
           else scale_scores<true, false, false>(r, scv, tb, lim, dw, mx);
         } else if constexpr (MOD == MOD_USER) {
-          if (DM && dense) scale_scores<false, true, DM, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
-          else if (limited) scale_scores<false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
-          else scale_scores<false, false, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          // a PARTIAL tile of a user mask_mod's block mask: the expression masks each entry
+          const bool umask = (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
+          if (umask) {
+            if (limited) scale_scores<false, true, false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+            else scale_scores<false, false, false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          } else if (DM && dense) {
+            scale_scores<false, true, DM, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          } else if (limited) {
+            scale_scores<false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          } else {
+            scale_scores<false, false, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+          }
         } else if (raw) {
           if (DM && dense) scale_scores<false, true, DM, false, true>(r, scv, tb, lim, dw, mx);
           else if (limited) scale_scores<false, true, false, false, true>(r, scv, tb, lim, dw, mx);

@@ -72,6 +72,10 @@ struct FwdParams {
   // unnormalised} instead of out and lse; nsplit = 1 and part = nullptr otherwise
   int nsplit, kps;
   float* part;
+  // ALiBi / checkerboard bias folded into S = Q K^T as one more K = 16 step
+  // (the AUG_MOD columns of the augmented operands), and 1 / scale
+  int fold;
+  float inv_scale;
 };
 constexpr int FWD_PART = 68;      // floats per partial row (16-byte aligned O)
 #ifndef __CUDACC_RTC__
@@ -124,11 +128,16 @@ struct BwdParams {
   float sc;               // scale * log2(e)
   float scale;
   unsigned long long timeout_ns;
+  int fold;               // ALiBi / checkerboard bias folded into the score products
+  float inv_scale;        // 1 / scale
 };
 #ifndef __CUDACC_RTC__
 cudaError_t launch_bwd_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
 cudaError_t launch_bwd_kernel(const BwdParams& p, const void* kern, bool dkdv, cudaStream_t st);
+// head dim 512 (f16/bf16, Sq and Skv multiples of 128; no dense mask, no user mod)
+cudaError_t launch_bwd512_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
+cudaError_t launch_bwd512_dq(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
 #endif  // host
 
 // ---------------------------------------------------------------- small kernels
@@ -157,8 +166,7 @@ struct DecodeParams {
   float* lse;
   const uint8_t* key_mask;   // (B, Skv) or nullptr
   float* partial;            // (B*H, nsplit, 2 + 64): m, l, o[64]
-  unsigned* counter;         // (B*H)
-  int* status;               // workspace status word, or nullptr
+  unsigned* counter;         // (B*H) completion tickets, zero between calls
   int B, H, Skv, nsplit, keys_per_split;
   float sc;
   int mod;

@@ -210,29 +210,37 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
     }
     return;
   }
-  // D_i = rowsum(dO o O) and -lse log2(e): 8 elements per lane, two rows per lane
-  // (row and row + half_rows) so that four 16-byte loads are in flight per thread
-  const int lpr = D / 8;   // lanes per row
+  // D_i = rowsum(dO o O) and -lse log2(e): 8 elements per lane and chunk (a row
+  // spans at most 32 lanes: D / 256 chunks per lane beyond D = 256), two rows
+  // per lane (row and row + half_rows) so that four 16-byte loads are in flight
+  const int lpr = D / 8 < 32 ? D / 8 : 32;   // lanes per row
+  const int per = D / (8 * lpr);            // 8-element chunks per lane
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row0 = tid / lpr;
   const int part = (int)(tid % lpr);
   float acc[2] = {0.f, 0.f};
-  float a[2][8], g[2][8];
+  for (int j = 0; j < per; ++j) {
+    float a[2][8], g[2][8];
+    const int col = (part + j * lpr) * 8;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const long long row = row0 + k * half_rows;
-    if (row0 < half_rows && row < rows) {
-      load8<T>(out + row * D + part * 8, a[k]);
-      load8<T>(dout + row * D + part * 8, g[k]);
-    } else {
+    for (int k = 0; k < 2; ++k) {
+      const long long row = row0 + k * half_rows;
+      if (row0 < half_rows && row < rows) {
+        load8<T>(out + row * D + col, a[k]);
+        load8<T>(dout + row * D + col, g[k]);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a[k][i] = g[k][i] = 0.f;
+        for (int i = 0; i < 8; ++i) a[k][i] = g[k][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[k] = fmaf(a[k][i], g[k][i], acc[k]);
     }
   }
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[k] = fmaf(a[k][i], g[k][i], acc[k]);
     for (int off = lpr / 2; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
     const long long row = row0 + k * half_rows;
     if (row0 < half_rows && row < rows && part == 0) {
@@ -248,7 +256,7 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
                                   uint8_t* summary, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const long long half_rows = (rows + 1) / 2;
-  const long long threads = half_rows * (D / 8);
+  const long long threads = half_rows * (D / 8 < 32 ? D / 8 : 32);
   const unsigned pre_blocks = (unsigned)((threads + 255) / 256);
   const unsigned pack_blocks = km ? (unsigned)(B * (((Skv + 127) / 128 + 1) / 2)) : 0u;
   const unsigned grid = pre_blocks + pack_blocks;

@@ -376,12 +376,13 @@ DEVI uint32_t km_word(const uint32_t* bits, int b, int Skv, int key) {
 
 // One f32 value x as three 16-bit terms, x = t0 + t1 + 2048 t2, written to columns
 // 0..2 of row r of a K = 16 operand (no swizzle).  The 2048 t2 term keeps f16 in
-// range; t0 + t1 carry the rest to about 2^-22 relative.  -inf goes to t2 alone.
+// range; t0 + t1 carry the rest to about 2^-22 relative.  An infinity goes to t2
+// alone (-inf for a row with no kept key; +inf when a negative scale divided it).
 template <bool BF16>
 DEVI void split3(float x, uint8_t* op, int r) {
   float a2, a0, a1;
-  if (x == -INFINITY) {
-    a2 = -INFINITY;
+  if (fabsf(x) == INFINITY) {
+    a2 = x;
     a0 = a1 = 0.f;
   } else {
     a2 = from16<BF16>(to16<BF16>(x * (1.f / 2048.f)));
@@ -392,6 +393,17 @@ DEVI void split3(float x, uint8_t* op, int r) {
   *reinterpret_cast<uint16_t*>(op + k16_offset(r, 0)) = to16<BF16>(a0);
   *reinterpret_cast<uint16_t*>(op + k16_offset(r, 1)) = to16<BF16>(a1);
   *reinterpret_cast<uint16_t*>(op + k16_offset(r, 2)) = to16<BF16>(a2);
+}
+
+// x as three 16-bit terms t0 + t1 + t2 (each the rounded remainder of the
+// previous ones): about 3 x 8 significant bits in bf16, 3 x 11 in f16.  For
+// finite values of moderate size (|x| well inside the 16-bit range).
+template <bool BF16>
+DEVI void split3_plain(float x, uint16_t (&t)[3]) {
+  t[0] = to16<BF16>(x);
+  const float r1 = x - from16<BF16>(t[0]);
+  t[1] = to16<BF16>(r1);
+  t[2] = to16<BF16>(r1 - from16<BF16>(t[1]));
 }
 
 }  // namespace attn

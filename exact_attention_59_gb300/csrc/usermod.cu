@@ -10,9 +10,16 @@
 // instantiation), so the generated kernels have the built-in ones' layout,
 // pipelines and bounded waits.  Compilation needs no GPU; the cubin is loaded
 // on a device the first time a call on that device uses it.
+//
+// A user mask_mod (create_block_mask takes any mask function in the
+// flaxattention README) is a second C expression, nonzero = keep; it is
+// compiled into the same kernels (evaluated on the entries of PARTIAL tiles of
+// a block mask whose mask_mod is ATTN_MASKMOD_USER) and into a block-mask
+// builder (usermask.cuh) that gives the tile states.
 #include <dlfcn.h>
 #include <nvrtc.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -26,12 +33,13 @@
 
 struct attn_user_mod_st {
   attn_dtype dtype;
+  bool has_mask;
   std::vector<char> cubin;
-  std::string names[3];   // lowered names: forward, dK/dV, dQ
+  std::string names[4];   // lowered names: forward, dK/dV, dQ, block-mask builder (with a mask)
   std::mutex mu;
   struct Loaded {
     cudaLibrary_t lib;
-    cudaKernel_t k[3];
+    cudaKernel_t k[4];
   };
   std::map<int, Loaded> per_device;
 };
@@ -56,12 +64,12 @@ void put_log(char* log, size_t log_bytes, const std::string& text) {
 
 }  // namespace
 
-extern "C" attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dtype, attn_user_mod* mod, char* log,
-                                            size_t log_bytes) {
-  if (!bias_expr || !mod) return ATTN_ERR_INVALID_ARG;
+extern "C" attn_status attn_user_mod_create_masked(const char* bias_expr, const char* mask_expr, attn_dtype dtype,
+                                                   attn_user_mod* mod, char* log, size_t log_bytes) {
+  if (!mod) return ATTN_ERR_INVALID_ARG;
   *mod = nullptr;
-  const size_t len = std::strlen(bias_expr);
-  if (len == 0 || len > 4096) return ATTN_ERR_INVALID_ARG;
+  const size_t blen = bias_expr ? std::strlen(bias_expr) : 0, mlen = mask_expr ? std::strlen(mask_expr) : 0;
+  if ((blen == 0 && mlen == 0) || blen > 4096 || mlen > 4096) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   const std::string dir = csrc_dir();
   if (FILE* f = std::fopen((dir + "/fwd_d64.cu").c_str(), "r")) {
@@ -70,16 +78,21 @@ extern "C" attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dt
     put_log(log, log_bytes, "kernel sources not found in " + dir);
     return ATTN_ERR_UNSUPPORTED;
   }
-  const std::string src = "#define ATTN_USER_BIAS_EXPR (" + std::string(bias_expr) +
-                          ")\n#include \"fwd_d64.cu\"\n#include \"bwd_d64.cu\"\n";
+  const bool has_mask = mlen > 0;
+  std::string src = "#define ATTN_USER_BIAS_EXPR (" + std::string(blen ? bias_expr : "0.0f") + ")\n";
+  if (has_mask) src += "#define ATTN_USER_MASK_EXPR (" + std::string(mask_expr) + ")\n";
+  src += "#include \"fwd_d64.cu\"\n#include \"bwd_d64.cu\"\n";
+  if (has_mask) src += "#include \"usermask.cuh\"\n";
   const char* bf = dtype == ATTN_BF16 ? "true" : "false";
-  const std::string exprs[3] = {std::string("attn::fwd_d64_kernel<") + bf + ", 4, 0>",
+  const std::string exprs[4] = {std::string("attn::fwd_d64_kernel<") + bf + ", 4, 0>",
                                 std::string("attn::bwd_dkdv_kernel<") + bf + ", 4, false>",
-                                std::string("attn::bwd_dq_kernel<") + bf + ", 4, false>"};
+                                std::string("attn::bwd_dq_kernel<") + bf + ", 4, false>",
+                                std::string("attn::user_block_mask_kernel")};
+  const int nk = has_mask ? 4 : 3;
   nvrtcProgram prog;
   if (nvrtcCreateProgram(&prog, src.c_str(), "user_score_mod.cu", 0, nullptr, nullptr) != NVRTC_SUCCESS)
     return ATTN_ERR_CUDA;
-  for (const std::string& e : exprs) nvrtcAddNameExpression(prog, e.c_str());
+  for (int i = 0; i < nk; ++i) nvrtcAddNameExpression(prog, exprs[i].c_str());
   const std::string inc = "-I" + dir;
   // -default-device: the kernels' lambdas carry no execution-space annotation
   const char* opts[] = {"--gpu-architecture=sm_103a", "-std=c++17", "-default-device", inc.c_str()};
@@ -91,15 +104,16 @@ extern "C" attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dt
   put_log(log, log_bytes, text);
   if (rc != NVRTC_SUCCESS) {
     nvrtcDestroyProgram(&prog);
-    return ATTN_ERR_INVALID_ARG;   // the expression does not compile: the log says why
+    return ATTN_ERR_INVALID_ARG;   // an expression does not compile: the log says why
   }
   attn_user_mod m = new attn_user_mod_st();
   m->dtype = dtype;
+  m->has_mask = has_mask;
   size_t n = 0;
   nvrtcGetCUBINSize(prog, &n);
   m->cubin.resize(n);
   nvrtcGetCUBIN(prog, m->cubin.data());
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < nk; ++i) {
     const char* lowered = nullptr;
     nvrtcGetLoweredName(prog, exprs[i].c_str(), &lowered);
     m->names[i] = lowered ? lowered : "";
@@ -107,6 +121,12 @@ extern "C" attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dt
   nvrtcDestroyProgram(&prog);
   *mod = m;
   return ATTN_OK;
+}
+
+extern "C" attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dtype, attn_user_mod* mod, char* log,
+                                            size_t log_bytes) {
+  if (!bias_expr || !mod || bias_expr[0] == '\0') return ATTN_ERR_INVALID_ARG;
+  return attn_user_mod_create_masked(bias_expr, nullptr, dtype, mod, log, log_bytes);
 }
 
 extern "C" void attn_user_mod_destroy(attn_user_mod mod) {
@@ -125,18 +145,20 @@ extern "C" void attn_user_mod_destroy(attn_user_mod mod) {
 
 namespace attn {
 
-attn_status user_mod_kernels(attn_user_mod mod, attn_dtype dtype, const void* (&kern)[3]) {
-  if (!mod) return ATTN_ERR_INVALID_ARG;
-  if (mod->dtype != dtype) return ATTN_ERR_UNSUPPORTED;   // built for the other 16-bit type
+namespace {
+
+// The mod's kernels on the current device (its code loaded there on first use).
+attn_status loaded_kernels(attn_user_mod mod, const void* (&kern)[4]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  const int nk = mod->has_mask ? 4 : 3;
   std::lock_guard<std::mutex> g(mod->mu);
   auto it = mod->per_device.find(dev);
   if (it == mod->per_device.end()) {
-    attn_user_mod_st::Loaded L;
+    attn_user_mod_st::Loaded L{};
     if (cudaLibraryLoadData(&L.lib, mod->cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < nk; ++i) {
       if (cudaLibraryGetKernel(&L.k[i], L.lib, mod->names[i].c_str()) != cudaSuccess) {
         cudaLibraryUnload(L.lib);
         return ATTN_ERR_CUDA;
@@ -144,8 +166,39 @@ attn_status user_mod_kernels(attn_user_mod mod, attn_dtype dtype, const void* (&
     }
     it = mod->per_device.emplace(dev, L).first;
   }
-  for (int i = 0; i < 3; ++i) kern[i] = reinterpret_cast<const void*>(it->second.k[i]);
+  for (int i = 0; i < 4; ++i) kern[i] = i < nk ? reinterpret_cast<const void*>(it->second.k[i]) : nullptr;
   return ATTN_OK;
 }
 
+}  // namespace
+
+attn_status user_mod_kernels(attn_user_mod mod, attn_dtype dtype, const void* (&kern)[3]) {
+  if (!mod) return ATTN_ERR_INVALID_ARG;
+  if (mod->dtype != dtype) return ATTN_ERR_UNSUPPORTED;   // built for the other 16-bit type
+  const void* all[4];
+  const attn_status st = loaded_kernels(mod, all);
+  if (st != ATTN_OK) return st;
+  for (int i = 0; i < 3; ++i) kern[i] = all[i];
+  return ATTN_OK;
+}
+
+bool user_mod_has_mask(attn_user_mod mod) { return mod && mod->has_mask; }
+
 }  // namespace attn
+
+extern "C" attn_status attn_build_block_mask_user(attn_user_mod mod, int B, int H, int Sq, int Skv, int bq, int bkv,
+                                                  uint8_t* tiles, attn_stream_t stream) {
+  using namespace attn;
+  if (!mod || !mod->has_mask || !tiles || B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0 || bq <= 0 || bkv <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (bq != 128 || bkv != 128) return ATTN_ERR_UNSUPPORTED;
+  const void* kern[4];
+  const attn_status st = loaded_kernels(mod, kern);
+  if (st != ATTN_OK) return st;
+  const long long ntiles = (long long)B * H * ((Sq + 127) / 128) * ((Skv + 127) / 128);
+  const unsigned grid = (unsigned)std::min<long long>(ntiles, 152LL * 16);
+  void* args[] = {&B, &H, &Sq, &Skv, &tiles};
+  return cudaLaunchKernel(kern[3], dim3(grid), dim3(256), args, 0, (cudaStream_t)stream) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}

@@ -10,4 +10,7 @@ namespace attn {
 // for the other 16-bit type.
 attn_status user_mod_kernels(attn_user_mod mod, attn_dtype dtype, const void* (&kern)[3]);
 
+// Whether `mod` was built with a mask expression (attn_user_mod_create_masked).
+bool user_mod_has_mask(attn_user_mod mod);
+
 }  // namespace attn

@@ -46,6 +46,8 @@
  *    with attn_poll_status().
  *  - Masked scores are -inf: a row with no kept key gets O = 0, lse = -inf
  *    and zero gradients.
+ *  - `scale` multiplies q k^T; it must be finite and nonzero (negative is
+ *    allowed), else ATTN_ERR_INVALID_ARG.  The pages use 1/sqrt(D).
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
@@ -88,8 +90,11 @@ typedef enum {
   ATTN_MOD_CAUSAL = 3
 } attn_score_mod;
 
-/* mask_mod of a block mask (flaxattention README: create_block_mask(causal_mask, ...)). */
-typedef enum { ATTN_MASKMOD_NONE = 0, ATTN_MASKMOD_CAUSAL = 1 } attn_mask_mod;
+/* mask_mod of a block mask (flaxattention README: create_block_mask(causal_mask, ...)).
+ * ATTN_MASKMOD_USER: the mask expression of the run-time-compiled user mod
+ * given with the call (attn_fwd_user / attn_bwd_user only; see
+ * attn_user_mod_create_masked), which built the tile states. */
+typedef enum { ATTN_MASKMOD_NONE = 0, ATTN_MASKMOD_CAUSAL = 1, ATTN_MASKMOD_USER = 2 } attn_mask_mod;
 
 /* Block-mask tile states. */
 enum { ATTN_TILE_EMPTY = 0, ATTN_TILE_PARTIAL = 1, ATTN_TILE_FULL = 2 };
@@ -279,6 +284,31 @@ attn_status attn_decode_chunk(const attn_shape* shape, const void* q, const void
 typedef struct attn_user_mod_st* attn_user_mod;
 attn_status attn_user_mod_create(const char* bias_expr, attn_dtype dtype, attn_user_mod* mod, char* log,
                                  size_t log_bytes);
+/* A user score_mod with a user mask_mod (flaxattention README "Example usage":
+ * create_block_mask(mask_mod, B, H, Sq, Skv) takes any mask function and
+ * FlexAttention skips the tiles it empties).  mask_expr is a C expression in
+ * the int variables b, h, q, kv (positions), nonzero = the query attends to
+ * the key; bias_expr (nullable or empty: no bias) is as in
+ * attn_user_mod_create.  Besides the forward, dK/dV and dQ kernels the mod
+ * then holds a block-mask builder (attn_build_block_mask_user).  A block mask
+ * with mask_mod = ATTN_MASKMOD_USER, passed with this mod to attn_fwd_user /
+ * attn_bwd_user, skips EMPTY tiles, takes FULL tiles whole and evaluates
+ * mask_expr on every entry of a PARTIAL tile: the tiles must come from the
+ * same mod.  Errors as attn_user_mod_create (ATTN_ERR_INVALID_ARG also when
+ * both expressions are NULL or empty). */
+attn_status attn_user_mod_create_masked(const char* bias_expr, const char* mask_expr, attn_dtype dtype,
+                                        attn_user_mod* mod, char* log, size_t log_bytes);
+
+/* Tile states of `mod`'s mask expression (the analogue of create_block_mask
+ * with a user mask function): tiles is device uint8 (B, H, ceil(Sq/bq),
+ * ceil(Skv/bkv)); a tile is FULL when the expression keeps every in-range
+ * (q, kv) of it, EMPTY when it keeps none, else PARTIAL.  Asynchronous on
+ * `stream` (the current device).  bq = bkv = 128 only (ATTN_ERR_UNSUPPORTED
+ * otherwise); ATTN_ERR_INVALID_ARG for a NULL pointer, a non-positive size or
+ * a mod without a mask expression. */
+attn_status attn_build_block_mask_user(attn_user_mod mod, int B, int H, int Sq, int Skv, int bq, int bkv,
+                                       uint8_t* tiles, attn_stream_t stream);
+
 /* Frees a user score_mod (NULL is ignored).  Waits for all work on each
  * device the mod was loaded on before unloading its code, so a call still
  * queued on a stream finishes first; it must not race with a new call. */

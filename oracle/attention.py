@@ -44,7 +44,12 @@ Readings where the sources above are silent:
   are partial (the plain formula has no block size at all);
 * a user score_mod (the README's hooks take arbitrary callables) is an
   additive bias f(b, h, q_idx, kv_idx), -inf to mask, the form of every mod
-  the pages name.
+  the pages name;
+* a user mask_mod (``create_block_mask`` takes any mask function; the README
+  passes ``causal_mask``) is a predicate g(b, h, q_idx, kv_idx), true = keep,
+  evaluated like the built-in ones: its tile states come from evaluating it on
+  every entry of every tile of every (b, h), and it masks the entries of
+  PARTIAL tiles.
 
 Parity unpinned: the ALiBi and checkerboard definitions themselves (no page
 defines them; they are pinned only against their own closed forms), and the
@@ -117,11 +122,18 @@ def score_bias(mod, h: int, H: int, q_idx: np.ndarray, kv_idx: np.ndarray, b: in
     return np.broadcast_to(bias, shape).astype(np.float64), keep
 
 
-def mask_mod_keep(mask_mod, q_idx: np.ndarray, kv_idx: np.ndarray) -> np.ndarray:
-    """Elementwise mask_mod (flaxattention ``causal_mask``): True = attend."""
-    mm = _maskmod_id(mask_mod)
+def mask_mod_keep(mask_mod, q_idx: np.ndarray, kv_idx: np.ndarray, b: int = 0, h: int = 0) -> np.ndarray:
+    """Elementwise mask_mod (flaxattention ``causal_mask``): True = attend.
+
+    ``mask_mod`` is a built-in id or name, or a callable g(b, h, q_idx, kv_idx)
+    of integer arrays (q_idx a column, kv_idx a row) giving True to keep.
+    """
     qi = np.asarray(q_idx, dtype=np.int64)[:, None]
     kj = np.asarray(kv_idx, dtype=np.int64)[None, :]
+    if callable(mask_mod):
+        out = np.asarray(mask_mod(b, h, qi, kj), dtype=bool)
+        return np.broadcast_to(out, (qi.shape[0], kj.shape[1])).copy()
+    mm = _maskmod_id(mask_mod)
     if mm == MASKMOD_NONE:
         return np.ones((qi.shape[0], kj.shape[1]), dtype=bool)
     if mm == MASKMOD_CAUSAL:
@@ -139,22 +151,34 @@ def build_block_mask(mask_mod, B: int, H: int, Sq: int, Skv: int,
 
     A tile is FULL if every entry is kept, EMPTY if none is, PARTIAL otherwise.
     The result has shape (B, H, ceil(Sq/block_q), ceil(Skv/block_kv)), uint8.
+    A built-in mask_mod is the same for every (b, h); a callable one is
+    evaluated for each (b, h).
     """
     nqb = -(-Sq // block_q)
     nkb = -(-Skv // block_kv)
-    states = np.zeros((nqb, nkb), dtype=np.uint8)
-    for qb in range(nqb):
-        qi = np.arange(qb * block_q, min(Sq, (qb + 1) * block_q))
-        for kb in range(nkb):
-            kj = np.arange(kb * block_kv, min(Skv, (kb + 1) * block_kv))
-            keep = mask_mod_keep(mask_mod, qi, kj)
-            if keep.all():
-                states[qb, kb] = TILE_FULL
-            elif keep.any():
-                states[qb, kb] = TILE_PARTIAL
-            else:
-                states[qb, kb] = TILE_EMPTY
-    return np.broadcast_to(states, (B, H, nqb, nkb)).copy()
+
+    def states_of(b, h):
+        states = np.zeros((nqb, nkb), dtype=np.uint8)
+        for qb in range(nqb):
+            qi = np.arange(qb * block_q, min(Sq, (qb + 1) * block_q))
+            for kb in range(nkb):
+                kj = np.arange(kb * block_kv, min(Skv, (kb + 1) * block_kv))
+                keep = mask_mod_keep(mask_mod, qi, kj, b, h)
+                if keep.all():
+                    states[qb, kb] = TILE_FULL
+                elif keep.any():
+                    states[qb, kb] = TILE_PARTIAL
+                else:
+                    states[qb, kb] = TILE_EMPTY
+        return states
+
+    if not callable(mask_mod):
+        return np.broadcast_to(states_of(0, 0), (B, H, nqb, nkb)).copy()
+    out = np.zeros((B, H, nqb, nkb), dtype=np.uint8)
+    for b in range(B):
+        for h in range(H):
+            out[b, h] = states_of(b, h)
+    return out
 
 
 class BlockMask:
@@ -163,7 +187,7 @@ class BlockMask:
     def __init__(self, tiles, mask_mod, block_q: int = 128, block_kv: int = 128):
         self.tiles = np.asarray(tiles, dtype=np.uint8)
         assert self.tiles.ndim == 4
-        self.mask_mod = _maskmod_id(mask_mod)
+        self.mask_mod = mask_mod if callable(mask_mod) else _maskmod_id(mask_mod)
         self.block_q = int(block_q)
         self.block_kv = int(block_kv)
 
@@ -200,7 +224,7 @@ def keep_matrix(b: int, h: int, H: int, q_idx, kv_idx, key_mask=None,
     if block_mask is not None:
         st = block_mask.states(b, h)
         ts = st[(q_idx // block_mask.block_q)[:, None], (kv_idx // block_mask.block_kv)[None, :]]
-        mm = mask_mod_keep(block_mask.mask_mod, q_idx, kv_idx)
+        mm = mask_mod_keep(block_mask.mask_mod, q_idx, kv_idx, b, h)
         keep &= (ts != TILE_EMPTY) & ((ts == TILE_FULL) | mm)
     return keep
 

@@ -92,6 +92,7 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, _shape(lib), km=FAKE + 1) == lib.ATTN_ERR_ALIGN
     assert _fwd(lib, _shape(lib), mod=9) == lib.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, _shape(lib), scale=float("nan")) == lib.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, _shape(lib), scale=0.0) == lib.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, _shape(lib), ws=None) == lib.ATTN_ERR_WORKSPACE
     assert _fwd(lib, _shape(lib), ws=FAKE + 16) == lib.ATTN_ERR_ALIGN
     assert _fwd(lib, _shape(lib), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE
@@ -107,12 +108,23 @@ def test_bwd_and_decode_reject_bad_arguments(lib):
     L = lib.load()
     s = _shape(lib)
     args = [FAKE] * 6
-    assert L.attn_bwd(ctypes.byref(_shape(lib, D=512)), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+    assert L.attn_bwd(ctypes.byref(_shape(lib, D=96)), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30,
                       None) == lib.ATTN_ERR_UNSUPPORTED
+    assert L.attn_bwd(ctypes.byref(_shape(lib, D=512, dt=0)), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE,
+                      1 << 30, None) == lib.ATTN_ERR_UNSUPPORTED
+    assert L.attn_bwd(ctypes.byref(_shape(lib, D=512, Sq=200)), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE,
+                      1 << 30, None) == lib.ATTN_ERR_SHAPE
     assert L.attn_bwd(ctypes.byref(s), *args, None, None, 0, 0.1, None, FAKE, FAKE, FAKE, 1 << 30,
                       None) == lib.ATTN_ERR_INVALID_ARG
     assert L.attn_bwd(ctypes.byref(s), *args, None, None, 0, 0.1, FAKE, FAKE, FAKE, FAKE, 10,
                       None) == lib.ATTN_ERR_WORKSPACE
+    # a zero scale is refused everywhere (masks and -lse / scale ride on the score products)
+    assert L.attn_bwd(ctypes.byref(s), *args, None, None, 0, 0.0, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                      None) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_bwd_dkdv(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, None, 0, 0.0, FAKE, FAKE, FAKE, 1 << 30,
+                           None) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_bwd_dq(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, None, 0, 0.0, FAKE, FAKE, 1 << 30,
+                         None) == lib.ATTN_ERR_INVALID_ARG
     d = _shape(lib, Sq=2, Skv=100)
     assert L.attn_decode(ctypes.byref(d), FAKE, FAKE, FAKE, None, 0, 0.1, FAKE, FAKE, FAKE, 1 << 30,
                          None) == lib.ATTN_ERR_SHAPE
@@ -219,3 +231,45 @@ def test_user_score_mod_compiles_without_a_gpu(lib):
     # a call with no handle is refused before anything is launched
     assert L.attn_fwd_user(ctypes.byref(_shape(lib)), FAKE, FAKE, FAKE, None, None, None, 0.125, FAKE, FAKE, FAKE,
                            1 << 30, None, None) == lib.ATTN_ERR_INVALID_ARG
+
+
+def test_user_mask_mod_compiles_without_a_gpu(lib):
+    """A mask expression (with or without a bias) compiles into the kernels and the
+    block-mask builder with no GPU; a broken one gives a compiler log; the builder
+    and the forward refuse bad arguments before anything is launched."""
+    import torch
+    L = lib.load()
+    h = ctypes.c_void_p()
+    buf = ctypes.create_string_buffer(1 << 16)
+    assert L.attn_user_mod_create_masked(None, b"(q / 64) == (kv / 64)", lib.ATTN_F16, ctypes.byref(h), buf,
+                                         len(buf)) == lib.ATTN_OK
+    assert h.value
+    assert L.attn_build_block_mask_user(h, 1, 1, 256, 256, 64, 64, FAKE, None) == lib.ATTN_ERR_UNSUPPORTED
+    assert L.attn_build_block_mask_user(h, 0, 1, 256, 256, 128, 128, FAKE, None) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_build_block_mask_user(h, 1, 1, 256, 256, 128, 128, None, None) == lib.ATTN_ERR_INVALID_ARG
+    L.attn_user_mod_destroy(h)
+    assert L.attn_user_mod_create_masked(b"0.1f * (float)h", b"kv <= q", lib.ATTN_BF16, ctypes.byref(h), buf,
+                                         len(buf)) == lib.ATTN_OK
+    L.attn_user_mod_destroy(h)
+    assert L.attn_user_mod_create_masked(None, b"kv <= q &&", lib.ATTN_BF16, ctypes.byref(h), buf,
+                                         len(buf)) == lib.ATTN_ERR_INVALID_ARG
+    assert b"error" in buf.value
+    assert L.attn_user_mod_create_masked(None, None, lib.ATTN_BF16, ctypes.byref(h), buf,
+                                         len(buf)) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_user_mod_create_masked(b"", b"", lib.ATTN_BF16, ctypes.byref(h), buf,
+                                         len(buf)) == lib.ATTN_ERR_INVALID_ARG
+    # a mod without a mask expression builds no block mask
+    plain = lib.compile_score_mod("0.0f", dtype=torch.bfloat16)
+    assert L.attn_build_block_mask_user(plain.handle, 1, 1, 256, 256, 128, 128, FAKE, None) == \
+        lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_build_block_mask_user(None, 1, 1, 256, 256, 128, 128, FAKE, None) == lib.ATTN_ERR_INVALID_ARG
+    # a user block mask goes only with a user mod that has a mask expression
+    bm = lib.BlockMaskC(FAKE, 1, 1, 128, 128, 2)
+    assert _fwd(lib, _shape(lib), bm=bm) == lib.ATTN_ERR_INVALID_ARG
+    assert L.attn_fwd_user(ctypes.byref(_shape(lib)), FAKE, FAKE, FAKE, None, plain.handle, ctypes.byref(bm), 0.125,
+                           FAKE, FAKE, FAKE, 10, None, None) == lib.ATTN_ERR_INVALID_ARG
+    masked = lib.compile_mask_mod("kv <= q", dtype=torch.bfloat16)
+    assert masked.mask_expr == "kv <= q"
+    # with a mask expression the block mask is accepted; the tiny workspace then fails
+    assert L.attn_fwd_user(ctypes.byref(_shape(lib)), FAKE, FAKE, FAKE, None, masked.handle, ctypes.byref(bm), 0.125,
+                           FAKE, FAKE, FAKE, 10, None, None) == lib.ATTN_ERR_WORKSPACE

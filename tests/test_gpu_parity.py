@@ -36,15 +36,22 @@ def _oracle_bm(bm_kind, B, H, Sq, Skv):
 
 
 def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", backward=True, heads=None,
-                  check_det=True, key_mask_override=None, strict=False, D=64, dense=None, oracle_mod=None):
+                  check_det=True, key_mask_override=None, strict=False, D=64, dense=None, oracle_mod=None,
+                  scale=None, user_mask=None):
     """``dense``: optional uint8 CPU tensor (B|1, H|1, Sq, Skv), the dense (query, key) mask.
-    ``oracle_mod``: the oracle's form of ``mod`` when it differs (a user score_mod)."""
+    ``oracle_mod``: the oracle's form of ``mod`` when it differs (a user score_mod).
+    ``user_mask``: the oracle's callable of the mask expression that ``mod`` (a
+    user mod) was compiled with; the block mask is then built from ``mod`` for
+    every (b, h) and must equal the oracle's tile states."""
     omod = mod if oracle_mod is None else oracle_mod
     c, d = make_dev(B, H, Sq, Skv, D, dtype, key_mask=key_mask, dout=dout)
     if key_mask_override is not None:
         c["key_mask"] = key_mask_override.clone()
         d["key_mask"] = key_mask_override.cuda()
     bm = E.create_block_mask(bm_kind, 1, 1, Sq, Skv) if bm_kind else None
+    if user_mask is not None:
+        bm = E.create_block_mask(mod, B, H, Sq, Skv)
+        np.testing.assert_array_equal(bm.tiles.cpu().numpy(), OR.build_block_mask(user_mask, B, H, Sq, Skv))
     dm = E.pack_dense_mask(dense.cuda(), B, H) if dense is not None else None
     dn = None if dense is None else dense.numpy()
     tdt = d["q"].dtype
@@ -53,12 +60,12 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
     lb, lse = guarded((B, H, Sq), torch.float32)
     vis = torch.full((B, H, nqb, nkb), 7, dtype=torch.uint8, device="cuda")
     E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod, out=out, lse=lse,
-               debug_visited=vis, dense_mask=dm)
+               debug_visited=vis, dense_mask=dm, scale=scale)
     grads = None
     if backward:
         gb = [guarded(d[n].shape, tdt) for n in ("q", "k", "v")]
         E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
-                   score_mod=mod, dq=gb[0][1], dk=gb[1][1], dv=gb[2][1], dense_mask=dm)
+                   score_mod=mod, dq=gb[0][1], dk=gb[1][1], dv=gb[2][1], dense_mask=dm, scale=scale)
         grads = gb
     shp = E.make_shape(d["q"], d["k"])
     assert E.poll_status(E.workspace(E.OP_FWD, shp, d["q"].device)) == E.ATTN_OK
@@ -68,9 +75,11 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
 
     km = None if c["key_mask"] is None else c["key_mask"].numpy()
     obm = _oracle_bm(bm_kind, B, H, Sq, Skv)
+    if user_mask is not None:
+        obm = OR.BlockMask(OR.build_block_mask(user_mask, B, H, Sq, Skv), user_mask)
     q64, k64, v64 = f64(c["q"]), f64(c["k"]), f64(c["v"])
     o_ref, lse_ref = OR.attn_fwd(q64, k64, v64, key_mask=km, block_mask=obm, score_mod=omod, heads=heads,
-                                 dense_mask=dn)
+                                 dense_mask=dn, scale=scale)
     sel = (slice(None),) if heads is None else tuple(np.array(x) for x in zip(*heads))
     tol = TOL[dtype]
     compare("out", f64(out)[sel], o_ref[sel], tol["o_max"], tol["o_mean"], dtype=dtype, kind="out",
@@ -87,7 +96,7 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
     np.testing.assert_array_equal(vis.cpu().numpy(), vis_ref)
     if backward:
         dq_r, dk_r, dv_r = OR.attn_bwd(q64, k64, v64, f64(c["dout"]), key_mask=km, block_mask=obm, score_mod=omod,
-                                       heads=heads, dense_mask=dn)
+                                       heads=heads, dense_mask=dn, scale=scale)
         for name, (buf, g), ref, shp in zip(("dq", "dk", "dv"), grads, (dq_r, dk_r, dv_r),
                                             ((B, H, Sq, D), (B, H, Skv, D), (B, H, Skv, D))):
             assert canary_ok(buf, shp), f"{name}: canary overwritten"
@@ -95,12 +104,12 @@ def run_and_check(B, H, Sq, Skv, dtype, mod, key_mask, bm_kind, dout="randn", ba
                     relative=not strict)
     if check_det:
         out2, lse2 = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], block_mask=bm, score_mod=mod,
-                                dense_mask=dm)
+                                dense_mask=dm, scale=scale)
         assert torch.equal(out2.view(torch.uint8), out.view(torch.uint8)), "forward not bitwise reproducible"
         assert torch.equal(lse2.view(torch.uint8), lse.view(torch.uint8)), "lse not bitwise reproducible"
-        if backward and D == 64:
+        if backward:
             g2 = E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"], block_mask=bm,
-                            score_mod=mod, dense_mask=dm)
+                            score_mod=mod, dense_mask=dm, scale=scale)
             for a, (_, b_) in zip(g2, grads):
                 assert torch.equal(a.view(torch.uint8), b_.view(torch.uint8)), "backward not bitwise reproducible"
 
@@ -122,6 +131,19 @@ def test_small_variants(B, H, S, dtype, mod, km, bm):
 @pytest.mark.parametrize("km,bm", [(False, None), (True, "causal")])
 def test_f32_variants(mod, km, bm):
     run_and_check(1, 2, 256, 256, "f32", mod, km, bm)
+
+
+# The ALiBi / checkerboard bias rides on the score MMA as bias / scale in three
+# 16-bit terms when that stays small (|bias / scale| <= 2^12); otherwise (tiny
+# scales) the kernels add it per score.  Both paths, and negative scales (the
+# key-mask term flips its infinity; no unscaled-maximum shortcut), against the
+# oracle, for every mod.
+@pytest.mark.parametrize("mod", ["alibi", "checkerboard", "none", "causal"])
+@pytest.mark.parametrize("scale,km,bm", [(1e-4, True, None), (-1e-4, False, "causal"), (-0.125, True, None),
+                                         (0.3, False, "causal"), (-0.3, True, "causal")])
+def test_mod_bias_paths(mod, scale, km, bm):
+    run_and_check(2, 2, 384, 300, "bf16", mod, km, bm, scale=scale)
+    run_and_check(1, 2, 200, 384, "f16", mod, km, bm, scale=scale)
 
 
 def test_rectangular_and_single_tile():
@@ -334,6 +356,41 @@ def test_user_score_mod(name, km, bm, Sq, Skv, dtype):
     run_and_check(2, 2, Sq, Skv, dtype, m, km, bm, oracle_mod=f)
 
 
+# Mask_mods compiled at run time: (mask expression, its oracle form, bias expression
+# or None, the bias's oracle form).  The block mask comes from the expression on
+# the GPU (tile states checked against the oracle's, every (b, h)); EMPTY tiles
+# are skipped (visited map), PARTIAL tiles evaluate the expression per entry.
+USER_MASKS = {
+    "window": ("(q - kv < 200) && (kv - q < 200)", lambda b, h, q, kv: np.abs(q - kv) < 200, None, None),
+    "document": ("(q / 100) == (kv / 100)", lambda b, h, q, kv: (q // 100) == (kv // 100), None, None),
+    "per_head": ("(h & 1) ? (kv >= q) : (kv <= q)", lambda b, h, q, kv: np.where(h % 2 == 1, kv >= q, kv <= q),
+                 None, None),
+    "batch_window_bias": ("(kv <= q) && (q - kv < 128 * (b + 1))", lambda b, h, q, kv: (kv <= q) & (q - kv < 128 * (b + 1)),
+                          "0.05f * (float)(kv - q)", lambda b, h, q, kv: 0.05 * (kv - q)),
+}
+
+
+@pytest.mark.parametrize("name,km,Sq,Skv", [("window", False, 640, 640), ("document", True, 384, 300),
+                                            ("per_head", False, 300, 384), ("batch_window_bias", True, 512, 512)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_user_mask_mod(name, km, Sq, Skv, dtype):
+    mexpr, mfn, bexpr, bfn = USER_MASKS[name]
+    m = E.compile_mask_mod(mexpr, bias_expr=bexpr, dtype=torch.bfloat16 if dtype == "bf16" else torch.float16)
+    run_and_check(2, 2, Sq, Skv, dtype, m, km, None, oracle_mod=bfn if bfn is not None else "none", user_mask=mfn)
+
+
+def test_user_mask_mod_builtin_entry_points_refuse_it():
+    """A block mask whose mask_mod is the user's goes only with that user mod."""
+    _, d = make_dev(1, 1, 256, 256, 64, "bf16")
+    m = E.compile_mask_mod("kv <= q")
+    bm = E.create_block_mask(m, 1, 1, 256, 256)
+    with pytest.raises(E.AttnError):
+        E.attn_fwd(d["q"], d["k"], d["v"], block_mask=bm)
+    plain = E.compile_score_mod("0.0f")   # a user mod without a mask expression
+    with pytest.raises(E.AttnError):
+        E.attn_fwd(d["q"], d["k"], d["v"], block_mask=bm, score_mod=plain)
+
+
 def test_user_score_mod_matches_builtin_alibi():
     """ALiBi written as a user expression gives the built-in ALiBi's result to rounding."""
     B, H, S = 2, 4, 384
@@ -386,14 +443,17 @@ def test_user_score_mod_dropped_while_queued():
     compare("out", f64(out), o_ref, TOL["bf16"]["o_max"], TOL["bf16"]["o_mean"], dtype="bf16", kind="out")
 
 
-def test_fully_masked_batches_and_blocks():
-    """Batch 1 has no key at all; batch 0 has whole 128-key blocks padded (skipped tiles)."""
+@pytest.mark.parametrize("scale", [None, -0.125])
+def test_fully_masked_batches_and_blocks(scale):
+    """Batch 1 has no key at all; batch 0 has whole 128-key blocks padded (skipped
+    tiles); also with a negative scale (rows with no key divide -inf by it)."""
     km = torch.ones((2, 512), dtype=torch.uint8)
     km[1] = 0
     km[0, 128:256] = 0
     km[0, 384:] = 0
     for dt in ("bf16", "f16", "f32"):
-        run_and_check(2, 2, 256, 512, dt, "none", True, None, key_mask_override=km)
+        for mod in ("none", "alibi"):
+            run_and_check(2, 2, 256, 512, dt, mod, True, None, key_mask_override=km, scale=scale)
 
 
 # ---------------------------------------------------------------- full-size workloads
@@ -468,15 +528,17 @@ D512 = [(B, H, S, dt, mod, bmk)
 
 
 @pytest.mark.parametrize("B,H,S,dtype,mod,bm", D512)
-def test_d512_forward_variants(B, H, S, dtype, mod, bm):
-    run_and_check(B, H, S, S, dtype, mod, False, bm, backward=False, D=512)
+def test_d512_variants(B, H, S, dtype, mod, bm):
+    """Head dim 512, forward and backward (the flash-attention-jax docs' long-sequence
+    head size; their value_and_grad_difference compares dq, dk, dv as well)."""
+    run_and_check(B, H, S, S, dtype, mod, False, bm, D=512)
 
 
 @pytest.mark.parametrize("mod,bm", [("none", None), ("alibi", "causal"), ("checkerboard", None), ("causal", None)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_d512_key_mask(mod, bm, dtype):
     """Head dim 512 with the key-padding mask (flash-attention-jax's (batch, seq) mask)."""
-    run_and_check(2, 1, 384, 512, dtype, mod, True, bm, backward=False, D=512)
+    run_and_check(2, 1, 384, 512, dtype, mod, True, bm, D=512)
 
 
 def test_d512_key_mask_padded_blocks():
@@ -485,7 +547,7 @@ def test_d512_key_mask_padded_blocks():
     km[1] = 0
     km[0, 128:256] = 0
     km[0, 384:] = 0
-    run_and_check(2, 2, 256, 512, "bf16", "none", True, None, backward=False, D=512, key_mask_override=km)
+    run_and_check(2, 2, 256, 512, "bf16", "none", True, None, D=512, key_mask_override=km)
 
 
 def test_flash_attention_entry_points():
@@ -527,8 +589,9 @@ def test_flash_attention_page_example_sampled_rows():
 
 
 def test_d512_rectangular():
-    run_and_check(1, 2, 128, 1024, "bf16", "alibi", False, None, backward=False, D=512)
-    run_and_check(1, 1, 384, 128, "bf16", "none", False, None, backward=False, D=512)
+    run_and_check(1, 2, 128, 1024, "bf16", "alibi", False, None, D=512)
+    run_and_check(1, 1, 384, 128, "bf16", "none", False, None, D=512)
+    run_and_check(2, 1, 256, 384, "f16", "causal", True, "causal", D=512, scale=-0.05)
 
 
 @pytest.mark.slow

@@ -512,3 +512,94 @@ def test_user_mod_finite_differences():
             return _loss(args["q"], args["k"], args["v"], do, **kw)
         gfd = _fd_grad(fn, x)
         assert np.abs(gfd - g).max() / max(1e-12, np.abs(g).max()) < 1e-6, name
+
+
+# ---------------------------------------------------------------------------
+# user mask_mods (callables g(b, h, q_idx, kv_idx) -> keep)
+# ---------------------------------------------------------------------------
+
+def test_user_mask_mod_causal_equals_builtin():
+    """A callable causal mask gives the built-in causal tile states and the same
+    attention, forward and backward, on a ragged shape."""
+    B, H, Sq, Skv, D = 2, 2, 300, 260, 4
+    g = lambda b, h, q, kv: kv <= q  # noqa: E731
+    np.testing.assert_array_equal(A.build_block_mask(g, B, H, Sq, Skv), A.build_block_mask("causal", B, H, Sq, Skv))
+    q, k, v, do = (_rand(B, H, n, D, seed=s) for n, s in ((Sq, 160), (Skv, 161), (Skv, 162), (Sq, 163)))
+    bu = A.BlockMask(A.build_block_mask(g, B, H, Sq, Skv), g)
+    bb = A.BlockMask(A.build_block_mask("causal", 1, 1, Sq, Skv), "causal")
+    for x, y in zip(A.attn_fwd(q, k, v, block_mask=bu), A.attn_fwd(q, k, v, block_mask=bb)):
+        np.testing.assert_array_equal(x, y)
+    for x, y in zip(A.attn_bwd(q, k, v, do, block_mask=bu), A.attn_bwd(q, k, v, do, block_mask=bb)):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("w", [1, 100, 200, 300])
+def test_user_mask_mod_sliding_window_closed_form(w):
+    """|q - kv| < w: over tile (i, j) of 128 x 128 the distance ranges from
+    max(0, 128 |i - j| - 127) to 128 |i - j| + 127, so the tile is EMPTY when the
+    smallest distance is >= w, FULL when the largest is < w, else PARTIAL."""
+    S = 640
+    g = lambda b, h, q, kv: np.abs(q - kv) < w  # noqa: E731
+    st = A.build_block_mask(g, 1, 1, S, S)[0, 0]
+    n = S // 128
+    for i in range(n):
+        for j in range(n):
+            lo, hi = max(0, 128 * abs(i - j) - 127), 128 * abs(i - j) + 127
+            want = A.TILE_EMPTY if lo >= w else (A.TILE_FULL if hi < w else A.TILE_PARTIAL)
+            assert st[i, j] == want, (i, j)
+
+
+@pytest.mark.parametrize("L", [50, 100, 128, 300])
+def test_user_mask_mod_document_closed_form(L):
+    """Documents of L tokens (q // L == kv // L): tile (i, j) is EMPTY when the
+    document ranges of its rows and columns are disjoint and FULL when both are
+    the same single document."""
+    S = 512
+    g = lambda b, h, q, kv: (q // L) == (kv // L)  # noqa: E731
+    st = A.build_block_mask(g, 1, 1, S, S)[0, 0]
+    for i in range(S // 128):
+        for j in range(S // 128):
+            ri = (128 * i // L, (128 * i + 127) // L)
+            rj = (128 * j // L, (128 * j + 127) // L)
+            if ri[1] < rj[0] or rj[1] < ri[0]:
+                want = A.TILE_EMPTY
+            elif ri[0] == ri[1] == rj[0] == rj[1]:
+                want = A.TILE_FULL
+            else:
+                want = A.TILE_PARTIAL
+            assert st[i, j] == want, (i, j)
+
+
+def test_user_mask_mod_depends_on_batch_and_head():
+    """A mask that keeps kv <= q for (b, h) = (0, 1) and kv >= q elsewhere: the tile
+    states of (0, 1) are those of causal, the others their transpose."""
+    B, H, S = 2, 2, 384
+    g = lambda b, h, q, kv: np.where((b == 0) & (h == 1), kv <= q, kv >= q)  # noqa: E731
+    st = A.build_block_mask(g, B, H, S, S)
+    causal = A.build_block_mask("causal", 1, 1, S, S)[0, 0]
+    for b in range(B):
+        for h in range(H):
+            want = causal if (b, h) == (0, 1) else causal.T
+            np.testing.assert_array_equal(st[b, h], want)
+
+
+def test_user_mask_mod_brute_force():
+    """Attention through a user mask's block mask against loops over the kept pairs
+    (the mask depends on b, h, q and kv and is not symmetric)."""
+    B, H, S, D = 2, 2, 6, 3
+    q, k, v = _rand(B, H, S, D, seed=170), _rand(B, H, S, D, seed=171), _rand(B, H, S, D, seed=172)
+
+    def keep(b, h, qq, kk):
+        return ((qq + 2 * kk + b + h) % 3 != 0) | (kk == qq)
+    bm = A.BlockMask(A.build_block_mask(keep, B, H, S, S, 4, 4), keep, 4, 4)
+    o, lse = A.attn_fwd(q, k, v, block_mask=bm, scale=0.6)
+    for b in range(B):
+        for h in range(H):
+            for i in range(S):
+                z = {j: 0.6 * sum(q[b, h, i, d] * k[b, h, j, d] for d in range(D))
+                     for j in range(S) if (i + 2 * j + b + h) % 3 != 0 or i == j}
+                top = max(z.values())
+                tot = sum(math.exp(x - top) for x in z.values())
+                assert abs(lse[b, h, i] - (top + math.log(tot))) < 1e-12
+                ref = sum(math.exp(x - top) / tot * v[b, h, j] for j, x in z.items())
+                np.testing.assert_allclose(o[b, h, i], ref, rtol=1e-12, atol=1e-12)

@@ -44,6 +44,10 @@ MUTANTS = {
                       "return dm[0, 0 if dm.shape[1] == 1 else h]"),
     "dense_bcast_h": ("return dm[0 if dm.shape[0] == 1 else b, 0 if dm.shape[1] == 1 else h]",
                       "return dm[0 if dm.shape[0] == 1 else b, 0]"),
+    "user_mask_swapped": ("out = np.asarray(mask_mod(b, h, qi, kj), dtype=bool)",
+                          "out = np.asarray(mask_mod(b, h, kj, qi), dtype=bool)"),
+    "user_mask_head_of_first": ("keep = mask_mod_keep(mask_mod, qi, kj, b, h)",
+                                "keep = mask_mod_keep(mask_mod, qi, kj, 0, 0)"),
     "full_tile_masked": ("keep &= (ts != TILE_EMPTY) & ((ts == TILE_FULL) | mm)",
                          "keep &= (ts != TILE_EMPTY) & mm"),
 }
@@ -71,6 +75,8 @@ PINS = [
     lambda: [T.test_dense_mask_brute_force(bs) for bs in [(2, 3), (1, 3), (2, 1)]],
     lambda: [T.test_query_offset_equals_rows_of_full(m) for m in T.MODS],
     lambda: T.test_user_mod_brute_force(),
+    lambda: T.test_user_mask_mod_depends_on_batch_and_head(),
+    lambda: T.test_user_mask_mod_brute_force(),
 ]
 
 
