@@ -15,12 +15,8 @@
 
 using namespace attn;
 
-namespace {
-
-constexpr long long kMaxRows = (1LL << 31) - 1;
-
 // Device-side wait limit, read at every call (ATTN_TIMEOUT_NS, default 2 s).
-unsigned long long timeout_ns() {
+unsigned long long attn::attn_timeout_ns() {
   const char* e = std::getenv("ATTN_TIMEOUT_NS");
   unsigned long long v = 2000000000ULL;
   if (e && *e) {
@@ -30,6 +26,12 @@ unsigned long long timeout_ns() {
   }
   return v;
 }
+
+namespace {
+
+constexpr long long kMaxRows = (1LL << 31) - 1;
+
+unsigned long long timeout_ns() { return attn::attn_timeout_ns(); }
 
 // Test hook, off unless ATTN_DEBUG_INJECT_STALL=1: the D = 64 forward's producer
 // withholds its first K/V copy, so the kernel's bounded waits run out and it

@@ -194,13 +194,18 @@ __global__ void __launch_bounds__(DEC_THREADS, (1024 / DEC_THREADS > 0 ? 1024 / 
       mine[1] = L;
     }
   }
-  // ---- the last CTA of this (b, h) merges all splits
-  __threadfence();
+  // ---- the last CTA of this (b, h) merges all splits.  The CTA barrier orders the
+  // partial's stores before thread 0's fence, whose gpu-scope ordering covers
+  // them (cumulativity), so one fence per CTA publishes the partial before its ticket.
   __syncthreads();
-  if (tid == 0) ticket = atomicAdd(p.counter + bh, 1u);
+  if (tid == 0) {
+    __threadfence();
+    ticket = atomicAdd(p.counter + bh, 1u);
+  }
   __syncthreads();
   if (ticket != (unsigned)(p.nsplit - 1)) return;
-  __threadfence();
+  if (tid == 0) __threadfence();
+  __syncthreads();
   // max over the splits: threads stride over them, then a CTA reduction
   const float* all = p.partial + (size_t)bh * p.nsplit * (2 + 64);
   float Mx = -INFINITY;

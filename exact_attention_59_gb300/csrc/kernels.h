@@ -172,6 +172,8 @@ struct DecodeParams {
   int mod;
 };
 #ifndef __CUDACC_RTC__
+// Device-side wait limit (ATTN_TIMEOUT_NS, default 2 s), read at every call.
+unsigned long long attn_timeout_ns();
 int decode_num_splits(int B, int H, int Skv);
 cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t st);
 #endif  // host
