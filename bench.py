@@ -573,12 +573,14 @@ def run_profile_case(args):
     BLD.build()
     E.load()
     dev = torch.device("cuda", 0)
-    w = WL
-    c = IN.make_case(args.batch, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=True)
-    d = {k: v.to(dev) for k, v in c.items()}
+    w = {"keypad": WL, "checkerboard": W.CHECKERBOARD_FP16, "causal_alibi": W.FLEX_CAUSAL_ALIBI_BF16}[args.wl]
+    c = IN.make_case(args.batch, w.H, w.Sq, w.Skv, w.D, w.dtype, with_key_mask=w.key_mask, dout=w.dout)
+    d = {k: v.to(dev) for k, v in c.items() if v is not None}
+    km = d.get("key_mask")
+    bm = E.create_block_mask(w.block_mask, 1, 1, w.Sq, w.Skv) if w.block_mask else None
     for _ in range(args.steps):
-        out, lse = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"])
-        E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=d["key_mask"])
+        out, lse = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=km, block_mask=bm, score_mod=w.score_mod)
+        E.attn_bwd(d["q"], d["k"], d["v"], out, lse, d["dout"], key_mask=km, block_mask=bm, score_mod=w.score_mod)
     if args.d512:
         S = args.d512
         q = IN.randn((1, 2, S, 512), IN.SEED + 1, "bf16").to(dev)
@@ -611,6 +613,8 @@ def main():
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
                     help="profile: a few untimed steps at --batch, for ncu captures")
     ap.add_argument("--batch", type=int, default=16)
+    ap.add_argument("--wl", choices=["keypad", "checkerboard", "causal_alibi"], default="keypad",
+                    help="profile mode: the workload whose fwd+bwd runs (at --batch)")
     ap.add_argument("--decode", action="store_true", help="profile mode: also run decode at --batch")
     ap.add_argument("--d512", type=int, default=0,
                     help="profile mode: also run the causal 1 x 2 x S x S x 512 bf16 forward at this S")
