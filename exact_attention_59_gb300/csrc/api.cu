@@ -293,6 +293,7 @@ SimtParams simt_params(const attn_shape* s, const void* q, const void* k, const 
   p.mod = (int)mod;
   p.sc = scale * kLog2e;
   p.scale = scale;
+  p.timeout_ns = timeout_ns();
   return p;
 }
 
@@ -419,7 +420,8 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
     p.o = (float*)out;
     p.lse = lse;
     p.visited = debug_visited;
-    return cuda_status(launch_simt_fwd(p, st));
+    p.status = at<int>(ws, 0);
+    return cuda_status(launch_f32_fwd(p, st));
   }
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -515,7 +517,8 @@ attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, con
     p.dv = (float*)dv;
     p.delta = at<float>(ws, w.delta);
     p.lse2 = at<float>(ws, w.lse2);
-    return cuda_status(launch_simt_bwd_dkdv(p, st));
+    p.status = at<int>(ws, 0);
+    return cuda_status(launch_f32_dkdv(p, st));
   }
   bool ok;
   BwdParams p = bwd_params(s, q, k, v, dout, key_mask, bm, mod, scale, ws, ok);
@@ -551,7 +554,8 @@ attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const
     p.dq = (float*)dq;
     p.delta = at<float>(ws, w.delta);
     p.lse2 = at<float>(ws, w.lse2);
-    return cuda_status(launch_simt_bwd_dq(p, st));
+    p.status = at<int>(ws, 0);
+    return cuda_status(launch_f32_dq(p, st));
   }
   bool ok;
   BwdParams p = bwd_params(s, q, k, v, dout, key_mask, bm, mod, scale, ws, ok);

@@ -199,11 +199,14 @@ struct SimtParams {
   uint8_t* visited;
   int B, H, Sq, Skv, nqb, nkb, mod;
   float sc, scale;
+  int* status;                    // workspace status word (the tensor-core kernels' bounded waits)
+  unsigned long long timeout_ns;
 };
 #ifndef __CUDACC_RTC__
-cudaError_t launch_simt_fwd(const SimtParams& p, cudaStream_t st);
-cudaError_t launch_simt_bwd_dkdv(const SimtParams& p, cudaStream_t st);
-cudaError_t launch_simt_bwd_dq(const SimtParams& p, cudaStream_t st);
+// float32 on the tensor cores (tcgen05 kind::tf32, three products per contraction)
+cudaError_t launch_f32_fwd(const SimtParams& p, cudaStream_t st);
+cudaError_t launch_f32_dq(const SimtParams& p, cudaStream_t st);
+cudaError_t launch_f32_dkdv(const SimtParams& p, cudaStream_t st);
 #endif  // host
 
 }  // namespace attn
