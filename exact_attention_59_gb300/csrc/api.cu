@@ -161,7 +161,7 @@ attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATT
 // f32 and D = 512.
 attn_status check_prefill(const attn_shape* s, bool backward) {
   if (!shape_ok(s)) return ATTN_ERR_INVALID_ARG;
-  const bool ragged_ok = s->D == 64 && s->dtype != ATTN_F32;
+  const bool ragged_ok = s->D == 64;
   if (!ragged_ok && (s->Sq % 128 != 0 || s->Skv % 128 != 0)) return ATTN_ERR_SHAPE;
   if (tiles_of(s->Skv) > FWD_MAXKB || tiles_of(s->Sq) > FWD_MAXKB) return ATTN_ERR_SHAPE;
   (void)backward;   // D = 512 has a forward and a backward, f16/bf16
@@ -307,7 +307,7 @@ attn_status check_dm(const attn_shape* s, const attn_dense_mask* dm) {
   if (!dm->packed || (dm->bcast_b != 0 && dm->bcast_b != 1) || (dm->bcast_h != 0 && dm->bcast_h != 1))
     return ATTN_ERR_INVALID_ARG;
   if (!aligned(dm->packed, 256)) return ATTN_ERR_ALIGN;
-  if (s->D != 64 || s->dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+  if (s->D != 64) return ATTN_ERR_UNSUPPORTED;
   if (dm->packed_bytes < dense_mask_layout(dense_mask_count(s, dm->bcast_b, dm->bcast_h), s->Sq, s->Skv).total)
     return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
@@ -417,6 +417,7 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   const WsLayout w = layout(ATTN_OP_FWD, s);
   if (s->dtype == ATTN_F32) {
     SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
+    p.dm = dm_view(s, dm);
     p.o = (float*)out;
     p.lse = lse;
     p.visited = debug_visited;
@@ -511,6 +512,7 @@ attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, con
   cudaStream_t st = (cudaStream_t)stream;
   if (s->dtype == ATTN_F32) {
     SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
+    p.dm = dm_view(s, dm);
     const WsLayout w = layout(ATTN_OP_BWD, s);
     p.dout = (const float*)dout;
     p.dk = (float*)dk;
@@ -549,6 +551,7 @@ attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const
   cudaStream_t st = (cudaStream_t)stream;
   if (s->dtype == ATTN_F32) {
     SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
+    p.dm = dm_view(s, dm);
     const WsLayout w = layout(ATTN_OP_BWD, s);
     p.dout = (const float*)dout;
     p.dq = (float*)dq;

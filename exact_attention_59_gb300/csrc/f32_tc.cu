@@ -20,7 +20,9 @@
 //   dK/dV:    per 128-key tile, per 64-query step: S^T = K Q^T, dP^T = V dO^T,
 //             P^T and dS^T, dV += P^T dO, dK += dS^T Q.
 // Tile skipping and masks as in the 16-bit kernels (block-mask states, key
-// padding, causal rule); every wait on an MMA is bounded.
+// padding, the causal rule, the packed dense mask's tile states and bits), any
+// Sq and Skv (partial last tiles: rows past the end are zeros in the operand
+// tiles, get no weight, and are not written); every wait on an MMA is bounded.
 #include "kernels.h"
 
 namespace attn {
@@ -57,11 +59,13 @@ DEVI uint32_t swz32(int r, int c, int rows) {
 
 // A row-major (rows x 64) f32 tile from global memory into the hi / lo tiles,
 // as is (element (r, c) at (r, c)) or transposed (at (c, r), the tile then has
-// 64 rows and `rows` K columns).  All 128 threads, 16-byte global loads.
-DEVI void load_split(const float* g, int rows, uint8_t* hi, uint8_t* lo, bool transpose) {
+// 64 rows and `rows` K columns); rows from `valid` on (past the end of the
+// sequence) are zeros and are not read.  All 128 threads, 16-byte global loads.
+DEVI void load_split(const float* g, int rows, uint8_t* hi, uint8_t* lo, bool transpose, int valid) {
   for (int i = threadIdx.x; i < rows * 16; i += F32_T) {
     const int r = i >> 4, c0 = (i & 15) * 4;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(g + (size_t)r * 64 + c0));
+    const float4 v = r < valid ? __ldg(reinterpret_cast<const float4*>(g + (size_t)r * 64 + c0))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
     const float x[4] = {v.x, v.y, v.z, v.w};
     if (!transpose) {
       float h[4], l[4];
@@ -220,32 +224,43 @@ __global__ void __launch_bounds__(F32_T, 1) f32_fwd_kernel(const __grid_constant
   const int b = bh / p.H, h = bh % p.H;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int q = qt * 128 + tid;
+  const bool q_in = q < p.Sq;   // rows past Sq (a partial last tile) are computed, not written
   f32_setup(sm);
   const uint32_t tm = sm.tmem_base, lo = static_cast<uint32_t>(32 * warp) << 16;
   constexpr uint32_t C_S = 0, C_O = 64, C_PH = 128, C_PL = 192;
-  load_split(p.q + ((size_t)bh * p.Sq + qt * 128) * 64, 128, sm.t0hi, sm.t0lo, false);
+  load_split(p.q + ((size_t)bh * p.Sq + qt * 128) * 64, 128, sm.t0hi, sm.t0lo, false, p.Sq - qt * 128);
   const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+  const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;   // dense-mask index of (b, h)
   float m = -INFINITY, l = 0.f;
   uint32_t phase = 0;
   int n = 0;
   bool ok = true;
   for (int kb = 0; kb < p.nkb && ok; ++kb) {
     const int st = f32_tile_state(p, b, h, qt, kb);
-    // keys of the block kept by the key mask (the tile is skipped when none is)
+    const int ds = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb] : TILE_FULL;
+    // keys of the block that exist and that the key mask keeps (the tile is skipped when none is)
     const int kv_t = kb * 128 + tid;
-    const bool keep_t = p.key_mask ? p.key_mask[(size_t)b * p.Skv + kv_t] != 0 : true;
+    const bool keep_t = kv_t < p.Skv && (p.key_mask ? p.key_mask[(size_t)b * p.Skv + kv_t] != 0 : true);
     const bool any = __syncthreads_or(keep_t);
-    const bool visit = st != TILE_EMPTY && any;
+    const bool visit = st != TILE_EMPTY && ds != TILE_EMPTY && any;
     if (p.visited && tid == 0) p.visited[((size_t)bh * p.nqb + qt) * p.nkb + kb] = visit ? 1 : 0;
     if (!visit) continue;
     const bool causal = MOD == MOD_CAUSAL || (st == TILE_PARTIAL && p.bm_mod == MASKMOD_CAUSAL);
     for (int half = 0; half < 2 && ok; ++half) {
       const int kv0 = kb * 128 + F32_STEP * half;
+      if (kv0 >= p.Skv) break;   // a partial last block
       __syncthreads();   // the previous step's readers of keep and the tiles are done
       if (tid >= F32_STEP * half && tid < F32_STEP * (half + 1)) sm.keep[tid - F32_STEP * half] = keep_t ? 1 : 0;
       const size_t kvrow = (size_t)bh * p.Skv + kv0;
-      load_split(p.k + kvrow * 64, F32_STEP, sm.s0hi, sm.s0lo, false);   // K: B of S = Q K^T
-      load_split(p.v + kvrow * 64, F32_STEP, sm.s1hi, sm.s1lo, true);    // V^T: B of O += P V
+      load_split(p.k + kvrow * 64, F32_STEP, sm.s0hi, sm.s0lo, false, p.Skv - kv0);   // K: B of S = Q K^T
+      load_split(p.v + kvrow * 64, F32_STEP, sm.s1hi, sm.s1lo, true, p.Skv - kv0);    // V^T: B of O += P V
+      // this row's dense-mask bits for the step's 64 keys (a PARTIAL dense tile)
+      uint32_t dw0 = 0xffffffffu, dw1 = 0xffffffffu;
+      if (ds == TILE_PARTIAL && q_in) {
+        const uint32_t* w = p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) + 4 * kb + 2 * half;
+        dw0 = __ldg(w);
+        dw1 = __ldg(w + 1);
+      }
       f32_publish();
       if (tid == 0) {
         mma3_ss(tm + C_S, sm.t0hi, sm.t0lo, sm.s0hi, sm.s0lo, F32_STEP, false);
@@ -260,7 +275,7 @@ __global__ void __launch_bounds__(F32_T, 1) f32_fwd_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float v = f32_logit<MOD>(__uint_as_float(r[c]), p.sc, slope2, q, kv0 + c, causal);
-          v = sm.keep[c] ? v : -INFINITY;
+          v = (sm.keep[c] && (((c < 32 ? dw0 : dw1) >> (c & 31)) & 1u)) ? v : -INFINITY;
           x[c] = v;
           mx = fmaxf(mx, v);
         }
@@ -293,8 +308,9 @@ __global__ void __launch_bounds__(F32_T, 1) f32_fwd_kernel(const __grid_constant
       ++n;
     }
   }
+  // the TMEM load stays warp-wide (tcgen05.ld is .sync.aligned): only the global
+  // stores of rows past Sq are left out
   if (ok) {
-    float* orow = p.o + ((size_t)bh * p.Sq + q) * 64;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     uint32_t o[64];
     if (n > 0) {
@@ -303,12 +319,16 @@ __global__ void __launch_bounds__(F32_T, 1) f32_fwd_kernel(const __grid_constant
 #pragma unroll
       for (int c = 0; c < 64; ++c) o[c] = 0u;
     }
+    if (q_in) {
+      float* orow = p.o + ((size_t)bh * p.Sq + q) * 64;
 #pragma unroll
-    for (int c = 0; c < 64; c += 4)
-      *reinterpret_cast<float4*>(orow + c) = make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
-                                                         __uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
-    const float mf = (m == -INFINITY) ? 0.f : m;
-    p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (mf + lg2(l)) * kLn2 : -INFINITY;
+      for (int c = 0; c < 64; c += 4)
+        *reinterpret_cast<float4*>(orow + c) = make_float4(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv,
+                                                           __uint_as_float(o[c + 2]) * inv,
+                                                           __uint_as_float(o[c + 3]) * inv);
+      const float mf = (m == -INFINITY) ? 0.f : m;
+      p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (mf + lg2(l)) * kLn2 : -INFINITY;
+    }
   }
   f32_teardown(sm, p, phase, !ok);
 }
@@ -324,32 +344,43 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dq_kernel(const __grid_constant_
   const int b = bh / p.H, h = bh % p.H;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int q = qt * 128 + tid;
+  const bool q_in = q < p.Sq;
   f32_setup(sm);
   const uint32_t tm = sm.tmem_base, lo = static_cast<uint32_t>(32 * warp) << 16;
   constexpr uint32_t C_S = 0, C_DP = 64, C_DSH = 128, C_DSL = 192, C_DQ = 256;
   const size_t qrow = (size_t)bh * p.Sq + qt * 128;
-  load_split(p.q + qrow * 64, 128, sm.t0hi, sm.t0lo, false);
-  load_split(p.dout + qrow * 64, 128, sm.t1hi, sm.t1lo, false);
+  load_split(p.q + qrow * 64, 128, sm.t0hi, sm.t0lo, false, p.Sq - qt * 128);
+  load_split(p.dout + qrow * 64, 128, sm.t1hi, sm.t1lo, false, p.Sq - qt * 128);
   const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
-  const float nl2 = p.lse2[(size_t)bh * p.Sq + q];   // -lse log2(e)
-  const float nd = p.delta[(size_t)bh * p.Sq + q];   // -D
+  // rows past Sq get P = 0 and are not written
+  const float nl2 = q_in ? p.lse2[(size_t)bh * p.Sq + q] : -INFINITY;   // -lse log2(e)
+  const float nd = q_in ? p.delta[(size_t)bh * p.Sq + q] : 0.f;         // -D
+  const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
   uint32_t phase = 0;
   int n = 0;
   bool ok = true;
   for (int kb = 0; kb < p.nkb && ok; ++kb) {
     const int st = f32_tile_state(p, b, h, qt, kb);
+    const int dst = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb] : TILE_FULL;
     const int kv_t = kb * 128 + tid;
-    const bool keep_t = p.key_mask ? p.key_mask[(size_t)b * p.Skv + kv_t] != 0 : true;
+    const bool keep_t = kv_t < p.Skv && (p.key_mask ? p.key_mask[(size_t)b * p.Skv + kv_t] != 0 : true);
     const bool any = __syncthreads_or(keep_t);
-    if (st == TILE_EMPTY || !any) continue;
+    if (st == TILE_EMPTY || dst == TILE_EMPTY || !any) continue;
     const bool causal = MOD == MOD_CAUSAL || (st == TILE_PARTIAL && p.bm_mod == MASKMOD_CAUSAL);
     for (int half = 0; half < 2 && ok; ++half) {
       const int kv0 = kb * 128 + F32_STEP * half;
+      if (kv0 >= p.Skv) break;
       __syncthreads();
       if (tid >= F32_STEP * half && tid < F32_STEP * (half + 1)) sm.keep[tid - F32_STEP * half] = keep_t ? 1 : 0;
       const size_t kvrow = (size_t)bh * p.Skv + kv0;
-      load_split(p.k + kvrow * 64, F32_STEP, sm.s0hi, sm.s0lo, false);   // K: B of S = Q K^T
-      load_split(p.v + kvrow * 64, F32_STEP, sm.s1hi, sm.s1lo, false);   // V: B of dP = dO V^T
+      load_split(p.k + kvrow * 64, F32_STEP, sm.s0hi, sm.s0lo, false, p.Skv - kv0);   // K: B of S = Q K^T
+      load_split(p.v + kvrow * 64, F32_STEP, sm.s1hi, sm.s1lo, false, p.Skv - kv0);   // V: B of dP = dO V^T
+      uint32_t dw0 = 0xffffffffu, dw1 = 0xffffffffu;
+      if (dst == TILE_PARTIAL && q_in) {
+        const uint32_t* w = p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) + 4 * kb + 2 * half;
+        dw0 = __ldg(w);
+        dw1 = __ldg(w + 1);
+      }
       f32_publish();
       if (tid == 0) {
         mma3_ss(tm + C_S, sm.t0hi, sm.t0lo, sm.s0hi, sm.s0lo, F32_STEP, false);
@@ -358,7 +389,7 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dq_kernel(const __grid_constant_
       }
       if (!(ok = f32_wait(sm, p, phase, 63))) break;
       // K^T (B of dQ += dS K) replaces V, which the products above have read
-      load_split(p.k + kvrow * 64, F32_STEP, sm.s1hi, sm.s1lo, true);
+      load_split(p.k + kvrow * 64, F32_STEP, sm.s1hi, sm.s1lo, true, p.Skv - kv0);
       float ds[64];
       {
         uint32_t r[64], dp[64];
@@ -367,7 +398,7 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dq_kernel(const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float x = f32_logit<MOD>(__uint_as_float(r[c]), p.sc, slope2, q, kv0 + c, causal) + nl2;
-          x = sm.keep[c] ? x : -INFINITY;
+          x = (sm.keep[c] && (((c < 32 ? dw0 : dw1) >> (c & 31)) & 1u)) ? x : -INFINITY;
           const float pp = ex2(x);
           ds[c] = pp * (__uint_as_float(dp[c]) + nd);
         }
@@ -382,8 +413,7 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dq_kernel(const __grid_constant_
       ++n;
     }
   }
-  if (ok) {
-    float* row = p.dq + ((size_t)bh * p.Sq + q) * 64;
+  if (ok) {   // warp-wide TMEM load; rows past Sq are not stored
     uint32_t o[64];
     if (n > 0) {
       tmem_ld64(tm + lo + C_DQ, o);
@@ -391,11 +421,14 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dq_kernel(const __grid_constant_
 #pragma unroll
       for (int c = 0; c < 64; ++c) o[c] = 0u;
     }
+    if (q_in) {
+      float* row = p.dq + ((size_t)bh * p.Sq + q) * 64;
 #pragma unroll
-    for (int c = 0; c < 64; c += 4)
-      *reinterpret_cast<float4*>(row + c) =
-          make_float4(__uint_as_float(o[c]) * p.scale, __uint_as_float(o[c + 1]) * p.scale,
-                      __uint_as_float(o[c + 2]) * p.scale, __uint_as_float(o[c + 3]) * p.scale);
+      for (int c = 0; c < 64; c += 4)
+        *reinterpret_cast<float4*>(row + c) =
+            make_float4(__uint_as_float(o[c]) * p.scale, __uint_as_float(o[c + 1]) * p.scale,
+                        __uint_as_float(o[c + 2]) * p.scale, __uint_as_float(o[c + 3]) * p.scale);
+    }
   }
   f32_teardown(sm, p, phase, !ok);
 }
@@ -415,29 +448,42 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dkdv_kernel(const __grid_constan
   const uint32_t tm = sm.tmem_base, lo = static_cast<uint32_t>(32 * warp) << 16;
   constexpr uint32_t C_S = 0, C_DP = 64, C_PH = 128, C_PL = 192, C_DSH = 256, C_DSL = 320, C_DV = 384, C_DK = 448;
   const size_t kvrow = (size_t)bh * p.Skv + kb * 128;
-  // a padded key's dK and dV rows are zero; its P^T and dS^T rows stay confined to it
-  const bool my_key = p.key_mask ? p.key_mask[(size_t)b * p.Skv + kv] != 0 : true;
+  // a padded key's dK and dV rows are zero; its P^T and dS^T rows stay confined to
+  // it; rows past Skv (a partial last block) are not written
+  const bool kv_in = kv < p.Skv;
+  const bool my_key = kv_in && (p.key_mask ? p.key_mask[(size_t)b * p.Skv + kv] != 0 : true);
   const bool any_key = __syncthreads_or(my_key);
-  load_split(p.k + kvrow * 64, 128, sm.t0hi, sm.t0lo, false);   // K: A of S^T = K Q^T
-  load_split(p.v + kvrow * 64, 128, sm.t1hi, sm.t1lo, false);   // V: A of dP^T = V dO^T
+  load_split(p.k + kvrow * 64, 128, sm.t0hi, sm.t0lo, false, p.Skv - kb * 128);   // K: A of S^T = K Q^T
+  load_split(p.v + kvrow * 64, 128, sm.t1hi, sm.t1lo, false, p.Skv - kb * 128);   // V: A of dP^T = V dO^T
   const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+  const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
   uint32_t phase = 0;
   int n = 0;
   bool ok = true;
   for (int qt = 0; qt < p.nqb && ok && any_key; ++qt) {
     const int st = f32_tile_state(p, b, h, qt, kb);
-    if (st == TILE_EMPTY) continue;
+    const int dst = p.dm.tiles ? p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb] : TILE_FULL;
+    if (st == TILE_EMPTY || dst == TILE_EMPTY) continue;
     const bool causal = MOD == MOD_CAUSAL || (st == TILE_PARTIAL && p.bm_mod == MASKMOD_CAUSAL);
     for (int half = 0; half < 2 && ok; ++half) {
       const int q0 = qt * 128 + F32_STEP * half;
+      if (q0 >= p.Sq) break;   // a partial last q tile
       const size_t qrow = (size_t)bh * p.Sq + q0;
       __syncthreads();
-      if (tid < F32_STEP) {
-        sm.colv[0][tid] = p.lse2[qrow + tid];   // -lse log2(e)
-        sm.colv[1][tid] = p.delta[qrow + tid];  // -D
+      if (tid < F32_STEP) {   // queries past Sq get P = 0
+        const bool in = q0 + tid < p.Sq;
+        sm.colv[0][tid] = in ? p.lse2[qrow + tid] : -INFINITY;   // -lse log2(e)
+        sm.colv[1][tid] = in ? p.delta[qrow + tid] : 0.f;        // -D
       }
-      load_split(p.q + qrow * 64, F32_STEP, sm.s0hi, sm.s0lo, false);      // Q: B of S^T
-      load_split(p.dout + qrow * 64, F32_STEP, sm.s1hi, sm.s1lo, false);   // dO: B of dP^T
+      load_split(p.q + qrow * 64, F32_STEP, sm.s0hi, sm.s0lo, false, p.Sq - q0);      // Q: B of S^T
+      load_split(p.dout + qrow * 64, F32_STEP, sm.s1hi, sm.s1lo, false, p.Sq - q0);   // dO: B of dP^T
+      // this key's dense-mask bits for the step's 64 queries (a PARTIAL dense tile)
+      uint32_t dw0 = 0xffffffffu, dw1 = 0xffffffffu;
+      if (dst == TILE_PARTIAL && kv_in) {
+        const uint32_t* w = p.dm.colbits + (dmi * p.Skv + kv) * (4LL * p.nqb) + 4 * qt + 2 * half;
+        dw0 = __ldg(w);
+        dw1 = __ldg(w + 1);
+      }
       f32_publish();
       if (tid == 0) {
         mma3_ss(tm + C_S, sm.t0hi, sm.t0lo, sm.s0hi, sm.s0lo, F32_STEP, false);
@@ -446,8 +492,8 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dkdv_kernel(const __grid_constan
       }
       if (!(ok = f32_wait(sm, p, phase, 65))) break;
       // dO^T and Q^T (B of dV += P^T dO and dK += dS^T Q) replace Q and dO, which are read
-      load_split(p.dout + qrow * 64, F32_STEP, sm.s0hi, sm.s0lo, true);
-      load_split(p.q + qrow * 64, F32_STEP, sm.s1hi, sm.s1lo, true);
+      load_split(p.dout + qrow * 64, F32_STEP, sm.s0hi, sm.s0lo, true, p.Sq - q0);
+      load_split(p.q + qrow * 64, F32_STEP, sm.s1hi, sm.s1lo, true, p.Sq - q0);
       float pr[64], ds[64];
       {
         uint32_t r[64], dp[64];
@@ -455,7 +501,8 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dkdv_kernel(const __grid_constan
         tmem_ld64(tm + lo + C_DP, dp);
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float x = f32_logit<MOD>(__uint_as_float(r[c]), p.sc, slope2, q0 + c, kv, causal) + sm.colv[0][c];
+          float x = f32_logit<MOD>(__uint_as_float(r[c]), p.sc, slope2, q0 + c, kv, causal) + sm.colv[0][c];
+          x = (((c < 32 ? dw0 : dw1) >> (c & 31)) & 1u) ? x : -INFINITY;
           pr[c] = ex2(x);
           ds[c] = pr[c] * (__uint_as_float(dp[c]) + sm.colv[1][c]);
         }
@@ -472,7 +519,7 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dkdv_kernel(const __grid_constan
       ++n;
     }
   }
-  if (ok) {
+  if (ok) {   // warp-wide TMEM loads; rows past Skv are not stored
     for (int g = 0; g < 2; ++g) {   // g = 0: dV, 1: dK (times scale)
       const float mul = (g == 0 ? 1.f : p.scale) * (my_key ? 1.f : 0.f);
       float* row = (g == 0 ? p.dv : p.dk) + ((size_t)bh * p.Skv + kv) * 64;
@@ -483,6 +530,7 @@ __global__ void __launch_bounds__(F32_T, 1) f32_dkdv_kernel(const __grid_constan
 #pragma unroll
         for (int c = 0; c < 64; ++c) o[c] = 0u;
       }
+      if (!kv_in) continue;
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         float4 w;

@@ -201,6 +201,7 @@ struct SimtParams {
   float sc, scale;
   int* status;                    // workspace status word (the tensor-core kernels' bounded waits)
   unsigned long long timeout_ns;
+  DenseMaskView dm;               // dense (query, key) mask, dm.tiles = nullptr if none
 };
 #ifndef __CUDACC_RTC__
 // float32 on the tensor cores (tcgen05 kind::tf32, three products per contraction)

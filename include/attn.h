@@ -25,13 +25,15 @@
  *  - key_mask is uint8 (B, Skv), nonzero = attend; NULL = no key mask.
  *  - Every pointer must be 16-byte aligned (the TMA engine needs it), else
  *    ATTN_ERR_ALIGN.
- *  - Prefill (attn_fwd / attn_bwd) in f16/bf16 with D = 64 takes any
+ *  - Prefill (attn_fwd / attn_bwd) with D = 64 (f16, bf16 and f32) takes any
  *    Sq, Skv >= 1 (up to 2048 tiles of 128): the last q and kv tiles may be
  *    partial; keys past Skv get no weight and rows past Sq are not written.
- *    float32 and D = 512 need Sq and Skv to be multiples of 128, as the
- *    attnax Pallas forward requires seq_q % block_q == 0 and
- *    seq_kv % block_kv == 0 with block_q = block_kv = 128; else
- *    ATTN_ERR_SHAPE.  D must be 64 (all dtypes) or 512 (bf16/f16 forward).
+ *    D = 512 needs Sq and Skv to be multiples of 128, as the attnax Pallas
+ *    forward requires seq_q % block_q == 0 and seq_kv % block_kv == 0 with
+ *    block_q = block_kv = 128; else ATTN_ERR_SHAPE.  D must be 64 (all
+ *    dtypes) or 512 (bf16/f16, forward and backward).
+ *  - float32 runs on the tensor cores too: each contraction as three TF32
+ *    products (hi x hi + hi x lo + lo x hi of the TF32 parts), f32 accumulate.
  *  - The library allocates no memory and keeps no state.  Scratch space
  *    ("workspace") is caller-owned device memory of attn_workspace_size()
  *    bytes, 256-byte aligned, and must be zero-filled before its first use;
@@ -127,7 +129,7 @@ typedef struct {
  * per 128 x 128 tile; tiles with no kept pair are skipped, tiles with every
  * pair kept are not tested per entry); the packed form can be reused by any
  * number of forward and backward calls of the same shape.  Taken on the
- * f16/bf16 D = 64 path (ATTN_ERR_UNSUPPORTED elsewhere). */
+ * D = 64 path, every dtype (ATTN_ERR_UNSUPPORTED at D = 512). */
 typedef struct {
   const void* packed;    /* device, 256-byte aligned, written by attn_pack_dense_mask */
   size_t packed_bytes;   /* its size: at least attn_dense_mask_bytes() */
@@ -176,7 +178,7 @@ attn_status attn_fwd(const attn_shape* shape, const void* q, const void* k, cons
  * The visited map also leaves out tiles with no pair kept by dm.  Errors as
  * attn_fwd, plus ATTN_ERR_INVALID_ARG (dm->packed NULL, flag not 0/1,
  * packed_bytes too small), ATTN_ERR_ALIGN (dm->packed) and
- * ATTN_ERR_UNSUPPORTED (f32 or D = 512). */
+ * ATTN_ERR_UNSUPPORTED (D = 512). */
 attn_status attn_fwd_dense(const attn_shape* shape, const void* q, const void* k, const void* v,
                            const uint8_t* key_mask, const attn_dense_mask* dm, const attn_block_mask* bm,
                            attn_score_mod mod, float scale, void* out, float* lse, void* ws,
@@ -186,7 +188,7 @@ attn_status attn_fwd_dense(const attn_shape* shape, const void* q, const void* k
  * Takes the forward's out and lse and the same key_mask, bm, mod and scale.
  * Runs three kernels: a preprocess (D_i = rowsum(dout * out)), a dK/dV pass
  * over kv blocks and a dQ pass over q blocks; no atomics, so results are
- * bitwise reproducible.  D = 64 only. */
+ * bitwise reproducible.  D = 64 (all dtypes) and 512 (f16/bf16). */
 attn_status attn_bwd(const attn_shape* shape, const void* q, const void* k, const void* v,
                      const void* out, const float* lse, const void* dout,
                      const uint8_t* key_mask, const attn_block_mask* bm, attn_score_mod mod,

@@ -78,7 +78,8 @@ def _fwd(lib, shape, q=FAKE, k=FAKE, v=FAKE, km=None, bm=None, mod=0, scale=0.12
 def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, None) == lib.ATTN_ERR_INVALID_ARG
     # any lengths on the f16/bf16 D=64 path, multiples of 128 elsewhere
-    assert _fwd(lib, _shape(lib, Sq=200, dt=0)) == lib.ATTN_ERR_SHAPE
+    assert _fwd(lib, _shape(lib, Sq=200, dt=0), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE   # f32 ragged accepted
+    assert _fwd(lib, _shape(lib, Sq=200, D=512)) == lib.ATTN_ERR_SHAPE
     assert _fwd(lib, _shape(lib, Skv=130, D=512)) == lib.ATTN_ERR_SHAPE
     assert _fwd(lib, _shape(lib, Sq=200, Skv=130), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE   # shape accepted
     assert _fwd(lib, _shape(lib, Sq=1, Skv=1), ws_bytes=100) == lib.ATTN_ERR_WORKSPACE
@@ -169,23 +170,25 @@ def test_dense_mask_sizes_and_validation(lib):
     assert pack(n=full - 1) == lib.ATTN_ERR_INVALID_ARG
     assert pack(shape=_shape(lib, Skv=2048 * 128 + 1)) == lib.ATTN_ERR_SHAPE
 
-    def fwd(shape=s, dm=None):
+    def fwd(shape=s, dm=None, n=1 << 30):
         return L.attn_fwd_dense(ctypes.byref(shape), FAKE, FAKE, FAKE, None,
                                 ctypes.byref(dm) if dm is not None else None, None, 0, 0.125, FAKE, FAKE, FAKE,
-                                1 << 30, None, None)
+                                n, None, None)
 
-    def bwd(shape=s, dm=None):
+    def bwd(shape=s, dm=None, n=1 << 30):
         return L.attn_bwd_dense(ctypes.byref(shape), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
                                 ctypes.byref(dm) if dm is not None else None, None, 0, 0.125, FAKE, FAKE, FAKE,
-                                FAKE, 1 << 30, None)
+                                FAKE, n, None)
     ok = lib.DenseMaskC(FAKE, full, 0, 0)
     for call in (fwd, bwd):
         assert call(dm=lib.DenseMaskC(None, full, 0, 0)) == lib.ATTN_ERR_INVALID_ARG
         assert call(dm=lib.DenseMaskC(FAKE, full, 0, 2)) == lib.ATTN_ERR_INVALID_ARG
         assert call(dm=lib.DenseMaskC(FAKE + 64, full, 0, 0)) == lib.ATTN_ERR_ALIGN
         assert call(dm=lib.DenseMaskC(FAKE, full - 256, 0, 0)) == lib.ATTN_ERR_INVALID_ARG
-        assert call(shape=_shape(lib, B=2, H=4, Sq=256, Skv=256, dt=0), dm=ok) == lib.ATTN_ERR_UNSUPPORTED
-        assert call(shape=_shape(lib, Sq=300, dt=0), dm=ok) == lib.ATTN_ERR_SHAPE
+        # float32 takes the dense mask and ragged lengths: validation passes up to the (too small) workspace
+        assert call(shape=_shape(lib, B=2, H=4, Sq=256, Skv=256, dt=0), dm=ok, n=100) == lib.ATTN_ERR_WORKSPACE
+        assert call(shape=_shape(lib, Sq=300, dt=0), dm=ok, n=100) == lib.ATTN_ERR_WORKSPACE
+        assert call(shape=_shape(lib, Sq=300, D=512), dm=ok) == lib.ATTN_ERR_SHAPE
     assert fwd(shape=_shape(lib, B=2, H=4, Sq=256, Skv=256, D=512), dm=ok) == lib.ATTN_ERR_UNSUPPORTED
     # with no dense mask the calls are attn_fwd / attn_bwd (same validation)
     assert fwd(shape=_shape(lib, D=96)) == _fwd(lib, _shape(lib, D=96)) == lib.ATTN_ERR_UNSUPPORTED

@@ -146,6 +146,23 @@ def test_mod_bias_paths(mod, scale, km, bm):
     run_and_check(1, 2, 200, 384, "f16", mod, km, bm, scale=scale)
 
 
+# float32 (three TF32 products on the tensor cores) with ragged lengths and the
+# dense mask: the plain 1e-4 / 1e-3 bounds.
+F32_MORE = [
+    (1, 2, 200, 333, "alibi", True, None, None),
+    (2, 1, 130, 77, "causal", False, "causal", None),
+    (1, 1, 1, 129, "checkerboard", True, None, None),
+    (2, 2, 256, 300, "checkerboard", True, None, "tiles"),
+    (1, 2, 333, 129, "none", False, "causal", "random"),
+]
+
+
+@pytest.mark.parametrize("B,H,Sq,Skv,mod,km,bm,dense", F32_MORE)
+def test_f32_ragged_and_dense(B, H, Sq, Skv, mod, km, bm, dense):
+    dn = None if dense is None else _dense(dense, 1, H, Sq, Skv)
+    run_and_check(B, H, Sq, Skv, "f32", mod, km, bm, dense=dn)
+
+
 def test_rectangular_and_single_tile():
     run_and_check(1, 2, 128, 512, "bf16", "alibi", True, None)
     run_and_check(2, 2, 512, 128, "f16", "checkerboard", False, None)
