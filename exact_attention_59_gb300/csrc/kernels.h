@@ -170,6 +170,8 @@ struct DecodeParams {
   int B, H, Skv, nsplit, keys_per_split;
   float sc;
   int mod;
+  int cluster, ngroups;      // set by launch_decode: CTAs per cluster, clusters per (b, h),
+  int rounds;                // and rounds of keys per CTA
 };
 #ifndef __CUDACC_RTC__
 // Device-side wait limit (ATTN_TIMEOUT_NS, default 2 s), read at every call.

@@ -150,6 +150,46 @@ DEVI bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& c) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch and L2 prefetch
+// ---------------------------------------------------------------------------
+// The grid launched after this one in the stream (with the programmatic
+// stream-serialization attribute) may start once every CTA of this grid has
+// executed this, or exited.
+DEVI void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Blocks until the grids this one depends on have completed and their memory
+// operations are visible; returns at once for a grid launched without the attribute.
+DEVI void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Asks L2 to fetch [p, p + bytes) from global memory (p 16-byte aligned, bytes a
+// multiple of 16); nothing is returned and no completion is tracked.
+DEVI void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters: rank, barrier, distributed shared memory
+// ---------------------------------------------------------------------------
+DEVI uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives once per phase, then waits.
+DEVI void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
+DEVI void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+DEVI void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Address, in the cluster's shared window, of this CTA's shared-memory address
+// `addr` as it lies in the CTA of rank `rank`.
+DEVI uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+DEVI void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), 2-D tiles, completion on an mbarrier
 // ---------------------------------------------------------------------------
 DEVI void tma_prefetch_desc(const CUtensorMap* m) {

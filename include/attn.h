@@ -218,10 +218,17 @@ attn_status attn_bwd_dq(const attn_shape* shape, const void* q, const void* k, c
                         attn_stream_t stream);
 
 /* Single-query decode (shape->Sq must be 1; q_idx = 0): split-KV partial
- * softmax per (b, h, split of up to 128 keys), K and V streamed straight into
- * registers with 16-byte loads, combined in the same launch by the last split
- * to finish (flaxattention README "Decoding").  f16/bf16, D = 64.  The kernel
- * has no device-side wait, so it has no timeout to report. */
+ * softmax per (b, h, split), K and V streamed straight into registers with
+ * 16-byte loads in rounds of 128 keys per split, the splits of a (b, h)
+ * merged in the same launch: within a thread-block cluster of up to 8 splits
+ * through distributed shared memory, across the clusters of a long (b, h)
+ * through the workspace by the last cluster to finish (flaxattention README
+ * "Decoding").  f16/bf16, D = 64.  The kernel is launched with programmatic
+ * dependent launch: it may start while the previous kernel in `stream`
+ * drains, but reads q, k, v, the key mask and writes anything only after that
+ * kernel has completed, so stream order holds as for any launch.  Its only
+ * waits are cluster barriers among CTAs that run together and always reach
+ * them (no spin on memory), so it has no timeout to report. */
 attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, const void* v,
                         const uint8_t* key_mask, attn_score_mod mod, float scale, void* out,
                         float* lse, void* ws, size_t ws_bytes, attn_stream_t stream);
@@ -242,8 +249,9 @@ attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, c
  *     looks up the array's device address there (cudaGetSymbolAddress); the
  *     first call on a device also loads the library's device code on it, so
  *     make that first call before any stream capture.
- *   - Like attn_decode, its kernel has no device-side wait, so there is no
- *     timeout to report and no status word.
+ *   - Like attn_decode, its kernel spins on no memory word (its only waits
+ *     are cluster barriers), so there is no timeout to report and no status
+ *     word.
  *   - Every call on a device shares the one array.  Each call zeroes the
  *     tickets it uses (an asynchronous memset on `stream`) before its kernel.
  *     Calls that overlap in time on the GPU (other streams, other threads)

@@ -7,6 +7,8 @@ for the 131072-token case).  Outputs are NaN-filled before the call, followed
 by canary bytes, and each call is repeated to check bitwise reproducibility.
 """
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -523,6 +525,74 @@ def test_decode_workload_full_size():
     o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod=w.score_mod)
     compare("decode out", f64(out), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
     compare("decode lse", f64(lse), l_ref, TOL["f16"]["lse_max"], dtype="f16", kind="lse")
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_decode_back_to_back_calls_share_a_workspace(graph):
+    """Decode launches overlap their predecessor (programmatic dependent launch):
+    calls issued back to back on one stream, one workspace and one set of
+    tickets, each on its own K/V, all match the oracle."""
+    B, H, Skv, D, n = 3, 4, 1000, 64, 5
+    cases = [make_dev(B, H, 1, Skv, D, "f16", key_mask=(i % 2 == 1), dout=None, seed=IN.SEED + 400 + i)
+             for i in range(n)]
+    outs = [torch.empty((B, H, 1, D), dtype=torch.float16, device="cuda") for _ in range(n)]
+    lses = [torch.empty((B, H, 1), dtype=torch.float32, device="cuda") for _ in range(n)]
+    ws = E.workspace(E.OP_DECODE, E.make_shape(cases[0][1]["q"], cases[0][1]["k"]), torch.device("cuda"))
+
+    def run():
+        for (c, d), o, l in zip(cases, outs, lses):
+            E.attn_decode(d["q"], d["k"], d["v"], key_mask=d["key_mask"], score_mod="alibi", out=o, lse=l, ws=ws)
+
+    run()
+    torch.cuda.synchronize()
+    if graph:
+        for o in outs:
+            o.zero_()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+            run()
+        g.replay()
+        torch.cuda.synchronize()
+    for (c, d), o, l in zip(cases, outs, lses):
+        kmn = None if c["key_mask"] is None else c["key_mask"].numpy()
+        o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=kmn, score_mod="alibi")
+        compare("decode out", f64(o), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+        compare("decode lse", f64(l), l_ref, TOL["f16"]["lse_max"], dtype="f16", kind="lse")
+    assert E.poll_status(ws) == 0
+
+
+def test_decode_reads_a_key_the_previous_call_wrote():
+    """The first decode writes its output into the last key row of the second
+    one's K, and the second keeps only that key.  The second call asks L2 for
+    its rows before the first has finished; it must still see the new row
+    (out = that key's V row, lse = its score)."""
+    D, Skv1, Skv2 = 64, 65536, 256
+    c1, d1 = make_dev(1, 1, 1, Skv1, D, "f16", dout=None, seed=IN.SEED + 431)
+    c2, d2 = make_dev(1, 1, 1, Skv2, D, "f16", dout=None, seed=IN.SEED + 432)
+    k2 = d2["k"]
+    old_row = k2[0, 0, Skv2 - 1].clone()
+    km2 = torch.zeros((1, Skv2), dtype=torch.uint8, device="cuda")
+    km2[0, Skv2 - 1] = 1
+    out1 = k2[:, :, Skv2 - 1:Skv2, :]   # a (1, 1, 1, 64) view of K's last row
+    assert out1.is_contiguous()
+    # every buffer exists before the two calls, so nothing is launched between them
+    lse1 = torch.empty((1, 1, 1), dtype=torch.float32, device="cuda")
+    out2 = torch.empty((1, 1, 1, D), dtype=torch.float16, device="cuda")
+    lse2 = torch.empty((1, 1, 1), dtype=torch.float32, device="cuda")
+    ws1 = E.workspace(E.OP_DECODE, E.make_shape(d1["q"], d1["k"]), torch.device("cuda"))
+    ws2 = E.workspace(E.OP_DECODE, E.make_shape(d2["q"], k2), torch.device("cuda"))
+    for _ in range(3):
+        k2[0, 0, Skv2 - 1] = old_row
+        E.attn_decode(d1["q"], d1["k"], d1["v"], score_mod="none", out=out1, lse=lse1, ws=ws1)
+        E.attn_decode(d2["q"], k2, d2["v"], key_mask=km2, score_mod="none", out=out2, lse=lse2, ws=ws2)
+        torch.cuda.synchronize()
+        new_row = k2[0, 0, Skv2 - 1]
+        assert not torch.equal(new_row, old_row)
+        assert torch.equal(out2[0, 0, 0], d2["v"][0, 0, Skv2 - 1])
+        want = float((d2["q"][0, 0, 0].double() * new_row.double()).sum()) / math.sqrt(D)
+        assert abs(float(lse2[0, 0, 0]) - want) <= 1e-4 * max(1.0, abs(want))
 
 
 # ---------------------------------------------------------------- block-mask builder
