@@ -740,6 +740,8 @@ attn_status attn_decode_chunk(const attn_shape* s, const void* q, const void* k,
   p.nsplit = cs.nsplit;
   p.kps = cs.kps;
   p.part = cs.nsplit > 1 ? at<float>(ws, w.partial) : nullptr;
+  p.kraw = k;
+  p.vraw = v;
   const bool bf16 = s->dtype == ATTN_BF16;
   ATTN_TRY(cuda_status(launch_fwd_d64(p, bf16, (int)mod, st)));
   if (cs.nsplit == 1) return ATTN_OK;   // one kv range: the kernel wrote out and lse itself

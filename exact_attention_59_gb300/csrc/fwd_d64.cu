@@ -123,6 +123,22 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   const int b = bh / p.H, h = bh % p.H;
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const bool valid1 = qt1 < p.nqb;
+  if constexpr (CHUNK) {
+    // launched with programmatic dependent launch: this CTA's first K and V rows
+    // (kv blocks from kb_lo, contiguous, 128 bytes a row) go towards L2, the next
+    // grid may launch, and nothing is read or written before the grids ahead of
+    // this one have completed (L2 is the point of coherence: a line fetched
+    // early still reflects writes made before the wait)
+    if (tid < 2 && p.kraw && p.vraw) {   // (at most 2 FWD_NST blocks: the ring streams the rest)
+      const long long r0 = (long long)bh * p.Skv + (long long)kb_lo * 128;
+      const long long r1 = (long long)bh * p.Skv + min((long long)p.Skv, (long long)min(kb_hi, kb_lo + 2 * FWD_NST) * 128);
+      if (r1 > r0)
+        prefetch_l2_bulk(static_cast<const unsigned char*>(tid == 0 ? p.kraw : p.vraw) + r0 * 128,
+                         static_cast<uint32_t>((r1 - r0) * 128));
+    }
+    griddep_launch_dependents();
+    griddep_wait();
+  }
 
   // ---- setup: barriers, TMEM, per-kv-block flags
   if (tid == 0) {
@@ -371,6 +387,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       const int q = qt * 128 + row;
       const int qpos = q + q_off;   // the row's position among the keys (score mods, causal rule)
       const bool writer = quad == 3 && lane == 0;   // first warp of the group (warp 3 or 7)
+      // the split variant's chunk of queries may end inside the tile: a warp whose
+      // 32 rows all lie past Sq does no arithmetic, only the group's arrivals
+      const bool idle = CHUNK && qt * 128 + 32 * quad >= p.Sq;
       const uint64_t scv = f2(p.sc, p.sc);
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
       const int parity = (MOD == MOD_CHECKER) ? (qpos & 1) : 0;
@@ -403,6 +422,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         // the stage's bias table was written before its full barrier was armed
         if (use_table && !wait_warp(smem_u32(&sm.full[s]), ((u - 1) / FWD_NST) & 1, c)) { ok = false; break; }
         tc_fence_after();
+        if (idle) {
+          // the same arrivals in the same order as the rows that compute: S free,
+          // then (after P_t(n-1) V) P ready; the P and O rows of these lanes are
+          // never read into a written row
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.sfree[t]));
+          if (n > 0) {
+            if (!wait_warp(smem_u32(&sm.odone[t]), (n - 1) & 1, c)) { ok = false; break; }
+            tc_fence_after();
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.pready[t]));
+          ++n;
+          continue;
+        }
         uint32_t r[128];
         tmem_ld128(tS, r);
         // S_t(n) is in registers: the MMA thread may compute S_t(n+1) over it now
@@ -569,15 +603,24 @@ cudaError_t launch_fwd_d64_kernel(const FwdParams& p, const void* kern, cudaStre
 
 template <bool BF16, int MOD>
 static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
-  auto kern = p.nsplit > 1 || p.q_off != 0 ? fwd_d64_kernel<BF16, MOD, FWD_CHUNK>
-              : p.dm.tiles             ? fwd_d64_kernel<BF16, MOD, FWD_DENSE>
-                                       : fwd_d64_kernel<BF16, MOD, FWD_PLAIN>;
+  const bool chunk = p.nsplit > 1 || p.q_off != 0;
+  auto kern = chunk         ? fwd_d64_kernel<BF16, MOD, FWD_CHUNK>
+              : p.dm.tiles ? fwd_d64_kernel<BF16, MOD, FWD_DENSE>
+                           : fwd_d64_kernel<BF16, MOD, FWD_PLAIN>;
   const size_t smem = fwd_d64_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.npairs * p.B * p.H * p.nsplit);
-  kern<<<grid, FWD_THREADS, smem, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.npairs * p.B * p.H * p.nsplit));
+  cfg.blockDim = dim3(FWD_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = chunk ? 1 : 0;   // the split variant waits itself
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 #endif  // host
 
@@ -587,6 +630,10 @@ static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
 template <bool BF16>
 __global__ void __launch_bounds__(256) split_merge_kernel(const float* __restrict__ part, int nsplit, long long rows,
                                                           int Sq, void* __restrict__ out, float* __restrict__ lse) {
+  // launched with programmatic dependent launch behind the split forward: the
+  // partial rows are read only once that grid has completed
+  griddep_launch_dependents();
+  griddep_wait();
   const long long r = blockIdx.x * 8LL + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -617,12 +664,18 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const float* __restric
 cudaError_t launch_split_merge(const float* part, int nsplit, long long rows, int Sq, void* out, float* lse, bool bf16,
                                cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)((rows + 7) / 8);
-  if (bf16)
-    split_merge_kernel<true><<<grid, 256, 0, st>>>(part, nsplit, rows, Sq, out, lse);
-  else
-    split_merge_kernel<false><<<grid, 256, 0, st>>>(part, nsplit, rows, Sq, out, lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return bf16 ? cudaLaunchKernelEx(&cfg, split_merge_kernel<true>, part, nsplit, rows, Sq, out, lse)
+              : cudaLaunchKernelEx(&cfg, split_merge_kernel<false>, part, nsplit, rows, Sq, out, lse);
 }
 
 cudaError_t launch_fwd_d64(const FwdParams& p, bool bf16, int mod, cudaStream_t st) {

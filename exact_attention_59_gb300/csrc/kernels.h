@@ -72,6 +72,8 @@ struct FwdParams {
   // unnormalised} instead of out and lse; nsplit = 1 and part = nullptr otherwise
   int nsplit, kps;
   float* part;
+  const void* kraw;               // K and V base pointers (the split variant asks L2 for its rows)
+  const void* vraw;
   // ALiBi / checkerboard bias folded into S = Q K^T as one more K = 16 step
   // (the AUG_MOD columns of the augmented operands), and 1 / scale
   int fold;
