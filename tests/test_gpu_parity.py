@@ -270,6 +270,7 @@ CHUNK = [
     (2, 1, 200, 640, "f16", "causal", False, 440),
     (1, 2, 3, 129, "bf16", "alibi", False, 1000),
     (8, 8, 4, 2048, "f16", "causal", False, None),
+    (1, 1, 8, 100, "f16", "none", False, 0),   # one kv block, offset 0: one tile slot has no block
 ]
 
 
