@@ -30,7 +30,7 @@
 // that CTA merges them in rank order: no global-memory round trip.  A (b, h)
 // with more splits than one cluster holds has several clusters; their first
 // CTAs write (m, l, o) to the workspace and the last of them to finish
-// (atomic ticket, no spin) merges those in a fixed order and re-arms the ticket.
+// (atomic ticket, zeroed by the launcher, no spin) merges those in a fixed order.
 // Launched with programmatic dependent launch: a CTA first asks L2 for its
 // first K and V rows, lets the next grid in the stream launch, and only then waits
 // for the grids before it (griddepcontrol.wait).  Every load into registers
@@ -359,10 +359,7 @@ __global__ void __launch_bounds__(DEC_THREADS, ATTN_DEC_MINB) decode_kernel(cons
       uint32_t* op = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) + (size_t)bh * 64 + d);
       *op = pack2<BF16>(val, nb);
     }
-    if (d == 0) {
-      p.lse[bh] = Lsum > 0.f ? (Mxu + lg2(Lsum)) * kLn2 : -INFINITY;
-      p.counter[bh] = 0u;   // re-arm for the next call
-    }
+    if (d == 0) p.lse[bh] = Lsum > 0.f ? (Mxu + lg2(Lsum)) * kLn2 : -INFINITY;
   }
 }
 
@@ -426,6 +423,10 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t st) {
   const long long ctas_per_head = (long long)q.ngroups * q.cluster;
   q.keys_per_split = (int)((p.Skv + ctas_per_head - 1) / ctas_per_head);
   if (BH * ctas_per_head > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (q.ngroups > 1) {   // the clusters' tickets start at zero in every call
+    const cudaError_t e = cudaMemsetAsync(q.counter, 0, (size_t)BH * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+  }
   return bf16 ? launch_decode_t<true>(q, st) : launch_decode_t<false>(q, st);
 }
 

@@ -73,8 +73,6 @@ extern "C" attn_status attn_decode_noalloc(const attn_shape* s, const void* q, c
   if (st != ATTN_OK) return st;
   float* partial = static_cast<float*>(base);
   unsigned* counter = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(base) + partial_bytes);
-  // The tickets must start at zero; the array keeps whatever the previous call left.
-  if (cudaMemsetAsync(counter, 0, counter_bytes, (cudaStream_t)stream) != cudaSuccess) return ATTN_ERR_CUDA;
 
   DecodeParams p{};
   p.q = q;

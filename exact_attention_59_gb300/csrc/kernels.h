@@ -168,7 +168,7 @@ struct DecodeParams {
   float* lse;
   const uint8_t* key_mask;   // (B, Skv) or nullptr
   float* partial;            // (B*H, nsplit, 2 + 64): m, l, o[64]
-  unsigned* counter;         // (B*H) completion tickets, zero between calls
+  unsigned* counter;         // (B*H) completion tickets (zeroed by launch_decode when used)
   int B, H, Skv, nsplit, keys_per_split;
   float sc;
   int mod;

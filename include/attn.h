@@ -36,8 +36,10 @@
  *    products (hi x hi + hi x lo + lo x hi of the TF32 parts), f32 accumulate.
  *  - The library allocates no memory and keeps no state.  Scratch space
  *    ("workspace") is caller-owned device memory of attn_workspace_size()
- *    bytes, 256-byte aligned, and must be zero-filled before its first use;
- *    every call leaves it ready for the next one.  Calls on one workspace
+ *    bytes, 256-byte aligned, and must be zero-filled before its first use
+ *    (its first word is the status word, below); any call and shape may use
+ *    it after that (completion tickets are zeroed by the call that uses
+ *    them, with an asynchronous memset on `stream`).  Calls on one workspace
  *    must not overlap in time (use one workspace per stream).
  *  - Calls are asynchronous on `stream` and never synchronise, except
  *    attn_poll_status().  Arguments are validated before anything is
@@ -252,8 +254,9 @@ attn_status attn_decode(const attn_shape* shape, const void* q, const void* k, c
  *   - Like attn_decode, its kernel spins on no memory word (its only waits
  *     are cluster barriers), so there is no timeout to report and no status
  *     word.
- *   - Every call on a device shares the one array.  Each call zeroes the
- *     tickets it uses (an asynchronous memset on `stream`) before its kernel.
+ *   - Every call on a device shares the one array.  A call whose (b, h)
+ *     rows need more than one cluster of splits (more than 4096 keys) zeroes
+ *     the tickets it uses with an asynchronous memset on `stream` first.
  *     Calls that overlap in time on the GPU (other streams, other threads)
  *     race on the array and give wrong results: serialise them. */
 attn_status attn_decode_noalloc(const attn_shape* shape, const void* q, const void* k, const void* v,

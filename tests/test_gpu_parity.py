@@ -528,6 +528,40 @@ def test_decode_workload_full_size():
     compare("decode lse", f64(lse), l_ref, TOL["f16"]["lse_max"], dtype="f16", kind="lse")
 
 
+def test_workspace_serves_several_shapes():
+    """One workspace, used by calls of different shapes in turn: each call's
+    completion tickets may lie where the previous call wrote partial rows, so
+    the calls must not depend on what is left there (forward remainder items
+    run in two halves; decode with several clusters per head)."""
+    dev = torch.device("cuda")
+    shapes = [(2, 2, 384, 300, "bf16"), (1, 2, 200, 384, "f16"), (2, 3, 256, 640, "f16")]
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+    def size(op, B, H, S, T, dt):
+        q = torch.empty((B, H, S, 64), dtype=tdt[dt], device=dev)
+        k = torch.empty((B, H, T, 64), dtype=tdt[dt], device=dev)
+        return E.workspace_size(op, E.make_shape(q, k))
+
+    need = max(size(E.OP_FWD, *sh) for sh in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    for i, (B, H, S, T, dt) in enumerate(shapes * 2):
+        c, d = make_dev(B, H, S, T, 64, dt, key_mask=(i % 2 == 0), dout=None, seed=IN.SEED + 500 + i)
+        out, lse = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], score_mod="alibi", ws=ws)
+        torch.cuda.synchronize()
+        km = None if c["key_mask"] is None else c["key_mask"].numpy()
+        o_ref, l_ref = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=km, score_mod="alibi")
+        compare("out", f64(out), o_ref, TOL[dt]["o_max"], TOL[dt]["o_mean"], dtype=dt, kind="out")
+    dshapes = [(2, 2, 5000), (3, 2, 9000), (1, 1, 4500)]
+    dneed = max(size(E.OP_DECODE, B, H, 1, T, "f16") for B, H, T in dshapes)
+    dws = torch.zeros(dneed, dtype=torch.uint8, device=dev)
+    for i, (B, H, T) in enumerate(dshapes * 2):
+        c, d = make_dev(B, H, 1, T, 64, "f16", dout=None, seed=IN.SEED + 600 + i)
+        out, lse = E.attn_decode(d["q"], d["k"], d["v"], score_mod="checkerboard", ws=dws)
+        torch.cuda.synchronize()
+        o_ref, l_ref = OR.attn_decode(f64(c["q"]), f64(c["k"]), f64(c["v"]), score_mod="checkerboard")
+        compare("decode out", f64(out), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+
+
 @pytest.mark.parametrize("graph", [False, True])
 def test_decode_back_to_back_calls_share_a_workspace(graph):
     """Decode launches overlap their predecessor (programmatic dependent launch):
