@@ -60,11 +60,14 @@ static_assert(offsetof(FwdSmem, cb) % 16 == 0, "cb must be 16-byte aligned");
 // With RAW (no table, no user bias, scale > 0) the scores stay unscaled: the
 // masks and the maximum work on s itself (max of s * scale = scale * max of s),
 // and the exponential pass applies the scale in its one FFMA.
-template <bool TABLE, bool LIMITED, bool DENSE, bool USER = false, bool RAW = false, bool UMASK = false>
-DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4],
+// N = the columns passed: column cc here is column cc of the caller's share,
+// whose table `tb`, limit `lim`, dense words `dw` (x = its columns 0-31,
+// y = 32-63, ...) and first key `ukv0` the caller has offset to that share.
+template <int N, bool TABLE, bool LIMITED, bool DENSE, bool USER = false, bool RAW = false, bool UMASK = false>
+DEVI void scale_scores(uint32_t (&r)[N], uint64_t scv, const float* tb, int lim, uint4 dw, float (&mx)[4],
                        int ub = 0, int uh = 0, int uq = 0, int ukv0 = 0) {
 #pragma unroll
-  for (int i = 0; i < 64; i += 2) {
+  for (int i = 0; i < N / 2; i += 2) {
     float4 bias = make_float4(0.f, 0.f, 0.f, 0.f);
     if (TABLE) bias = *reinterpret_cast<const float4*>(tb + 2 * i);
 #pragma unroll
@@ -104,6 +107,7 @@ DEVI void scale_scores(uint32_t (&r)[128], uint64_t scv, const float* tb, int li
 //   FWD_DENSE  with the dense-mask path;
 //   FWD_CHUNK  queries at a position offset, kv blocks split over CTAs (decode).
 constexpr int FWD_PLAIN = 0, FWD_DENSE = 1, FWD_CHUNK = 2;
+
 
 template <bool BF16, int MOD, int VAR>
 __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_constant__ FwdParams p) {
@@ -437,11 +441,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           ++n;
           continue;
         }
-        uint32_t r[128];
-        tmem_ld128(tS, r);
-        // S_t(n) is in registers: the MMA thread may compute S_t(n+1) over it now
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm.sfree[t]));
         const int kv0 = kb * 128;
         const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128 + q_off) ||
                             ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
@@ -452,35 +451,47 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const int lim = causal ? min(qpos - kv0, kvlim) : kvlim;
         const float* tb = sm.cb[s][parity];
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        // one straight-line copy of the pass per (table, causal) pair: a runtime
-        // test inside the unrolled loop would cost instructions on every score
-        // (a block with dense-mask bits always takes the limited copy too)
-        if (use_table) {
-          if (DM && dense) scale_scores<true, true, DM>(r, scv, tb, lim, dw, mx);
-          else if (limited) scale_scores<true, true, false>(r, scv, tb, lim, dw, mx);
-          else scale_scores<true, false, false>(r, scv, tb, lim, dw, mx);
-        } else if constexpr (MOD == MOD_USER) {
-          // a PARTIAL tile of a user mask_mod's block mask: the expression masks each entry
-          const bool umask = (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
-          if (umask) {
-            if (limited) scale_scores<false, true, false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
-            else scale_scores<false, false, false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
-          } else if (DM && dense) {
-            scale_scores<false, true, DM, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
-          } else if (limited) {
-            scale_scores<false, true, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+        // The scale / mask / maximum pass over the NCK columns from column c0k on
+        // (the block's constants above are set before S is read).  One
+        // straight-line copy of the pass per (table, causal) pair: a runtime test
+        // inside the unrolled loop would cost instructions on every score (a block
+        // with dense-mask bits always takes the limited copy too).
+        constexpr int NCK = 128;
+        auto pass = [&](uint32_t (&rc)[NCK], int c0k) {
+          const uint4 dwk = dw;
+          if (use_table) {
+            if (DM && dense) scale_scores<NCK, true, true, DM>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+            else if (limited) scale_scores<NCK, true, true, false>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+            else scale_scores<NCK, true, false, false>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+          } else if constexpr (MOD == MOD_USER) {
+            // a PARTIAL tile of a user mask_mod's block mask: the expression masks each entry
+            const bool umask = (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
+            if (umask) {
+              if (limited) scale_scores<NCK, false, true, false, true, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx, b, h, qpos, kv0 + c0k);
+              else scale_scores<NCK, false, false, false, true, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx, b, h, qpos, kv0 + c0k);
+            } else if (DM && dense) {
+              scale_scores<NCK, false, true, DM, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx, b, h, qpos, kv0 + c0k);
+            } else if (limited) {
+              scale_scores<NCK, false, true, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx, b, h, qpos, kv0 + c0k);
+            } else {
+              scale_scores<NCK, false, false, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx, b, h, qpos, kv0 + c0k);
+            }
+          } else if (raw) {
+            if (DM && dense) scale_scores<NCK, false, true, DM, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+            else if (limited) scale_scores<NCK, false, true, false, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+            else scale_scores<NCK, false, false, false, false, true>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
           } else {
-            scale_scores<false, false, false, true>(r, scv, tb, lim, dw, mx, b, h, qpos, kv0);
+            if (DM && dense) scale_scores<NCK, false, true, DM>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+            else if (limited) scale_scores<NCK, false, true, false>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
+            else scale_scores<NCK, false, false, false>(rc, scv, tb + c0k, lim - c0k, dwk, mx);
           }
-        } else if (raw) {
-          if (DM && dense) scale_scores<false, true, DM, false, true>(r, scv, tb, lim, dw, mx);
-          else if (limited) scale_scores<false, true, false, false, true>(r, scv, tb, lim, dw, mx);
-          else scale_scores<false, false, false, false, true>(r, scv, tb, lim, dw, mx);
-        } else {
-          if (DM && dense) scale_scores<false, true, DM>(r, scv, tb, lim, dw, mx);
-          else if (limited) scale_scores<false, true, false>(r, scv, tb, lim, dw, mx);
-          else scale_scores<false, false, false>(r, scv, tb, lim, dw, mx);
-        }
+        };
+        uint32_t r[128];
+        tmem_ld128(tS, r);
+        // S_t(n) is in registers: the MMA thread may compute S_t(n+1) over it now
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.sfree[t]));
+        pass(r, 0);
         // ALiBi's per-row constant for this block, slope2 (kv0 - q), is kept out of the
         // per-score work: scores here are x' = x - base
         const float base = (MOD == MOD_ALIBI) ? slope2 * float(kv0 - qpos) : 0.f;
