@@ -362,13 +362,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
           dwv = __ldg(reinterpret_cast<const uint2*>(p.dm.colbits + (dmi * p.Skv + kv) * (4LL * p.nqb) + 4 * qb +
                                                      2 * w));
       }
-      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t rr[64];
-      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
-      // S^T(u) is in registers: the next S^T may be computed over it
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.sfree));
+      // the block's bias constants, ahead of the wait (they do not depend on S^T)
       uint64_t chk = 0;
       if constexpr (MOD == MOD_CHECKER) {
         const float hb = ((kv + q0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
@@ -378,6 +372,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       // with the bias folded into S^T, one constant per (kv block, q block) is left
       const float fb = (MOD == MOD_ALIBI) ? slope2 * float(kb * 128 - qb * 128) : 0.f;
       const uint64_t fbv = f2(fb, fb);
+      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t rr[64];
+      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
+      // S^T(u) is in registers: the next S^T may be computed over it
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.sfree));
       float pr[64];
       uint32_t pk[32];
       // one straight-line copy per causal/not: no runtime test inside the unrolled loop
@@ -776,13 +777,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
           dwv = __ldg(reinterpret_cast<const uint2*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) + 4 * kb +
                                                      2 * w));
       }
-      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t rr[64];
-      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
-      // S(u) is in registers: the next S may be computed over it
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.sfree));
+      // the block's bias constants, ahead of the wait (they do not depend on S)
       uint64_t chk = 0;
       if constexpr (MOD == MOD_CHECKER) {
         const float hb = ((q + k0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
@@ -792,6 +787,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
       // with the bias folded into S, all that is left per pair is this row's constant
       const float fb = (MOD == MOD_ALIBI) ? slope2 * float(kb * 128 - q) : 0.f;
       const uint64_t addf = fadd2(nl2v, f2(fb, fb));
+      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t rr[64];
+      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
+      // S(u) is in registers: the next S may be computed over it
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.sfree));
       float pr[64];
       // one straight-line copy per causal/not: no runtime test inside the unrolled loop
       auto probs = [&](auto causal_c, auto dense_c, auto fold_c) {

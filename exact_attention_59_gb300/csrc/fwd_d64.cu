@@ -422,6 +422,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           if (dense && q < p.Sq)
             dw = __ldg(reinterpret_cast<const uint4*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb)) + kb);
         }
+        // the block's mask constants, ahead of the wait (they do not depend on S)
+        const int kv0 = kb * 128;
+        const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128 + q_off) ||
+                            ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+        // keep column cc iff cc <= lim: the causal limit and, in a partial last kv
+        // block, the end of the keys
+        const int kvlim = p.Skv - 1 - kv0;
+        const bool limited = causal || kvlim < 127;
+        const int lim = causal ? min(qpos - kv0, kvlim) : kvlim;
+        const float* tb = sm.cb[s][parity];
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (!wait_warp(smem_u32(&sm.sfull[t]), n & 1, c)) { ok = false; break; }
         // the stage's bias table was written before its full barrier was armed
         if (use_table && !wait_warp(smem_u32(&sm.full[s]), ((u - 1) / FWD_NST) & 1, c)) { ok = false; break; }
@@ -441,16 +452,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           ++n;
           continue;
         }
-        const int kv0 = kb * 128;
-        const bool causal = (MOD == MOD_CAUSAL && kv0 + 127 > qt * 128 + q_off) ||
-                            ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-        // keep column cc iff cc <= lim: the causal limit and, in a partial last kv
-        // block, the end of the keys
-        const int kvlim = p.Skv - 1 - kv0;
-        const bool limited = causal || kvlim < 127;
-        const int lim = causal ? min(qpos - kv0, kvlim) : kvlim;
-        const float* tb = sm.cb[s][parity];
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // The scale / mask / maximum pass over the NCK columns from column c0k on
         // (the block's constants above are set before S is read).  One
         // straight-line copy of the pass per (table, causal) pair: a runtime test
