@@ -105,36 +105,6 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
     tma_load_2d(smem_u32(sm.k), &p.tm_k, smem_u32(&sm.kvfull), 0, bh * p.Skv + kb * 128);
     tma_load_2d(smem_u32(sm.v), &p.tm_v, smem_u32(&sm.kvfull), 0, bh * p.Skv + kb * 128);
   }
-  if (warp == 2) {
-    // list of q blocks that see this kv block, in ascending order, 32 candidates
-    // per ballot (the whole CTA waits for it: it is kept off any single thread)
-    const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
-    int n = 0;
-    if (ks != 0) {
-      for (int q0 = 0; q0 < p.nqb; q0 += 32) {
-        const int qb = q0 + lane;
-        bool keep = false;
-        uint8_t fl = 0;
-        if (qb < p.nqb) {
-          const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-          int ds = TILE_FULL;   // the dense tile state: dense build only
-          if constexpr (DM)
-            ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
-          keep = st != TILE_EMPTY && ds != TILE_EMPTY;
-          fl = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
-               (ds == TILE_PARTIAL ? KB_DENSE : 0);
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, keep);
-        if (keep) {
-          const int pos = n + __popc(m & ((1u << lane) - 1u));
-          sm.list[pos] = (uint16_t)qb;
-          sm.lflags[pos] = fl;
-        }
-        n += __popc(m);
-      }
-    }
-    if (lane == 0) sm.nlist = n;
-  }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
@@ -187,6 +157,43 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dkdv_kernel(const __grid_constan
       }
     }
     fence_async_smem();   // generic-proxy writes, read by the tensor core
+  }
+  // Launched with programmatic dependent launch behind the preprocess: the set-up
+  // above (barriers, K and V copies, TMEM, the augmented operands) reads nothing
+  // it writes; its outputs (key-mask bits and summary, -lse log2(e), -D) are read
+  // only from here on.  Then the dQ pass, which needs the same outputs but
+  // nothing of this pass, may launch: it fills the SMs of this grid's last wave.
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 2) {
+    // list of q blocks that see this kv block, in ascending order, 32 candidates
+    // per ballot (the whole CTA waits for it: it is kept off any single thread)
+    const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
+    int n = 0;
+    if (ks != 0) {
+      for (int q0 = 0; q0 < p.nqb; q0 += 32) {
+        const int qb = q0 + lane;
+        bool keep = false;
+        uint8_t fl = 0;
+        if (qb < p.nqb) {
+          const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
+          int ds = TILE_FULL;   // the dense tile state: dense build only
+          if constexpr (DM)
+            ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
+          keep = st != TILE_EMPTY && ds != TILE_EMPTY;
+          fl = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
+               (ds == TILE_PARTIAL ? KB_DENSE : 0);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int pos = n + __popc(m & ((1u << lane) - 1u));
+          sm.list[pos] = (uint16_t)qb;
+          sm.lflags[pos] = fl;
+        }
+        n += __popc(m);
+      }
+    }
+    if (lane == 0) sm.nlist = n;
   }
   tc_fence_before();
   __syncthreads();
@@ -896,19 +903,39 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // Launched with programmatic dependent launch behind the dK/dV pass, whose
+  // results it does not read (the preprocess it needs was complete before that
+  // pass let it launch): it waits for that grid only here, so that its own
+  // completion still implies the whole backward's for later work in the stream.
+  if (tid == 0) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
 #ifndef __CUDACC_RTC__
+// Both passes are launched with programmatic dependent launch (the dK/dV pass
+// behind the preprocess, the dQ pass behind the dK/dV pass); see the kernels.
+static cudaError_t launch_bwd_pdl(const BwdParams& p, const void* kern, bool dkdv, size_t smem, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.H * (dkdv ? p.nkb : p.nqb)));
+  cfg.blockDim = dim3(BWD_T);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<BwdParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 // Backward kernels of these layouts built elsewhere (a run-time-compiled
 // score_mod): the same shared memory, grid and block as the built-in variants.
 cudaError_t launch_bwd_kernel(const BwdParams& p, const void* kern, bool dkdv, cudaStream_t st) {
   const size_t smem = (dkdv ? sizeof(DkdvSmem) : sizeof(DqSmem)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.B * p.H * (dkdv ? p.nkb : p.nqb));
-  void* args[] = {const_cast<BwdParams*>(&p)};
-  return cudaLaunchKernel(kern, dim3(grid), dim3(BWD_T), args, smem, st);
+  return launch_bwd_pdl(p, kern, dkdv, smem, st);
 }
 
 template <typename Smem, bool BF16, int MOD, bool DKDV>
@@ -922,9 +949,7 @@ static cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st) {
   static const cudaError_t e1 = cudaFuncSetAttribute(masked, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const cudaError_t e = p.dm.tiles ? e1 : e0;
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.B * p.H * (DKDV ? p.nkb : p.nqb));
-  kern<<<grid, BWD_T, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_bwd_pdl(p, reinterpret_cast<const void*>(kern), DKDV, smem, st);
 }
 
 template <typename Smem, bool DKDV>
