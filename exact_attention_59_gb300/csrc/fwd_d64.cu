@@ -142,6 +142,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     }
     griddep_launch_dependents();
     griddep_wait();
+  } else {
+    // a grid launched behind this one with programmatic dependent launch (the
+    // backward preprocess) may start on SMs this grid leaves idle; it waits for
+    // this grid before it reads anything this grid writes
+    griddep_launch_dependents();
   }
 
   // ---- setup: barriers, TMEM, per-kv-block flags

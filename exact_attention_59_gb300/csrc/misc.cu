@@ -185,7 +185,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
                                                              long long half_rows, unsigned pre_blocks,
                                                              const uint8_t* __restrict__ km, int Skv,
                                                              uint32_t* __restrict__ bits, uint8_t* __restrict__ summary) {
+  // Launched with programmatic dependent launch behind the forward: dout (an
+  // input) is asked into L2 before the wait; out and lse (the forward's) are read
+  // and everything is written only after it.
   if (blockIdx.x >= pre_blocks) {
+    griddep_wait();
     // key-mask packing, fused into the same launch: 128 threads per (b, kv block)
     const int nkb = (Skv + 127) / 128, nkb2 = (nkb + 1) / 2;
     const int idx = (int)(blockIdx.x - pre_blocks);
@@ -218,6 +222,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row0 = tid / lpr;
   const int part = (int)(tid % lpr);
+  if (threadIdx.x < 2) {   // this CTA's dout rows: [r0, r0 + n) and the same + half_rows
+    const long long r0 = (long long)blockIdx.x * blockDim.x / lpr;
+    const long long r1 = r0 + threadIdx.x * half_rows;
+    const long long n = min((long long)blockDim.x / lpr, rows - r1);
+    if (r0 < half_rows && n > 0)
+      prefetch_l2_bulk(dout + r1 * D, static_cast<uint32_t>(n * D * sizeof(T)));
+  }
+  griddep_wait();
+  griddep_launch_dependents();   // the dK/dV pass may set up (it waits for this grid itself)
   float acc[2] = {0.f, 0.f};
   for (int j = 0; j < per; ++j) {
     float a[2][8], g[2][8];
@@ -260,16 +273,24 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
   const unsigned pre_blocks = (unsigned)((threads + 255) / 256);
   const unsigned pack_blocks = km ? (unsigned)(B * (((Skv + 127) / 128 + 1) / 2)) : 0u;
   const unsigned grid = pre_blocks + pack_blocks;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (dtype == 0)
-    bwd_preprocess_kernel<float><<<grid, 256, 0, st>>>((const float*)out, (const float*)dout, lse, rows, D, delta,
-                                                         lse2, half_rows, pre_blocks, km, Skv, bits, summary);
-  else if (dtype == 1)
-    bwd_preprocess_kernel<h16><<<grid, 256, 0, st>>>((const h16*)out, (const h16*)dout, lse, rows, D, delta, lse2,
-                                                       half_rows, pre_blocks, km, Skv, bits, summary);
-  else
-    bwd_preprocess_kernel<b16><<<grid, 256, 0, st>>>((const b16*)out, (const b16*)dout, lse, rows, D, delta, lse2,
-                                                       half_rows, pre_blocks, km, Skv, bits, summary);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, bwd_preprocess_kernel<float>, (const float*)out, (const float*)dout, lse, rows, D,
+                              delta, lse2, half_rows, pre_blocks, km, Skv, bits, summary);
+  if (dtype == 1)
+    return cudaLaunchKernelEx(&cfg, bwd_preprocess_kernel<h16>, (const h16*)out, (const h16*)dout, lse, rows, D,
+                              delta, lse2, half_rows, pre_blocks, km, Skv, bits, summary);
+  return cudaLaunchKernelEx(&cfg, bwd_preprocess_kernel<b16>, (const b16*)out, (const b16*)dout, lse, rows, D, delta,
+                            lse2, half_rows, pre_blocks, km, Skv, bits, summary);
 }
 
 }  // namespace attn
