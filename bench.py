@@ -44,7 +44,7 @@ UNIT = "TFLOP/s"
 # DRAM bytes (read + write) of one bwd_dkdv_kernel launch at the bench workload, from
 # `ncu --set full` of `python bench.py --mode profile --batch 8 --steps 1`.  Set it
 # back to None when the kernel changes until it is captured again.
-DKDV_TRAFFIC_BYTES = 80.4e6
+DKDV_TRAFFIC_BYTES = 80.9e6
 
 
 def counted_flops(w, backward=True):
