@@ -528,6 +528,40 @@ def test_decode_workload_full_size():
     compare("decode lse", f64(lse), l_ref, TOL["f16"]["lse_max"], dtype="f16", kind="lse")
 
 
+def test_chained_calls_read_what_the_previous_call_wrote():
+    """Forward, backward, decode and chunked decode queued on one stream with no
+    synchronisation, each consuming the previous call's output: kernels that
+    start early under programmatic dependent launch must still read only
+    completed results.  The forward's out becomes the backward's dout and the
+    next forward's v; the backward's dq becomes a decode's k; the decode's out
+    feeds the chunked decode's q."""
+    B, H, S, D = 2, 2, 384, 64
+    c, d = make_dev(B, H, S, S, D, "f16", key_mask=True, seed=IN.SEED + 800)
+    q, k, v, km = d["q"], d["k"], d["v"], d["key_mask"]
+    out1, lse1 = E.attn_fwd(q, k, v, key_mask=km, score_mod="alibi")
+    dq, dk, dv = E.attn_bwd(q, k, v, out1, lse1, out1, key_mask=km, score_mod="alibi")   # dout = out1
+    out2, lse2 = E.attn_fwd(q, k, out1, score_mod="checkerboard")                          # v = out1
+    qd = q[:, :, :1].contiguous()
+    out3, lse3 = E.attn_decode(qd, dq, v, score_mod="none")                                # k = dq
+    out4, lse4 = E.attn_decode_chunk(out2[:, :, :4].contiguous(), k, v, S - 4, score_mod="causal")
+    torch.cuda.synchronize()
+    kmn = c["key_mask"].numpy()
+    q64, k64, v64 = f64(c["q"]), f64(c["k"]), f64(c["v"])
+    o1_ref, _ = OR.attn_fwd(q64, k64, v64, key_mask=kmn, score_mod="alibi")
+    compare("out1", f64(out1), o1_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+    o1 = f64(out1)
+    dq_r, dk_r, dv_r = OR.attn_bwd(q64, k64, v64, o1, key_mask=kmn, score_mod="alibi")
+    for name, g, r in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        compare(name, f64(g), r, TOL["f16"]["g_max"], TOL["f16"]["g_mean"], dtype="f16", kind="grad")
+    o2_ref, _ = OR.attn_fwd(q64, k64, o1, score_mod="checkerboard")
+    compare("out2", f64(out2), o2_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+    o3_ref, l3_ref = OR.attn_decode(f64(qd), f64(dq), v64, score_mod="none")
+    compare("out3", f64(out3), o3_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+    compare("lse3", f64(lse3), l3_ref, TOL["f16"]["lse_max"], dtype="f16", kind="lse")
+    o4_ref, _ = OR.attn_decode(f64(out2[:, :, :4]), k64, v64, score_mod="causal", q_offset=S - 4)
+    compare("out4", f64(out4), o4_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
+
+
 def test_workspace_serves_several_shapes():
     """One workspace, used by calls of different shapes in turn: each call's
     completion tickets may lie where the previous call wrote partial rows, so
