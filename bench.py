@@ -46,6 +46,10 @@ UNIT = "TFLOP/s"
 # back to None when the kernel changes until it is captured again.
 DKDV_TRAFFIC_BYTES = 80.9e6
 
+# Buffer sets of the end-to-end pipeline (device inputs and outputs, host
+# outputs): step i's kernels wait for the download of step i - E2E_SETS.
+E2E_SETS = 3
+
 
 def counted_flops(w, backward=True):
     f = 4.0 * w.B * w.H * w.Sq * w.Skv * w.D * (0.5 if w.causal else 1.0)
@@ -287,8 +291,9 @@ def bench_e2e(E, dev, args, w, results=E2E_ALL):
     (q, k, v, dout, key mask) from pinned host memory into the device and reads
     back the step's `results` (by default every output: out, lse, dq, dk, dv)
     into pinned host memory, inside the timed region.  Copies run on their own
-    streams, double-buffered, so step i+1's upload and step i-1's download
-    overlap step i's kernels (as a training input pipeline would)."""
+    streams over E2E_SETS buffer sets, so step i+1's upload and step i-1's
+    download overlap step i's kernels (as a training input pipeline would), and
+    step i's kernels wait only for the download of step i - E2E_SETS."""
     hosts = []
     for j in range(2):
         c = IN.make_case(w.B, w.H, w.Sq, w.Skv, w.D, w.dtype, seed=IN.SEED + 7000 + j, with_key_mask=True)
@@ -296,12 +301,12 @@ def bench_e2e(E, dev, args, w, results=E2E_ALL):
     shapes = {"out": hosts[0]["q"].shape, "lse": hosts[0]["q"].shape[:3], "dq": hosts[0]["q"].shape,
               "dk": hosts[0]["k"].shape, "dv": hosts[0]["v"].shape}
     dts = {n: (torch.float32 if n == "lse" else hosts[0]["q"].dtype) for n in shapes}
-    outs_h = [{n: torch.empty(shapes[n], dtype=dts[n]).pin_memory() for n in results} for _ in range(2)]
-    ins_d = [{k: torch.empty_like(v, device=dev) for k, v in hosts[0].items()} for _ in range(2)]
+    outs_h = [{n: torch.empty(shapes[n], dtype=dts[n]).pin_memory() for n in results} for _ in range(E2E_SETS)]
+    ins_d = [{k: torch.empty_like(v, device=dev) for k, v in hosts[0].items()} for _ in range(E2E_SETS)]
     outs_d = [{"lse": torch.empty(hosts[0]["q"].shape[:3], dtype=torch.float32, device=dev),
                "out": torch.empty_like(hosts[0]["q"], device=dev), "dq": torch.empty_like(hosts[0]["q"], device=dev),
                "dk": torch.empty_like(hosts[0]["k"], device=dev), "dv": torch.empty_like(hosts[0]["v"], device=dev)}
-              for _ in range(2)]
+              for _ in range(E2E_SETS)]
     shape = E.make_shape(ins_d[0]["q"], ins_d[0]["k"])
     ws_f = E.workspace(E.OP_FWD, shape, dev)
     ws_b = E.workspace(E.OP_BWD, shape, dev)
@@ -315,32 +320,32 @@ def bench_e2e(E, dev, args, w, results=E2E_ALL):
     # the kernels of one step on buffer set j, captured once as a CUDA graph
     # (the same API calls; the copies stay outside, on their own streams)
     with torch.cuda.stream(s_cmp):
-        compute(0)
-        compute(1)
+        for j in range(E2E_SETS):
+            compute(j)
     torch.cuda.synchronize()
-    graphs = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
-    for j in range(2):
+    graphs = [torch.cuda.CUDAGraph() for _ in range(E2E_SETS)]
+    for j in range(E2E_SETS):
         with torch.cuda.stream(s_cmp):
             with torch.cuda.graph(graphs[j], stream=s_cmp):
                 compute(j)
     torch.cuda.synchronize()
     ev = lambda: torch.cuda.Event()
-    up_done, cmp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    first = [True, True]
+    up_done, cmp_done, down_done = ([ev() for _ in range(E2E_SETS)] for _ in range(3))
+    first = [True] * E2E_SETS
 
     def step(i):
-        j = i % 2
+        j = i % E2E_SETS
         di, do, hi, ho = ins_d[j], outs_d[j], hosts[i % 2], outs_h[j]
         with torch.cuda.stream(s_up):
             if not first[j]:
-                s_up.wait_event(cmp_done[j])          # step i-2 has finished reading these inputs
+                s_up.wait_event(cmp_done[j])          # step i - E2E_SETS has finished reading these inputs
             for k in di:
                 di[k].copy_(hi[k], non_blocking=True)
             up_done[j].record(s_up)
         with torch.cuda.stream(s_cmp):
             s_cmp.wait_event(up_done[j])
             if not first[j]:
-                s_cmp.wait_event(down_done[j])        # step i-2's results have left these buffers
+                s_cmp.wait_event(down_done[j])        # step i - E2E_SETS's results have left these buffers
             graphs[j].replay()
             cmp_done[j].record(s_cmp)
         with torch.cuda.stream(s_down):
@@ -350,10 +355,10 @@ def bench_e2e(E, dev, args, w, results=E2E_ALL):
             down_done[j].record(s_down)
         first[j] = False
 
-    for i in range(4):
+    for i in range(2 * E2E_SETS):
         step(i)
     torch.cuda.synchronize()
-    n = max(4, min(args.steps, 40))
+    n = max(2 * E2E_SETS, min(args.steps, 40))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s_up)
     for i in range(n):
@@ -367,7 +372,7 @@ def bench_e2e(E, dev, args, w, results=E2E_ALL):
     h2d = sum(v.numel() * v.element_size() for v in hosts[0].values())
     d2h = sum(v.numel() * v.element_size() for v in outs_h[0].values())
     return {"ms": ms, "h2d": h2d, "d2h": d2h, "results": list(results),
-            "pipeline": "double-buffered, copies on separate streams, kernels replayed as a CUDA graph; "
+            "pipeline": f"{E2E_SETS} buffer sets, copies on separate streams, kernels replayed as a CUDA graph; "
                         f"read back: {', '.join(results)}"}
 
 
