@@ -454,6 +454,10 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   p.fold = um ? 0 : mod_fold_ok(mod, scale, s->H);
   p.inv_scale = scale != 0.f ? 1.f / scale : 0.f;
   p.nsplit = 1;   // whole kv range per CTA, q_off = 0
+  // persistent CTAs, one per SM, taking the items from the counter in the
+  // workspace header (kWsItemCounter)
+  p.items = at<unsigned>(ws, kWsItemCounter);
+  p.ctas = (int)std::min<long long>((long long)p.npairs * p.B * p.H, sm_count());
   if (um) return cuda_status(launch_fwd_d64_kernel(p, uk[0], st));
   return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
 }

@@ -7,10 +7,17 @@
 // README's "log2 trick": the scale and the mods' biases carry a log2(e) factor
 // and every exp is one MUFU ex2.
 //
-// One CTA owns two 128-row query tiles of one (b, h) and streams the union of
-// their kv-block lists once:
-//   warp 0      TMA producer: both Q tiles once, then K and V tiles of each kv
-//               block into a FWD_NST-stage ring (128B swizzle, 16 KB per tile).
+// A work item is two 128-row query tiles of one (b, h); the CTA streams the
+// union of their kv-block lists once.  The grid is one CTA per SM (at most one
+// per item), and the CTAs take items from an atomic counter in the workspace,
+// longest causal pairs first; the split variant (a chunk of queries, or a kv
+// range per CTA) runs one item per CTA instead.  Items pass through two slots
+// (the item and its kv-block flags), so the next item's query tiles and first
+// blocks load while the softmax finishes the previous one.
+//   warp 0      producer: takes the items, fills the slots, loads both Q tiles of
+//               an item once the previous item's S products are done with them,
+//               then K and V tiles of each kv block into a FWD_NST-stage ring
+//               (128B swizzle, 16 KB per tile), continuing across items.
 //   warps 1-2   warp 1 allocates 512 TMEM columns; lane 0 of warp 1 + t issues
 //               tile t's tcgen05.mma: S_t = Q_t K^T (128x128, f32 in TMEM) and
 //               O_t += P_t V with P_t read from TMEM.  Two issuing threads keep
@@ -36,12 +43,17 @@ struct __align__(1024) FwdSmem {
   // qaug (per query row, resident) x kaug[s] (per key of stage s).
   __align__(128) uint8_t qaug[4096];
   __align__(128) uint8_t kaug[FWD_NST][4096];
+  __align__(128) uint8_t qaug_h[2][256];   // folded ALiBi: an item slot's query side (8 rows, repeated)
   uint64_t full[FWD_NST], empty[FWD_NST];
-  uint64_t qfull, sfull[2], sfree[2], pready[2], odone[2], fin[2];
+  uint64_t qfull, qfree, sfull[2], sfree[2], pready[2], odone[2], fin[2];
+  uint64_t item_ready[2], item_free[2];   // per item slot: written by the producer / done with by the rest
   alignas(16) float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
   uint32_t tmem_base;
   int abort;
-  uint8_t flags[2][FWD_MAXKB];
+  // Two item slots, filled by the producer in turn: the item (-1 = no more) and
+  // its flags per tile and kv block.
+  int item[2];
+  uint8_t flags[2][2][FWD_MAXKB];
 };
 
 // the bias table is read 16 bytes at a time
@@ -117,25 +129,41 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr bool DM = VAR == FWD_DENSE, CHUNK = VAR == FWD_CHUNK;
   const int BH = p.B * p.H;
-  const int L = CHUNK ? blockIdx.x % (p.npairs * BH) : blockIdx.x;
-  const int split = CHUNK ? blockIdx.x / (p.npairs * BH) : 0;   // kv-block range of this CTA
+  const int n_items = p.npairs * BH;   // (pair of query tiles, b, h), longest causal pairs first
+  // The split variant runs one item per CTA over its range of kv blocks.  Otherwise
+  // CTAs take items from the counter p.items in turn (one CTA per SM), or, with no
+  // counter, one item each, blockIdx.x.
+  const int split = CHUNK ? blockIdx.x / n_items : 0;   // kv-block range of this CTA
   const int kb_lo = CHUNK ? split * p.kps : 0;
   const int kb_hi = CHUNK && p.nsplit > 1 ? min(p.nkb, kb_lo + p.kps) : p.nkb;
   const int q_off = CHUNK ? p.q_off : 0;
-  const int pair = p.npairs - 1 - L / BH;   // longest causal pairs first
-  const int bh = L % BH;
-  const int b = bh / p.H, h = bh % p.H;
-  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
-  const bool valid1 = qt1 < p.nqb;
+  const bool persistent = !CHUNK && p.items != nullptr;
+  // an item's coordinates
+  struct Item {
+    int bh, b, h, qt0, qt1;
+    bool valid1;
+  };
+  auto item_of = [&](int L) {
+    Item it;
+    const int pair = p.npairs - 1 - L / BH;
+    it.bh = L % BH;
+    it.b = it.bh / p.H;
+    it.h = it.bh % p.H;
+    it.qt0 = 2 * pair;
+    it.qt1 = 2 * pair + 1;
+    it.valid1 = it.qt1 < p.nqb;
+    return it;
+  };
   if constexpr (CHUNK) {
     // launched with programmatic dependent launch: this CTA's first K and V rows
     // (kv blocks from kb_lo, contiguous, 128 bytes a row) go towards L2, the next
     // grid may launch, and nothing is read or written before the grids ahead of
     // this one have completed (L2 is the point of coherence: a line fetched
     // early still reflects writes made before the wait)
+    const int bh0 = item_of(blockIdx.x % n_items).bh;
     if (tid < 2 && p.kraw && p.vraw) {   // (at most 2 FWD_NST blocks: the ring streams the rest)
-      const long long r0 = (long long)bh * p.Skv + (long long)kb_lo * 128;
-      const long long r1 = (long long)bh * p.Skv + min((long long)p.Skv, (long long)min(kb_hi, kb_lo + 2 * FWD_NST) * 128);
+      const long long r0 = (long long)bh0 * p.Skv + (long long)kb_lo * 128;
+      const long long r1 = (long long)bh0 * p.Skv + min((long long)p.Skv, (long long)min(kb_hi, kb_lo + 2 * FWD_NST) * 128);
       if (r1 > r0)
         prefetch_l2_bulk(static_cast<const unsigned char*>(tid == 0 ? p.kraw : p.vraw) + r0 * 128,
                          static_cast<uint32_t>((r1 - r0) * 128));
@@ -149,50 +177,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     griddep_launch_dependents();
   }
 
-  // ---- setup: barriers, TMEM, per-kv-block flags
+  // ---- setup: barriers, TMEM (the items' flags and query tiles come from the producer)
   if (tid == 0) {
     for (int s = 0; s < FWD_NST; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), valid1 ? 2 : 1);   // one arrival per tile per kv block
+      mbar_init(smem_u32(&sm.empty[s]), 2);   // one arrival per tile per kv block (a tile with no rows arrives too)
     }
     mbar_init(smem_u32(&sm.qfull), 1);
+    mbar_init(smem_u32(&sm.qfree), 2);        // both MMA threads, once per item
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&sm.sfull[t]), 1);
       mbar_init(smem_u32(&sm.sfree[t]), 128);
       mbar_init(smem_u32(&sm.pready[t]), 128);
       mbar_init(smem_u32(&sm.odone[t]), 1);
       mbar_init(smem_u32(&sm.fin[t]), 1);
+      mbar_init(smem_u32(&sm.item_ready[t]), 1);
+      mbar_init(smem_u32(&sm.item_free[t]), 2 + 256);   // both MMA threads and every softmax thread
     }
     sm.abort = 0;
     fence_mbar_init();
     fence_async_smem();
-    // the CTA's query tiles do not depend on the flags: their copy goes out now
-    // and lands under the rest of the set-up
-    tma_prefetch_desc(&p.tm_q);
-    mbar_expect_tx(smem_u32(&sm.qfull), (valid1 ? 2 : 1) * FWD_TILE_BYTES);
-    tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, smem_u32(&sm.qfull), 0, bh * p.Sq + qt0 * 128);
-    if (valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, smem_u32(&sm.qfull), 0, bh * p.Sq + qt1 * 128);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
     tmem_relinquish();
-  }
-  const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;   // dense-mask index of (b, h)
-  for (int kb = tid; kb < p.nkb; kb += FWD_THREADS) {
-    const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
-    for (int t = 0; t < 2; ++t) {
-      const int qt = qt0 + t;
-      uint8_t f = 0;
-      if (qt < p.nqb && ks != 0 && (!CHUNK || (kb >= kb_lo && kb < kb_hi))) {
-        const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qt * p.nkb + kb] : TILE_FULL;
-        int ds = TILE_FULL;   // dense tile state: dense build only
-        if constexpr (DM) ds = p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb];
-        if (st != TILE_EMPTY && ds != TILE_EMPTY)
-          f = KB_VISIT | (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) |
-              (ks == 1 ? KB_KEYMASK : 0) | (ds == TILE_PARTIAL ? KB_DENSE : 0);
-      }
-      sm.flags[t][kb] = f;
-    }
   }
   constexpr bool kTableMod = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
   // Terms that depend on the query row or the key column alone ride on the S
@@ -202,10 +210,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   //   with `fold`, the mod's bias over scale in columns AUG_MOD .. +2, as three
   //   16-bit terms of one f32 value:
   //     checkerboard  (-1)^q_pos t_i  x  (-1)^c        (t = 0.5 / scale)
-  //     ALiBi         1               x  t_i(c)        (t(c) = slope_h c / scale)
+  //     ALiBi         t_i             x  c / 128       (t = 128 slope_h / scale)
   //   c = key column in the block (a kv block starts at a multiple of 128, so
-  //   (-1)^kv = (-1)^c); ALiBi's remaining slope_h (kv0 - q_pos) is a constant per
-  //   row and block, added to the row maximum (below).  Without `fold` (scale 0,
+  //   (-1)^kv = (-1)^c; c / 128 is exact in both 16-bit types, and each product
+  //   t_i c / 128 is exact in f32); ALiBi's t depends on the head: its query
+  //   side is the same in every row, 8 rows per item slot (qaug_h) that the
+  //   descriptor repeats over the tile, written by the producer with the
+  //   slot's flags.  ALiBi's remaining
+  //   slope_h (kv0 - q_pos) is a constant per row and block, added to the row
+  //   maximum (below).  Without `fold` (scale 0,
   //   or a bias too large for three 16-bit terms) the producer's per-column table
   //   carries the mod and the mask instead.
   const bool fold = kTableMod && p.fold;
@@ -214,6 +227,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   if (aug) {
     uint4* z = reinterpret_cast<uint4*>(sm.qaug);
     for (int i = tid; i < (1 + FWD_NST) * 4096 / 16; i += FWD_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < 2 * 256 / 16) reinterpret_cast<uint4*>(sm.qaug_h)[tid] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     if (tid < 128) {
       const int r = tid;   // query row of the tile, and key column of a block
@@ -229,10 +243,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
             qt3[i] = qodd ? uint16_t(t[i] ^ 0x8000u) : t[i];   // the sign bit of f16 and bf16
             kt3[i] = (r & 1) ? to16<BF16>(-1.f) : one;
           }
-        } else {
-          const float slope = exp2f(-8.0f * float(h + 1) / float(p.H));
-          split3_plain<BF16>(slope * float(r) * p.inv_scale, kt3);
-          for (int i = 0; i < 3; ++i) qt3[i] = one;
+        } else {   // the query side depends on the head: written per item by the producer
+          for (int i = 0; i < 3; ++i) {
+            qt3[i] = 0;
+            kt3[i] = to16<BF16>(float(r) * (1.f / 128.f));
+          }
         }
         for (int i = 0; i < 3; ++i) {
           *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_MOD + i)) = qt3[i];
@@ -249,68 +264,137 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    // ======================= TMA producer (lane 0) + bias tables (all lanes) =======================
+    // ======================= producer: items, query tiles, K/V ring, per-stage columns =======================
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
     const uint32_t qbar = smem_u32(&sm.qfull);
-    if (lane == 0) {   // the query tiles went out in the set-up
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
     }
-    const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
     int last_u[FWD_NST];
     for (int s = 0; s < FWD_NST; ++s) last_u[s] = -1;
-    int u = 0;
-    for (int kb = 0; kb < p.nkb; ++kb) {
-      const uint8_t fu = sm.flags[0][kb] | sm.flags[1][kb];
-      if (!(fu & KB_VISIT)) continue;
-      const int s = u % FWD_NST;
-      if (u >= FWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) break;
-      if (aug && p.km_bits) {
-        // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column AUG_KEY of kaug[s]
-        uint32_t bits = 0xffffffffu;
-        if (fu & KB_KEYMASK) bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
-        // the infinity whose product with the scale is -inf (scale != 0)
-        const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int col = 4 * lane + i;
-          *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, AUG_KEY)) =
-              ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+    int u = 0, last_q = -1;
+    bool ok = true;
+    for (int ci = 0; ok; ++ci) {
+      const int sl = ci & 1;
+      int L = 0;
+      if (lane == 0) L = persistent ? (int)atomicAdd(p.items, 1u) : (ci == 0 ? (int)(blockIdx.x % n_items) : n_items);
+      L = __shfl_sync(0xffffffffu, L, 0);
+      // the slot's previous item (ci - 2) is done with everywhere
+      if (ci >= 2 && !wait_warp(smem_u32(&sm.item_free[sl]), ((ci - 2) >> 1) & 1, c)) break;
+      if (L >= n_items) {   // no more items: the others stop at this slot
+        if (lane == 0) {
+          sm.item[sl] = -1;
+          mbar_arrive(smem_u32(&sm.item_ready[sl]));
         }
-        fence_async_smem();
-      } else if (use_table) {
-        // lane owns columns 4 lane .. 4 lane + 3 of this kv block
-        uint32_t bits = 0xffffffffu;
-        if (p.km_bits && (fu & KB_KEYMASK)) bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int col = 4 * lane + i;
-          float base = ((bits >> (col & 31)) & 1u) ? 0.f : -INFINITY;
-          if constexpr (MOD == MOD_ALIBI) base += slope2 * float(col);
-          float e = base, o = base;
-          if constexpr (MOD == MOD_CHECKER) {
-            const float hb = (col & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // row parity 0
-            e = base + hb;
-            o = base - hb;
+        break;
+      }
+      const Item it = item_of(L);
+      const long long dmi = (long long)it.b * p.dm.mb + (long long)it.h * p.dm.mh;   // dense-mask index of (b, h)
+      for (int kb = lane; kb < p.nkb; kb += 32) {
+        const int ks = p.km_sum ? p.km_sum[it.b * p.nkb + kb] : 2;
+        for (int t = 0; t < 2; ++t) {
+          const int qt = t ? it.qt1 : it.qt0;
+          uint8_t f = 0;
+          if (qt < p.nqb && ks != 0 && kb >= kb_lo && kb < kb_hi) {
+            const int st =
+                p.bm_tiles ? p.bm_tiles[it.b * p.bm_sb + it.h * p.bm_sh + (long long)qt * p.nkb + kb] : TILE_FULL;
+            int ds = TILE_FULL;   // dense tile state: dense build only
+            if constexpr (DM) ds = p.dm.tiles[(dmi * p.nqb + qt) * p.nkb + kb];
+            if (st != TILE_EMPTY && ds != TILE_EMPTY)
+              f = KB_VISIT | (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) |
+                  (ks == 1 ? KB_KEYMASK : 0) | (ds == TILE_PARTIAL ? KB_DENSE : 0);
           }
-          sm.cb[s][0][col] = e;
-          sm.cb[s][1][col] = o;
+          sm.flags[sl][t][kb] = f;
+        }
+      }
+      if (lane == 0) {
+        sm.item[sl] = L;
+        if (MOD == MOD_ALIBI && fold) {
+          // the item's head in the query side of the folded ALiBi term: columns
+          // AUG_MOD .. +2 and AUG_KEY (the key mask's constant one) of a row are 8
+          // contiguous bytes (the rest of the slot stays zero).  (One thread at
+          // fixed offsets: stores from every lane of the producer cost the kernel
+          // registers.)
+          static_assert(AUG_MOD == 0 && AUG_KEY == 3, "one 8-byte store per query row");
+          uint16_t t3[3];
+          split3_plain<BF16>(128.f * exp2f(-8.0f * float(it.h + 1) / float(p.H)) * p.inv_scale, t3);
+          const uint2 w = make_uint2(uint32_t(t3[0]) | (uint32_t(t3[1]) << 16),
+                                     uint32_t(t3[2]) | (uint32_t(to16<BF16>(1.f)) << 16));
+#pragma unroll
+          for (int r = 0; r < 8; ++r) *reinterpret_cast<uint2*>(sm.qaug_h[sl] + k16_offset(r, 0)) = w;
+          fence_async_smem();
         }
       }
       __syncwarp();
-      // test hook: withhold the first copy so the consumers' bounded waits run out
-      const bool withhold = p.inject_stall && u == 0;
-      if (lane == 0 && !withhold) {
-        const uint32_t fb = smem_u32(&sm.full[s]);
-        mbar_expect_tx(fb, 2 * FWD_TILE_BYTES);   // release: the tables above are visible to its waiters
-        tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
-        tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
+      if (lane == 0) mbar_arrive(smem_u32(&sm.item_ready[sl]));   // release: the slot is visible to its waiters
+      // the query tiles, once the previous item's S products are done with them
+      if (ci >= 1 && !wait_warp(smem_u32(&sm.qfree), (ci - 1) & 1, c)) break;
+      if (lane == 0) {
+        mbar_expect_tx(qbar, (it.valid1 ? 2 : 1) * FWD_TILE_BYTES);
+        tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, qbar, 0, it.bh * p.Sq + it.qt0 * 128);
+        if (it.valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, qbar, 0, it.bh * p.Sq + it.qt1 * 128);
       }
-      if (!withhold) last_u[s] = u;
-      ++u;
+      last_q = ci;
+      const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(it.h, p.H) : 0.f;
+      for (int kb = 0; kb < p.nkb; ++kb) {
+        const uint8_t fu = sm.flags[sl][0][kb] | sm.flags[sl][1][kb];
+        if (!(fu & KB_VISIT)) continue;
+        const int s = u % FWD_NST;
+        if (u >= FWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) {
+          ok = false;
+          break;
+        }
+        if (aug) {
+          if (p.km_bits) {
+            // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column AUG_KEY of kaug[s]
+            uint32_t bits = 0xffffffffu;
+            if (fu & KB_KEYMASK) bits = km_word(p.km_bits, it.b, p.Skv, kb * 128 + 4 * lane);
+            // the infinity whose product with the scale is -inf (scale != 0)
+            const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int col = 4 * lane + i;
+              *reinterpret_cast<uint16_t*>(sm.kaug[s] + k16_offset(col, AUG_KEY)) =
+                  ((bits >> (col & 31)) & 1u) ? uint16_t(0) : ninf;
+            }
+          }
+          fence_async_smem();
+        } else if (use_table) {
+          // lane owns columns 4 lane .. 4 lane + 3 of this kv block
+          uint32_t bits = 0xffffffffu;
+          if (p.km_bits && (fu & KB_KEYMASK)) bits = km_word(p.km_bits, it.b, p.Skv, kb * 128 + 4 * lane);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int col = 4 * lane + i;
+            float base = ((bits >> (col & 31)) & 1u) ? 0.f : -INFINITY;
+            if constexpr (MOD == MOD_ALIBI) base += slope2 * float(col);
+            float e = base, o = base;
+            if constexpr (MOD == MOD_CHECKER) {
+              const float hb = (col & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // row parity 0
+              e = base + hb;
+              o = base - hb;
+            }
+            sm.cb[s][0][col] = e;
+            sm.cb[s][1][col] = o;
+          }
+        }
+        __syncwarp();
+        // test hook: withhold the first copy so the consumers' bounded waits run out
+        const bool withhold = p.inject_stall && u == 0;
+        if (lane == 0 && !withhold) {
+          const uint32_t fb = smem_u32(&sm.full[s]);
+          mbar_expect_tx(fb, 2 * FWD_TILE_BYTES);   // release: the columns above are visible to its waiters
+          tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, it.bh * p.Skv + kb * 128);
+          tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, it.bh * p.Skv + kb * 128);
+        }
+        if (!withhold) last_u[s] = u;
+        ++u;
+      }
     }
     if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-      drain_wait(qbar, 0, p.timeout_ns);
+      if (last_q >= 0) drain_wait(qbar, last_q & 1, p.timeout_ns);
       for (int s = 0; s < FWD_NST; ++s)
         if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / FWD_NST) & 1, p.timeout_ns);
     }
@@ -322,61 +406,78 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     // P_t(n) is in TMEM (pready).  Each tile arrives once per kv block on the
     // stage's empty barrier: a commit after its P V, or a plain arrival for a
     // block it skips.
+    // Both threads run every item (a tile past the last query tile visits no
+    // block but still arrives); the first P V of an item overwrites O.
     const int t = warp - 1;
-    if (lane == 0 && (t == 0 || valid1)) {
+    if (lane == 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 2 + 16 * t};
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
       const uint32_t tS = tmem + 256 * t, tP = tS + 128, tO = tS + 192;
       const uint64_t qd = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
-      const uint64_t qad = sdesc_k16(smem_u32(sm.qaug));
+      const uint64_t qad0 = sdesc_k16(smem_u32(sm.qaug));
       uint64_t dk_[FWD_NST], dv_[FWD_NST];
       for (int s = 0; s < FWD_NST; ++s) {
         dk_[s] = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
         dv_[s] = sdesc_sw128(smem_u32(sm.v[s]), 8192, 1024);
       }
-      uint32_t n = 0;        // S products issued for this tile
+      uint32_t n = 0;        // S products issued for this tile, over all items
+      uint32_t n0 = 0;       // ... before the current item
       int s_pend = -1;       // stage of the block whose P V is still to issue
       uint32_t j_pend = 0;   // that block's index among this tile's visited blocks
-      bool ok = wait_one(smem_u32(&sm.qfull), 0, c);
+      bool ok = true;
       auto issue_pv = [&]() -> bool {   // P_t(j_pend) V (stage s_pend), then release the stage
         if (!wait_one(smem_u32(&sm.pready[t]), j_pend & 1, c)) return false;
         tc_fence_after();
         const uint64_t vd = dv_[s_pend];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tP + kk * 8, vd + 128 * kk, IDESC_PV, (kk > 0 || j_pend > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tO, tP + kk * 8, vd + 128 * kk, IDESC_PV, (kk > 0 || j_pend > n0) ? 1u : 0u);
         tc_commit(smem_u32(&sm.odone[t]));
         tc_commit(smem_u32(&sm.empty[s_pend]));
         s_pend = -1;
         return true;
       };
       int u = 0;
-      for (int kb = 0; ok && kb < p.nkb; ++kb) {
-        const uint8_t f = sm.flags[t][kb];
-        if (!((f | sm.flags[t ^ 1][kb]) & KB_VISIT)) continue;
-        const int s = u % FWD_NST;
-        if (!(f & KB_VISIT)) {
-          // not this tile's block: first let any pending P V go (its stage must not be held)
-          if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
+      for (int ci = 0; ok; ++ci) {
+        const int sl = ci & 1;
+        if (!wait_one(smem_u32(&sm.item_ready[sl]), (ci >> 1) & 1, c)) break;
+        if (sm.item[sl] < 0) break;
+        if (!wait_one(smem_u32(&sm.qfull), ci & 1, c)) break;
+        n0 = n;
+        const uint64_t qad = (MOD == MOD_ALIBI && fold) ? sdesc_k16_rows8(smem_u32(sm.qaug_h[sl])) : qad0;
+        for (int kb = 0; ok && kb < p.nkb; ++kb) {
+          const uint8_t f = sm.flags[sl][t][kb];
+          if (!((f | sm.flags[sl][t ^ 1][kb]) & KB_VISIT)) continue;
+          const int s = u % FWD_NST;
+          if (!(f & KB_VISIT)) {
+            // not this tile's block: first let any pending P V go (its stage must not be held)
+            if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
+            if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
+            mbar_arrive(smem_u32(&sm.empty[s]));
+            ++u;
+            continue;
+          }
           if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
-          mbar_arrive(smem_u32(&sm.empty[s]));
-          ++u;
-          continue;
-        }
-        if (!wait_one(smem_u32(&sm.full[s]), (u / FWD_NST) & 1, c)) { ok = false; break; }
-        if (n > 0 && !wait_one(smem_u32(&sm.sfree[t]), (n - 1) & 1, c)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t kd = dk_[s];
+          if (n > 0 && !wait_one(smem_u32(&sm.sfree[t]), (n - 1) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kd = dk_[s];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tS, qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
-        if (aug) mma_ss(tS, qad, sdesc_k16(smem_u32(sm.kaug[s])), IDESC_S, 1u);
-        tc_commit(smem_u32(&sm.sfull[t]));
-        if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
-        s_pend = s;
-        j_pend = n++;
-        ++u;
+          for (int kk = 0; kk < 4; ++kk) mma_ss(tS, qd + 2 * kk, kd + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
+          if (aug) mma_ss(tS, qad, sdesc_k16(smem_u32(sm.kaug[s])), IDESC_S, 1u);
+          tc_commit(smem_u32(&sm.sfull[t]));
+          if (s_pend >= 0 && !issue_pv()) { ok = false; break; }
+          s_pend = s;
+          j_pend = n++;
+          ++u;
+        }
+        if (!ok) break;
+        // arrives once this item's S products (all issued by now) have read the
+        // query tiles: the producer reloads them under the item's last P V
+        tc_commit(smem_u32(&sm.qfree));
+        if (s_pend >= 0 && !issue_pv()) break;
+        mbar_arrive(smem_u32(&sm.item_free[sl]));
       }
-      if (ok && s_pend >= 0 && !issue_pv()) ok = false;
       // every MMA issued by this thread completes before the CTA lets go of TMEM
       tc_commit(smem_u32(&sm.fin[t]));
       drain_wait(smem_u32(&sm.fin[t]), 0, p.timeout_ns);
@@ -386,31 +487,44 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     // ======================= softmax warpgroups =======================
     const int t = (warp - 3) >> 2;
     const int quad = warp & 3;   // TMEM lanes [32 quad, 32 quad + 32)
-    const int qt = qt0 + t;
-    if (qt < p.nqb) {
-      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 3 + t};
-      const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
-      const uint32_t tS = tmem + lane_off + 256 * t;
-      const uint32_t tP = tS + 128, tO = tS + 192;
-      const int row = 32 * quad + lane;
+    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 3 + t};
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
+    const uint32_t tS = tmem + lane_off + 256 * t;
+    const uint32_t tP = tS + 128, tO = tS + 192;
+    const int row = 32 * quad + lane;
+    const uint64_t scv = f2(p.sc, p.sc);
+    // unscaled scores in the max pass (scale > 0 keeps the order of the maximum)
+    const bool raw = !use_table && MOD != MOD_USER && p.sc > 0.f;
+    uint32_t n = 0;   // blocks of this tile, over all items (the barriers' phases)
+    int u = 0;        // blocks of the items' unions (the ring's stages)
+    bool ok = true;
+    for (int ci = 0; ok; ++ci) {
+      const int sl = ci & 1;
+      if (!wait_warp(smem_u32(&sm.item_ready[sl]), (ci >> 1) & 1, c)) break;
+      const int L = sm.item[sl];
+      if (L < 0) break;
+      const Item it = item_of(L);
+      const int b = it.b, h = it.h, bh = it.bh;
+      const int qt = t ? it.qt1 : it.qt0;
+      if (qt >= p.nqb) {   // no rows of this tile in the item: the union's blocks only
+        for (int kb = 0; kb < p.nkb; ++kb) u += ((sm.flags[sl][0][kb] | sm.flags[sl][1][kb]) & KB_VISIT) ? 1 : 0;
+        mbar_arrive(smem_u32(&sm.item_free[sl]));
+        continue;
+      }
+      const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;   // dense-mask index of (b, h)
       const int q = qt * 128 + row;
       const int qpos = q + q_off;   // the row's position among the keys (score mods, causal rule)
       const bool writer = quad == 3 && lane == 0;   // first warp of the group (warp 3 or 7)
       // the split variant's chunk of queries may end inside the tile: a warp whose
       // 32 rows all lie past Sq does no arithmetic, only the group's arrivals
       const bool idle = CHUNK && qt * 128 + 32 * quad >= p.Sq;
-      const uint64_t scv = f2(p.sc, p.sc);
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
       const int parity = (MOD == MOD_CHECKER) ? (qpos & 1) : 0;
-      // unscaled scores in the max pass (scale > 0 keeps the order of the maximum)
-      const bool raw = !use_table && MOD != MOD_USER && p.sc > 0.f;
       float m_run = -INFINITY, l = 0.f;
-      uint32_t n = 0;
-      int u = 0;
-      bool ok = true;
+      const uint32_t n0 = n;   // this item's first block of the tile
       for (int kb = 0; kb < p.nkb; ++kb) {
-        const uint8_t f = sm.flags[t][kb];
-        const bool in_union = (f | sm.flags[t ^ 1][kb]) & KB_VISIT;
+        const uint8_t f = sm.flags[sl][t][kb];
+        const bool in_union = (f | sm.flags[sl][t ^ 1][kb]) & KB_VISIT;
         if (p.visited && writer)
           p.visited[((size_t)bh * p.nqb + qt) * p.nkb + kb] = (f & KB_VISIT) ? 1 : 0;
         if (!(f & KB_VISIT)) {
@@ -556,7 +670,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         ++n;
       }
       tmem_st_wait();
-      if (ok && n > 0) {
+      if (ok && n > n0) {
         if (!wait_warp(smem_u32(&sm.odone[t]), (n - 1) & 1, c))
           ok = false;
         else
@@ -565,7 +679,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       if (ok) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         uint32_t o[64], w[32];
-        if (n > 0) {
+        if (n > n0) {
           tmem_ld64(tO, o);
         } else {
 #pragma unroll
@@ -591,6 +705,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           p.lse[(size_t)bh * p.Sq + q] = l > 0.f ? (m_fin + lg2(l)) * kLn2 : -INFINITY;
         }
       }
+      if (!ok) break;
+      // the epilogue has read O out (its TMEM load waits): the next item's first P V may overwrite it
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.item_free[sl]));
     }
   }
 
@@ -599,6 +717,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // the last CTA to finish re-arms the item counter for the next call (this
+  // thread made the CTA's last claim, so every claim precedes the reset)
+  if (persistent && tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.items + 1, 1u) == gridDim.x - 1u) {
+      p.items[0] = 0u;
+      p.items[1] = 0u;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -613,7 +740,7 @@ cudaError_t launch_fwd_d64_kernel(const FwdParams& p, const void* kern, cudaStre
   const size_t smem = fwd_d64_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(p.npairs * p.B * p.H * p.nsplit);
+  const unsigned grid = (unsigned)(p.items ? p.ctas : p.npairs * p.B * p.H * p.nsplit);
   void* args[] = {const_cast<FwdParams*>(&p)};
   return cudaLaunchKernel(kern, dim3(grid), dim3(FWD_THREADS), args, smem, st);
 }
@@ -628,7 +755,7 @@ static cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.npairs * p.B * p.H * p.nsplit));
+  cfg.gridDim = dim3((unsigned)(p.items && !chunk ? p.ctas : p.npairs * p.B * p.H * p.nsplit));
   cfg.blockDim = dim3(FWD_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -74,6 +74,12 @@ struct FwdParams {
   float* part;
   const void* kraw;               // K and V base pointers (the split variant asks L2 for its rows)
   const void* vraw;
+  // Persistent CTAs: `ctas` CTAs take the items in launch order from the counter
+  // items[0]; items[1] counts the CTAs that finished, and the last one resets
+  // both to zero (the pair sits at a fixed workspace offset, zero before the
+  // first call).  items = nullptr: one CTA per item.
+  unsigned* items;
+  int ctas;
   // ALiBi / checkerboard bias folded into S = Q K^T as one more K = 16 step
   // (the AUG_MOD columns of the augmented operands), and 1 / scale
   int fold;

@@ -273,6 +273,16 @@ DEVI uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 DEVI uint32_t k16_offset(int r, int c) {
   return (uint32_t)(r >> 3) * 256u + (uint32_t)(c >> 3) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(c & 7) * 2u;
 }
+// The same layout with a stride of 0 between 8-row groups: every group of 8
+// rows of the operand reads the one group at saddr (256 bytes), an operand
+// whose rows repeat with period 8.
+DEVI uint64_t sdesc_k16_rows8(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= 1ull << 46;
+  return d;
+}
 DEVI uint64_t sdesc_k16(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);

@@ -596,6 +596,43 @@ def test_workspace_serves_several_shapes():
         compare("decode out", f64(out), o_ref, TOL["f16"]["o_max"], TOL["f16"]["o_mean"], dtype="f16", kind="out")
 
 
+@pytest.mark.parametrize("B,H,S,dtype,mod,km,bm", [
+    (3, 12, 1100, "bf16", "alibi", True, "causal"),
+    (3, 12, 1100, "f16", "checkerboard", False, None),
+    (2, 28, 640, "f16", "causal", True, None),
+])
+def test_forward_items_outnumber_the_ctas(B, H, S, dtype, mod, km, bm):
+    """More (query-tile pair, b, h) items than SMs: each of the forward's CTAs
+    (one per SM) runs several items, of different heads and query tiles, in turn
+    (ALiBi's slope changes from item to item; an odd tile count leaves the last
+    pair one tile); outputs, visited tiles and bitwise reproducibility as usual."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert B * H * ((-(-S // 128) + 1) // 2) > nsm
+    run_and_check(B, H, S, S, dtype, mod, km, bm, backward=False)
+
+
+def test_forward_item_counter_left_at_zero():
+    """The forward's CTAs take items from a counter pair in the workspace header
+    (bytes 16 .. 23); the last CTA to finish sets it back to zero, so that calls of
+    any shape can follow on the same workspace."""
+    dev = torch.device("cuda")
+    shapes = [(3, 12, 1100, "bf16"), (1, 3, 300, "f16"), (3, 12, 1100, "f16"), (2, 2, 128, "bf16")]
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
+    need = max(E.workspace_size(E.OP_FWD, E.make_shape(torch.empty((B, H, S, 64), dtype=tdt[dt], device=dev),
+                                                       torch.empty((B, H, S, 64), dtype=tdt[dt], device=dev)))
+               for B, H, S, dt in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    for i, (B, H, S, dt) in enumerate(shapes):
+        c, d = make_dev(B, H, S, S, 64, dt, key_mask=True, dout=None, seed=IN.SEED + 700 + i)
+        out, lse = E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], score_mod="alibi", ws=ws)
+        torch.cuda.synchronize()
+        assert not ws[16:24].any(), f"item counter left at {ws[16:24].view(torch.int32).tolist()}"
+        assert E.poll_status(ws) == E.ATTN_OK
+        o_ref, _ = OR.attn_fwd(f64(c["q"]), f64(c["k"]), f64(c["v"]), key_mask=c["key_mask"].numpy(),
+                               score_mod="alibi")
+        compare("out", f64(out), o_ref, TOL[dt]["o_max"], TOL[dt]["o_mean"], dtype=dt, kind="out")
+
+
 @pytest.mark.parametrize("graph", [False, True])
 def test_decode_back_to_back_calls_share_a_workspace(graph):
     """Decode launches overlap their predecessor (programmatic dependent launch):
