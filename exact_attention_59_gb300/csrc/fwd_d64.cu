@@ -128,6 +128,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr bool DM = VAR == FWD_DENSE, CHUNK = VAR == FWD_CHUNK;
+  // the waits' slow paths take their context by address in the run-time-compiled
+  // score_mod build (measured faster there, and slower in the built-in mods)
+  using WC = WaitCtxT<MOD == MOD_USER>;
   const int BH = p.B * p.H;
   const int n_items = p.npairs * BH;   // (pair of query tiles, b, h), longest causal pairs first
   // The split variant runs one item per CTA over its range of kv blocks.  Otherwise
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
 
   if (warp == 0) {
     // ======================= producer: items, query tiles, K/V ring, per-stage columns =======================
-    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 1};
+    WC c{&sm.abort, p.status, p.timeout_ns, 1};
     const uint32_t qbar = smem_u32(&sm.qfull);
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     // block but still arrives); the first P V of an item overwrites O.
     const int t = warp - 1;
     if (lane == 0) {
-      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 2 + 16 * t};
+      WC c{&sm.abort, p.status, p.timeout_ns, 2 + 16 * t};
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
       const uint32_t tS = tmem + 256 * t, tP = tS + 128, tO = tS + 192;
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     // ======================= softmax warpgroups =======================
     const int t = (warp - 3) >> 2;
     const int quad = warp & 3;   // TMEM lanes [32 quad, 32 quad + 32)
-    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 3 + t};
+    WC c{&sm.abort, p.status, p.timeout_ns, 3 + t};
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     const uint32_t tS = tmem + lane_off + 256 * t;
     const uint32_t tP = tS + 128, tO = tS + 192;

@@ -44,12 +44,19 @@ DEVI uint32_t lane_id() { return threadIdx.x & 31u; }
 // ---------------------------------------------------------------------------
 // Abort / status plumbing
 // ---------------------------------------------------------------------------
-struct WaitCtx {
+// A bounded wait's context.  BY_ADDR: the slow paths below take the context's
+// address (the context then sits in the thread's stack frame) instead of its
+// fields, so a call site passes three words instead of seven.  Which form a
+// kernel runs faster with is a matter of measurement: by address helped the
+// run-time-compiled score_mod forward and slowed the backward passes.
+template <bool BY_ADDR>
+struct WaitCtxT {
   volatile int* abort;   // shared memory, CTA-wide
   int* status;           // global status word (workspace offset 0)
   uint64_t timeout_ns;
   int site;              // which wait, recorded in the status word's upper bits
 };
+using WaitCtx = WaitCtxT<false>;
 
 DEVI void raise_abort(const WaitCtx& c) {
   *c.abort = 1;
@@ -136,17 +143,28 @@ DEVI void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
   }
 }
 
+static __device__ __noinline__ bool wait_one_slow_at(uint32_t bar, uint32_t parity, const WaitCtxT<true>* c) {
+  return wait_one_slow(bar, parity, c->abort, c->status, c->timeout_ns, c->site);
+}
+static __device__ __noinline__ bool wait_warp_slow_at(uint32_t bar, uint32_t parity, const WaitCtxT<true>* c) {
+  return wait_warp_slow(bar, parity, c->abort, c->status, c->timeout_ns, c->site);
+}
+
 // One thread waits for phase `parity` of `bar` to complete.  False = gave up.
-DEVI bool wait_one(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+template <bool BY_ADDR>
+DEVI bool wait_one(uint32_t bar, uint32_t parity, const WaitCtxT<BY_ADDR>& c) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_one_slow(bar, parity, c.abort, c.status, c.timeout_ns, c.site);
+  if constexpr (BY_ADDR) return wait_one_slow_at(bar, parity, &c);
+  else return wait_one_slow(bar, parity, c.abort, c.status, c.timeout_ns, c.site);
 }
 
 // A whole warp waits; the outcome is warp-uniform (so .sync.aligned tcgen05
 // instructions that follow are executed by all 32 lanes together).
-DEVI bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& c) {
+template <bool BY_ADDR>
+DEVI bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtxT<BY_ADDR>& c) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return wait_warp_slow(bar, parity, c.abort, c.status, c.timeout_ns, c.site);
+  if constexpr (BY_ADDR) return wait_warp_slow_at(bar, parity, &c);
+  else return wait_warp_slow(bar, parity, c.abort, c.status, c.timeout_ns, c.site);
 }
 
 // ---------------------------------------------------------------------------
