@@ -532,8 +532,12 @@ attn_status bwd_dkdv_impl(const attn_shape* s, const void* q, const void* k, con
   p.dk = dk;
   p.dv = dv;
   p.dm = dm_view(s, dm);
-  if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, true, st));
   if (s->D == 512) return cuda_status(launch_bwd512_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
+  // persistent CTAs, one per SM, taking the items from the counter in the
+  // workspace header (kWsDkdvCounter)
+  p.items = at<unsigned>(ws, kWsDkdvCounter);
+  p.ctas = (int)std::min<long long>((long long)p.nkb * p.B * p.H, sm_count());
+  if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, true, st));
   return cuda_status(launch_bwd_dkdv(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 

@@ -138,6 +138,11 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int fold;               // ALiBi / checkerboard bias folded into the score products
   float inv_scale;        // 1 / scale
+  // dK/dV pass, head dim 64: persistent CTAs (ctas of them) take work items from
+  // the counter pair at items (items taken, CTAs finished; zero between calls);
+  // null: one CTA per item
+  unsigned* items;
+  int ctas;
 };
 #ifndef __CUDACC_RTC__
 cudaError_t launch_bwd_dkdv(const BwdParams& p, bool bf16, int mod, cudaStream_t st);
