@@ -573,8 +573,12 @@ attn_status bwd_dq_impl(const attn_shape* s, const void* q, const void* k, const
   if (!ok) return ATTN_ERR_CUDA;
   p.dq = dq;
   p.dm = dm_view(s, dm);
-  if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, false, st));
   if (s->D == 512) return cuda_status(launch_bwd512_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
+  // persistent CTAs, one per SM, taking the items from the counter in the
+  // workspace header (kWsDqCounter)
+  p.items = at<unsigned>(ws, kWsDqCounter);
+  p.ctas = (int)std::min<long long>((long long)p.nqb * p.B * p.H, sm_count());
+  if (ukern) return cuda_status(launch_bwd_kernel(p, ukern, false, st));
   return cuda_status(launch_bwd_dq(p, s->dtype == ATTN_BF16, (int)mod, st));
 }
 

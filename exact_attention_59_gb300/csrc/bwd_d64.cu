@@ -18,8 +18,9 @@
 //     computes S^T = K_j Q_i^T and dP^T = V_j dO_i^T directly (kv rows on TMEM
 //     lanes), so P^T and dS^T are left in TMEM and feed dV += P^T dO_i and
 //     dK += dS^T Q_i as the A operand.
-//   dQ pass: one CTA per (b, h, q block i); S = Q_i K_j^T, dP = dO_i V_j^T,
-//     dS into TMEM, dQ += dS K_j.
+//   dQ pass: work items (b, h, q block i), taken by persistent CTAs in the same
+//     way; S = Q_i K_j^T, dP = dO_i V_j^T, dS into TMEM, dQ += dS K_j (the dQ
+//     accumulator alternates between two TMEM regions from item to item).
 // Both: warp 0 TMA, warp 1 TMEM owner + MMA issue (lane 0), warps 2-5 and
 // 6-9 split the 128 columns of each 128x128 score tile in two halves of 64.
 // S is double-buffered in TMEM so the next S product overlaps this tile's
@@ -629,17 +630,25 @@ struct __align__(1024) DqSmem {
   uint8_t q[BWD_TILE], dO[BWD_TILE];
   uint8_t k[BWD_NST][BWD_TILE], v[BWD_NST][BWD_TILE];
   // Column terms folded into S = Q K^T as one more K = 16 step, as in the
-  // forward (columns AUG_MOD / AUG_KEY): qaug per query row (resident), kaug[s]
-  // per key of stage s (K = 16 operands without swizzle, 4 KB each).
-  __align__(128) uint8_t qaug[4096];
+  // forward (columns AUG_MOD / AUG_KEY; K = 16 operands without swizzle):
+  // kaug[s] per key of stage s (4 KB each); the query side is the same in every
+  // row up to a period of 2, so it is 8 rows (256 bytes, one per item slot) that
+  // the descriptor repeats over the 128 query rows.
   __align__(128) uint8_t kaug[BWD_NST][4096];
-  uint64_t qfull, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, dsready, dqdone, fin, done;
+  __align__(128) uint8_t qaug[2][256];
+  alignas(16) float rowc[2][2][128];   // per item slot: -lse log2(e) and -D of its 128 query rows
+  uint64_t qfull, qfree, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, dsready, dqdone, fin, finb;
+  uint64_t done[2];                       // per item slot: the item's dQ is complete
+  uint64_t item_ready[2], item_free[2];   // per item slot: written by the producer / done with by the rest
   uint32_t tmem_base;
   int abort;
-  int nlist;
-  uint16_t list[BWD_MAXB];
-  uint8_t lflags[BWD_MAXB];
+  // Two item slots, filled by the producer in turn: the item (-1 = no more), the
+  // number of kv blocks its q block sees and their list, in order, with flags.
+  int item[2], nlist[2];
+  uint16_t list[2][BWD_MAXB];
+  uint8_t lflags[2][BWD_MAXB];
 };
+static_assert(sizeof(DqSmem) + 1024 <= 227 * 1024, "dQ shared memory (+ 1 KB alignment slack)");
 
 template <bool BF16, int MOD, bool DM>
 __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -647,13 +656,26 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = p.B * p.H;
-  const int L = blockIdx.x;
-  const int qb = p.nqb - 1 - L / BH;   // longest causal rows first
-  const int bh = L % BH;
-  const int b = bh / p.H, h = bh % p.H;
+  // Work items are (q block, b, h), numbered longest causal rows first.  CTAs
+  // take them from the counter p.items in turn (one CTA per SM), or, with no
+  // counter, one item each.
+  const int n_items = p.nqb * BH;
+  const bool persistent = p.items != nullptr;
+  struct Item {
+    int qb, bh, b, h;
+  };
+  auto item_of = [&](int L) {
+    Item it;
+    it.qb = p.nqb - 1 - L / BH;
+    it.bh = L % BH;
+    it.b = it.bh / p.H;
+    it.h = it.bh % p.H;
+    return it;
+  };
 
   if (tid == 0) {
     mbar_init(smem_u32(&sm.qfull), 1);
+    mbar_init(smem_u32(&sm.qfree), 1);   // thread A's commit after an item's score products
     for (int s = 0; s < BWD_NST; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 1);
@@ -665,45 +687,15 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     mbar_init(smem_u32(&sm.dsready), 256);
     mbar_init(smem_u32(&sm.dqdone), 1);
     mbar_init(smem_u32(&sm.fin), 1);
-    mbar_init(smem_u32(&sm.done), 1);
+    mbar_init(smem_u32(&sm.finb), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.done[t]), 1);
+      mbar_init(smem_u32(&sm.item_ready[t]), 1);
+      mbar_init(smem_u32(&sm.item_free[t]), 2 + 256);   // both MMA threads and every elementwise thread
+    }
     sm.abort = 0;
     fence_mbar_init();
     fence_async_smem();
-    // Q and dO of this q block do not depend on the work list: their copy goes
-    // out now and lands under the rest of the set-up
-    tma_prefetch_desc(&p.tm_q);
-    tma_prefetch_desc(&p.tm_do);
-    mbar_expect_tx(smem_u32(&sm.qfull), 2 * BWD_TILE);
-    tma_load_2d(smem_u32(sm.q), &p.tm_q, smem_u32(&sm.qfull), 0, bh * p.Sq + qb * 128);
-    tma_load_2d(smem_u32(sm.dO), &p.tm_do, smem_u32(&sm.qfull), 0, bh * p.Sq + qb * 128);
-  }
-  if (warp == 2) {
-    // list of kv blocks this q block sees, in ascending order, 32 candidates per
-    // ballot (as in the dK/dV pass)
-    int n = 0;
-    for (int k0 = 0; k0 < p.nkb; k0 += 32) {
-      const int kb = k0 + lane;
-      bool keep = false;
-      uint8_t fl = 0;
-      if (kb < p.nkb) {
-        const int ks = p.km_sum ? p.km_sum[b * p.nkb + kb] : 2;
-        const int st = p.bm_tiles ? p.bm_tiles[b * p.bm_sb + h * p.bm_sh + (long long)qb * p.nkb + kb] : TILE_FULL;
-        int ds = TILE_FULL;   // the dense tile state: dense build only
-        if constexpr (DM)
-          ds = p.dm.tiles[(((long long)b * p.dm.mb + (long long)h * p.dm.mh) * p.nqb + qb) * p.nkb + kb];
-        keep = ks != 0 && st != TILE_EMPTY && ds != TILE_EMPTY;
-        fl = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
-             (ds == TILE_PARTIAL ? KB_DENSE : 0);
-      }
-      const unsigned m = __ballot_sync(0xffffffffu, keep);
-      if (keep) {
-        const int pos = n + __popc(m & ((1u << lane) - 1u));
-        sm.list[pos] = (uint16_t)kb;
-        sm.lflags[pos] = fl;
-      }
-      n += __popc(m);
-    }
-    if (lane == 0) sm.nlist = n;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -711,37 +703,34 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   }
   // The key-padding mask and (with `fold`) the ALiBi / checkerboard bias ride on
   // the S product, with the operands of the forward (fwd_d64.cu): checkerboard
-  // (-1)^q t_i x (-1)^c, ALiBi 1 x t_i(c), t = bias / scale in three 16-bit
-  // terms; ALiBi's slope_h (kv0 - q) is a per-row constant of each block.
+  // (-1)^q t_i x (-1)^c (t = 0.5 / scale), ALiBi t_i x c / 128 (t = 128 slope_h /
+  // scale, written into the item slot's query side by the producer), in three
+  // 16-bit terms; ALiBi's slope_h (kv0 - q) is a per-row constant of each block.
   constexpr bool kModTerm = (MOD == MOD_ALIBI || MOD == MOD_CHECKER);
   const bool fold = kModTerm && p.fold;
   const bool aug = fold || p.km_bits != nullptr;
   if (aug) {
-    uint4* z = reinterpret_cast<uint4*>(sm.qaug);
-    for (int i = tid; i < (int)((1 + BWD_NST) * 4096 / 16); i += BWD_T) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    uint4* z = reinterpret_cast<uint4*>(sm.kaug);
+    for (int i = tid; i < (int)((BWD_NST * 4096 + 2 * 256) / 16); i += BWD_T) z[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    if (tid < 128) {
-      const int r = tid;   // query row of the block, and key column of a kv block
-      const uint16_t one = to16<BF16>(1.f);
-      *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_KEY)) = one;
-      if (fold) {
-        uint16_t qt3[3], kt3[3];
-        if constexpr (MOD == MOD_CHECKER) {
-          uint16_t t[3];
-          split3_plain<BF16>(0.5f * p.inv_scale, t);
-          for (int i = 0; i < 3; ++i) {
-            qt3[i] = (r & 1) ? uint16_t(t[i] ^ 0x8000u) : t[i];   // q block starts at a multiple of 128
-            kt3[i] = (r & 1) ? to16<BF16>(-1.f) : one;
-          }
-        } else {
-          split3_plain<BF16>(exp2f(-8.0f * float(h + 1) / float(p.H)) * float(r) * p.inv_scale, kt3);
-          for (int i = 0; i < 3; ++i) qt3[i] = one;
-        }
-        for (int i = 0; i < 3; ++i) {
-          *reinterpret_cast<uint16_t*>(sm.qaug + k16_offset(r, AUG_MOD + i)) = qt3[i];
-          for (int st = 0; st < BWD_NST; ++st)
-            *reinterpret_cast<uint16_t*>(sm.kaug[st] + k16_offset(r, AUG_MOD + i)) = kt3[i];
-        }
+    const uint16_t one = to16<BF16>(1.f);
+    if (tid < 128 && fold) {
+      const int r = tid;   // key column of a kv block
+      uint16_t kt3[3];
+      for (int i = 0; i < 3; ++i)
+        kt3[i] = MOD == MOD_CHECKER ? ((r & 1) ? to16<BF16>(-1.f) : one) : to16<BF16>(float(r) * (1.f / 128.f));
+      for (int st = 0; st < BWD_NST; ++st)
+        for (int i = 0; i < 3; ++i) *reinterpret_cast<uint16_t*>(sm.kaug[st] + k16_offset(r, AUG_MOD + i)) = kt3[i];
+    }
+    if (tid >= 128 && tid < 128 + 16) {   // both slots' query sides: 8 rows each
+      const int sl = (tid - 128) >> 3, r = tid & 7;
+      uint8_t* o = sm.qaug[sl];
+      *reinterpret_cast<uint16_t*>(o + k16_offset(r, AUG_KEY)) = one;
+      if (MOD == MOD_CHECKER && fold) {
+        uint16_t t[3];
+        split3_plain<BF16>(0.5f * p.inv_scale, t);
+        for (int i = 0; i < 3; ++i)   // a q block starts at a multiple of 128: the row's parity is r's
+          *reinterpret_cast<uint16_t*>(o + k16_offset(r, AUG_MOD + i)) = (r & 1) ? uint16_t(t[i] ^ 0x8000u) : t[i];
       }
     }
     fence_async_smem();   // generic-proxy writes, read by the tensor core
@@ -750,27 +739,122 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const int N = sm.nlist;
-  // TMEM columns: S 128, dP 128, dS (16-bit pairs) 64, dQ 64
+  // TMEM columns: S 128, dP 128, dS (16-bit pairs) 64, dQ 64 per item slot
   constexpr uint32_t C_S = 0, C_DP = 128, C_DS = 256, C_DQ = 320;
 
   if (warp == 0) {
-    if (N > 0) {
-      WaitCtx c{&sm.abort, p.status, p.timeout_ns, 21};
-      if (lane == 0) {   // Q and dO went out in the set-up
-        tma_prefetch_desc(&p.tm_k);
-        tma_prefetch_desc(&p.tm_v);
+    // ---- producer: takes the items and fills their slots (list of kv blocks, the
+    // rows' -lse log2(e) and -D, the head's query-side term), loads an item's Q
+    // and dO once the previous item's score products are done with them, then
+    // streams its K / V blocks through the ring (continuing across items).
+    WaitCtx c{&sm.abort, p.status, p.timeout_ns, 21};
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+    }
+    int last_u[BWD_NST];
+    for (int s = 0; s < BWD_NST; ++s) last_u[s] = -1;
+    int u = 0, last_q = -1;
+    bool ok = true;
+    for (int ci = 0; ok; ++ci) {
+      const int sl = ci & 1;
+      int L = 0;
+      if (lane == 0) L = persistent ? (int)atomicAdd(p.items, 1u) : (ci == 0 ? (int)blockIdx.x : n_items);
+      L = __shfl_sync(0xffffffffu, L, 0);
+      // the slot's previous item (ci - 2) is done with everywhere
+      if (ci >= 2 && !wait_warp(smem_u32(&sm.item_free[sl]), ((ci - 2) >> 1) & 1, c)) break;
+      if (L >= n_items) {   // no more items: the others stop at this slot
+        if (lane == 0) {
+          sm.item[sl] = -1;
+          mbar_arrive(smem_u32(&sm.item_ready[sl]));
+        }
+        break;
       }
-      int last_u[BWD_NST];
-      for (int s = 0; s < BWD_NST; ++s) last_u[s] = -1;
-      for (int u = 0; u < N; ++u) {
+      const Item it = item_of(L);
+      // the kv blocks this q block sees, in ascending order, 32 candidates per ballot
+      int n = 0;
+      for (int k0 = 0; k0 < p.nkb; k0 += 32) {
+        const int kb = k0 + lane;
+        bool keep = false;
+        uint8_t fl = 0;
+        if (kb < p.nkb) {
+          const int ks = p.km_sum ? p.km_sum[it.b * p.nkb + kb] : 2;
+          const int st =
+              p.bm_tiles ? p.bm_tiles[it.b * p.bm_sb + it.h * p.bm_sh + (long long)it.qb * p.nkb + kb] : TILE_FULL;
+          int ds = TILE_FULL;   // the dense tile state: dense build only
+          if constexpr (DM)
+            ds = p.dm.tiles[(((long long)it.b * p.dm.mb + (long long)it.h * p.dm.mh) * p.nqb + it.qb) * p.nkb + kb];
+          keep = ks != 0 && st != TILE_EMPTY && ds != TILE_EMPTY;
+          fl = (st == TILE_PARTIAL && p.bm_mod != MASKMOD_NONE ? KB_MASKMOD : 0) | (ks == 1 ? KB_KEYMASK : 0) |
+               (ds == TILE_PARTIAL ? KB_DENSE : 0);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int pos = n + __popc(m & ((1u << lane) - 1u));
+          sm.list[sl][pos] = (uint16_t)kb;
+          sm.lflags[sl][pos] = fl;
+        }
+        n += __popc(m);
+      }
+      {   // the rows' -lse log2(e) and -D (lane: rows 4 lane .. 4 lane + 3); rows past
+          // Sq (partial last q block) get P = 0 and are not written
+        const long long row = (long long)it.bh * p.Sq + it.qb * 128;
+        float4 nl, nd;
+        if ((p.Sq & 3) == 0 && it.qb * 128 + 128 <= p.Sq) {   // whole block, 16-byte aligned rows
+          nl = __ldg(reinterpret_cast<const float4*>(p.lse2 + row) + lane);
+          nd = __ldg(reinterpret_cast<const float4*>(p.delta + row) + lane);
+        } else {
+          float a[4], d[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const bool in = it.qb * 128 + 4 * lane + i < p.Sq;
+            a[i] = in ? __ldg(p.lse2 + row + 4 * lane + i) : -INFINITY;
+            d[i] = in ? __ldg(p.delta + row + 4 * lane + i) : 0.f;
+          }
+          nl = make_float4(a[0], a[1], a[2], a[3]);
+          nd = make_float4(d[0], d[1], d[2], d[3]);
+        }
+        reinterpret_cast<float4*>(sm.rowc[sl][0])[lane] = nl;
+        reinterpret_cast<float4*>(sm.rowc[sl][1])[lane] = nd;
+      }
+      if (lane == 0) {
+        sm.item[sl] = L;
+        sm.nlist[sl] = n;
+        if (MOD == MOD_ALIBI && fold) {
+          // the head's factor of the folded slope_h c term in the slot's query side
+          // (one thread at fixed offsets: stores from every lane of the producer
+          // cost the kernel registers)
+          uint16_t t3[3];
+          split3_plain<BF16>(128.f * exp2f(-8.0f * float(it.h + 1) / float(p.H)) * p.inv_scale, t3);
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            for (int e = 0; e < 3; ++e)
+              *reinterpret_cast<uint16_t*>(sm.qaug[sl] + k16_offset(r, AUG_MOD + e)) = t3[e];
+          fence_async_smem();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.item_ready[sl]));   // release: the slot is visible to its waiters
+      // Q and dO of the item, once the previous item's score products are done with them
+      if (ci >= 1 && !wait_warp(smem_u32(&sm.qfree), (ci - 1) & 1, c)) break;
+      if (lane == 0) {
+        mbar_expect_tx(smem_u32(&sm.qfull), 2 * BWD_TILE);
+        tma_load_2d(smem_u32(sm.q), &p.tm_q, smem_u32(&sm.qfull), 0, it.bh * p.Sq + it.qb * 128);
+        tma_load_2d(smem_u32(sm.dO), &p.tm_do, smem_u32(&sm.qfull), 0, it.bh * p.Sq + it.qb * 128);
+      }
+      last_q = ci;
+      for (int j = 0; j < n; ++j) {
         const int s = u % BWD_NST;
-        if (u >= BWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) break;
-        const int kb = sm.list[u];
+        if (u >= BWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / BWD_NST) - 1) & 1, c)) {
+          ok = false;
+          break;
+        }
+        const int kb = sm.list[sl][j];
         if (aug && p.km_bits) {   // lane owns keys 4 lane .. 4 lane + 3: column AUG_KEY of kaug[s]
           uint32_t bits = 0xffffffffu;
-          if (sm.lflags[u] & KB_KEYMASK)
-            bits = km_word(p.km_bits, b, p.Skv, kb * 128 + 4 * lane);
+          if (sm.lflags[sl][j] & KB_KEYMASK) bits = km_word(p.km_bits, it.b, p.Skv, kb * 128 + 4 * lane);
           // the infinity whose product with the scale is -inf (scale != 0)
           const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
 #pragma unroll
@@ -785,54 +869,62 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         if (lane == 0) {
           const uint32_t fb = smem_u32(&sm.full[s]);
           mbar_expect_tx(fb, 2 * BWD_TILE);   // release: the bias column above is visible to its waiters
-          tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, bh * p.Skv + kb * 128);
-          tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, bh * p.Skv + kb * 128);
+          tma_load_2d(smem_u32(sm.k[s]), &p.tm_k, fb, 0, it.bh * p.Skv + kb * 128);
+          tma_load_2d(smem_u32(sm.v[s]), &p.tm_v, fb, 0, it.bh * p.Skv + kb * 128);
         }
         last_u[s] = u;
-      }
-      if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-        for (int s = 0; s < BWD_NST; ++s)
-          if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
+        ++u;
       }
     }
-    if (lane == 0) drain_wait(smem_u32(&sm.qfull), 0, p.timeout_ns);   // issued in the set-up, even for N = 0
+    if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
+      if (last_q >= 0) drain_wait(smem_u32(&sm.qfull), last_q & 1, p.timeout_ns);
+      for (int s = 0; s < BWD_NST; ++s)
+        if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / BWD_NST) & 1, p.timeout_ns);
+    }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issue, thread A: S = Q K^T (+ key-padding bias) and dP = dO V^T, each
-    // issued as soon as the softmax warps hold the previous one in registers.
-    if (lane == 0 && N > 0) {
+    // ---- MMA issue, thread A: S = Q K^T (+ column terms) and dP = dO V^T, each
+    // issued as soon as the elementwise warps hold the previous one in registers
+    // (u counts blocks over all items of the CTA: the barriers' phases).
+    if (lane == 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 22};
       constexpr uint32_t ID_SS = idesc_f16(128, 128, BF16, false, false);
       const uint64_t qd = sdesc_sw128(smem_u32(sm.q), 16, 1024), od = sdesc_sw128(smem_u32(sm.dO), 16, 1024);
-      const uint64_t qad = sdesc_k16(smem_u32(sm.qaug));
-      auto issue_s = [&](int u) {   // S_u = Q K_u^T (+ key-padding bias)
-        const int s = u % BWD_NST;
-        const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
+      uint32_t u = 0;
+      bool ok = true;
+      for (int ci = 0; ok; ++ci) {
+        const int sl = ci & 1;
+        if (!wait_one(smem_u32(&sm.item_ready[sl]), (ci >> 1) & 1, c)) break;
+        if (sm.item[sl] < 0) break;
+        const int n = sm.nlist[sl];
+        const uint64_t qad = sdesc_k16_rows8(smem_u32(sm.qaug[sl]));
+        if (!wait_one(smem_u32(&sm.qfull), ci & 1, c)) break;
+        for (int j = 0; j < n; ++j, ++u) {
+          const int s = u % BWD_NST;
+          if (!wait_one(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
+          if (u > 0 && !wait_one(smem_u32(&sm.sfree), (u - 1) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          {   // S_u = Q K_u^T (+ column terms)
+            const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_S, qd + 2 * kk, kd + 2 * kk, ID_SS, kk > 0);
-        if (aug) mma_ss(tmem + C_S, qad, sdesc_k16(smem_u32(sm.kaug[s])), ID_SS, 1u);
-        tc_commit(smem_u32(&sm.sfull));
-      };
-      auto issue_dp = [&](int u) {  // dP_u = dO V_u^T
-        const uint64_t vd = sdesc_sw128(smem_u32(sm.v[u % BWD_NST]), 16, 1024);
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_S, qd + 2 * kk, kd + 2 * kk, ID_SS, kk > 0);
+            if (aug) mma_ss(tmem + C_S, qad, sdesc_k16(smem_u32(sm.kaug[s])), ID_SS, 1u);
+            tc_commit(smem_u32(&sm.sfull));
+          }
+          if (u > 0 && !wait_one(smem_u32(&sm.dpfree), (u - 1) & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          {   // dP_u = dO V_u^T
+            const uint64_t vd = sdesc_sw128(smem_u32(sm.v[s]), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_DP, od + 2 * kk, vd + 2 * kk, ID_SS, kk > 0);
-        tc_commit(smem_u32(&sm.dpfull));
-      };
-      bool ok = wait_one(smem_u32(&sm.qfull), 0, c) && wait_one(smem_u32(&sm.full[0]), 0, c);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
-      }
-      for (int u = 0; ok && u + 1 < N; ++u) {
-        if (!wait_one(smem_u32(&sm.full[(u + 1) % BWD_NST]), ((u + 1) / BWD_NST) & 1, c)) { ok = false; break; }
-        if (!wait_one(smem_u32(&sm.sfree), u & 1, c)) { ok = false; break; }
-        tc_fence_after();
-        issue_s(u + 1);
-        if (!wait_one(smem_u32(&sm.dpfree), u & 1, c)) { ok = false; break; }
-        tc_fence_after();
-        issue_dp(u + 1);
+            for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + C_DP, od + 2 * kk, vd + 2 * kk, ID_SS, kk > 0);
+            tc_commit(smem_u32(&sm.dpfull));
+          }
+        }
+        if (!ok) break;
+        // both arrive once this item's score products are complete: Q and dO may be
+        // reloaded, and the slot (its query side) refilled
+        tc_commit(smem_u32(&sm.qfree));
+        tc_commit(smem_u32(&sm.item_free[sl]));
       }
       // every MMA issued by this thread completes before the CTA lets go of TMEM
       tc_commit(smem_u32(&sm.fin));
@@ -840,162 +932,183 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     }
     __syncwarp();
   } else if (warp == 10) {
-    // ---- MMA issue, thread B: dQ += dS K, A operand from TMEM where the softmax
-    // warps left dS.
-    if (lane == 0 && N > 0) {
+    // ---- MMA issue, thread B: dQ += dS K, A operand from TMEM where the
+    // elementwise warps left dS; the dQ accumulator alternates between two TMEM
+    // regions by item slot, so an item's products need not wait for the previous
+    // item's epilogue (a slot is refilled only after its epilogue).
+    if (lane == 0) {
       WaitCtx c{&sm.abort, p.status, p.timeout_ns, 24};
       constexpr uint32_t ID_TS = idesc_f16(128, 64, BF16, false, true);
+      uint32_t u = 0;
       bool ok = true;
-      for (int u = 0; ok && u < N; ++u) {
-        const int s = u % BWD_NST;
-        if (!wait_one(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
-        if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 8192, 1024);
+      for (int ci = 0; ok; ++ci) {
+        const int sl = ci & 1;
+        if (!wait_one(smem_u32(&sm.item_ready[sl]), (ci >> 1) & 1, c)) break;
+        if (sm.item[sl] < 0) break;
+        const int n = sm.nlist[sl];
+        const uint32_t tdq = tmem + C_DQ + 64 * sl;
+        for (int j = 0; j < n; ++j, ++u) {
+          const int s = u % BWD_NST;
+          if (!wait_one(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
+          if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 8192, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(tmem + C_DQ, tmem + C_DS + 8 * kk, kd + 128 * kk, ID_TS, (u > 0 || kk > 0));
-        tc_commit(smem_u32(&sm.dqdone));
-        tc_commit(smem_u32(&sm.empty[s]));
+          for (int kk = 0; kk < 8; ++kk) mma_ts(tdq, tmem + C_DS + 8 * kk, kd + 128 * kk, ID_TS, (j > 0 || kk > 0));
+          tc_commit(smem_u32(&sm.dqdone));
+          tc_commit(smem_u32(&sm.empty[s]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm.done[sl]));   // this item's dQ is complete once it arrives
+        mbar_arrive(smem_u32(&sm.item_free[sl]));
       }
-      tc_commit(smem_u32(&sm.done));
-      drain_wait(smem_u32(&sm.done), 0, p.timeout_ns);
+      tc_commit(smem_u32(&sm.finb));
+      drain_wait(smem_u32(&sm.finb), 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
     const int w = (warp - 2) >> 2;   // kv columns [64 w, 64 w + 64)
     const int quad = warp & 3;
     const int r = 32 * quad + lane;
-    const int q = qb * 128 + r;
     const uint32_t lane_off = static_cast<uint32_t>(32 * quad) << 16;
     WaitCtx c{&sm.abort, p.status, p.timeout_ns, 23 + w};
-    const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
-    // rows past Sq (partial last q tile) get P = 0 and are not written
-    const float nl2 = q < p.Sq ? p.lse2[(size_t)bh * p.Sq + q] : -INFINITY;   // -lse log2(e)
-    const float nd = q < p.Sq ? p.delta[(size_t)bh * p.Sq + q] : 0.f;        // -D
-    const uint64_t scv = f2(p.sc, p.sc), nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
+    const uint64_t scv = f2(p.sc, p.sc);
+    uint32_t u = 0;   // blocks over all items (the barriers' phases)
     bool ok = true;
-    for (int u = 0; u < N; ++u) {
-      const int kb = sm.list[u];
-      const uint8_t f = sm.lflags[u];
-      const int k0 = kb * 128 + 64 * w;   // first key of this half
-      const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
-                          ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
-      const bool umask = MOD == MOD_USER && (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
-      // keep column cc of this half iff cc <= lim: the causal limit and, in a
-      // partial last kv block, the end of the keys
-      const int kvl = p.Skv - 1 - k0;
-      const bool limited = causal || kvl < 63;
-      const int lim = causal ? min(q - k0, kvl) : kvl;
-      // this row's dense-mask bits for the half's 64 keys
-      bool dense = false;
-      uint2 dwv = make_uint2(0u, 0u);
-      if constexpr (DM) {
-        dense = f & KB_DENSE;
-        const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
-        if (dense && q < p.Sq)
-          dwv = __ldg(reinterpret_cast<const uint2*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) + 4 * kb +
-                                                     2 * w));
-      }
-      // the block's bias constants, ahead of the wait (they do not depend on S)
-      uint64_t chk = 0;
-      if constexpr (MOD == MOD_CHECKER) {
-        const float hb = ((q + k0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
-        chk = f2(hb, -hb);
-      }
-      const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
-      // with the bias folded into S, all that is left per pair is this row's constant
-      const float fb = (MOD == MOD_ALIBI) ? slope2 * float(kb * 128 - q) : 0.f;
-      const uint64_t addf = fadd2(nl2v, f2(fb, fb));
-      if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t rr[64];
-      tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
-      // S(u) is in registers: the next S may be computed over it
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.sfree));
-      float pr[64];
-      // one straight-line copy per causal/not: no runtime test inside the unrolled loop
-      auto probs = [&](auto causal_c, auto dense_c, auto fold_c) {
-        constexpr bool CAUSAL = decltype(causal_c)::value;
-        constexpr bool DENSE = decltype(dense_c)::value;
-        constexpr bool FOLD = decltype(fold_c)::value;
+    for (int ci = 0; ok; ++ci) {
+      const int sl = ci & 1;
+      if (!wait_warp(smem_u32(&sm.item_ready[sl]), (ci >> 1) & 1, c)) break;
+      const int L = sm.item[sl];
+      if (L < 0) break;
+      const Item it = item_of(L);
+      const int qb = it.qb, bh = it.bh, b = it.b, h = it.h;
+      const int N = sm.nlist[sl];
+      const int q = qb * 128 + r;
+      const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(h, p.H) : 0.f;
+      const float nl2 = sm.rowc[sl][0][r];   // -lse log2(e); -inf past Sq
+      const float nd = sm.rowc[sl][1][r];    // -D
+      const uint64_t nl2v = f2(nl2, nl2), ndv = f2(nd, nd);
+      for (int j = 0; j < N; ++j, ++u) {
+        const int kb = sm.list[sl][j];
+        const uint8_t f = sm.lflags[sl][j];
+        const int k0 = kb * 128 + 64 * w;   // first key of this half
+        const bool causal = (MOD == MOD_CAUSAL && kb * 128 + 127 > qb * 128) ||
+                            ((f & KB_MASKMOD) && p.bm_mod == MASKMOD_CAUSAL);
+        const bool umask = MOD == MOD_USER && (f & KB_MASKMOD) && p.bm_mod == MASKMOD_USER;
+        // keep column cc of this half iff cc <= lim: the causal limit and, in a
+        // partial last kv block, the end of the keys
+        const int kvl = p.Skv - 1 - k0;
+        const bool limited = causal || kvl < 63;
+        const int lim = causal ? min(q - k0, kvl) : kvl;
+        // this row's dense-mask bits for the half's 64 keys
+        bool dense = false;
+        uint2 dwv = make_uint2(0u, 0u);
+        if constexpr (DM) {
+          dense = f & KB_DENSE;
+          const long long dmi = (long long)b * p.dm.mb + (long long)h * p.dm.mh;
+          if (dense && q < p.Sq)
+            dwv = __ldg(reinterpret_cast<const uint2*>(p.dm.rowbits + (dmi * p.Sq + q) * (4LL * p.nkb) + 4 * kb +
+                                                       2 * w));
+        }
+        // the block's bias constants, ahead of the wait (they do not depend on S)
+        uint64_t chk = 0;
+        if constexpr (MOD == MOD_CHECKER) {
+          const float hb = ((q + k0) & 1) ? -0.5f * kLog2e : 0.5f * kLog2e;   // even column
+          chk = f2(hb, -hb);
+        }
+        const float abase = (MOD == MOD_ALIBI) ? slope2 * float(k0 - q) : 0.f;
+        // with the bias folded into S, all that is left per pair is this row's constant
+        const float fb = (MOD == MOD_ALIBI) ? slope2 * float(kb * 128 - q) : 0.f;
+        const uint64_t addf = fadd2(nl2v, f2(fb, fb));
+        if (!wait_warp(smem_u32(&sm.sfull), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t rr[64];
+        tmem_ld64(tmem + lane_off + C_S + 64 * w, rr);
+        // S(u) is in registers: the next S may be computed over it
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.sfree));
+        float pr[64];
+        // one straight-line copy per causal/not: no runtime test inside the unrolled loop
+        auto probs = [&](auto causal_c, auto dense_c, auto fold_c) {
+          constexpr bool CAUSAL = decltype(causal_c)::value;
+          constexpr bool DENSE = decltype(dense_c)::value;
+          constexpr bool FOLD = decltype(fold_c)::value;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            uint64_t add = FOLD ? addf : nl2v;
+            if constexpr (MOD == MOD_CHECKER && !FOLD) add = fadd2(add, chk);
+            if constexpr (MOD == MOD_ALIBI && !FOLD)
+              add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
+            float x0, x1;
+            unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
+            if constexpr (MOD == MOD_USER) {
+              x0 = fmaf(user_bias(b, h, q, k0 + 2 * i), kLog2e, x0);
+              x1 = fmaf(user_bias(b, h, q, k0 + 2 * i + 1), kLog2e, x1);
+              if (umask) {   // a PARTIAL tile of a user mask_mod's block mask
+                x0 = user_keep(b, h, q, k0 + 2 * i) ? x0 : -INFINITY;
+                x1 = user_keep(b, h, q, k0 + 2 * i + 1) ? x1 : -INFINITY;
+              }
+            }
+            if (CAUSAL) {
+              x0 = 2 * i > lim ? -INFINITY : x0;
+              x1 = 2 * i + 1 > lim ? -INFINITY : x1;
+            }
+            if constexpr (DENSE) {
+              const uint32_t dwi = i < 16 ? dwv.x : dwv.y;
+              x0 = (dwi & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
+              x1 = (dwi & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
+            }
+            pr[2 * i] = ex2(x0);
+            pr[2 * i + 1] = ex2(x1);
+          }
+        };
+        auto probs_any = [&](auto fold_c) {
+          if (dense) {   // with dense bits, the limited copy too (never with DM = false)
+            if constexpr (DM) probs(bconst<true>{}, bconst<true>{}, fold_c);
+          } else if (limited) {
+            probs(bconst<true>{}, bconst<false>{}, fold_c);
+          } else {
+            probs(bconst<false>{}, bconst<false>{}, fold_c);
+          }
+        };
+        if constexpr (kModTerm) {
+          if (fold) probs_any(bconst<true>{});
+          else probs_any(bconst<false>{});
+        } else {
+          probs_any(bconst<false>{});
+        }
+        if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.dpfree));
+        uint32_t dsk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          uint64_t add = FOLD ? addf : nl2v;
-          if constexpr (MOD == MOD_CHECKER && !FOLD) add = fadd2(add, chk);
-          if constexpr (MOD == MOD_ALIBI && !FOLD)
-            add = fadd2(add, f2(fmaf(slope2, float(2 * i), abase), fmaf(slope2, float(2 * i + 1), abase)));
-          float x0, x1;
-          unf2(ffma2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), scv, add), x0, x1);
-          if constexpr (MOD == MOD_USER) {
-            x0 = fmaf(user_bias(b, h, q, k0 + 2 * i), kLog2e, x0);
-            x1 = fmaf(user_bias(b, h, q, k0 + 2 * i + 1), kLog2e, x1);
-            if (umask) {   // a PARTIAL tile of a user mask_mod's block mask
-              x0 = user_keep(b, h, q, k0 + 2 * i) ? x0 : -INFINITY;
-              x1 = user_keep(b, h, q, k0 + 2 * i + 1) ? x1 : -INFINITY;
-            }
-          }
-          if (CAUSAL) {
-            x0 = 2 * i > lim ? -INFINITY : x0;
-            x1 = 2 * i + 1 > lim ? -INFINITY : x1;
-          }
-          if constexpr (DENSE) {
-            const uint32_t dwi = i < 16 ? dwv.x : dwv.y;
-            x0 = (dwi & (1u << ((2 * i) & 31))) ? x0 : -INFINITY;
-            x1 = (dwi & (1u << ((2 * i + 1) & 31))) ? x1 : -INFINITY;
-          }
-          pr[2 * i] = ex2(x0);
-          pr[2 * i + 1] = ex2(x1);
+          float d0, d1;
+          unf2(fmul2(f2(pr[2 * i], pr[2 * i + 1]),
+                     fadd2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), ndv)),
+               d0, d1);
+          dsk[i] = pack2<BF16>(d0, d1);
         }
-      };
-      auto probs_any = [&](auto fold_c) {
-        if (dense) {   // with dense bits, the limited copy too (never with DM = false)
-          if constexpr (DM) probs(bconst<true>{}, bconst<true>{}, fold_c);
-        } else if (limited) {
-          probs(bconst<true>{}, bconst<false>{}, fold_c);
-        } else {
-          probs(bconst<false>{}, bconst<false>{}, fold_c);
+        // dQ(u-1) has finished reading the dS region
+        if (u > 0) {
+          if (!wait_warp(smem_u32(&sm.dqdone), (u - 1) & 1, c)) { ok = false; break; }
+          tc_fence_after();
         }
-      };
-      if constexpr (kModTerm) {
-        if (fold) probs_any(bconst<true>{});
-        else probs_any(bconst<false>{});
-      } else {
-        probs_any(bconst<false>{});
+        tmem_st32(tmem + lane_off + C_DS + 32 * w, dsk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.dsready));
       }
-      if (!wait_warp(smem_u32(&sm.dpfull), u & 1, c)) { ok = false; break; }
-      tc_fence_after();
-      tmem_ld64(tmem + lane_off + C_DP + 64 * w, rr);
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.dpfree));
-      uint32_t dsk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float d0, d1;
-        unf2(fmul2(f2(pr[2 * i], pr[2 * i + 1]), fadd2(f2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1])), ndv)),
-             d0, d1);
-        dsk[i] = pack2<BF16>(d0, d1);
-      }
-      // dQ(u-1) has finished reading the dS region
-      if (u > 0) {
-        if (!wait_warp(smem_u32(&sm.dqdone), (u - 1) & 1, c)) { ok = false; break; }
-        tc_fence_after();
-      }
-      tmem_st32(tmem + lane_off + C_DS + 32 * w, dsk);
       tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.dsready));
-    }
-    tmem_st_wait();
-    if (w == 0) {
-      if (ok && N > 0) {
-        if (!wait_warp(smem_u32(&sm.done), 0, c)) ok = false;
-        else tc_fence_after();
-      }
-      if (ok) {
+      if (!ok) break;
+      if (w == 0) {   // epilogue: warps 2-5 write the dQ rows (scaled)
+        if (!wait_warp(smem_u32(&sm.done[sl]), (ci >> 1) & 1, c)) break;
+        tc_fence_after();
         uint32_t rr[64], o[32];
         if (N > 0) {
-          tmem_ld64(tmem + lane_off + C_DQ, rr);
+          tmem_ld64(tmem + lane_off + C_DQ + 64 * sl, rr);
         } else {
 #pragma unroll
           for (int i = 0; i < 64; ++i) rr[i] = 0u;
@@ -1009,12 +1122,24 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
           for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
       }
+      // this item's slot (and, once its epilogue has read it, its dQ region) is done with
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.item_free[sl]));
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+  // the last CTA to finish re-arms the item counter for the next call (this
+  // thread made the CTA's last claim, so every claim precedes the reset)
+  if (persistent && tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.items + 1, 1u) == gridDim.x - 1u) {
+      p.items[0] = 0u;
+      p.items[1] = 0u;
+    }
+  }
   // Launched with programmatic dependent launch behind the dK/dV pass, whose
   // results it does not read (the preprocess it needs was complete before that
   // pass let it launch): it waits for that grid only here, so that its own
@@ -1028,7 +1153,7 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
 // behind the preprocess, the dQ pass behind the dK/dV pass); see the kernels.
 static cudaError_t launch_bwd_pdl(const BwdParams& p, const void* kern, bool dkdv, size_t smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(dkdv && p.items ? p.ctas : p.B * p.H * (dkdv ? p.nkb : p.nqb)));
+  cfg.gridDim = dim3((unsigned)(p.items ? p.ctas : p.B * p.H * (dkdv ? p.nkb : p.nqb)));
   cfg.blockDim = dim3(BWD_T);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

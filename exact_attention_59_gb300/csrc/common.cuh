@@ -60,9 +60,10 @@ constexpr uint8_t KB_KEYMASK = 4;  // some keys of the kv block are padding: tes
 constexpr uint8_t KB_DENSE = 8;    // the dense mask keeps only some pairs of the tile: test its bits
 
 // Workspace layout (offsets in bytes; every region 256-byte aligned).
-//   [0, 256)            status word (int32 at offset 0); forward and dK/dV item
-//                       counter pairs (2 x uint32 at kWsItemCounter and at
-//                       kWsDkdvCounter); the rest reserved
+//   [0, 256)            status word (int32 at offset 0); item counter pairs of
+//                       the forward, dK/dV and dQ passes (2 x uint32 each at
+//                       kWsItemCounter, kWsDkdvCounter, kWsDqCounter); the rest
+//                       reserved
 //   key-mask bits       uint32 (B, Skv/32)         if a key mask may be given
 //   key-mask summary    uint8  (B, ceil(Skv/128))  0 = no key kept, 1 = some, 2 = all
 //   bwd: delta          float  (B, H, Sq)          -D_i = -rowsum(dO * O)
@@ -70,12 +71,13 @@ constexpr uint8_t KB_DENSE = 8;    // the dense mask keeps only some pairs of th
 //   decode: partials    float  (B*H, nsplit, D + 2)
 //   decode: counters    uint32 (B*H)
 // Byte offsets, in the workspace's 256-byte header, of the item counter pairs
-// of the forward and of the dK/dV pass (two uint32 each: items taken, CTAs
-// finished; one pair per kernel, as the dQ pass may run beside the dK/dV pass's
-// last CTAs).  Zero between calls: the last CTA of a call resets its pair, and
-// the zero fill before first use starts them.
+// of the forward, the dK/dV pass and the dQ pass (two uint32 each: items taken,
+// CTAs finished; one pair per kernel, as the dQ pass may run beside the dK/dV
+// pass's last CTAs).  Zero between calls: the last CTA of a call resets its
+// pair, and the zero fill before first use starts them.
 constexpr size_t kWsItemCounter = 16;
 constexpr size_t kWsDkdvCounter = 24;
+constexpr size_t kWsDqCounter = 32;
 
 struct WsLayout {
   size_t status = 0, km_bits = 0, km_sum = 0, delta = 0, lse2 = 0, partial = 0, counter = 0, total = 0;

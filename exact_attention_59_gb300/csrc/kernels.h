@@ -138,9 +138,9 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int fold;               // ALiBi / checkerboard bias folded into the score products
   float inv_scale;        // 1 / scale
-  // dK/dV pass, head dim 64: persistent CTAs (ctas of them) take work items from
-  // the counter pair at items (items taken, CTAs finished; zero between calls);
-  // null: one CTA per item
+  // dK/dV and dQ passes, head dim 64: persistent CTAs (ctas of them) take work
+  // items from the counter pair at items (items taken, CTAs finished; zero
+  // between calls; one pair per pass); null: one CTA per item
   unsigned* items;
   int ctas;
 };

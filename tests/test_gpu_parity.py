@@ -605,8 +605,9 @@ def test_workspace_serves_several_shapes():
 ])
 def test_items_outnumber_the_ctas(B, H, S, dtype, mod, km, bm):
     """More work items than SMs: each of the forward's CTAs (one per SM) runs
-    several (query-tile pair, b, h) items and each of the dK/dV pass's several
-    (kv block, b, h) items, of different heads and blocks, in turn (ALiBi's slope
+    several (query-tile pair, b, h) items, each of the dK/dV pass's several
+    (kv block, b, h) items and each of the dQ pass's several (q block, b, h)
+    items, of different heads and blocks, in turn (ALiBi's slope
     changes from item to item; an odd tile count leaves the last pair one tile;
     causal lists differ in length); outputs, gradients, visited tiles and bitwise
     reproducibility as usual."""
@@ -616,10 +617,10 @@ def test_items_outnumber_the_ctas(B, H, S, dtype, mod, km, bm):
 
 
 def test_item_counters_left_at_zero():
-    """The forward's and the dK/dV pass's CTAs take items from counter pairs in
-    the workspace header (bytes 16 .. 23 and 24 .. 31); the last CTA to finish sets
-    its pair back to zero, so that calls of any shape can follow on the same
-    workspace."""
+    """The CTAs of the forward, the dK/dV pass and the dQ pass take items from
+    counter pairs in the workspace header (bytes 16 .. 23, 24 .. 31 and 32 .. 39);
+    the last CTA to finish sets its pair back to zero, so that calls of any shape
+    can follow on the same workspace."""
     dev = torch.device("cuda")
     shapes = [(3, 12, 1100, "bf16"), (1, 3, 300, "f16"), (3, 12, 1100, "f16"), (2, 2, 128, "bf16")]
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16}
@@ -638,6 +639,7 @@ def test_item_counters_left_at_zero():
         torch.cuda.synchronize()
         assert not ws[16:24].any(), f"forward item counter left at {ws[16:24].view(torch.int32).tolist()}"
         assert not bws[24:32].any(), f"dK/dV item counter left at {bws[24:32].view(torch.int32).tolist()}"
+        assert not bws[32:40].any(), f"dQ item counter left at {bws[32:40].view(torch.int32).tolist()}"
         assert E.poll_status(ws) == E.ATTN_OK and E.poll_status(bws) == E.ATTN_OK
         q64, k64, v64, km = f64(c["q"]), f64(c["k"]), f64(c["v"]), c["key_mask"].numpy()
         o_ref, _ = OR.attn_fwd(q64, k64, v64, key_mask=km, score_mod="alibi")
