@@ -42,9 +42,11 @@ UNIT = "TFLOP/s"
 
 
 # DRAM bytes (read + write) of one bwd_dkdv_kernel launch at the bench workload, from
-# `ncu --set full` of `python bench.py --mode profile --batch 8 --steps 1`.  Set it
-# back to None when the kernel changes until it is captured again.
-DKDV_TRAFFIC_BYTES = 80.9e6
+# `ncu --set full -k regex:bwd_dkdv -s 1 -c 1` of
+# `python bench.py --mode profile --wl keypad --batch 8 --steps 2` (68.5 MB read,
+# 9.5 MB written).  Set it back to None when the kernel changes until it is
+# captured again.
+DKDV_TRAFFIC_BYTES = 78.0e6
 
 # Buffer sets of the end-to-end pipeline (device inputs and outputs, host
 # outputs): step i's kernels wait for the download of step i - E2E_SETS.
