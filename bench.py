@@ -393,6 +393,9 @@ def bench_extras(E, dev):
             fn(i)
         b.record()
         torch.cuda.synchronize()
+        # a wait that ran out inside the kernels would make this a time-out, not a timing
+        code = E.poll_status_all(dev)
+        assert code == E.ATTN_OK, f"device-side status {code} ({E.status_string(code)}) in a context timing"
         return a.elapsed_time(b) / n
 
     for w in (W.FLEX_CAUSAL_ALIBI_BF16, W.CHECKERBOARD_FP16):

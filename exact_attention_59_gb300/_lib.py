@@ -423,3 +423,16 @@ def causal_flash_attention(q, k, v):
 def poll_status(ws: torch.Tensor) -> int:
     """Synchronises the current stream and returns (and clears) the workspace status code."""
     return int(load().attn_poll_status(_ptr(ws), _stream(ws.device)))
+
+
+def poll_status_all(device) -> int:
+    """poll_status over every workspace this module has allocated on `device` (the
+    calls made without an explicit `ws`): the first nonzero code, else ATTN_OK;
+    every status word read is cleared."""
+    idx = torch.device(device).index
+    code = ATTN_OK
+    for (dev_idx, _stream_handle, _op), ws in list(_ws_cache.items()):
+        if dev_idx == idx:
+            c = poll_status(ws)
+            code = c if code == ATTN_OK else code
+    return code

@@ -637,7 +637,11 @@ struct __align__(1024) DqSmem {
   __align__(128) uint8_t kaug[BWD_NST][4096];
   __align__(128) uint8_t qaug[2][256];
   alignas(16) float rowc[2][2][128];   // per item slot: -lse log2(e) and -D of its 128 query rows
-  uint64_t qfull, qfree, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, dsready, dqdone, fin, finb;
+  uint64_t qfull, qfree, full[BWD_NST], empty[BWD_NST], sfull, sfree, dpfull, dpfree, fin, finb;
+  // per dS buffer: dS written (dsready) and the dQ product that read it done
+  // (dqdone); a pair per buffer keeps each barrier within one phase of its
+  // waiter (the elementwise warps may run a block ahead of thread B)
+  uint64_t dsready[2], dqdone[2];
   uint64_t done[2];                       // per item slot: the item's dQ is complete
   uint64_t item_ready[2], item_free[2];   // per item slot: written by the producer / done with by the rest
   uint32_t tmem_base;
@@ -684,8 +688,10 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
     mbar_init(smem_u32(&sm.sfree), 256);
     mbar_init(smem_u32(&sm.dpfull), 1);
     mbar_init(smem_u32(&sm.dpfree), 256);
-    mbar_init(smem_u32(&sm.dsready), 256);
-    mbar_init(smem_u32(&sm.dqdone), 1);
+    mbar_init(smem_u32(&sm.dsready[0]), 256);
+    mbar_init(smem_u32(&sm.dsready[1]), 256);
+    mbar_init(smem_u32(&sm.dqdone[0]), 1);
+    mbar_init(smem_u32(&sm.dqdone[1]), 1);
     mbar_init(smem_u32(&sm.fin), 1);
     mbar_init(smem_u32(&sm.finb), 1);
     for (int t = 0; t < 2; ++t) {
@@ -739,8 +745,11 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  // TMEM columns: S 128, dP 128, dS (16-bit pairs) 64, dQ 64 per item slot
-  constexpr uint32_t C_S = 0, C_DP = 128, C_DS = 256, C_DQ = 320;
+  // TMEM columns: S 128, dP 128, dS (16-bit pairs) 64 per buffer (blocks
+  // alternate between two, so dS(u) is written while dQ += dS(u-1) K still
+  // reads the other), dQ 64 per item slot
+  constexpr uint32_t C_S = 0, C_DP = 128, C_DQ = 320;
+  auto c_ds = [](uint32_t u) -> uint32_t { return (u & 1u) ? 448u : 256u; };
 
   if (warp == 0) {
     // ---- producer: takes the items and fills their slots (list of kv blocks, the
@@ -950,12 +959,13 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
         for (int j = 0; j < n; ++j, ++u) {
           const int s = u % BWD_NST;
           if (!wait_one(smem_u32(&sm.full[s]), (u / BWD_NST) & 1, c)) { ok = false; break; }
-          if (!wait_one(smem_u32(&sm.dsready), u & 1, c)) { ok = false; break; }
+          if (!wait_one(smem_u32(&sm.dsready[u & 1]), (u >> 1) & 1, c)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kd = sdesc_sw128(smem_u32(sm.k[s]), 8192, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ts(tdq, tmem + C_DS + 8 * kk, kd + 128 * kk, ID_TS, (j > 0 || kk > 0));
-          tc_commit(smem_u32(&sm.dqdone));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tdq, tmem + c_ds(u) + 8 * kk, kd + 128 * kk, ID_TS, (j > 0 || kk > 0));
+          tc_commit(smem_u32(&sm.dqdone[u & 1]));
           tc_commit(smem_u32(&sm.empty[s]));
         }
         if (!ok) break;
@@ -1091,15 +1101,16 @@ __global__ void __launch_bounds__(BWD_T, 1) bwd_dq_kernel(const __grid_constant_
                d0, d1);
           dsk[i] = pack2<BF16>(d0, d1);
         }
-        // dQ(u-1) has finished reading the dS region
-        if (u > 0) {
-          if (!wait_warp(smem_u32(&sm.dqdone), (u - 1) & 1, c)) { ok = false; break; }
+        // dQ(u-2) has finished reading this dS buffer (dqdone[b] completes once per
+        // use of buffer b = u & 1: the use before this one is phase (u - 2) / 2)
+        if (u > 1) {
+          if (!wait_warp(smem_u32(&sm.dqdone[u & 1]), ((u - 2) >> 1) & 1, c)) { ok = false; break; }
           tc_fence_after();
         }
-        tmem_st32(tmem + lane_off + C_DS + 32 * w, dsk);
+        tmem_st32(tmem + lane_off + c_ds(u) + 32 * w, dsk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.dsready));
+        mbar_arrive(smem_u32(&sm.dsready[u & 1]));
       }
       tmem_st_wait();
       if (!ok) break;
