@@ -38,11 +38,11 @@
  *    ("workspace") is caller-owned device memory of attn_workspace_size()
  *    bytes, 256-byte aligned, and must be zero-filled before its first use
  *    (its first word is the status word, below; the item counters of the
- *    forward and of the two backward passes, which every call leaves at zero,
- *    lie in its first 256 bytes too);
- *    any call and shape may use it after that (completion tickets are zeroed
- *    by the call that uses them, with an asynchronous memset on `stream`).  Calls on one workspace
- *    must not overlap in time (use one workspace per stream).
+ *    forward and of the two backward passes, which every call leaves at
+ *    zero, lie in its first 256 bytes too); any call and shape may use it
+ *    after that (completion tickets are zeroed by the call that uses them,
+ *    with an asynchronous memset on `stream`).  Calls on one workspace must
+ *    not overlap in time (use one workspace per stream).
  *  - Calls are asynchronous on `stream` and never synchronise, except
  *    attn_poll_status().  Arguments are validated before anything is
  *    launched: a call that returns an error has launched nothing.
