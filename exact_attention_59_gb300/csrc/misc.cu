@@ -178,11 +178,16 @@ DEVI void load8<b16>(const b16* p, float (&f)[8]) {
   }
 }
 
+#ifndef ATTN_PRE_ROWS
+#define ATTN_PRE_ROWS 2
+#endif
+constexpr int PRE_ROWS = ATTN_PRE_ROWS;   // rows per lane of the preprocess
+
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ out, const T* __restrict__ dout,
                                                              const float* __restrict__ lse, long long rows, int D,
                                                              float* __restrict__ delta, float* __restrict__ lse2,
-                                                             long long half_rows, unsigned pre_blocks,
+                                                             long long part_rows, unsigned pre_blocks,
                                                              const uint8_t* __restrict__ km, int Skv,
                                                              uint32_t* __restrict__ bits, uint8_t* __restrict__ summary) {
   // Launched with programmatic dependent launch behind the forward: dout (an
@@ -215,30 +220,33 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
     return;
   }
   // D_i = rowsum(dO o O) and -lse log2(e): 8 elements per lane and chunk (a row
-  // spans at most 32 lanes: D / 256 chunks per lane beyond D = 256), two rows
-  // per lane (row and row + half_rows) so that four 16-byte loads are in flight
+  // spans at most 32 lanes: D / 256 chunks per lane beyond D = 256),
+  // PRE_ROWS rows per lane (row0 + k part_rows) so that 2 PRE_ROWS 16-byte
+  // loads are in flight
   const int lpr = D / 8 < 32 ? D / 8 : 32;   // lanes per row
   const int per = D / (8 * lpr);            // 8-element chunks per lane
   const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row0 = tid / lpr;
   const int part = (int)(tid % lpr);
-  if (threadIdx.x < 2) {   // this CTA's dout rows: [r0, r0 + n) and the same + half_rows
+  if (threadIdx.x < PRE_ROWS) {   // this CTA's dout rows: [r0, r0 + n) and the same + k part_rows
     const long long r0 = (long long)blockIdx.x * blockDim.x / lpr;
-    const long long r1 = r0 + threadIdx.x * half_rows;
+    const long long r1 = r0 + threadIdx.x * part_rows;
     const long long n = min((long long)blockDim.x / lpr, rows - r1);
-    if (r0 < half_rows && n > 0)
+    if (r0 < part_rows && n > 0)
       prefetch_l2_bulk(dout + r1 * D, static_cast<uint32_t>(n * D * sizeof(T)));
   }
   griddep_wait();
   griddep_launch_dependents();   // the dK/dV pass may set up (it waits for this grid itself)
-  float acc[2] = {0.f, 0.f};
+  float acc[PRE_ROWS];
+#pragma unroll
+  for (int k = 0; k < PRE_ROWS; ++k) acc[k] = 0.f;
   for (int j = 0; j < per; ++j) {
-    float a[2][8], g[2][8];
+    float a[PRE_ROWS][8], g[PRE_ROWS][8];
     const int col = (part + j * lpr) * 8;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const long long row = row0 + k * half_rows;
-      if (row0 < half_rows && row < rows) {
+    for (int k = 0; k < PRE_ROWS; ++k) {
+      const long long row = row0 + k * part_rows;
+      if (row0 < part_rows && row < rows) {
         load8<T>(out + row * D + col, a[k]);
         load8<T>(dout + row * D + col, g[k]);
       } else {
@@ -247,16 +255,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
       }
     }
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < PRE_ROWS; ++k) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[k] = fmaf(a[k][i], g[k][i], acc[k]);
     }
   }
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < PRE_ROWS; ++k) {
     for (int off = lpr / 2; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
-    const long long row = row0 + k * half_rows;
-    if (row0 < half_rows && row < rows && part == 0) {
+    const long long row = row0 + k * part_rows;
+    if (row0 < part_rows && row < rows && part == 0) {
       delta[row] = -acc[k];
       const float l = lse[row];
       lse2[row] = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
@@ -268,8 +276,8 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
                                   int D, float* delta, float* lse2, const uint8_t* km, int B, int Skv, uint32_t* bits,
                                   uint8_t* summary, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  const long long half_rows = (rows + 1) / 2;
-  const long long threads = half_rows * (D / 8 < 32 ? D / 8 : 32);
+  const long long part_rows = (rows + PRE_ROWS - 1) / PRE_ROWS;   // the distance between a lane's rows
+  const long long threads = part_rows * (D / 8 < 32 ? D / 8 : 32);
   const unsigned pre_blocks = (unsigned)((threads + 255) / 256);
   const unsigned pack_blocks = km ? (unsigned)(B * (((Skv + 127) / 128 + 1) / 2)) : 0u;
   const unsigned grid = pre_blocks + pack_blocks;
@@ -285,12 +293,12 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, const float
   cfg.numAttrs = 1;
   if (dtype == 0)
     return cudaLaunchKernelEx(&cfg, bwd_preprocess_kernel<float>, (const float*)out, (const float*)dout, lse, rows, D,
-                              delta, lse2, half_rows, pre_blocks, km, Skv, bits, summary);
+                              delta, lse2, part_rows, pre_blocks, km, Skv, bits, summary);
   if (dtype == 1)
     return cudaLaunchKernelEx(&cfg, bwd_preprocess_kernel<h16>, (const h16*)out, (const h16*)dout, lse, rows, D,
-                              delta, lse2, half_rows, pre_blocks, km, Skv, bits, summary);
+                              delta, lse2, part_rows, pre_blocks, km, Skv, bits, summary);
   return cudaLaunchKernelEx(&cfg, bwd_preprocess_kernel<b16>, (const b16*)out, (const b16*)dout, lse, rows, D, delta,
-                            lse2, half_rows, pre_blocks, km, Skv, bits, summary);
+                            lse2, part_rows, pre_blocks, km, Skv, bits, summary);
 }
 
 }  // namespace attn
