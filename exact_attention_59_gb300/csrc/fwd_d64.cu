@@ -15,7 +15,8 @@
 // (the item and its kv-block flags), so the next item's query tiles and first
 // blocks load while the softmax finishes the previous one.
 //   warp 0      producer: takes the items, fills the slots, loads both Q tiles of
-//               an item once the previous item's S products are done with them,
+//               an item into its slot's buffers (two items' query tiles are
+//               resident, so an item's tiles load while the previous item runs),
 //               then K and V tiles of each kv block into a FWD_NST-stage ring
 //               (128B swizzle, 16 KB per tile), continuing across items.
 //   warps 1-2   warp 1 allocates 512 TMEM columns; lane 0 of warp 1 + t issues
@@ -35,7 +36,7 @@
 namespace attn {
 
 struct __align__(1024) FwdSmem {
-  uint8_t q[2][FWD_TILE_BYTES];
+  uint8_t q[2][2][FWD_TILE_BYTES];   // per item slot: the item's two query tiles
   uint8_t k[FWD_NST][FWD_TILE_BYTES];
   uint8_t v[FWD_NST][FWD_TILE_BYTES];
   // Column terms folded into S = Q K^T as one more K = 16 step (K = 16 operands
@@ -45,7 +46,7 @@ struct __align__(1024) FwdSmem {
   __align__(128) uint8_t kaug[FWD_NST][4096];
   __align__(128) uint8_t qaug_h[2][256];   // folded ALiBi: an item slot's query side (8 rows, repeated)
   uint64_t full[FWD_NST], empty[FWD_NST];
-  uint64_t qfull, qfree, sfull[2], sfree[2], pready[2], odone[2], fin[2];
+  uint64_t qfull[2], sfull[2], sfree[2], pready[2], odone[2], fin[2];   // qfull: per item slot
   uint64_t item_ready[2], item_free[2];   // per item slot: written by the producer / done with by the rest
   alignas(16) float cb[FWD_NST][2][128];   // per-stage column bias (log2 units): key mask, ALiBi column term, checkerboard
   uint32_t tmem_base;
@@ -186,8 +187,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 2);   // one arrival per tile per kv block (a tile with no rows arrives too)
     }
-    mbar_init(smem_u32(&sm.qfull), 1);
-    mbar_init(smem_u32(&sm.qfree), 2);        // both MMA threads, once per item
+    mbar_init(smem_u32(&sm.qfull[0]), 1);
+    mbar_init(smem_u32(&sm.qfull[1]), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&sm.sfull[t]), 1);
       mbar_init(smem_u32(&sm.sfree[t]), 128);
@@ -269,7 +270,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   if (warp == 0) {
     // ======================= producer: items, query tiles, K/V ring, per-stage columns =======================
     WC c{&sm.abort, p.status, p.timeout_ns, 1};
-    const uint32_t qbar = smem_u32(&sm.qfull);
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     }
     int last_u[FWD_NST];
     for (int s = 0; s < FWD_NST; ++s) last_u[s] = -1;
-    int u = 0, last_q = -1;
+    int u = 0, last_q[2] = {-1, -1};
     bool ok = true;
     for (int ci = 0; ok; ++ci) {
       const int sl = ci & 1;
@@ -332,14 +332,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.item_ready[sl]));   // release: the slot is visible to its waiters
-      // the query tiles, once the previous item's S products are done with them
-      if (ci >= 1 && !wait_warp(smem_u32(&sm.qfree), (ci - 1) & 1, c)) break;
+      // the item's query tiles, into the slot's buffers (the S products of the
+      // slot's previous item, which read them, were complete before item_free)
       if (lane == 0) {
+        const uint32_t qbar = smem_u32(&sm.qfull[sl]);
         mbar_expect_tx(qbar, (it.valid1 ? 2 : 1) * FWD_TILE_BYTES);
-        tma_load_2d(smem_u32(sm.q[0]), &p.tm_q, qbar, 0, it.bh * p.Sq + it.qt0 * 128);
-        if (it.valid1) tma_load_2d(smem_u32(sm.q[1]), &p.tm_q, qbar, 0, it.bh * p.Sq + it.qt1 * 128);
+        tma_load_2d(smem_u32(sm.q[sl][0]), &p.tm_q, qbar, 0, it.bh * p.Sq + it.qt0 * 128);
+        if (it.valid1) tma_load_2d(smem_u32(sm.q[sl][1]), &p.tm_q, qbar, 0, it.bh * p.Sq + it.qt1 * 128);
       }
-      last_q = ci;
+      last_q[sl] = ci;
       const float slope2 = (MOD == MOD_ALIBI) ? alibi_slope_log2(it.h, p.H) : 0.f;
       for (int kb = 0; kb < p.nkb; ++kb) {
         const uint8_t fu = sm.flags[sl][0][kb] | sm.flags[sl][1][kb];
@@ -397,7 +398,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       }
     }
     if (lane == 0) {   // every copy issued has landed before the CTA exits (instant unless aborted)
-      if (last_q >= 0) drain_wait(qbar, last_q & 1, p.timeout_ns);
+      for (int t = 0; t < 2; ++t)
+        if (last_q[t] >= 0) drain_wait(smem_u32(&sm.qfull[t]), (last_q[t] >> 1) & 1, p.timeout_ns);
       for (int s = 0; s < FWD_NST; ++s)
         if (last_u[s] >= 0) drain_wait(smem_u32(&sm.full[s]), (last_u[s] / FWD_NST) & 1, p.timeout_ns);
     }
@@ -417,7 +419,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t IDESC_PV = idesc_f16(128, 64, BF16, false, true);
       const uint32_t tS = tmem + 256 * t, tP = tS + 128, tO = tS + 192;
-      const uint64_t qd = sdesc_sw128(smem_u32(sm.q[t]), 16, 1024);
       const uint64_t qad0 = sdesc_k16(smem_u32(sm.qaug));
       uint64_t dk_[FWD_NST], dv_[FWD_NST];
       for (int s = 0; s < FWD_NST; ++s) {
@@ -446,8 +447,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const int sl = ci & 1;
         if (!wait_one(smem_u32(&sm.item_ready[sl]), (ci >> 1) & 1, c)) break;
         if (sm.item[sl] < 0) break;
-        if (!wait_one(smem_u32(&sm.qfull), ci & 1, c)) break;
+        if (!wait_one(smem_u32(&sm.qfull[sl]), (ci >> 1) & 1, c)) break;
         n0 = n;
+        const uint64_t qd = sdesc_sw128(smem_u32(sm.q[sl][t]), 16, 1024);
         const uint64_t qad = (MOD == MOD_ALIBI && fold) ? sdesc_k16_rows8(smem_u32(sm.qaug_h[sl])) : qad0;
         for (int kb = 0; ok && kb < p.nkb; ++kb) {
           const uint8_t f = sm.flags[sl][t][kb];
@@ -475,9 +477,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           ++u;
         }
         if (!ok) break;
-        // arrives once this item's S products (all issued by now) have read the
-        // query tiles: the producer reloads them under the item's last P V
-        tc_commit(smem_u32(&sm.qfree));
         if (s_pend >= 0 && !issue_pv()) break;
         mbar_arrive(smem_u32(&sm.item_free[sl]));
       }

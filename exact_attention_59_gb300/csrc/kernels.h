@@ -43,7 +43,7 @@ cudaError_t launch_dense_mask_pack(const uint8_t* mask, long long nmask, int Sq,
 
 // ---------------------------------------------------------------- forward, D = 64
 #ifndef ATTN_FWD_NST
-#define ATTN_FWD_NST 4
+#define ATTN_FWD_NST 3
 #endif
 constexpr int FWD_NST = ATTN_FWD_NST;   // forward K/V stages
 constexpr int FWD_THREADS = 352;   // warp 0 TMA, warps 1-2 MMA issue (one per tile), warps 3-10 softmax
