@@ -207,6 +207,27 @@ def run_ours(args, rank, world):
     for e in evs:
         for j, n in enumerate(ph):
             ph[n].append(e[j].elapsed_time(e[j + 1]))
+    # each pass as a user issues it: K forwards back to back, then K backwards
+    # (preprocess, dK/dV, dQ, overlapping under programmatic dependent launch),
+    # events only around each run
+    def fwd_only(d):
+        E.attn_fwd(d["q"], d["k"], d["v"], key_mask=d["key_mask"], out=d["out"], lse=d["lse"], ws=ws_f)
+
+    def bwd_only(d):
+        E.attn_bwd_preprocess(d["q"], d["k"], d["out"], d["lse"], d["dout"], key_mask=d["key_mask"], ws=ws_b)
+        E.attn_bwd_dkdv(d["q"], d["k"], d["v"], d["dout"], d["dk"], d["dv"], key_mask=d["key_mask"], ws=ws_b)
+        E.attn_bwd_dq(d["q"], d["k"], d["v"], d["dout"], d["dq"], key_mask=d["key_mask"], ws=ws_b)
+
+    chained = {}
+    for name, fn in (("fwd", fwd_only), ("bwd", bwd_only)):
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        for i in range(args.steps):
+            fn(sets[i % nsets])
+        b_ev.record(stream)
+        torch.cuda.synchronize()
+        chained[name] = a_ev.elapsed_time(b_ev) / args.steps
+    assert E.poll_status(ws_f) == 0 and E.poll_status(ws_b) == 0, "device-side timeout in the chained passes"
 
     # ---- decode (config: checkerboard fp16, q 8x8x1x64, K/V 8x8x2048x64), CUDA graph, rotating K/V
     dec = bench_decode(E, dev, args)
@@ -219,7 +240,8 @@ def run_ours(args, rank, world):
     # ---- the other named workloads, for context (outside the timed region)
     extras = None if args.no_extras else bench_extras(E, dev)
 
-    res = {"ms": ms, "phases": {n: statistics.mean(v) for n, v in ph.items()}, "clocks": clk.summary(),
+    res = {"ms": ms, "phases": {n: statistics.mean(v) for n, v in ph.items()}, "chained": chained,
+           "clocks": clk.summary(),
            "decode": dec, "e2e": e2e, "e2e_lse": e2e_lse, "extras": extras}
     return res
 
@@ -666,6 +688,13 @@ def main():
             "bwd_tflops": 10.0 * WL.B * WL.H * WL.Sq * WL.Skv * WL.D / ((ph["pre"] + ph["dkdv"] + ph["dq"]) * 1e-3)
             / 1e12,
             "phase_ms": ph,
+            # each pass timed over K back-to-back calls (the backward's three launches
+            # overlapping as in the step), events only around the run
+            "chained": {"fwd_ms": res["chained"]["fwd"], "bwd_ms": res["chained"]["bwd"],
+                        "fwd_tflops": 4.0 * WL.B * WL.H * WL.Sq * WL.Skv * WL.D / (res["chained"]["fwd"] * 1e-3)
+                        / 1e12,
+                        "bwd_tflops": 10.0 * WL.B * WL.H * WL.Sq * WL.Skv * WL.D / (res["chained"]["bwd"] * 1e-3)
+                        / 1e12},
             "frac_of_peak": {"burst": value / burst, "sustained": value / sustained, "peak_source": src},
             "decode": {"workload": dec["workload"], "us_per_call": dec["us_per_call"], "GB/s": dec["GB/s"],
                        "frac_of_hbm": dec["GB/s"] / hbm,
