@@ -414,7 +414,6 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
     p.timeout_ns = timeout_ns();
     return cuda_status(launch_fwd_d512(p, s->dtype == ATTN_BF16, (int)mod, st));
   }
-  const WsLayout w = layout(ATTN_OP_FWD, s);
   if (s->dtype == ATTN_F32) {
     SimtParams p = simt_params(s, q, k, v, key_mask, bm, mod, scale);
     p.dm = dm_view(s, dm);
@@ -430,11 +429,9 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   if (!make_tmap(&p.tm_q, q, rq, 64, s->dtype) || !make_tmap(&p.tm_k, k, rk, 64, s->dtype) ||
       !make_tmap(&p.tm_v, v, rk, 64, s->dtype))
     return ATTN_ERR_CUDA;
-  ATTN_TRY(run_keymask(s, key_mask, ws, st));
   p.out = out;
   p.lse = lse;
-  p.km_bits = key_mask ? at<uint32_t>(ws, w.km_bits) : nullptr;
-  p.km_sum = key_mask ? at<uint8_t>(ws, w.km_sum) : nullptr;
+  p.km = key_mask;   // read as bytes by the kernel's producer: no packing launch
   p.bm_tiles = bm ? bm->tiles : nullptr;
   if (bm) bm_strides(s, bm, p.bm_sb, p.bm_sh);
   p.bm_mod = bm ? (int)bm->mask_mod : 0;
@@ -731,11 +728,9 @@ attn_status attn_decode_chunk(const attn_shape* s, const void* q, const void* k,
   if (!make_tmap(&p.tm_q, q, rq, 64, s->dtype) || !make_tmap(&p.tm_k, k, rk, 64, s->dtype) ||
       !make_tmap(&p.tm_v, v, rk, 64, s->dtype))
     return ATTN_ERR_CUDA;
-  ATTN_TRY(run_keymask(s, key_mask, ws, st));
   p.out = out;
   p.lse = lse;
-  p.km_bits = key_mask ? at<uint32_t>(ws, w.km_bits) : nullptr;
-  p.km_sum = key_mask ? at<uint8_t>(ws, w.km_sum) : nullptr;
+  p.km = key_mask;   // read as bytes by the kernel's producer: no packing launch
   p.status = at<int>(ws, 0);
   p.B = s->B;
   p.H = s->H;

@@ -122,6 +122,52 @@ DEVI void scale_scores(uint32_t (&r)[N], uint64_t scv, const float* tb, int lim,
 constexpr int FWD_PLAIN = 0, FWD_DENSE = 1, FWD_CHUNK = 2;
 
 
+// Keys key .. key + 3 of batch row b of a byte key mask (nonzero = keep; keys
+// at or past Skv count as masked), as the low 4 bits.
+DEVI uint32_t key_bits4(const uint8_t* km, int b, int Skv, int key) {
+  const uint8_t* row = km + (size_t)b * Skv;
+  if (key + 4 <= Skv && ((reinterpret_cast<uintptr_t>(row + key) & 3) == 0)) {
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(row + key));
+    return ((w & 0xffu) ? 1u : 0u) | ((w & 0xff00u) ? 2u : 0u) | ((w & 0xff0000u) ? 4u : 0u) |
+           ((w & 0xff000000u) ? 8u : 0u);
+  }
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (key + i < Skv && __ldg(row + key + i) != 0) r |= 1u << i;
+  return r;
+}
+
+// Key block kb of batch row b of a byte key mask: 0 no key kept, 1 some, 2 all
+// (of the block's keys below Skv).  A whole, 16-byte aligned block is read as
+// eight independent 16-byte loads and its nonzero bytes counted four at a time.
+DEVI int key_block_summary(const uint8_t* km, int b, int Skv, int kb) {
+  const int k0 = kb * 128, valid = min(128, Skv - k0);
+  const uint8_t* row = km + (size_t)b * Skv + k0;
+  int kept = 0;
+  if (valid == 128 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(row) + i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      kept += __popc(__vcmpne4(v[i].x, 0u)) + __popc(__vcmpne4(v[i].y, 0u)) + __popc(__vcmpne4(v[i].z, 0u)) +
+              __popc(__vcmpne4(v[i].w, 0u));
+    kept >>= 3;   // 8 bits per nonzero byte
+  } else {
+    for (int i = 0; i < valid; ++i) kept += __ldg(row + i) != 0 ? 1 : 0;
+  }
+  return kept == 0 ? 0 : (kept == valid ? 2 : 1);
+}
+
+// A lane's key-mask word for keys key .. key + 3 (key a multiple of 4): bit
+// (key + i) mod 32 is key + i's keep bit, from the packed bits or, without them,
+// from the byte mask (the other bits are not used).
+DEVI uint32_t lane_key_bits(const FwdParams& p, int b, int key) {
+  if (p.km_bits) return km_word(p.km_bits, b, p.Skv, key);
+  return key_bits4(p.km, b, p.Skv, key) << (key & 31);
+}
+
 template <bool BF16, int MOD, int VAR>
 __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -227,7 +273,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   //   carries the mod and the mask instead.
   const bool fold = kTableMod && p.fold;
   const bool use_table = kTableMod && !fold;   // the table then carries the key mask too
-  const bool aug = !use_table && (fold || p.km_bits != nullptr);
+  const bool kmask = p.km_bits != nullptr || p.km != nullptr;
+  const bool aug = !use_table && (fold || kmask);
   if (aug) {
     uint4* z = reinterpret_cast<uint4*>(sm.qaug);
     for (int i = tid; i < (1 + FWD_NST) * 4096 / 16; i += FWD_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -296,7 +343,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
       const Item it = item_of(L);
       const long long dmi = (long long)it.b * p.dm.mb + (long long)it.h * p.dm.mh;   // dense-mask index of (b, h)
       for (int kb = lane; kb < p.nkb; kb += 32) {
-        const int ks = p.km_sum ? p.km_sum[it.b * p.nkb + kb] : 2;
+        const int ks = p.km ? key_block_summary(p.km, it.b, p.Skv, kb) : p.km_sum ? p.km_sum[it.b * p.nkb + kb] : 2;
         for (int t = 0; t < 2; ++t) {
           const int qt = t ? it.qt1 : it.qt0;
           uint8_t f = 0;
@@ -351,10 +398,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           break;
         }
         if (aug) {
-          if (p.km_bits) {
+          if (kmask) {
             // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column AUG_KEY of kaug[s]
             uint32_t bits = 0xffffffffu;
-            if (fu & KB_KEYMASK) bits = km_word(p.km_bits, it.b, p.Skv, kb * 128 + 4 * lane);
+            if (fu & KB_KEYMASK) bits = lane_key_bits(p, it.b, kb * 128 + 4 * lane);
             // the infinity whose product with the scale is -inf (scale != 0)
             const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
 #pragma unroll
@@ -368,7 +415,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         } else if (use_table) {
           // lane owns columns 4 lane .. 4 lane + 3 of this kv block
           uint32_t bits = 0xffffffffu;
-          if (p.km_bits && (fu & KB_KEYMASK)) bits = km_word(p.km_bits, it.b, p.Skv, kb * 128 + 4 * lane);
+          if (kmask && (fu & KB_KEYMASK)) bits = lane_key_bits(p, it.b, kb * 128 + 4 * lane);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int col = 4 * lane + i;

@@ -56,6 +56,9 @@ struct FwdParams {
   float* lse;
   const uint32_t* km_bits;        // (B, Skv/32) or nullptr
   const uint8_t* km_sum;          // (B, nkb) or nullptr
+  // the key mask as given, bytes (B, Skv), nonzero = keep: read directly by the
+  // producer (block summaries and each lane's bits) when km_bits is nullptr
+  const uint8_t* km;
   const uint8_t* bm_tiles;        // block-mask states or nullptr
   long long bm_sb, bm_sh;         // element strides of b and h in bm_tiles (0 = broadcast)
   int bm_mod;
