@@ -455,6 +455,16 @@ static attn_status fwd_impl(const attn_shape* s, const void* q, const void* k, c
   // workspace header (kWsItemCounter)
   p.items = at<unsigned>(ws, kWsItemCounter);
   p.ctas = (int)std::min<long long>((long long)p.npairs * p.B * p.H, sm_count());
+  {
+    // the pairs past the last full round as single tiles, when every pair has two
+    // tiles, the split pairs fit one round, and the items are all alike (with a
+    // block mask or the causal rule the last items are the shortest: nothing to
+    // gain)
+    const long long n = (long long)p.npairs * p.B * p.H, rem = n % p.ctas;
+    const bool alike = bm == nullptr && mod != ATTN_MOD_CAUSAL;
+    p.single_tail = (alike && p.nqb % 2 == 0 && rem > 0 && 2 * rem <= p.ctas) ? 1 : 0;
+    p.n_whole = (int)(p.single_tail ? n - rem : n);
+  }
   if (um) return cuda_status(launch_fwd_d64_kernel(p, uk[0], st));
   return cuda_status(launch_fwd_d64(p, s->dtype == ATTN_BF16, (int)mod, st));
 }

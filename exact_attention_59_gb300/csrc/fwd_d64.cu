@@ -188,19 +188,27 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
   const int kb_hi = CHUNK && p.nsplit > 1 ? min(p.nkb, kb_lo + p.kps) : p.nkb;
   const int q_off = CHUNK ? p.q_off : 0;
   const bool persistent = !CHUNK && p.items != nullptr;
-  // an item's coordinates
+  const bool singles = persistent && p.single_tail;
+  const int n_claims = singles ? p.n_whole + 2 * (n_items - p.n_whole) : n_items;
+  // an item's coordinates (a single-tile item keeps its tile in slot 0 and
+  // leaves slot 1 empty, as the last pair of an odd tile count does)
   struct Item {
     int bh, b, h, qt0, qt1;
     bool valid1;
   };
   auto item_of = [&](int L) {
     Item it;
+    int which = -1;   // single-tile item: the pair's tile 0 or 1
+    if (singles && L >= p.n_whole) {
+      which = (L - p.n_whole) & 1;
+      L = p.n_whole + ((L - p.n_whole) >> 1);
+    }
     const int pair = p.npairs - 1 - L / BH;
     it.bh = L % BH;
     it.b = it.bh / p.H;
     it.h = it.bh % p.H;
-    it.qt0 = 2 * pair;
-    it.qt1 = 2 * pair + 1;
+    it.qt0 = 2 * pair + (which == 1 ? 1 : 0);
+    it.qt1 = which >= 0 ? p.nqb : 2 * pair + 1;
     it.valid1 = it.qt1 < p.nqb;
     return it;
   };
@@ -329,11 +337,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
     for (int ci = 0; ok; ++ci) {
       const int sl = ci & 1;
       int L = 0;
-      if (lane == 0) L = persistent ? (int)atomicAdd(p.items, 1u) : (ci == 0 ? (int)(blockIdx.x % n_items) : n_items);
+      if (lane == 0) L = persistent ? (int)atomicAdd(p.items, 1u) : (ci == 0 ? (int)(blockIdx.x % n_items) : n_claims);
       L = __shfl_sync(0xffffffffu, L, 0);
       // the slot's previous item (ci - 2) is done with everywhere
       if (ci >= 2 && !wait_warp(smem_u32(&sm.item_free[sl]), ((ci - 2) >> 1) & 1, c)) break;
-      if (L >= n_items) {   // no more items: the others stop at this slot
+      if (L >= n_claims) {   // no more items: the others stop at this slot
         if (lane == 0) {
           sm.item[sl] = -1;
           mbar_arrive(smem_u32(&sm.item_ready[sl]));

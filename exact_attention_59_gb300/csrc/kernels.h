@@ -83,6 +83,11 @@ struct FwdParams {
   // first call).  items = nullptr: one CTA per item.
   unsigned* items;
   int ctas;
+  // Claims below n_whole are (query-tile pair, b, h) items; with single_tail,
+  // each pair from n_whole on is claimed twice, once per query tile (the last,
+  // partly filled round then runs single tiles on more CTAs).  n_whole = all
+  // items without it.
+  int n_whole, single_tail;
   // ALiBi / checkerboard bias folded into S = Q K^T as one more K = 16 step
   // (the AUG_MOD columns of the augmented operands), and 1 / scale
   int fold;

@@ -602,6 +602,10 @@ def test_workspace_serves_several_shapes():
     (3, 12, 1100, "bf16", "alibi", True, "causal"),
     (3, 12, 1100, "f16", "checkerboard", False, None),
     (2, 28, 640, "f16", "causal", True, None),
+    # an even tile count and no block mask: the 8 pairs past the last full round
+    # (160 items on at most 152 CTAs) run as 16 single-tile items
+    (2, 20, 1024, "bf16", "alibi", True, None),
+    (2, 20, 1024, "f16", "checkerboard", True, None),
 ])
 def test_items_outnumber_the_ctas(B, H, S, dtype, mod, km, bm):
     """More work items than SMs: each of the forward's CTAs (one per SM) runs
