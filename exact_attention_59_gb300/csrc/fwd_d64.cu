@@ -10,8 +10,10 @@
 // A work item is two 128-row query tiles of one (b, h); the CTA streams the
 // union of their kv-block lists once.  The grid is one CTA per SM (at most one
 // per item), and the CTAs take items from an atomic counter in the workspace,
-// longest causal pairs first; the split variant (a chunk of queries, or a kv
-// range per CTA) runs one item per CTA instead.  Items pass through two slots
+// longest causal pairs first (the pairs past the last full round may be
+// claimed as single query tiles, so that the partly filled last round runs on
+// more CTAs); the split variant (a chunk of queries, or a kv range per CTA)
+// runs one item per CTA instead.  Items pass through two slots
 // (the item and its kv-block flags), so the next item's query tiles and first
 // blocks load while the softmax finishes the previous one.
 //   warp 0      producer: takes the items, fills the slots, loads both Q tiles of
