@@ -403,6 +403,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         const uint8_t fu = sm.flags[sl][0][kb] | sm.flags[sl][1][kb];
         if (!(fu & KB_VISIT)) continue;
         const int s = u % FWD_NST;
+        // the block's key bits do not depend on the stage: their load is issued
+        // before the wait for it, so its latency overlaps that wait
+        uint32_t kbits = 0xffffffffu;
+        if (kmask && (fu & KB_KEYMASK) && (aug || use_table)) kbits = lane_key_bits(p, it.b, kb * 128 + 4 * lane);
         if (u >= FWD_NST && !wait_warp(smem_u32(&sm.empty[s]), ((u / FWD_NST) - 1) & 1, c)) {
           ok = false;
           break;
@@ -410,8 +414,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
         if (aug) {
           if (kmask) {
             // lane owns keys 4 lane .. 4 lane + 3 of this kv block: column AUG_KEY of kaug[s]
-            uint32_t bits = 0xffffffffu;
-            if (fu & KB_KEYMASK) bits = lane_key_bits(p, it.b, kb * 128 + 4 * lane);
+            const uint32_t bits = kbits;
             // the infinity whose product with the scale is -inf (scale != 0)
             const uint16_t ninf = p.sc < 0.f ? (BF16 ? 0x7F80u : 0x7C00u) : (BF16 ? 0xFF80u : 0xFC00u);
 #pragma unroll
@@ -424,8 +427,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) fwd_d64_kernel(const __grid_co
           fence_async_smem();
         } else if (use_table) {
           // lane owns columns 4 lane .. 4 lane + 3 of this kv block
-          uint32_t bits = 0xffffffffu;
-          if (kmask && (fu & KB_KEYMASK)) bits = lane_key_bits(p, it.b, kb * 128 + 4 * lane);
+          const uint32_t bits = kbits;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int col = 4 * lane + i;
