@@ -140,6 +140,36 @@ def test_bwd_and_decode_reject_bad_arguments(lib):
     assert L.attn_poll_status(None, None) == lib.ATTN_ERR_INVALID_ARG
 
 
+def test_noalloc_decode_rejects_bad_arguments(lib):
+    """attn_decode_noalloc validates like attn_decode, and refuses a shape whose
+    split partials would not fit its built-in 4 MiB scratch (before it looks the
+    scratch up on the device)."""
+    fn = lib.load().attn_decode_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(lib.Shape), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+
+    def call(shape, q=FAKE, k=FAKE, v=FAKE, km=None, mod=0, scale=0.125, out=FAKE, lse=FAKE):
+        return fn(ctypes.byref(shape) if shape is not None else None, q, k, v, km, mod, scale, out, lse, None)
+
+    dec = dict(B=8, H=8, Sq=1, Skv=2048)
+    assert call(None) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **{**dec, "Skv": 0})) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **dec, dt=7)) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **{**dec, "Sq": 2})) == lib.ATTN_ERR_SHAPE
+    assert call(_shape(lib, **dec, D=128)) == lib.ATTN_ERR_UNSUPPORTED
+    assert call(_shape(lib, **dec, dt=0)) == lib.ATTN_ERR_UNSUPPORTED        # float32
+    assert call(_shape(lib, **dec), mod=4) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **dec), scale=0.0) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **dec), scale=float("inf")) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **dec), lse=None) == lib.ATTN_ERR_INVALID_ARG
+    assert call(_shape(lib, **dec), v=FAKE + 4) == lib.ATTN_ERR_ALIGN
+    assert call(_shape(lib, **dec), km=FAKE + 1) == lib.ATTN_ERR_ALIGN
+    assert call(_shape(lib, B=1024, H=1024, Sq=1, Skv=4096)) == lib.ATTN_ERR_SHAPE   # B H Skv >= 2^31
+    # 64 heads of 131072 keys: 1024 splits a head, 17 MB of partials
+    assert call(_shape(lib, **{**dec, "Skv": 131072})) == lib.ATTN_ERR_WORKSPACE
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     import exact_attention_59_gb300 as E
