@@ -140,6 +140,28 @@ def test_bwd_and_decode_reject_bad_arguments(lib):
     assert L.attn_poll_status(None, None) == lib.ATTN_ERR_INVALID_ARG
 
 
+def test_backward_phases_reject_bad_arguments(lib):
+    """The preprocess phase called alone, and the user-mod backward without a mod."""
+    L = lib.load()
+    s = _shape(lib)
+
+    def pre(shape=s, out=FAKE, lse=FAKE, dout=FAKE, km=None, ws=FAKE, n=1 << 30):
+        return L.attn_bwd_preprocess(ctypes.byref(shape) if shape is not None else None, out, lse, dout, km, ws, n,
+                                     None)
+    assert pre(shape=None) == lib.ATTN_ERR_INVALID_ARG
+    assert pre(shape=_shape(lib, D=96)) == lib.ATTN_ERR_UNSUPPORTED
+    assert pre(shape=_shape(lib, Sq=200, D=512)) == lib.ATTN_ERR_SHAPE
+    assert pre(out=None) == lib.ATTN_ERR_INVALID_ARG
+    assert pre(dout=None) == lib.ATTN_ERR_INVALID_ARG
+    assert pre(lse=FAKE + 4) == lib.ATTN_ERR_ALIGN
+    assert pre(km=FAKE + 3) == lib.ATTN_ERR_ALIGN
+    assert pre(ws=None) == lib.ATTN_ERR_WORKSPACE
+    assert pre(ws=FAKE + 128) == lib.ATTN_ERR_ALIGN
+    assert pre(n=100) == lib.ATTN_ERR_WORKSPACE
+    assert L.attn_bwd_user(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 0.125, FAKE, FAKE,
+                           FAKE, FAKE, 1 << 30, None) == lib.ATTN_ERR_INVALID_ARG
+
+
 def test_noalloc_decode_rejects_bad_arguments(lib):
     """attn_decode_noalloc validates like attn_decode, and refuses a shape whose
     split partials would not fit its built-in 4 MiB scratch (before it looks the
