@@ -131,6 +131,40 @@ def _cuda(*ts):
             raise ValueError("attention tensors must live on a CUDA device (no CPU path)")
 
 
+def _check_layout(q, k, v, out=None, lse=None, dout=None, dq=None, dk=None, dv=None, key_mask=None):
+    """The layout that the C ABI's plain pointers assume, checked before anything
+    is launched (a mismatch would read or write past a buffer): q (B, H, Sq, D),
+    k and v (B, H, Skv, D), the three of one dtype; out, dout and dq of B H Sq D
+    elements and dk, dv of B H Skv D, in that dtype; lse of B H Sq float32;
+    key_mask of B Skv bytes (uint8 or bool); every tensor contiguous and on q's
+    device.  Raises ValueError."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k and v must be 4-D: (batch, heads, seq, dim)")
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError(f"k {tuple(k.shape)} and v {tuple(v.shape)} must be ({B}, {H}, Skv, {D}) like q "
+                         f"{tuple(q.shape)}")
+    dt, dev = q.dtype, q.device
+    if k.dtype != dt or v.dtype != dt:
+        raise ValueError(f"q, k and v must share one dtype (got {q.dtype}, {k.dtype}, {v.dtype})")
+    for name, t, n in (("q", q, None), ("k", k, None), ("v", v, None), ("out", out, B * H * Sq * D),
+                       ("dout", dout, B * H * Sq * D), ("dq", dq, B * H * Sq * D), ("dk", dk, B * H * Skv * D),
+                       ("dv", dv, B * H * Skv * D)):
+        if t is None:
+            continue
+        if n is not None and (t.numel() != n or t.dtype != dt):
+            raise ValueError(f"{name} must hold {n} elements of {dt} (got {t.numel()} of {t.dtype})")
+        if not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"{name} must be contiguous and on {dev}")
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != B * H * Sq or not lse.is_contiguous()
+                            or lse.device != dev):
+        raise ValueError(f"lse must be a contiguous float32 tensor of {B * H * Sq} elements on {dev}")
+    if key_mask is not None and (key_mask.element_size() != 1 or key_mask.numel() != B * Skv
+                                 or not key_mask.is_contiguous() or key_mask.device != dev):
+        raise ValueError(f"key_mask must be a contiguous (batch, seq) = ({B}, {Skv}) uint8 or bool tensor on {dev}")
+
+
 def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -286,6 +320,7 @@ def _bm(bm):
 def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_mod="none", scale=None,
              out=None, lse=None, debug_visited=None, ws=None, dense_mask: DenseMask | None = None):
     """(out, lse) of the forward pass on q's device and current stream."""
+    _check_layout(q, k, v, out=out, lse=lse, key_mask=key_mask)
     _cuda(q, k, v, key_mask, out, lse)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -313,6 +348,7 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_
 def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod="none", scale=None,
              dq=None, dk=None, dv=None, ws=None, dense_mask: DenseMask | None = None):
     """(dq, dk, dv) of sum(dout * out)."""
+    _check_layout(q, k, v, out=out, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv, key_mask=key_mask)
     _cuda(q, k, v, out, lse, dout, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -339,6 +375,8 @@ def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod=
 
 
 def attn_bwd_preprocess(q, k, out, lse, dout, key_mask=None, ws=None):
+    _check_layout(q, k, k, out=out, lse=lse, dout=dout, key_mask=key_mask)
+    _cuda(q, k, out, lse, dout, key_mask)
     shape = make_shape(q, k)
     ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
     _check(load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(out), _ptr(lse), _ptr(dout), _ptr(key_mask),
@@ -347,6 +385,8 @@ def attn_bwd_preprocess(q, k, out, lse, dout, key_mask=None, ws=None):
 
 
 def attn_bwd_dkdv(q, k, v, dout, dk, dv, key_mask=None, block_mask=None, score_mod="none", scale=None, ws=None):
+    _check_layout(q, k, v, dout=dout, dk=dk, dv=dv, key_mask=key_mask)
+    _cuda(q, k, v, dout, dk, dv, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
@@ -356,6 +396,8 @@ def attn_bwd_dkdv(q, k, v, dout, dk, dv, key_mask=None, block_mask=None, score_m
 
 
 def attn_bwd_dq(q, k, v, dout, dq, key_mask=None, block_mask=None, score_mod="none", scale=None, ws=None):
+    _check_layout(q, k, v, dout=dout, dq=dq, key_mask=key_mask)
+    _cuda(q, k, v, dout, dq, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
@@ -366,6 +408,7 @@ def attn_bwd_dq(q, k, v, dout, dq, key_mask=None, block_mask=None, score_mod="no
 
 def attn_decode(q, k, v, key_mask=None, score_mod="none", scale=None, out=None, lse=None, ws=None):
     """(out, lse) for a single query per (b, h): q (B, H, 1, D)."""
+    _check_layout(q, k, v, out=out, lse=lse, key_mask=key_mask)
     _cuda(q, k, v, key_mask, out, lse)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -382,6 +425,7 @@ def attn_decode_chunk(q, k, v, q_offset: int, key_mask=None, score_mod="none", s
                       ws=None):
     """(out, lse) for a chunk of queries q (B, H, nq, D) at positions
     q_offset .. q_offset + nq - 1 of the keys k, v (B, H, Skv, D)."""
+    _check_layout(q, k, v, out=out, lse=lse, key_mask=key_mask)
     _cuda(q, k, v, key_mask, out, lse)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)

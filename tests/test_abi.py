@@ -200,6 +200,74 @@ def test_binding_refuses_cpu_tensors(lib):
         E.attn_fwd(q, q, q)
 
 
+def test_binding_checks_layout_before_the_device(lib):
+    """Every binding call checks the shapes, dtypes and contiguity that the C
+    ABI's plain pointers assume before anything else: well-formed CPU tensors
+    get as far as the device check, malformed ones are refused on layout."""
+    import torch
+    import exact_attention_59_gb300 as E
+    B, H, Sq, Skv, D = 2, 3, 40, 72, 64
+    f16 = torch.float16
+    q, dq, out, dout = (torch.zeros(B, H, Sq, D, dtype=f16) for _ in range(4))
+    k, v, dk, dv = (torch.zeros(B, H, Skv, D, dtype=f16) for _ in range(4))
+    lse = torch.zeros(B, H, Sq)
+    km = torch.ones(B, Skv, dtype=torch.uint8)
+    qd = torch.zeros(B, H, 1, D, dtype=f16)
+    calls = {
+        "fwd": lambda **o: E.attn_fwd(**{"q": q, "k": k, "v": v, "key_mask": km, "out": out, "lse": lse, **o}),
+        "bwd": lambda **o: E.attn_bwd(**{"q": q, "k": k, "v": v, "out": out, "lse": lse, "dout": dout,
+                                         "key_mask": km, "dq": dq, "dk": dk, "dv": dv, **o}),
+        "pre": lambda **o: E.attn_bwd_preprocess(**{"q": q, "k": k, "out": out, "lse": lse, "dout": dout,
+                                                    "key_mask": km, **o}),
+        "dkdv": lambda **o: E.attn_bwd_dkdv(**{"q": q, "k": k, "v": v, "dout": dout, "dk": dk, "dv": dv,
+                                               "key_mask": km, **o}),
+        "dq": lambda **o: E.attn_bwd_dq(**{"q": q, "k": k, "v": v, "dout": dout, "dq": dq, "key_mask": km, **o}),
+        "decode": lambda **o: E.attn_decode(**{"q": qd, "k": k, "v": v, "key_mask": km, **o}),
+        "chunk": lambda **o: E.attn_decode_chunk(**{"q": q, "k": k, "v": v, "q_offset": 0, "key_mask": km, **o}),
+    }
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="CUDA device"):
+            call()
+        with pytest.raises(ValueError, match="key_mask"):
+            call(key_mask=torch.ones(B, Skv, dtype=torch.int64))
+        with pytest.raises(ValueError, match="key_mask"):
+            call(key_mask=torch.ones(B, Skv + 1, dtype=torch.uint8))
+        with pytest.raises(ValueError, match="k .* and v"):
+            call(k=torch.zeros(B, H, Skv, 32, dtype=f16))
+        with pytest.raises(ValueError, match="k .* and v"):
+            call(k=torch.zeros(B + 1, H, Skv, D, dtype=f16))
+        with pytest.raises(ValueError, match="contiguous"):
+            call(k=torch.zeros(B, Skv, H, D, dtype=f16).transpose(1, 2))
+        if name != "pre":   # the preprocess takes no v
+            with pytest.raises(ValueError, match="k .* and v"):
+                call(v=torch.zeros(B, H, Skv - 1, D, dtype=f16))
+            with pytest.raises(ValueError, match="one dtype"):
+                call(v=torch.zeros(B, H, Skv, D, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="4-D"):
+        E.attn_fwd(q[0], k[0], v[0])
+    with pytest.raises(ValueError, match="out must hold"):
+        calls["fwd"](out=torch.zeros(B, H, Sq, D, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="out must hold"):
+        calls["decode"](out=torch.zeros(B, H, 2, D, dtype=f16))
+    with pytest.raises(ValueError, match="lse must"):
+        calls["fwd"](lse=torch.zeros(B, H, Sq, dtype=torch.float64))
+    with pytest.raises(ValueError, match="lse must"):
+        calls["bwd"](lse=torch.zeros(B, H, Sq + 1))
+    with pytest.raises(ValueError, match="dout must hold"):
+        calls["bwd"](dout=torch.zeros(B, H, Sq, D - 1, dtype=f16))
+    with pytest.raises(ValueError, match="dk must hold"):
+        calls["dkdv"](dk=torch.zeros(B, H, Sq, D, dtype=f16))
+    with pytest.raises(ValueError, match="dq must hold"):
+        calls["dq"](dq=torch.zeros(B, H, Skv, D, dtype=f16))
+    with pytest.raises(ValueError, match="dv must be contiguous"):
+        calls["bwd"](dv=torch.zeros(B, H, D, Skv, dtype=f16).transpose(2, 3))
+    # the binding's own entry points reach the same checks
+    with pytest.raises(ValueError, match="CUDA device"):
+        E.flash_attention(q, k, v, torch.randint(0, 2, (B, Skv)))
+    with pytest.raises(ValueError, match="key_mask"):
+        E.flash_attention(q, k, v, torch.randint(0, 2, (B, Skv + 3)))
+
+
 def test_dense_mask_sizes_and_validation(lib):
     """Packing and dense-mask calls validate before launching (FAKE pointers are never touched)."""
     L = lib.load()
