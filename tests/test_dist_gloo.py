@@ -49,7 +49,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of this (threaded) process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     import oracle.attention as OR
