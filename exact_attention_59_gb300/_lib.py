@@ -165,6 +165,25 @@ def _check_layout(q, k, v, out=None, lse=None, dout=None, dq=None, dk=None, dv=N
         raise ValueError(f"key_mask must be a contiguous (batch, seq) = ({B}, {Skv}) uint8 or bool tensor on {dev}")
 
 
+def _check_tiles(q, k, block_mask=None, debug_visited=None):
+    """A block mask's tile states must cover the call's (B|1, H|1) heads and its
+    query and key tiles, on q's device; debug_visited must be B H nqb nkb bytes
+    (the kernels index both by the call's shape).  Raises ValueError."""
+    B, H, Sq, _ = q.shape
+    Skv = k.shape[2]
+    if block_mask is not None:
+        t = block_mask.tiles
+        want = (-(-Sq // block_mask.block_q), -(-Skv // block_mask.block_kv))
+        if t.shape[0] not in (1, B) or t.shape[1] not in (1, H) or tuple(t.shape[2:]) != want or t.device != q.device:
+            raise ValueError(f"block mask tiles {tuple(t.shape)} do not fit ({B}|1, {H}|1, {want[0]}, {want[1]}) "
+                             f"on {q.device}")
+    if debug_visited is not None:
+        n = B * H * -(-Sq // 128) * -(-Skv // 128)
+        if (debug_visited.element_size() != 1 or debug_visited.numel() != n or not debug_visited.is_contiguous()
+                or debug_visited.device != q.device):
+            raise ValueError(f"debug_visited must be {n} contiguous bytes (B, H, nqb, nkb) on {q.device}")
+
+
 def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -321,6 +340,7 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_
              out=None, lse=None, debug_visited=None, ws=None, dense_mask: DenseMask | None = None):
     """(out, lse) of the forward pass on q's device and current stream."""
     _check_layout(q, k, v, out=out, lse=lse, key_mask=key_mask)
+    _check_tiles(q, k, block_mask, debug_visited)
     _cuda(q, k, v, key_mask, out, lse)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -349,6 +369,7 @@ def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod=
              dq=None, dk=None, dv=None, ws=None, dense_mask: DenseMask | None = None):
     """(dq, dk, dv) of sum(dout * out)."""
     _check_layout(q, k, v, out=out, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv, key_mask=key_mask)
+    _check_tiles(q, k, block_mask)
     _cuda(q, k, v, out, lse, dout, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -386,6 +407,7 @@ def attn_bwd_preprocess(q, k, out, lse, dout, key_mask=None, ws=None):
 
 def attn_bwd_dkdv(q, k, v, dout, dk, dv, key_mask=None, block_mask=None, score_mod="none", scale=None, ws=None):
     _check_layout(q, k, v, dout=dout, dk=dk, dv=dv, key_mask=key_mask)
+    _check_tiles(q, k, block_mask)
     _cuda(q, k, v, dout, dk, dv, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -397,6 +419,7 @@ def attn_bwd_dkdv(q, k, v, dout, dk, dv, key_mask=None, block_mask=None, score_m
 
 def attn_bwd_dq(q, k, v, dout, dq, key_mask=None, block_mask=None, score_mod="none", scale=None, ws=None):
     _check_layout(q, k, v, dout=dout, dq=dq, key_mask=key_mask)
+    _check_tiles(q, k, block_mask)
     _cuda(q, k, v, dout, dq, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)

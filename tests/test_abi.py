@@ -261,6 +261,18 @@ def test_binding_checks_layout_before_the_device(lib):
         calls["dq"](dq=torch.zeros(B, H, Skv, D, dtype=f16))
     with pytest.raises(ValueError, match="dv must be contiguous"):
         calls["bwd"](dv=torch.zeros(B, H, D, Skv, dtype=f16).transpose(2, 3))
+    # block-mask tiles and the visited map must match the call's tiles (40 x 72: one q tile, one kv tile)
+    ok_bm = E.BlockMask(torch.zeros((1, H, 1, 1), dtype=torch.uint8))
+    for name in ("fwd", "bwd", "dkdv", "dq"):
+        with pytest.raises(ValueError, match="CUDA device"):
+            calls[name](block_mask=ok_bm)
+        for tiles in ((1, 1, 2, 1), (1, 1, 1, 2), (B + 1, 1, 1, 1), (1, H + 1, 1, 1)):
+            with pytest.raises(ValueError, match="block mask tiles"):
+                calls[name](block_mask=E.BlockMask(torch.zeros(tiles, dtype=torch.uint8)))
+    with pytest.raises(ValueError, match="CUDA device"):
+        calls["fwd"](debug_visited=torch.zeros((B, H, 1, 1), dtype=torch.uint8))
+    with pytest.raises(ValueError, match="debug_visited"):
+        calls["fwd"](debug_visited=torch.zeros((B, H, 1, 2), dtype=torch.uint8))
     # the binding's own entry points reach the same checks
     with pytest.raises(ValueError, match="CUDA device"):
         E.flash_attention(q, k, v, torch.randint(0, 2, (B, Skv)))
