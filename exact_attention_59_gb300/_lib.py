@@ -165,12 +165,17 @@ def _check_layout(q, k, v, out=None, lse=None, dout=None, dq=None, dk=None, dv=N
         raise ValueError(f"key_mask must be a contiguous (batch, seq) = ({B}, {Skv}) uint8 or bool tensor on {dev}")
 
 
-def _check_tiles(q, k, block_mask=None, debug_visited=None):
+def _check_tiles(q, k, block_mask=None, debug_visited=None, dense_mask=None):
     """A block mask's tile states must cover the call's (B|1, H|1) heads and its
     query and key tiles, on q's device; debug_visited must be B H nqb nkb bytes
-    (the kernels index both by the call's shape).  Raises ValueError."""
+    (the kernels index both by the call's shape); a dense mask packed by
+    pack_dense_mask must have been packed for the call's (B, H, Sq, Skv).
+    Raises ValueError."""
     B, H, Sq, _ = q.shape
     Skv = k.shape[2]
+    packed_for = getattr(dense_mask, "shape", None)
+    if packed_for is not None and tuple(packed_for) != (B, H, Sq, Skv):
+        raise ValueError(f"dense mask packed for {tuple(packed_for)}, called with {(B, H, Sq, Skv)}")
     if block_mask is not None:
         t = block_mask.tiles
         want = (-(-Sq // block_mask.block_q), -(-Skv // block_mask.block_kv))
@@ -276,6 +281,7 @@ def pack_dense_mask(mask: torch.Tensor, B: int, H: int) -> DenseMask:
     _check(load().attn_pack_dense_mask(ctypes.byref(shape), _ptr(m), bb, bh, _ptr(packed), n,
                                        _stream(mask.device)), "attn_pack_dense_mask")
     dm = DenseMask(packed, bb, bh)
+    dm.shape = (B, H, int(mask.shape[2]), int(mask.shape[3]))   # the (B, H, Sq, Skv) it was packed for
     dm._source = m   # keeps a converted copy alive until the packing kernel has run
     return dm
 
@@ -340,7 +346,7 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_
              out=None, lse=None, debug_visited=None, ws=None, dense_mask: DenseMask | None = None):
     """(out, lse) of the forward pass on q's device and current stream."""
     _check_layout(q, k, v, out=out, lse=lse, key_mask=key_mask)
-    _check_tiles(q, k, block_mask, debug_visited)
+    _check_tiles(q, k, block_mask, debug_visited, dense_mask)
     _cuda(q, k, v, key_mask, out, lse)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
@@ -369,7 +375,7 @@ def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod=
              dq=None, dk=None, dv=None, ws=None, dense_mask: DenseMask | None = None):
     """(dq, dk, dv) of sum(dout * out)."""
     _check_layout(q, k, v, out=out, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv, key_mask=key_mask)
-    _check_tiles(q, k, block_mask)
+    _check_tiles(q, k, block_mask, dense_mask=dense_mask)
     _cuda(q, k, v, out, lse, dout, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)

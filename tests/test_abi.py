@@ -273,6 +273,16 @@ def test_binding_checks_layout_before_the_device(lib):
         calls["fwd"](debug_visited=torch.zeros((B, H, 1, 1), dtype=torch.uint8))
     with pytest.raises(ValueError, match="debug_visited"):
         calls["fwd"](debug_visited=torch.zeros((B, H, 1, 2), dtype=torch.uint8))
+    # a dense mask remembers the shape it was packed for
+    dm = E.DenseMask(torch.zeros(256, dtype=torch.uint8), 0, 0)
+    dm.shape = (B, H, Sq, Skv)
+    for name in ("fwd", "bwd"):
+        with pytest.raises(ValueError, match="CUDA device"):
+            calls[name](dense_mask=dm)
+        dm.shape = (B, H, Sq, Skv + 1)
+        with pytest.raises(ValueError, match="dense mask packed for"):
+            calls[name](dense_mask=dm)
+        dm.shape = (B, H, Sq, Skv)
     # the binding's own entry points reach the same checks
     with pytest.raises(ValueError, match="CUDA device"):
         E.flash_attention(q, k, v, torch.randint(0, 2, (B, Skv)))
