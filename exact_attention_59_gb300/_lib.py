@@ -218,6 +218,16 @@ def workspace(op: int, shape: Shape, device) -> torch.Tensor:
     return ws
 
 
+def _workspace(op: int, shape: Shape, q, ws):
+    """The cached workspace of (q's device, current stream, op), or the caller's,
+    which must be contiguous bytes on q's device (the kernels write into it)."""
+    if ws is None:
+        return workspace(op, shape, q.device)
+    if ws.element_size() != 1 or not ws.is_contiguous() or ws.device != q.device:
+        raise ValueError(f"ws must be a contiguous uint8 tensor on {q.device}")
+    return ws
+
+
 class BlockMask:
     """Device tile states (B|1, H|1, Sq/128, Skv/128) uint8 plus the mask_mod of partial tiles."""
 
@@ -236,6 +246,8 @@ def create_block_mask(mask_mod, B, H, Sq, Skv, device="cuda", block_q=128, block
     """Tile states built on the device: attn_build_block_mask for a built-in
     mask_mod ("none", "causal"), attn_build_block_mask_user for a UserScoreMod
     compiled with a mask expression (its tiles go with that mod's calls)."""
+    if torch.device(device).type != "cuda":
+        raise ValueError("block-mask tiles are built by a kernel: device must be a CUDA device (no CPU path)")
     if isinstance(mask_mod, UserScoreMod):
         if not mask_mod.mask_expr:
             raise ValueError("this user mod has no mask expression")
@@ -352,7 +364,7 @@ def attn_fwd(q, k, v, key_mask=None, block_mask: BlockMask | None = None, score_
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
-    ws = workspace(OP_FWD, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_FWD, shape, q, ws)
     if isinstance(score_mod, UserScoreMod):
         if dense_mask is not None:
             raise ValueError("a user score_mod runs without a dense mask")
@@ -382,7 +394,7 @@ def attn_bwd(q, k, v, out, lse, dout, key_mask=None, block_mask=None, score_mod=
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_BWD, shape, q, ws)
     if isinstance(score_mod, UserScoreMod):
         if dense_mask is not None:
             raise ValueError("a user score_mod runs without a dense mask")
@@ -405,7 +417,7 @@ def attn_bwd_preprocess(q, k, out, lse, dout, key_mask=None, ws=None):
     _check_layout(q, k, k, out=out, lse=lse, dout=dout, key_mask=key_mask)
     _cuda(q, k, out, lse, dout, key_mask)
     shape = make_shape(q, k)
-    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_BWD, shape, q, ws)
     _check(load().attn_bwd_preprocess(ctypes.byref(shape), _ptr(out), _ptr(lse), _ptr(dout), _ptr(key_mask),
                                       _ptr(ws), ws.numel(), _stream(q.device)), "attn_bwd_preprocess")
     return ws
@@ -417,7 +429,7 @@ def attn_bwd_dkdv(q, k, v, dout, dk, dv, key_mask=None, block_mask=None, score_m
     _cuda(q, k, v, dout, dk, dv, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
-    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_BWD, shape, q, ws)
     _check(load().attn_bwd_dkdv(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(key_mask),
                                 _bm(block_mask), _mod(score_mod), scale, _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
                                 _stream(q.device)), "attn_bwd_dkdv")
@@ -429,7 +441,7 @@ def attn_bwd_dq(q, k, v, dout, dq, key_mask=None, block_mask=None, score_mod="no
     _cuda(q, k, v, dout, dq, key_mask)
     shape = make_shape(q, k)
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
-    ws = workspace(OP_BWD, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_BWD, shape, q, ws)
     _check(load().attn_bwd_dq(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(key_mask),
                               _bm(block_mask), _mod(score_mod), scale, _ptr(dq), _ptr(ws), ws.numel(),
                               _stream(q.device)), "attn_bwd_dq")
@@ -443,7 +455,7 @@ def attn_decode(q, k, v, key_mask=None, score_mod="none", scale=None, out=None, 
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
-    ws = workspace(OP_DECODE, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_DECODE, shape, q, ws)
     code = load().attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _mod(score_mod),
                               scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device))
     _check(code, "attn_decode")
@@ -460,7 +472,7 @@ def attn_decode_chunk(q, k, v, q_offset: int, key_mask=None, score_mod="none", s
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if lse is None else lse
-    ws = workspace(OP_DECODE_CHUNK, shape, q.device) if ws is None else ws
+    ws = _workspace(OP_DECODE_CHUNK, shape, q, ws)
     code = load().attn_decode_chunk(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask),
                                     _mod(score_mod), scale, int(q_offset), _ptr(out), _ptr(lse), _ptr(ws),
                                     ws.numel(), _stream(q.device))

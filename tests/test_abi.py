@@ -283,6 +283,16 @@ def test_binding_checks_layout_before_the_device(lib):
         with pytest.raises(ValueError, match="dense mask packed for"):
             calls[name](dense_mask=dm)
         dm.shape = (B, H, Sq, Skv)
+    # a caller's workspace must be contiguous bytes on q's device; block masks are built on a GPU
+    from exact_attention_59_gb300 import _lib as L
+    shape = E.make_shape(q, k)
+    ws = torch.zeros(4096, dtype=torch.uint8)
+    assert L._workspace(E.OP_FWD, shape, q, ws) is ws
+    for bad in (torch.zeros(1024, dtype=torch.float32), torch.zeros(4096, 2, dtype=torch.uint8)[:, 0]):
+        with pytest.raises(ValueError, match="ws must be"):
+            L._workspace(E.OP_FWD, shape, q, bad)
+    with pytest.raises(ValueError, match="CUDA device"):
+        E.create_block_mask("causal", 1, 1, 256, 256, device="cpu")
     # the binding's own entry points reach the same checks
     with pytest.raises(ValueError, match="CUDA device"):
         E.flash_attention(q, k, v, torch.randint(0, 2, (B, Skv)))
