@@ -40,6 +40,21 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(declared_symbols()) >= set(lib.SYMBOLS)
 
 
+def test_missing_library_fails_loudly(tmp_path):
+    """With no built library there is no fallback: the first call raises."""
+    import subprocess
+    import sys
+    code = ("import exact_attention_59_gb300._lib as L, torch\n"
+            f"L.LIB_PATH = {str(tmp_path / 'absent.so')!r}\n"
+            "try:\n"
+            "    L.load()\n"
+            "except RuntimeError as e:\n"
+            "    print('raised:', e)\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "raised:" in r.stdout and "is missing" in r.stdout
+
+
 def test_status_strings(lib):
     for code in range(8):
         assert len(lib.status_string(code)) >= 2 and lib.status_string(code) != "unknown status"
