@@ -1,9 +1,9 @@
 // decode.cu - single-query attention (q_len = 1), split-KV, HBM-bound.
 //
-// The flaxattention README ("Decoding", query length 1) times this case and
-// lists "faster decoding attention" as a TODO.  It is a streaming read of K and
-// V (256 bytes per key at D = 64), so the kernel is shaped for bandwidth and
-// latency, not for the tensor core:
+// The flaxattention README ("Benchmark", decoding with query length 1) times
+// this case and puts a faster decode on its to-do list ("Issues / TODO").  It
+// is a streaming read of K and V (256 bytes per key at D = 64), so the kernel
+// is shaped for bandwidth and latency, not for the tensor core:
 //   one CTA per (b, h, split), each owning a contiguous range of up to
 //   rounds x DEC_KEYS keys of one (b, h), walked in `rounds` rounds of
 //   DEC_KEYS keys (128), DEC_WARP_KEYS per warp and round.  The launcher
